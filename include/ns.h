@@ -1,0 +1,133 @@
+/*
+ * ns.h -- C ABI of libns, batched quintic Newton-Schulz orthogonalization on
+ * one GB300 (sm_103a).
+ *
+ * The operation. For every matrix X (M x N, row-major) of a batch:
+ *     X <- X / (||X||_F + eps)
+ *     work on W = X^T when M > N (W is m x n, m = min(M,N), n = max(M,N))
+ *     repeat `steps` times:  A = W W^T;  B = b*A + c*A*A;  W = a*W + B*W
+ *     write W back into X (transposed back when M > N).
+ * The three pages this library follows -- "Fix megabatch_orthogonalize_async
+ * hang on empty FSDP2 shards" (microsoft/dion), "Balance LayerWise optimizer
+ * shards by Newton-Schulz cost, not parameter size" (Megatron-LM) and the
+ * xtuner Muon remainder-strategy PR -- run this iteration on stacks of
+ * same-shape 2-D momentum matrices but never print it; the form and the
+ * default coefficients (a,b,c) = (3.4445, -4.7750, 2.0315), 5 steps and
+ * eps = 1e-7 are Muon's standard quintic Newton-Schulz. The megabatch layout
+ * (a stack of same-shape matrices, per-rank zero padding) is the first page's
+ * "Concrete repro" and "Fix" sections; its "Fix" section also states the
+ * invariant that zero rows stay zero, which lets the library skip padded rows
+ * and columns instead of computing them. The cost model is the second page's
+ * "Changes" item 1.
+ *
+ * Conventions for every call:
+ *  - Pointers named X / X_host are caller-owned. Device pointers must be on
+ *    the current CUDA device. Nothing is retained after the call returns,
+ *    except the library's internal workspace cache (see ns_release_workspace).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream). All device work is stream-ordered on it; calls do not
+ *    synchronise unless stated.
+ *  - Return value: NS_OK (0) or a negative NS_E* code. Arguments are
+ *    validated before anything is launched; on a validation error nothing
+ *    runs and the matrices are untouched. No C++ exception crosses the ABI.
+ */
+#ifndef NS_H_
+#define NS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* element types of X */
+#define NS_F32 0  /* float32 in, float32 out, float32 arithmetic throughout */
+#define NS_BF16 1 /* bfloat16 in/out; bf16 tensor-core operands, fp32 accumulation */
+
+/* status codes */
+#define NS_OK 0
+#define NS_EINVAL (-1)   /* null pointer, negative dims/count/steps, bad dtype */
+#define NS_EALIGN (-2)   /* a matrix pointer is not aligned to its element size */
+#define NS_ENOMEM (-3)   /* workspace allocation failed / caller workspace too small */
+#define NS_ECUDA (-4)    /* a CUDA runtime or driver call failed */
+#define NS_ETIMEOUT (-5) /* a bounded device-side wait gave up (reported by ns_get_status) */
+#define NS_ENODEV (-6)   /* no usable sm_100-family device */
+
+/*
+ * ns_orthogonalize_batched -- Newton-Schulz of `count` matrices, in place.
+ *   X       host array of `count` device pointers; X[i] points at a
+ *           contiguous row-major matrix of shapes[2i] x shapes[2i+1]
+ *           elements of `dtype`. Matrices may differ in shape; a zero
+ *           dimension makes that matrix a no-op. Matrices must not overlap.
+ *   shapes  host array of 2*count int64 (M, N) pairs, read before return.
+ *   count   number of matrices (0 is valid and does nothing).
+ *   steps   number of iterations (>= 0; 0 = normalisation only).
+ *   coeffs  NULL for (3.4445, -4.7750, 2.0315), else a host array of three
+ *           floats (a, b, c) used by every step.
+ *   dtype   NS_F32 or NS_BF16.
+ *   stream  cudaStream_t.
+ * eps is 1e-7. Work is scheduled largest ns_cost first. Scratch memory comes
+ * from an internal per-(device, stream) workspace that grows on demand with
+ * stream-ordered allocation.
+ */
+int ns_orthogonalize_batched(void *const *X, const int64_t *shapes, int count, int steps,
+                             const float *coeffs, int dtype, void *stream);
+
+/*
+ * ns_orthogonalize_batched_ex -- as above, with an explicit eps and an
+ * explicit caller-owned device workspace of at least
+ * ns_workspace_bytes(shapes, count, dtype) bytes (256-byte aligned). The
+ * workspace must not be used by anything else until the stream has passed
+ * this call's work. Returns NS_ENOMEM if it is too small.
+ */
+int ns_orthogonalize_batched_ex(void *const *X, const int64_t *shapes, int count, int steps,
+                                const float *coeffs, float eps, int dtype, void *workspace,
+                                size_t workspace_bytes, void *stream);
+
+/* Device workspace bytes the _ex call needs for this batch (0 on bad input). */
+size_t ns_workspace_bytes(const int64_t *shapes, int count, int dtype);
+
+/*
+ * ns_orthogonalize_batched_host -- the same operation on HOST matrices:
+ * copies each X_host[i] to the device, runs ns_orthogonalize_batched on
+ * `stream`, copies the results back into X_host[i] and synchronises the
+ * stream before returning. Host buffers may be pageable or pinned (pinned
+ * copies overlap better). Device buffers are part of the internal workspace.
+ */
+int ns_orthogonalize_batched_host(void *const *X_host, const int64_t *shapes, int count,
+                                  int steps, const float *coeffs, int dtype, void *stream);
+
+/*
+ * ns_cost -- Newton-Schulz cost of an M x N matrix, max(M,N) * min(M,N)^2
+ * (second page, "Changes" item 1: the dominant term of the orthogonalization).
+ * Returns -1 if M or N is negative.
+ */
+int64_t ns_cost(int64_t M, int64_t N);
+
+/*
+ * ns_get_status -- synchronise `stream`, then return and clear the device
+ * status word of the current device: NS_OK, or NS_ETIMEOUT if a kernel's
+ * bounded wait gave up (its outputs are then unspecified), or NS_ECUDA if
+ * the synchronisation itself failed.
+ */
+int ns_get_status(void *stream);
+
+/* ns_strerror -- static description of a status code. */
+const char *ns_strerror(int code);
+
+/*
+ * ns_release_workspace -- synchronise the device and free the internal
+ * workspace cache of the current device. Returns NS_OK or NS_ECUDA.
+ */
+int ns_release_workspace(void);
+
+/* ns_num_kernel_launches -- kernels this library launched on this process
+ * since load (for launch accounting in benchmarks). */
+int64_t ns_num_kernel_launches(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NS_H_ */

@@ -1,0 +1,192 @@
+"""ctypes binding of libns (C ABI in include/ns.h).
+
+Argument marshalling only: torch tensors become device pointers, shapes become
+an int64 array, and the current torch CUDA stream becomes the cudaStream_t.
+Every step of the computation runs in the library's CUDA kernels. There is no
+fallback: if ``libns.so`` is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+NS_F32 = 0
+NS_BF16 = 1
+
+_ERRORS = {0: "NS_OK", -1: "NS_EINVAL", -2: "NS_EALIGN", -3: "NS_ENOMEM", -4: "NS_ECUDA",
+           -5: "NS_ETIMEOUT", -6: "NS_ENODEV"}
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_lock = threading.Lock()
+_lib = None
+
+
+class NSError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = int(code)
+        name = _ERRORS.get(self.code, str(code))
+        msg = f"{what}: {name}" if what else name
+        try:
+            desc = load_library().ns_strerror(self.code)
+            if desc:
+                msg += f" ({desc.decode()})"
+        except Exception:  # the library itself may be what is missing
+            pass
+        super().__init__(msg)
+
+
+def library_path() -> str:
+    return os.environ.get("NS_LIBRARY_PATH", os.path.join(_PKG, "libns.so"))
+
+
+def load_library() -> ctypes.CDLL:
+    """Load libns.so (built in-tree by ``newton_schulz_quintic_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"libns.so not found at {path}: build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'` "
+                "(no CPU fallback exists)")
+        lib = ctypes.CDLL(path)
+        vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        lib.ns_orthogonalize_batched.restype = i32
+        lib.ns_orthogonalize_batched.argtypes = [vp, vp, i32, i32, vp, i32, vp]
+        lib.ns_orthogonalize_batched_ex.restype = i32
+        lib.ns_orthogonalize_batched_ex.argtypes = [vp, vp, i32, i32, vp, ctypes.c_float, i32, vp,
+                                                    ctypes.c_size_t, vp]
+        lib.ns_orthogonalize_batched_host.restype = i32
+        lib.ns_orthogonalize_batched_host.argtypes = [vp, vp, i32, i32, vp, i32, vp]
+        lib.ns_workspace_bytes.restype = ctypes.c_size_t
+        lib.ns_workspace_bytes.argtypes = [vp, i32, i32]
+        lib.ns_cost.restype = i64
+        lib.ns_cost.argtypes = [i64, i64]
+        lib.ns_get_status.restype = i32
+        lib.ns_get_status.argtypes = [vp]
+        lib.ns_strerror.restype = ctypes.c_char_p
+        lib.ns_strerror.argtypes = [i32]
+        lib.ns_release_workspace.restype = i32
+        lib.ns_release_workspace.argtypes = []
+        lib.ns_num_kernel_launches.restype = i64
+        lib.ns_num_kernel_launches.argtypes = []
+        _lib = lib
+        return lib
+
+
+def _dtype_code(dtype) -> int:
+    import torch
+    if dtype == torch.float32:
+        return NS_F32
+    if dtype == torch.bfloat16:
+        return NS_BF16
+    raise TypeError(f"unsupported dtype {dtype}: use float32 or bfloat16")
+
+
+def _marshal(mats, coeffs):
+    n = len(mats)
+    ptrs = (ctypes.c_void_p * max(n, 1))(*[t.data_ptr() for t in mats])
+    shapes = (ctypes.c_int64 * max(2 * n, 1))(*[int(d) for t in mats for d in t.shape])
+    co = None
+    if coeffs is not None:
+        if len(coeffs) != 3:
+            raise ValueError("coeffs must be (a, b, c)")
+        co = (ctypes.c_float * 3)(*[float(v) for v in coeffs])
+    return ptrs, shapes, co
+
+
+def _check(mats, want_cuda: bool):
+    if not mats:
+        return None
+    dt = mats[0].dtype
+    dev = mats[0].device
+    for t in mats:
+        if t.dim() != 2:
+            raise ValueError("every matrix must be 2-D")
+        if t.dtype != dt or t.device != dev:
+            raise ValueError("all matrices must share dtype and device")
+        if not t.is_contiguous():
+            raise ValueError("matrices must be contiguous (row-major)")
+        if want_cuda and not t.is_cuda:
+            raise ValueError("matrices must be CUDA tensors")
+        if not want_cuda and t.is_cuda:
+            raise ValueError("host entry point takes CPU tensors")
+    return _dtype_code(dt)
+
+
+def orthogonalize_batched(mats, steps: int = 5, coeffs=None, eps: float | None = None,
+                          stream=None, workspace=None) -> None:
+    """In-place Newton-Schulz of a list of 2-D CUDA tensors (float32 or bfloat16).
+
+    ``stream`` defaults to torch's current stream on the tensors' device.
+    With ``eps`` or ``workspace`` given, the ``_ex`` entry point is used
+    (``workspace`` is a CUDA uint8 tensor of at least ``workspace_bytes``).
+    """
+    import torch
+    lib = load_library()
+    mats = list(mats)
+    code = _check(mats, want_cuda=True)
+    if code is None:
+        return
+    dev = mats[0].device
+    with torch.cuda.device(dev):
+        s = stream if stream is not None else torch.cuda.current_stream(dev)
+        sp = ctypes.c_void_p(s.cuda_stream)
+        ptrs, shapes, co = _marshal(mats, coeffs)
+        if eps is None and workspace is None:
+            rc = lib.ns_orthogonalize_batched(ptrs, shapes, len(mats), int(steps), co, code, sp)
+        else:
+            e = 1e-7 if eps is None else float(eps)
+            if workspace is None:
+                need = workspace_bytes([tuple(t.shape) for t in mats], mats[0].dtype)
+                workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+            rc = lib.ns_orthogonalize_batched_ex(ptrs, shapes, len(mats), int(steps), co, e, code,
+                                                 ctypes.c_void_p(workspace.data_ptr()),
+                                                 workspace.numel(), sp)
+    if rc != 0:
+        raise NSError(rc, "ns_orthogonalize_batched")
+
+
+def orthogonalize_batched_host(mats, steps: int = 5, coeffs=None, device=None, stream=None) -> None:
+    """In-place Newton-Schulz of CPU tensors through the library's host entry
+    point (host-to-device copies, compute, device-to-host copies, sync)."""
+    import torch
+    lib = load_library()
+    mats = list(mats)
+    code = _check(mats, want_cuda=False)
+    if code is None:
+        return
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        s = stream if stream is not None else torch.cuda.current_stream(dev)
+        ptrs, shapes, co = _marshal(mats, coeffs)
+        rc = lib.ns_orthogonalize_batched_host(ptrs, shapes, len(mats), int(steps), co, code,
+                                               ctypes.c_void_p(s.cuda_stream))
+    if rc != 0:
+        raise NSError(rc, "ns_orthogonalize_batched_host")
+
+
+def workspace_bytes(shapes, dtype) -> int:
+    lib = load_library()
+    code = dtype if isinstance(dtype, int) else _dtype_code(dtype)
+    shapes = list(shapes)
+    arr = (ctypes.c_int64 * max(2 * len(shapes), 1))(*[int(d) for s in shapes for d in s])
+    return int(lib.ns_workspace_bytes(arr, len(shapes), code))
+
+
+def cost(M: int, N: int) -> int:
+    """max(M,N) * min(M,N)^2, computed by the library."""
+    return int(load_library().ns_cost(int(M), int(N)))
+
+
+def get_status(stream=None) -> int:
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(load_library().ns_get_status(ctypes.c_void_p(s.cuda_stream)))
+
+
+def num_kernel_launches() -> int:
+    return int(load_library().ns_num_kernel_launches())

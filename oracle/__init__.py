@@ -1,0 +1,133 @@
+"""CPU fp64 oracle for batched quintic Newton-Schulz orthogonalization.
+
+TEST INFRASTRUCTURE ONLY. Only the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg may import this package. The CUDA library never
+loads, links or calls anything here, and this package imports nothing from the
+CUDA library: the only code the two sides share is the seeded input generator
+(``newton_schulz_quintic_gb300.inputs``), which holds none of the method's
+arithmetic.
+
+Two independent computations live here:
+
+* ``orthogonalize`` -- the iteration itself, step by step in fp64, in plain C
+  (``ns_oracle.c``): s = ||X||_F, X <- X/(s+eps), work on X^T when M > N, then
+  ``steps`` times A = X X^T, B = b A + c A^2, X = a X + B X.
+* ``svd_twin`` -- the closed form of the same map through LAPACK's SVD: every
+  step is an odd matrix polynomial, so it keeps the singular vectors and maps
+  each singular value through f(s) = a s + b s^3 + c s^5.
+
+The pages this follows ("Fix megabatch_orthogonalize_async hang on empty FSDP2
+shards", "Balance LayerWise optimizer shards by Newton-Schulz cost, not
+parameter size", and the xtuner Muon remainder-strategy PR) run the iteration
+but never print it; the step form and coefficients are the standard quintic
+Newton-Schulz of Muon. The zero-row invariant is from the first page's "Fix"
+section, the cost max(M,N)*min(M,N)^2 from the second page's "Changes" item 1.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+DEFAULT_COEFFS = (3.4445, -4.7750, 2.0315)
+DEFAULT_STEPS = 5
+DEFAULT_EPS = 1e-7
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ns_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_lock = threading.Lock()
+_libs: dict[int, ctypes.CDLL] = {}
+
+
+def lib_path(mutation: int = 0) -> str:
+    name = "libns_oracle.so" if mutation == 0 else f"libns_oracle_mut{mutation}.so"
+    return os.path.join(_BUILD, name)
+
+
+def build(mutation: int = 0, force: bool = False) -> str:
+    """Compile ns_oracle.c with gcc (mutation != 0 plants a numbered mistake)."""
+    out = lib_path(mutation)
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(_SRC):
+        return out
+    os.makedirs(_BUILD, exist_ok=True)
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-ffp-contract=off", "-fopenmp", "-shared", "-fPIC",
+           f"-DNS_ORACLE_MUTATION={int(mutation)}", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _lib(mutation: int = 0) -> ctypes.CDLL:
+    with _lock:
+        if mutation not in _libs:
+            lib = ctypes.CDLL(build(mutation))
+            lib.ns_oracle_cost.restype = ctypes.c_int64
+            lib.ns_oracle_cost.argtypes = [ctypes.c_int64, ctypes.c_int64]
+            lib.ns_oracle_frobenius.restype = ctypes.c_double
+            lib.ns_oracle_frobenius.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64]
+            lib.ns_oracle_orthogonalize.restype = ctypes.c_int
+            lib.ns_oracle_orthogonalize.argtypes = [
+                ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                ctypes.c_double, ctypes.c_double, ctypes.c_double, ctypes.c_double, ctypes.c_int]
+            _libs[mutation] = lib
+        return _libs[mutation]
+
+
+def cost(M: int, N: int) -> int:
+    """Newton-Schulz cost max(M,N)*min(M,N)^2 (second page, "Changes" item 1)."""
+    return int(_lib().ns_oracle_cost(int(M), int(N)))
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact widening of bfloat16 bit patterns (uint16) to float64: a bf16 is the
+    top half of an IEEE binary32, so shifting left by 16 gives the same value."""
+    u32 = bits.astype(np.uint32) << np.uint32(16)
+    return u32.view(np.float32).astype(np.float64)
+
+
+def to_f64(x) -> np.ndarray:
+    """Exact fp64 copy of a CPU tensor/array given in float32, float64 or bfloat16."""
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            x = x.detach().cpu().contiguous()
+            if x.dtype == torch.bfloat16:
+                return bf16_bits_to_f64(x.view(torch.int16).numpy().view(np.uint16))
+            return x.numpy().astype(np.float64)
+    except ImportError:  # pragma: no cover - torch is always present in this repo
+        pass
+    return np.asarray(x, dtype=np.float64)
+
+
+def orthogonalize(X, steps: int = DEFAULT_STEPS, coeffs=DEFAULT_COEFFS,
+                  eps: float = DEFAULT_EPS, orient: int = 0, mutation: int = 0) -> np.ndarray:
+    """Newton-Schulz of one M x N matrix in fp64; returns a new array.
+
+    orient 0 follows the rule (work on X^T when M > N); 1 never transposes and
+    2 always transposes (only the tests use 1 and 2).
+    """
+    W = np.ascontiguousarray(to_f64(X), dtype=np.float64).copy()
+    if W.ndim != 2:
+        raise ValueError("oracle takes 2-D matrices")
+    a, b, c = (float(v) for v in coeffs)
+    rc = _lib(mutation).ns_oracle_orthogonalize(
+        W.ctypes.data, W.shape[0], W.shape[1], int(steps), a, b, c, float(eps), int(orient))
+    if rc != 0:
+        raise RuntimeError(f"ns_oracle_orthogonalize failed with {rc}")
+    return W
+
+
+def orthogonalize_batched(mats, steps: int = DEFAULT_STEPS, coeffs=DEFAULT_COEFFS,
+                          eps: float = DEFAULT_EPS) -> list:
+    """The batched form: each matrix of the list independently."""
+    return [orthogonalize(X, steps, coeffs, eps) for X in mats]
+
+
+def frobenius(X) -> float:
+    W = np.ascontiguousarray(to_f64(X))
+    return float(_lib().ns_oracle_frobenius(W.ctypes.data, W.shape[0], W.shape[1]))

@@ -1,0 +1,54 @@
+"""Closed-form twin of the Newton-Schulz oracle, through LAPACK's SVD.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring).
+
+Each Newton-Schulz step X <- a X + (b X X^T + c (X X^T)^2) X equals
+X <- a X + b X X^T X + c X X^T X X^T X, an odd polynomial in X. Written with
+the thin SVD X = U diag(s) V^T, it is U diag(f(s)) V^T with
+f(s) = a s + b s^3 + c s^5, so the singular vectors never change and each
+singular value follows the scalar recurrence alone. After the normalisation
+X/(||X||_F + eps) and ``steps`` steps the exact result is
+U diag(f^steps(s_i / (||X||_F + eps))) V^T. This is a different computation
+from the step-by-step iteration (no matrix products, one SVD), so agreement
+between the two pins the oracle.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def quintic(s, coeffs):
+    """One step of the scalar map f(s) = a s + b s^3 + c s^5."""
+    a, b, c = coeffs
+    s = np.asarray(s, dtype=np.float64)
+    s2 = s * s
+    return s * (a + s2 * (b + c * s2))
+
+
+def quintic_iterate(s, steps, coeffs):
+    """f applied ``steps`` times."""
+    out = np.asarray(s, dtype=np.float64)
+    for _ in range(int(steps)):
+        out = quintic(out, coeffs)
+    return out
+
+
+def closed_form(X: np.ndarray, steps: int, coeffs, eps: float) -> np.ndarray:
+    """U diag(f^steps(s / (||X||_F + eps))) V^T for a 2-D fp64 array."""
+    X = np.asarray(X, dtype=np.float64)
+    if X.size == 0:
+        return X.copy()
+    fro = np.sqrt(np.sum(X * X))
+    U, s, Vt = np.linalg.svd(X, full_matrices=False)
+    g = quintic_iterate(s / (fro + eps), steps, coeffs)
+    return (U * g) @ Vt
+
+
+def polar(X: np.ndarray) -> np.ndarray:
+    """Orthogonal polar factor U V^T (all singular values set to one)."""
+    U, _, Vt = np.linalg.svd(np.asarray(X, dtype=np.float64), full_matrices=False)
+    return U @ Vt
+
+
+def singular_values(X: np.ndarray) -> np.ndarray:
+    return np.linalg.svd(np.asarray(X, dtype=np.float64), compute_uv=False)

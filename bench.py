@@ -1,0 +1,405 @@
+#!/usr/bin/env python
+"""Throughput benchmark of batched quintic Newton-Schulz on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-cpu-baseline]
+
+A step is one pass of the whole hot path -- norm, preparation and 5 x
+{gram, square, apply} -- over one batch of the workload (default: 8 bf16
+8192 x 6144 matrices, N(0, 0.02), one library call). Inputs are resident in
+HBM when the timed region starts and are restored from a pristine copy
+between steps, outside the timed events; the batch (768 MiB) is larger than
+L2, so no separate flush is needed. Each step is timed with CUDA events on
+the launching stream; `value` is matrices / second over the K timed steps
+(max over ranks of the time, all ranks' matrices).
+
+Multi-GPU (torchrun, one process per GPU): matrices are independent, so every
+rank processes its own batch with no collective in the data path (weak
+scaling); only the timing barrier and the max-reduction of times use the
+process group.
+
+`--impl reference` times the CPU fp64 oracle on the host cores instead: each
+step is one Newton-Schulz step of one matrix of the workload (a bounded
+sample), scaled to matrices / second.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+# ------------------------------------------------------------------ helpers
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=None)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--e2e-steps", type=int, default=3)
+    return p.parse_args()
+
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if (args.impl == "ours" and torch.cuda.is_available()) else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+        pg = dist
+    elif torch.cuda.is_available() and args.impl == "ours":
+        torch.cuda.set_device(local)
+    return world, rank, local, pg
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "sm_max_mhz": 2070.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def physical_gpu_index(local: int) -> int:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        items = [v.strip() for v in vis.split(",") if v.strip()]
+        if local < len(items) and items[local].isdigit():
+            return int(items[local])
+    return local
+
+
+def workload_flops(shapes, steps):
+    nominal = executed = apply = 0
+    for M, N in shapes:
+        m, n = min(M, N), max(M, N)
+        nominal += steps * (4 * m * m * n + 2 * m ** 3)
+        executed += steps * (3 * m * m * n + m ** 3)
+        apply += steps * (2 * m * m * n)
+    return nominal, executed, apply
+
+
+def traffic_record(kernel: str):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if it
+    was captured from the current kernel source (sha256 prefix matches)."""
+    src = os.path.join(ROOT, "newton_schulz_quintic_gb300", "csrc", "ns_tc.cu")
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        for line in open(path):
+            f = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
+            if f.get("kernel") == kernel and f.get("source_sha") == sha and f.get("workload"):
+                return f
+    except Exception:
+        return None
+    return None
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, world, rank, local, pg):
+    import torch
+    from newton_schulz_quintic_gb300 import api, inputs
+
+    api.load_library()
+    wl = inputs.WORKLOADS[args.workload or inputs.HEADLINE]
+    dev = torch.device("cuda", local)
+    host = [wl.matrix(i) for i in range(wl.count)]
+    pristine = [h.to(dev) for h in host]
+    work = [torch.empty_like(p) for p in pristine]
+    slices = wl.call_slices()
+    stream = torch.cuda.current_stream(dev)
+
+    def restore():
+        for w, p in zip(work, pristine):
+            w.copy_(p, non_blocking=True)
+
+    def one_step():
+        for sl in slices:
+            api.orthogonalize_batched(work[sl], steps=wl.steps)
+
+    for _ in range(max(args.warmup, 0)):
+        restore()
+        one_step()
+    torch.cuda.synchronize()
+    if api.get_status() != 0:
+        raise RuntimeError("device status word reports a timeout during warm-up")
+
+    clocks = ClockSampler(physical_gpu_index(local))
+    if rank == 0:
+        clocks.start()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    launches0 = api.num_kernel_launches()
+    api.set_kernel_timing(True)
+    ev = []
+    for _ in range(args.steps):
+        restore()
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        one_step()
+        e.record(stream)
+        ev.append((s, e))
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    ktimes = api.kernel_times()
+    api.set_kernel_timing(False)
+    launches = api.num_kernel_launches() - launches0
+    clock_rec = clocks.stop() if rank == 0 else None
+    if api.get_status() != 0:
+        raise RuntimeError("device status word reports a timeout during the timed steps")
+    total_ms = sum(s.elapsed_time(e) for s, e in ev)
+    if pg:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # end to end through the host entry point: pinned host inputs, H2D copy,
+    # compute, D2H copy of the result, all inside the timed region
+    pinned = [h.clone().pin_memory() for h in host]
+    e2e_bytes = sum(h.numel() * h.element_size() for h in host)
+    api.orthogonalize_batched_host(pinned[:1], steps=wl.steps, device=dev)  # warm
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        for sl in slices:
+            api.orthogonalize_batched_host(pinned[sl], steps=wl.steps, device=dev)
+    e2e_s = time.perf_counter() - t0
+    if pg:
+        t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_s = float(t.item())
+
+    if rank != 0:
+        return None
+
+    count = wl.count
+    ms_per_step = total_ms / args.steps
+    value = world * count * args.steps / (total_ms / 1e3)
+    nominal, executed, apply_flops = workload_flops(wl.shapes, wl.steps)
+    peaks, peak_kind = measured_peaks()
+    # dominant kernel: the apply GEMM (W' = a W + B W), 2 m^2 n flops per matrix per step
+    ams, alaunch = ktimes["apply"]
+    apply_per_launch = apply_flops * args.steps / max(alaunch, 1)
+    achieved = apply_per_launch / (ams / max(alaunch, 1) / 1e3) / 1e12 if alaunch else None
+    peak = peaks.get("bf16_tflops_sustained", 1700.0)
+    tr = traffic_record("apply")
+    gemm_ms = sum(ktimes[k][0] for k in ("gram", "square", "apply"))
+    out = {
+        "metric": "NS-orthogonalized matrices/s (bf16 tensor-core TFLOP/s and fraction of peak alongside)",
+        "value": round(value, 3),
+        "unit": "matrices/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if wl.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded N(0,0.02) bf16, per-matrix torch.Generator seeds)",
+        "config": {"workload": wl.name, "matrices": count, "shapes": [list(t) for t in sorted({tuple(x) for x in wl.shapes})],
+                   "ns_steps": wl.steps, "coeffs": [3.4445, -4.775, 2.0315], "calls": [s.stop - s.start for s in slices],
+                   "l2": "inputs (%.0f MiB) larger than L2; restored from a pristine copy between steps"
+                         % (e2e_bytes / 2 ** 20),
+                   "parallelism": f"replicas x{world} (independent matrices, no collective)"},
+        "tflops_nominal": round(world * nominal * args.steps / (total_ms / 1e3) / 1e12, 2),
+        "tflops_executed": round(world * executed * args.steps / (total_ms / 1e3) / 1e12, 2),
+        "frac_of_bf16_peak_nominal": round(nominal * args.steps / (total_ms / 1e3) / 1e12 / peak, 4),
+        "roofline": {
+            "kernel": "ns_tc_gemm_kernel<2> (apply: W' = aW + BW)",
+            "bound": "tensor",
+            "achieved": round(achieved, 2) if achieved else None,
+            "peak": peak,
+            "peak_source": f"{peak_kind} bf16_tflops_sustained (kernel timed inside a long step)",
+            "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4) if achieved else None,
+            "traffic": (int(float(tr["bytes_per_launch"])) if tr else None),
+            "algorithmic_flops_per_launch": apply_per_launch,
+        },
+        "kernels": {k: {"ms_total": round(v[0], 3), "launches": v[1],
+                        "share": round(v[0] / max(sum(x[0] for x in ktimes.values()), 1e-9), 4)}
+                    for k, v in ktimes.items() if v[1]},
+        "gemm_tflops_executed": round(executed * args.steps / (gemm_ms / 1e3) / 1e12, 2) if gemm_ms else None,
+        "gpu_launches": int(launches),
+        "e2e": {"value": round(world * count * args.e2e_steps / e2e_s, 3), "unit": "matrices/s",
+                "h2d_bytes_per_step": e2e_bytes, "d2h_bytes_per_step": e2e_bytes,
+                "api": "ns_orthogonalize_batched_host (pinned host buffers)"},
+        "clocks": clock_rec,
+    }
+    return out, wl
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def cpu_oracle_sample(wl, matrix_index=0):
+    """One Newton-Schulz step of one matrix of the workload with the oracle's
+    NumPy implementation; returns (seconds, description)."""
+    import numpy as np  # noqa: F401
+    import oracle
+    x = oracle.to_f64(wl.matrix(matrix_index))
+    t0 = time.perf_counter()
+    oracle.orthogonalize_np(x, steps=1)
+    dt = time.perf_counter() - t0
+    M, N = wl.shapes[matrix_index]
+    return dt, f"1 of {wl.steps} Newton-Schulz steps on 1 of {wl.count} matrices ({M}x{N}), " \
+               f"oracle.orthogonalize_np fp64, scaled to matrices/s as 1/({wl.steps} x step time)"
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, world, rank):
+    from newton_schulz_quintic_gb300 import inputs
+    if rank != 0:
+        return None
+    wl = inputs.WORKLOADS[args.workload or inputs.HEADLINE]
+    for _ in range(max(args.warmup, 0)):
+        cpu_oracle_sample(wl)
+    times = []
+    desc = ""
+    for _ in range(args.steps):
+        dt, desc = cpu_oracle_sample(wl)
+        times.append(dt)
+    per_matrix = wl.steps * statistics.mean(times)
+    value = 1.0 / per_matrix
+    out = {
+        "impl": "reference",
+        "metric": "NS-orthogonalized matrices/s (bf16 tensor-core TFLOP/s and fraction of peak alongside)",
+        "value": round(value, 6),
+        "unit": "matrices/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(statistics.mean(times) * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded N(0,0.02) bf16 inputs widened exactly to fp64)",
+        "config": {"workload": wl.name, "matrices": wl.count,
+                   "shapes": [list(t) for t in sorted({tuple(x) for x in wl.shapes})], "ns_steps": wl.steps},
+        "cpu_baseline": {"value": round(value, 6), "unit": "matrices/s", "cores": cores(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(value, 6), "unit": "matrices/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    return out
+
+
+def main():
+    args = parse_args()
+    world, rank, local, pg = dist_setup(args)
+    if args.impl == "reference":
+        out = run_reference(args, world, rank)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        if pg:
+            pg.barrier()
+            pg.destroy_process_group()
+        return
+    res = run_ours(args, world, rank, local, pg)
+    if res is not None:
+        out, wl = res
+        if world == 1 and not args.no_cpu_baseline:
+            dt, desc = cpu_oracle_sample(wl)
+            v = 1.0 / (wl.steps * dt)
+            out["cpu_baseline"] = {"value": round(v, 6), "unit": "matrices/s", "cores": cores(),
+                                   "kind": "oracle", "sample": desc}
+        print(json.dumps(out), flush=True)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -126,6 +126,19 @@ int ns_release_workspace(void);
  * since load (for launch accounting in benchmarks). */
 int64_t ns_num_kernel_launches(void);
 
+/*
+ * Per-kernel timing for measurement tools. While enabled, every kernel
+ * launch of later calls is bracketed by a pair of CUDA events recorded on the
+ * caller's stream (a few microseconds of overhead per launch).
+ * ns_set_kernel_timing(1) enables and clears the record, (0) disables it.
+ * ns_get_kernel_times synchronises on the recorded events and writes, for the
+ * kernel classes 0 norm, 1 prep, 2 gram, 3 square, 4 apply, 5 resident,
+ * the total milliseconds into ms[k] and the launch count into launches[k]
+ * for k < n (n <= 6). Returns NS_OK or NS_ECUDA.
+ */
+int ns_set_kernel_timing(int enable);
+int ns_get_kernel_times(double *ms, int64_t *launches, int n);
+
 #ifdef __cplusplus
 }
 #endif

@@ -73,6 +73,10 @@ def load_library() -> ctypes.CDLL:
         lib.ns_release_workspace.argtypes = []
         lib.ns_num_kernel_launches.restype = i64
         lib.ns_num_kernel_launches.argtypes = []
+        lib.ns_set_kernel_timing.restype = i32
+        lib.ns_set_kernel_timing.argtypes = [i32]
+        lib.ns_get_kernel_times.restype = i32
+        lib.ns_get_kernel_times.argtypes = [vp, vp, i32]
         _lib = lib
         return lib
 
@@ -190,3 +194,21 @@ def get_status(stream=None) -> int:
 
 def num_kernel_launches() -> int:
     return int(load_library().ns_num_kernel_launches())
+
+
+KERNEL_KINDS = ("norm", "prep", "gram", "square", "apply", "resident")
+
+
+def set_kernel_timing(enable: bool) -> None:
+    load_library().ns_set_kernel_timing(1 if enable else 0)
+
+
+def kernel_times() -> dict:
+    """{kind: (total_ms, launches)} recorded since set_kernel_timing(True)."""
+    n = len(KERNEL_KINDS)
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_int64 * n)()
+    rc = load_library().ns_get_kernel_times(ms, cnt, n)
+    if rc != 0:
+        raise NSError(rc, "ns_get_kernel_times")
+    return {k: (float(ms[i]), int(cnt[i])) for i, k in enumerate(KERNEL_KINDS)}

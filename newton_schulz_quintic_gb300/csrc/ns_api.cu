@@ -1,0 +1,571 @@
+// ns_api.cu -- C ABI of libns (include/ns.h) and its host planner.
+//
+// The planner validates the batch, decides per matrix between the
+// shared-memory resident kernel (small m) and the GEMM path, orders the
+// GEMM-path matrices by Newton-Schulz cost max(M,N)*min(M,N)^2 (largest
+// first, the ordering rule of the second page's "Changes" items 1-2), lays out
+// one device workspace, builds the per-phase tile lists and TMA descriptors,
+// uploads them, and launches:
+//   resident kernel (all small matrices at once)
+//   norm  ->  prep  ->  steps x { gram -> square -> apply }  (all large matrices)
+// The megabatch of the first page's "Concrete repro" is just `count`
+// matrices of one shape; remainder batches (the xtuner PR's ragged
+// all-to-all commit) are calls with a smaller `count`, so no zero matrix is
+// ever orthogonalised.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <vector>
+
+#include "../../include/ns.h"
+#include "ns_internal.h"
+
+namespace ns {
+
+static std::atomic<int64_t> g_launches{0};
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+// Device status word (one per device, file-scope; see ns_get_status).
+__device__ int g_status_word;
+
+namespace {
+
+constexpr float kDefaultCoeffs[3] = {3.4445f, -4.7750f, 2.0315f};
+constexpr int kResidentMaxM = 64;
+constexpr int kResidentSmemMax = 200 * 1024;
+constexpr size_t kAlign = 1024;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+int64_t round8(int64_t v) { return (v + 7) / 8 * 8; }
+
+// ------------------------------------------------------------ device info
+struct DevInfo {
+  bool ok = false;
+  int sms = 0;
+  int *status = nullptr;
+};
+std::mutex g_mu;
+std::map<int, DevInfo> g_dev;
+
+int device_info(DevInfo **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return NS_ECUDA;
+  auto it = g_dev.find(dev);
+  if (it == g_dev.end()) {
+    DevInfo di;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return NS_ECUDA;
+    di.ok = prop.major == 10;  // sm_100 family (sm_103a is what this library is built for)
+    di.sms = prop.multiProcessorCount;
+    void *sym = nullptr;
+    if (cudaGetSymbolAddress(&sym, g_status_word) != cudaSuccess) return NS_ECUDA;
+    di.status = static_cast<int *>(sym);
+    it = g_dev.emplace(dev, di).first;
+  }
+  *out = &it->second;
+  return it->second.ok ? NS_OK : NS_ENODEV;
+}
+
+// ------------------------------------------------------------ TMA encode
+using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                              const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeFn g_encode = nullptr;
+
+int get_encode() {
+  if (g_encode) return NS_OK;
+  void *fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+          cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn)
+    return NS_ECUDA;
+  g_encode = reinterpret_cast<EncodeFn>(fn);
+  return NS_OK;
+}
+
+// bf16 row-major rows x cols matrix with a pitch of `pitch` elements; box
+// {64 columns, 128 rows} with 128-byte swizzle; out-of-range reads give 0.
+int encode_bf16(CUtensorMap *map, void *base, int64_t rows, int64_t cols, int64_t pitch) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(std::max<int64_t>(cols, 1)),
+                        static_cast<cuuint64_t>(std::max<int64_t>(rows, 1))};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch * 2)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kTcBK), static_cast<cuuint32_t>(kTcBM)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? NS_OK : NS_ECUDA;
+}
+
+// ------------------------------------------------------------ layout
+struct BigMat {
+  int index;  // caller index
+  int64_t M, N, m, n, pm, pn;
+  int transposed;
+  size_t off_x, off_xt0, off_xt1, off_a, off_b;
+};
+
+struct Layout {
+  int dtype = 0;
+  int elt = 2;
+  std::vector<BigMat> big;   // cost order
+  std::vector<int> res;      // caller indices on the resident path
+  int res_maxm = 0, res_smem = 0;
+  std::vector<Tile> tiles01, tiles2;
+  std::vector<int> prefix;   // prep tile prefix, big.size()+1
+  size_t off_mats = 0, off_res = 0, off_t01 = 0, off_t2 = 0, off_prefix = 0, blob_end = 0;
+  size_t off_partials = 0, off_ext = 0, off_buffers = 0, total = 0;
+};
+
+int validate(void *const *X, const int64_t *shapes, int count, int steps, int dtype, bool check_ptrs) {
+  if (count < 0 || steps < 0) return NS_EINVAL;
+  if (dtype != NS_F32 && dtype != NS_BF16) return NS_EINVAL;
+  if (count == 0) return NS_OK;
+  if (!shapes || (check_ptrs && !X)) return NS_EINVAL;
+  const size_t elt = dtype == NS_BF16 ? 2 : 4;
+  for (int i = 0; i < count; ++i) {
+    const int64_t M = shapes[2 * i], N = shapes[2 * i + 1];
+    if (M < 0 || N < 0) return NS_EINVAL;
+    if (M > INT32_MAX / 2 || N > INT32_MAX / 2) return NS_EINVAL;
+    if (M * N > (int64_t(1) << 40)) return NS_EINVAL;
+    if (check_ptrs && M * N > 0) {
+      if (!X[i]) return NS_EINVAL;
+      if (reinterpret_cast<uintptr_t>(X[i]) % elt) return NS_EALIGN;
+    }
+  }
+  return NS_OK;
+}
+
+void build_layout(const int64_t *shapes, int count, int dtype, Layout &L) {
+  L = Layout();
+  L.dtype = dtype;
+  L.elt = dtype == NS_BF16 ? 2 : 4;
+  std::vector<int> order;
+  for (int i = 0; i < count; ++i) {
+    const int64_t M = shapes[2 * i], N = shapes[2 * i + 1];
+    if (M == 0 || N == 0) continue;
+    const int64_t m = std::min(M, N), n = std::max(M, N);
+    if (m <= kResidentMaxM && resident_smem_bytes(static_cast<int>(m), static_cast<int>(n), dtype) <= kResidentSmemMax) {
+      L.res.push_back(i);
+      L.res_maxm = std::max<int>(L.res_maxm, static_cast<int>(m));
+      L.res_smem = std::max(L.res_smem, resident_smem_bytes(static_cast<int>(m), static_cast<int>(n), dtype));
+    } else {
+      order.push_back(i);
+    }
+  }
+  // largest Newton-Schulz cost first; ties keep the caller's order
+  std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
+    return ns_cost(shapes[2 * a], shapes[2 * a + 1]) > ns_cost(shapes[2 * b], shapes[2 * b + 1]);
+  });
+  const int BM = dtype == NS_BF16 ? kTcBM : kSimtBM;
+  const int BN = dtype == NS_BF16 ? kTcBN : kSimtBN;
+  L.prefix.push_back(0);
+  for (int idx : order) {
+    BigMat b{};
+    b.index = idx;
+    b.M = shapes[2 * idx];
+    b.N = shapes[2 * idx + 1];
+    b.transposed = b.M > b.N;
+    b.m = std::min(b.M, b.N);
+    b.n = std::max(b.M, b.N);
+    b.pm = round8(b.m);
+    b.pn = round8(b.n);
+    const int mi = static_cast<int>(L.big.size());
+    // gram / square: tiles with some column index >= some row index
+    for (int64_t r0 = 0; r0 < b.m; r0 += BM)
+      for (int64_t c0 = 0; c0 < b.m; c0 += BN)
+        if (c0 + BN > r0) L.tiles01.push_back(Tile{mi, static_cast<int>(r0), static_cast<int>(c0), 0});
+    // apply: rows of W^T (over n) x columns (over m)
+    for (int64_t r0 = 0; r0 < b.n; r0 += BM)
+      for (int64_t c0 = 0; c0 < b.m; c0 += BN)
+        L.tiles2.push_back(Tile{mi, static_cast<int>(r0), static_cast<int>(c0), 0});
+    const int64_t pt = ((b.M + kPrepTile - 1) / kPrepTile) * ((b.N + kPrepTile - 1) / kPrepTile);
+    L.prefix.push_back(L.prefix.back() + static_cast<int>(pt));
+    L.big.push_back(b);
+  }
+  size_t off = 0;
+  L.off_mats = off;
+  off = align_up(off + L.big.size() * sizeof(MatDesc), kAlign);
+  L.off_res = off;
+  off = align_up(off + L.res.size() * sizeof(ResDesc), 256);
+  L.off_t01 = off;
+  off = align_up(off + L.tiles01.size() * sizeof(Tile), 256);
+  L.off_t2 = off;
+  off = align_up(off + L.tiles2.size() * sizeof(Tile), 256);
+  L.off_prefix = off;
+  off = align_up(off + L.prefix.size() * sizeof(int), 256);
+  L.blob_end = off;
+  L.off_partials = off;
+  off = align_up(off + L.big.size() * kNormBlocks * sizeof(float), 256);
+  L.off_ext = off;
+  off = align_up(off + L.big.size() * 2 * sizeof(int), kAlign);
+  L.off_buffers = off;
+  for (BigMat &b : L.big) {
+    b.off_x = off;
+    off = align_up(off + static_cast<size_t>(b.m * b.pn) * L.elt, kAlign);
+    b.off_xt0 = off;
+    off = align_up(off + static_cast<size_t>(b.n * b.pm) * L.elt, kAlign);
+    b.off_xt1 = off;
+    off = align_up(off + static_cast<size_t>(b.n * b.pm) * L.elt, kAlign);
+    b.off_a = off;
+    off = align_up(off + static_cast<size_t>(b.m * b.pm) * L.elt, kAlign);
+    b.off_b = off;
+    off = align_up(off + static_cast<size_t>(b.m * b.pm) * L.elt, kAlign);
+  }
+  L.total = std::max<size_t>(off, 256);
+}
+
+int build_blob(const Layout &L, void *const *X, const int64_t *shapes, uint8_t *ws, std::vector<uint8_t> &blob) {
+  blob.assign(L.blob_end, 0);
+  if (L.dtype == NS_BF16 && !L.big.empty()) {
+    int rc = get_encode();
+    if (rc) return rc;
+  }
+  uint8_t *mats = blob.data() + L.off_mats;  // host bytes; copied, never dereferenced as MatDesc
+  for (size_t k = 0; k < L.big.size(); ++k) {
+    const BigMat &b = L.big[k];
+    MatDesc d;
+    std::memset(&d, 0, sizeof(d));
+    d.x = ws + b.off_x;
+    d.xt[0] = ws + b.off_xt0;
+    d.xt[1] = ws + b.off_xt1;
+    d.a = ws + b.off_a;
+    d.b = ws + b.off_b;
+    d.user = X[b.index];
+    d.M = static_cast<int>(b.M);
+    d.N = static_cast<int>(b.N);
+    d.m = static_cast<int>(b.m);
+    d.n = static_cast<int>(b.n);
+    d.pm = static_cast<int>(b.pm);
+    d.pn = static_cast<int>(b.pn);
+    d.transposed = b.transposed;
+    d.index = b.index;
+    if (L.dtype == NS_BF16) {
+      int rc = encode_bf16(&d.tm_x, d.x, b.m, b.n, b.pn);
+      rc = rc ? rc : encode_bf16(&d.tm_a, d.a, b.m, b.m, b.pm);
+      rc = rc ? rc : encode_bf16(&d.tm_b, d.b, b.m, b.m, b.pm);
+      rc = rc ? rc : encode_bf16(&d.tm_xt[0], d.xt[0], b.n, b.m, b.pm);
+      rc = rc ? rc : encode_bf16(&d.tm_xt[1], d.xt[1], b.n, b.m, b.pm);
+      if (rc) return rc;
+    }
+    std::memcpy(mats + k * sizeof(MatDesc), &d, sizeof(d));
+  }
+  uint8_t *res = blob.data() + L.off_res;
+  for (size_t k = 0; k < L.res.size(); ++k) {
+    const int i = L.res[k];
+    ResDesc r{};
+    r.user = X[i];
+    r.M = static_cast<int>(shapes[2 * i]);
+    r.N = static_cast<int>(shapes[2 * i + 1]);
+    r.transposed = r.M > r.N;
+    r.m = std::min(r.M, r.N);
+    r.n = std::max(r.M, r.N);
+    std::memcpy(res + k * sizeof(ResDesc), &r, sizeof(r));
+  }
+  if (!L.tiles01.empty())
+    std::memcpy(blob.data() + L.off_t01, L.tiles01.data(), L.tiles01.size() * sizeof(Tile));
+  if (!L.tiles2.empty()) std::memcpy(blob.data() + L.off_t2, L.tiles2.data(), L.tiles2.size() * sizeof(Tile));
+  std::memcpy(blob.data() + L.off_prefix, L.prefix.data(), L.prefix.size() * sizeof(int));
+  return NS_OK;
+}
+
+// ------------------------------------------------------------ workspace cache
+struct CachedWs {
+  uint8_t *ptr = nullptr;
+  size_t bytes = 0;
+  std::vector<uint8_t> last_blob;  // blob currently resident at ptr
+};
+std::map<std::pair<int, cudaStream_t>, CachedWs> g_ws;
+
+int ensure_ws(CachedWs &c, size_t bytes, cudaStream_t s) {
+  if (c.ptr && c.bytes >= bytes) return NS_OK;
+  if (c.ptr) {
+    if (cudaFreeAsync(c.ptr, s) != cudaSuccess) return NS_ECUDA;
+    c.ptr = nullptr;
+    c.bytes = 0;
+  }
+  c.last_blob.clear();
+  void *p = nullptr;
+  if (cudaMallocAsync(&p, bytes, s) != cudaSuccess) {
+    cudaGetLastError();
+    return NS_ENOMEM;
+  }
+  c.ptr = static_cast<uint8_t *>(p);
+  c.bytes = bytes;
+  return NS_OK;
+}
+
+// ------------------------------------------------------------ kernel timing
+constexpr int kKinds = 6;
+struct TimedLaunch {
+  int kind;
+  cudaEvent_t start, stop;
+};
+bool g_timing = false;
+std::vector<TimedLaunch> g_timed;
+
+// Launch `fn` bracketed by events when timing is on.
+template <typename F>
+int timed(int kind, cudaStream_t s, F &&fn) {
+  if (!g_timing) return fn();
+  TimedLaunch t{kind, nullptr, nullptr};
+  if (cudaEventCreate(&t.start) != cudaSuccess || cudaEventCreate(&t.stop) != cudaSuccess) return -1;
+  cudaEventRecord(t.start, s);
+  const int rc = fn();
+  cudaEventRecord(t.stop, s);
+  g_timed.push_back(t);
+  return rc;
+}
+
+// ------------------------------------------------------------ execution
+int execute(const Layout &L, uint8_t *ws, int steps, const float *co, float eps, DevInfo *di, cudaStream_t s) {
+  const MatDesc *mats = reinterpret_cast<const MatDesc *>(ws + L.off_mats);
+  if (!L.res.empty()) {
+    ResParams rp{};
+    rp.mats = reinterpret_cast<const ResDesc *>(ws + L.off_res);
+    rp.nmats = static_cast<int>(L.res.size());
+    rp.dtype = L.dtype;
+    rp.steps = steps;
+    rp.ca = co[0];
+    rp.cb = co[1];
+    rp.cc = co[2];
+    rp.eps = eps;
+    if (timed(5, s, [&] { return launch_resident(rp, L.res_maxm, L.res_smem, s); })) return NS_ECUDA;
+  }
+  if (L.big.empty()) return NS_OK;
+  const int nbig = static_cast<int>(L.big.size());
+  int *ext = reinterpret_cast<int *>(ws + L.off_ext);
+  if (cudaMemsetAsync(ext, 0, nbig * 2 * sizeof(int), s) != cudaSuccess) return NS_ECUDA;
+  PrepParams pp{};
+  pp.mats = mats;
+  pp.nmats = nbig;
+  pp.partials = reinterpret_cast<float *>(ws + L.off_partials);
+  pp.ext = ext;
+  pp.tile_prefix = reinterpret_cast<const int *>(ws + L.off_prefix);
+  pp.eps = eps;
+  pp.dtype = L.dtype;
+  pp.to_user = steps == 0;
+  if (timed(0, s, [&] { return launch_norm(pp, s); })) return NS_ECUDA;
+  if (timed(1, s, [&] { return launch_prep(pp, L.prefix.back(), s); })) return NS_ECUDA;
+  PhaseParams ph{};
+  ph.mats = mats;
+  ph.ext = ext;
+  ph.status = di->status;
+  ph.ca = co[0];
+  ph.cb = co[1];
+  ph.cc = co[2];
+  const Tile *t01 = reinterpret_cast<const Tile *>(ws + L.off_t01);
+  const Tile *t2 = reinterpret_cast<const Tile *>(ws + L.off_t2);
+  for (int step = 0; step < steps; ++step) {
+    ph.step = step;
+    ph.final_step = step == steps - 1;
+    for (int phase = 0; phase < 3; ++phase) {
+      ph.tiles = phase < 2 ? t01 : t2;
+      ph.ntiles = static_cast<int>(phase < 2 ? L.tiles01.size() : L.tiles2.size());
+      int rc = timed(2 + phase, s, [&] {
+        return L.dtype == NS_BF16 ? launch_tc_phase(phase, ph, di->sms, s) : launch_simt_phase(phase, ph, s);
+      });
+      if (rc) return NS_ECUDA;
+    }
+  }
+  return NS_OK;
+}
+
+int run(void *const *X, const int64_t *shapes, int count, int steps, const float *coeffs, float eps, int dtype,
+        void *user_ws, size_t user_ws_bytes, cudaStream_t s) {
+  int rc = validate(X, shapes, count, steps, dtype, true);
+  if (rc) return rc;
+  if (!(eps >= 0.f)) return NS_EINVAL;
+  if (count == 0) return NS_OK;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DevInfo *di = nullptr;
+  rc = device_info(&di);
+  if (rc) return rc;
+  Layout L;
+  build_layout(shapes, count, dtype, L);
+  if (L.big.empty() && L.res.empty()) return NS_OK;
+  const float *co = coeffs ? coeffs : kDefaultCoeffs;
+
+  uint8_t *ws = nullptr;
+  std::vector<uint8_t> blob;
+  CachedWs *cache = nullptr;
+  if (user_ws) {
+    if (user_ws_bytes < L.total) return NS_ENOMEM;
+    if (reinterpret_cast<uintptr_t>(user_ws) % 256) return NS_EALIGN;
+    ws = static_cast<uint8_t *>(user_ws);
+  } else {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cache = &g_ws[{dev, s}];
+    rc = ensure_ws(*cache, L.total, s);
+    if (rc) return rc;
+    ws = cache->ptr;
+  }
+  rc = build_blob(L, X, shapes, ws, blob);
+  if (rc) return rc;
+  if (!cache || cache->last_blob != blob) {
+    if (cudaMemcpyAsync(ws, blob.data(), blob.size(), cudaMemcpyHostToDevice, s) != cudaSuccess) return NS_ECUDA;
+    if (cache) cache->last_blob = blob;
+  }
+  return execute(L, ws, steps, co, eps, di, s);
+}
+
+}  // namespace
+}  // namespace ns
+
+using namespace ns;
+
+extern "C" {
+
+int64_t ns_cost(int64_t M, int64_t N) {
+  if (M < 0 || N < 0) return -1;
+  const int64_t hi = M > N ? M : N, lo = M > N ? N : M;
+  return hi * lo * lo;
+}
+
+int ns_orthogonalize_batched(void *const *X, const int64_t *shapes, int count, int steps, const float *coeffs,
+                             int dtype, void *stream) {
+  return run(X, shapes, count, steps, coeffs, 1e-7f, dtype, nullptr, 0, static_cast<cudaStream_t>(stream));
+}
+
+int ns_orthogonalize_batched_ex(void *const *X, const int64_t *shapes, int count, int steps, const float *coeffs,
+                                float eps, int dtype, void *workspace, size_t workspace_bytes, void *stream) {
+  if (!workspace && count > 0) return NS_EINVAL;
+  return run(X, shapes, count, steps, coeffs, eps, dtype, workspace, workspace_bytes,
+             static_cast<cudaStream_t>(stream));
+}
+
+size_t ns_workspace_bytes(const int64_t *shapes, int count, int dtype) {
+  if (validate(nullptr, shapes, count, 0, dtype, false)) return 0;
+  Layout L;
+  build_layout(shapes, count, dtype, L);
+  return L.total;
+}
+
+int ns_orthogonalize_batched_host(void *const *X_host, const int64_t *shapes, int count, int steps,
+                                  const float *coeffs, int dtype, void *stream) {
+  int rc = validate(X_host, shapes, count, steps, dtype, true);
+  if (rc) return rc;
+  if (count == 0) return NS_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t elt = dtype == NS_BF16 ? 2 : 4;
+  std::vector<size_t> off(count);
+  size_t total = 0;
+  for (int i = 0; i < count; ++i) {
+    off[i] = total;
+    total = align_up(total + static_cast<size_t>(shapes[2 * i] * shapes[2 * i + 1]) * elt, 256);
+  }
+  uint8_t *dbuf = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    DevInfo *di = nullptr;
+    rc = device_info(&di);
+    if (rc) return rc;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    // staging buffers are keyed apart from the compute workspace of this stream
+    CachedWs &c = g_ws[{dev + (1 << 20), s}];
+    rc = ensure_ws(c, std::max<size_t>(total, 256), s);
+    if (rc) return rc;
+    dbuf = c.ptr;
+  }
+  std::vector<void *> dptr(count);
+  for (int i = 0; i < count; ++i) {
+    const size_t bytes = static_cast<size_t>(shapes[2 * i] * shapes[2 * i + 1]) * elt;
+    dptr[i] = dbuf + off[i];
+    if (bytes && cudaMemcpyAsync(dptr[i], X_host[i], bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return NS_ECUDA;
+  }
+  rc = run(dptr.data(), shapes, count, steps, coeffs, 1e-7f, dtype, nullptr, 0, s);
+  if (rc) return rc;
+  for (int i = 0; i < count; ++i) {
+    const size_t bytes = static_cast<size_t>(shapes[2 * i] * shapes[2 * i + 1]) * elt;
+    if (bytes && cudaMemcpyAsync(X_host[i], dptr[i], bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+      return NS_ECUDA;
+  }
+  return cudaStreamSynchronize(s) == cudaSuccess ? NS_OK : NS_ECUDA;
+}
+
+int ns_get_status(void *stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return NS_ECUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(int)) != cudaSuccess) return NS_ECUDA;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int)) != cudaSuccess) return NS_ECUDA;
+  return v == 0 ? NS_OK : NS_ETIMEOUT;
+}
+
+const char *ns_strerror(int code) {
+  switch (code) {
+    case NS_OK: return "success";
+    case NS_EINVAL: return "invalid argument";
+    case NS_EALIGN: return "matrix pointer not aligned to its element size";
+    case NS_ENOMEM: return "workspace allocation failed or caller workspace too small";
+    case NS_ECUDA: return "CUDA runtime or driver error";
+    case NS_ETIMEOUT: return "a bounded device-side wait gave up";
+    case NS_ENODEV: return "no sm_100-family device is current";
+    default: return "unknown status";
+  }
+}
+
+int ns_release_workspace(void) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return NS_ECUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return NS_ECUDA;
+  for (auto it = g_ws.begin(); it != g_ws.end();) {
+    const int key_dev = it->first.first & ((1 << 20) - 1);
+    if (key_dev == dev) {
+      if (it->second.ptr) cudaFree(it->second.ptr);
+      it = g_ws.erase(it);
+    } else {
+      ++it;
+    }
+  }
+  return NS_OK;
+}
+
+int64_t ns_num_kernel_launches(void) { return g_launches.load(); }
+
+static void drop_timed() {
+  for (auto &t : g_timed) {
+    cudaEventDestroy(t.start);
+    cudaEventDestroy(t.stop);
+  }
+  g_timed.clear();
+}
+
+int ns_set_kernel_timing(int enable) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  drop_timed();
+  g_timing = enable != 0;
+  return NS_OK;
+}
+
+int ns_get_kernel_times(double *ms, int64_t *launches, int n) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (n < 0 || n > kKinds || (n > 0 && (!ms || !launches))) return NS_EINVAL;
+  double acc[kKinds] = {};
+  int64_t cnt[kKinds] = {};
+  for (auto &t : g_timed) {
+    if (cudaEventSynchronize(t.stop) != cudaSuccess) return NS_ECUDA;
+    float e = 0.f;
+    if (cudaEventElapsedTime(&e, t.start, t.stop) != cudaSuccess) return NS_ECUDA;
+    acc[t.kind] += e;
+    cnt[t.kind] += 1;
+  }
+  for (int k = 0; k < n; ++k) {
+    ms[k] = acc[k];
+    launches[k] = cnt[k];
+  }
+  return NS_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,423 @@
+// ns_simt.cu -- CUDA-core kernels of libns:
+//   * per-matrix Frobenius norm (partial sums) and non-zero extent,
+//   * preparation: normalise by ||Y||_F + eps, round to the working type and
+//     write both orientations W and W^T,
+//   * the shared-memory resident kernel that runs every step of a small
+//     matrix inside one CTA,
+//   * the fp32 tiled GEMM phases (gram / square / apply) for large fp32
+//     matrices.
+// The bf16 tensor-core phases live in ns_tc.cu.
+#include <cuda_runtime.h>
+
+#include "ns_device.cuh"
+
+namespace ns {
+
+// ============================================================== norm + extent
+// Grid kNormBlocks * nmats. Block b of matrix i visits rows b, b+kNormBlocks,
+// ... in a fixed order, so the partial sums are the same on every run. It also
+// records the largest row and column index that holds a non-zero, in the
+// caller's orientation; zero rows/columns beyond them stay zero through every
+// step (the first page's "Fix" section) and are skipped by the GEMM phases.
+template <int DT>
+__global__ void __launch_bounds__(256) ns_norm_kernel(PrepParams p) {
+  using T = typename Elem<DT>::T;
+  const int mat = blockIdx.x / kNormBlocks;
+  const int blk = blockIdx.x % kNormBlocks;
+  const MatDesc &d = p.mats[mat];
+  const T *y = static_cast<const T *>(d.user);
+  const int M = d.M, N = d.N;
+  constexpr int VEC = 16 / sizeof(T);
+  const bool vec = (N % VEC == 0) && ((reinterpret_cast<uintptr_t>(y) & 15) == 0);
+
+  float acc = 0.f;
+  int rmax = -1, cmax = -1;
+  for (int r = blk; r < M; r += kNormBlocks) {
+    const T *row = y + static_cast<size_t>(r) * N;
+    bool any = false;
+    if (vec) {
+      const uint4 *row4 = reinterpret_cast<const uint4 *>(row);
+      for (int c4 = threadIdx.x; c4 < N / VEC; c4 += blockDim.x) {
+        uint4 raw = __ldg(row4 + c4);
+        const T *e = reinterpret_cast<const T *>(&raw);
+#pragma unroll
+        for (int u = 0; u < VEC; ++u) {
+          const float v = Elem<DT>::to_f(e[u]);
+          acc = fmaf(v, v, acc);
+          if (v != 0.f) {
+            any = true;
+            cmax = max(cmax, c4 * VEC + u);
+          }
+        }
+      }
+    } else {
+      for (int c = threadIdx.x; c < N; c += blockDim.x) {
+        const float v = Elem<DT>::load(row + c);
+        acc = fmaf(v, v, acc);
+        if (v != 0.f) {
+          any = true;
+          cmax = max(cmax, c);
+        }
+      }
+    }
+    if (any) rmax = r;
+  }
+
+  __shared__ float s_sum[8];
+  __shared__ int s_r[8], s_c[8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  acc = warp_sum(acc);
+  rmax = warp_max(rmax);
+  cmax = warp_max(cmax);
+  if (lane == 0) {
+    s_sum[warp] = acc;
+    s_r[warp] = rmax;
+    s_c[warp] = cmax;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    int rr = -1, cc = -1;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+      t += s_sum[w];
+      rr = max(rr, s_r[w]);
+      cc = max(cc, s_c[w]);
+    }
+    p.partials[mat * kNormBlocks + blk] = t;
+    if (rr >= 0) atomicMax(&p.ext[2 * mat + 0], rr + 1);
+    if (cc >= 0) atomicMax(&p.ext[2 * mat + 1], cc + 1);
+  }
+}
+
+int launch_norm(const PrepParams &p, cudaStream_t s) {
+  if (p.nmats <= 0) return 0;
+  const unsigned grid = static_cast<unsigned>(kNormBlocks) * static_cast<unsigned>(p.nmats);
+  if (p.dtype == kBF16)
+    ns_norm_kernel<kBF16><<<grid, 256, 0, s>>>(p);
+  else
+    ns_norm_kernel<kF32><<<grid, 256, 0, s>>>(p);
+  count_launch();
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+// ============================================================== preparation
+// One block per 64x64 tile of the caller's Y. Every block sums the
+// matrix's kNormBlocks partials in the same fixed order, so all blocks agree
+// on s = ||Y||_F. It writes y / (s + eps), rounded to the working type, into
+// W and W^T (or back into Y when no step follows).
+template <int DT>
+__global__ void __launch_bounds__(256) ns_prep_kernel(PrepParams p) {
+  using T = typename Elem<DT>::T;
+  const int bid = blockIdx.x;
+  int lo = 0, hi = p.nmats;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (p.tile_prefix[mid] <= bid) lo = mid; else hi = mid;
+  }
+  const int mat = lo;
+  const MatDesc &d = p.mats[mat];
+  const int M = d.M, N = d.N;
+  const int local = bid - p.tile_prefix[mat];
+  const int tcols = (N + kPrepTile - 1) / kPrepTile;
+  const int r0 = (local / tcols) * kPrepTile, c0 = (local % tcols) * kPrepTile;
+
+  __shared__ float s_denom;
+  __shared__ float tile[kPrepTile][kPrepTile + 1];
+  const int tid = threadIdx.x;
+  if (tid < 32) {
+    float v = 0.f;
+    for (int i = tid; i < kNormBlocks; i += 32) v += p.partials[mat * kNormBlocks + i];
+    v = warp_sum(v);
+    if (tid == 0) s_denom = sqrtf(v) + p.eps;
+  }
+  const T *y = static_cast<const T *>(d.user);
+  __syncthreads();
+  const float denom = s_denom;
+  for (int e = tid; e < kPrepTile * kPrepTile; e += 256) {
+    const int rr = e / kPrepTile, cc = e % kPrepTile;
+    const int r = r0 + rr, c = c0 + cc;
+    float v = 0.f;
+    if (r < M && c < N) v = __fdiv_rn(Elem<DT>::load(y + static_cast<size_t>(r) * N + c), denom);
+    tile[rr][cc] = v;
+  }
+  __syncthreads();
+
+  if (p.to_user) {
+    T *u = static_cast<T *>(d.user);
+    for (int e = tid; e < kPrepTile * kPrepTile; e += 256) {
+      const int rr = e / kPrepTile, cc = e % kPrepTile;
+      const int r = r0 + rr, c = c0 + cc;
+      if (r < M && c < N) u[static_cast<size_t>(r) * N + c] = Elem<DT>::from_f(tile[rr][cc]);
+    }
+    return;
+  }
+  // same orientation as Y: W when not transposed, W^T when transposed
+  T *same = static_cast<T *>(d.transposed ? d.xt[0] : d.x);
+  const int same_pitch = d.transposed ? d.pm : d.pn;
+  // transposed orientation: W^T when not transposed, W when transposed
+  T *flip = static_cast<T *>(d.transposed ? d.x : d.xt[0]);
+  const int flip_pitch = d.transposed ? d.pn : d.pm;
+  for (int e = tid; e < kPrepTile * kPrepTile; e += 256) {
+    const int rr = e / kPrepTile, cc = e % kPrepTile;
+    const int r = r0 + rr, c = c0 + cc;
+    if (r < M && c < N) same[static_cast<size_t>(r) * same_pitch + c] = Elem<DT>::from_f(tile[rr][cc]);
+  }
+  for (int e = tid; e < kPrepTile * kPrepTile; e += 256) {
+    const int q = e / kPrepTile, pp = e % kPrepTile;  // output row c0+q, column r0+pp
+    const int r = r0 + pp, c = c0 + q;
+    if (r < M && c < N) flip[static_cast<size_t>(c) * flip_pitch + r] = Elem<DT>::from_f(tile[pp][q]);
+  }
+}
+
+int launch_prep(const PrepParams &p, int total_tiles, cudaStream_t s) {
+  if (total_tiles <= 0) return 0;
+  if (p.dtype == kBF16)
+    ns_prep_kernel<kBF16><<<total_tiles, 256, 0, s>>>(p);
+  else
+    ns_prep_kernel<kF32><<<total_tiles, 256, 0, s>>>(p);
+  count_launch();
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+// ============================================================== resident
+// One CTA runs the whole method for one small matrix (m <= MAXM) held in
+// shared memory: W (m x n, working type), A and B (m x m, fp32). Loads Y
+// once, writes the result once. Sums are fixed-order, so results repeat
+// bit for bit.
+int resident_smem_bytes(int m, int n, int dtype) {
+  const size_t elt = dtype == kBF16 ? 2 : 4;
+  size_t x = (static_cast<size_t>(m) * n * elt + 15) & ~static_cast<size_t>(15);
+  size_t t = x + 2 * static_cast<size_t>(m) * m * 4;
+  return t > (1u << 30) ? (1 << 30) : static_cast<int>(t);
+}
+
+template <int DT, int MAXM>
+__global__ void __launch_bounds__(256, 1) ns_resident_kernel(ResParams p) {
+  using T = typename Elem<DT>::T;
+  extern __shared__ __align__(16) uint8_t smem[];
+  const ResDesc d = p.mats[blockIdx.x];
+  const int M = d.M, N = d.N, m = d.m, n = d.n, tr = d.transposed;
+  T *xs = reinterpret_cast<T *>(smem);
+  float *as = reinterpret_cast<float *>(smem + ((static_cast<size_t>(m) * n * sizeof(T) + 15) & ~size_t(15)));
+  float *bs = as + m * m;
+  T *y = static_cast<T *>(d.user);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  constexpr int NW = 8;
+
+  __shared__ float s_sum[NW];
+  __shared__ int s_r[NW], s_c[NW];
+  __shared__ float s_denom;
+  __shared__ int s_meff, s_neff;
+
+  // 1. load (orienting to W) + sum of squares + non-zero extent
+  float acc = 0.f;
+  int rmax = -1, cmax = -1;
+  const int total = M * N;
+  for (int e = tid; e < total; e += 256) {
+    const int r = e / N, c = e - r * N;
+    const T v = y[e];
+    const float f = Elem<DT>::to_f(v);
+    acc = fmaf(f, f, acc);
+    if (f != 0.f) {
+      rmax = max(rmax, r);
+      cmax = max(cmax, c);
+    }
+    if (tr) xs[c * n + r] = v; else xs[r * n + c] = v;
+  }
+  acc = warp_sum(acc);
+  rmax = warp_max(rmax);
+  cmax = warp_max(cmax);
+  if (lane == 0) {
+    s_sum[warp] = acc;
+    s_r[warp] = rmax;
+    s_c[warp] = cmax;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float t = 0.f;
+    int rr = -1, cc = -1;
+    for (int w = 0; w < NW; ++w) {
+      t += s_sum[w];
+      rr = max(rr, s_r[w]);
+      cc = max(cc, s_c[w]);
+    }
+    s_denom = sqrtf(t) + p.eps;
+    s_meff = tr ? cc + 1 : rr + 1;
+    s_neff = tr ? rr + 1 : cc + 1;
+  }
+  __syncthreads();
+  const float denom = s_denom;
+  const int meff = s_meff, neff = s_neff;
+
+  // 2. normalise
+  for (int e = tid; e < m * n; e += 256) xs[e] = Elem<DT>::from_f(__fdiv_rn(Elem<DT>::to_f(xs[e]), denom));
+  __syncthreads();
+
+  // 3. iterate on the non-zero block [0, meff) x [0, neff)
+  for (int step = 0; step < p.steps; ++step) {
+    // A = W W^T (upper triangle, mirrored); one warp per entry
+    for (int q = warp; q < meff * meff; q += NW) {
+      const int i = q / meff, j = q - i * meff;
+      if (j < i) continue;
+      float s = 0.f;
+      for (int k = lane; k < neff; k += 32)
+        s = fmaf(Elem<DT>::to_f(xs[i * n + k]), Elem<DT>::to_f(xs[j * n + k]), s);
+      s = warp_sum(s);
+      if (lane == 0) {
+        as[i * m + j] = s;
+        as[j * m + i] = s;
+      }
+    }
+    __syncthreads();
+    // B = b A + c A A (upper triangle, mirrored)
+    for (int q = tid; q < meff * meff; q += 256) {
+      const int i = q / meff, j = q - i * meff;
+      if (j < i) continue;
+      float s = 0.f;
+      for (int k = 0; k < meff; ++k) s = fmaf(as[i * m + k], as[k * m + j], s);
+      const float v = p.cb * as[i * m + j] + p.cc * s;
+      bs[i * m + j] = v;
+      bs[j * m + i] = v;
+    }
+    __syncthreads();
+    // W = a W + B W, column by column (a column depends only on itself)
+    for (int j = tid; j < neff; j += 256) {
+      float col[MAXM];
+#pragma unroll
+      for (int k = 0; k < MAXM; ++k) col[k] = (k < meff) ? Elem<DT>::to_f(xs[k * n + j]) : 0.f;
+      for (int i = 0; i < meff; ++i) {
+        float s = 0.f;
+#pragma unroll
+        for (int k = 0; k < MAXM; ++k)
+          if (k < meff) s = fmaf(bs[i * m + k], col[k], s);
+        const float xi = Elem<DT>::to_f(xs[i * n + j]);
+        xs[i * n + j] = Elem<DT>::from_f(p.ca * xi + s);
+      }
+    }
+    __syncthreads();
+  }
+
+  // 4. write back in the caller's orientation
+  for (int e = tid; e < total; e += 256) {
+    const int r = e / N, c = e - r * N;
+    y[e] = tr ? xs[c * n + r] : xs[r * n + c];
+  }
+}
+
+template <int DT, int MAXM>
+static int launch_resident_t(const ResParams &p, int smem, cudaStream_t s) {
+  auto k = ns_resident_kernel<DT, MAXM>;
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -1;
+  k<<<p.nmats, 256, smem, s>>>(p);
+  count_launch();
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+int launch_resident(const ResParams &p, int maxm, int smem, cudaStream_t s) {
+  if (p.nmats <= 0) return 0;
+  if (p.dtype == kBF16) {
+    if (maxm <= 16) return launch_resident_t<kBF16, 16>(p, smem, s);
+    if (maxm <= 32) return launch_resident_t<kBF16, 32>(p, smem, s);
+    return launch_resident_t<kBF16, 64>(p, smem, s);
+  }
+  if (maxm <= 16) return launch_resident_t<kF32, 16>(p, smem, s);
+  if (maxm <= 32) return launch_resident_t<kF32, 32>(p, smem, s);
+  return launch_resident_t<kF32, 64>(p, smem, s);
+}
+
+// ============================================================== fp32 GEMM phases
+// One 64x64 output tile per block, 256 threads with 4x4 outputs each,
+// C[r, c] = sum_k P[r, k] Q[c, k] over k < K (both operands K-contiguous).
+//   phase 0 (gram)   P = Q = W           K = n   -> A (upper + mirror)
+//   phase 1 (square) P = Q = A           K = m   -> B = b A + c C (upper + mirror)
+//   phase 2 (apply)  P = W^T, Q = B      K = m   -> W' = a W + (B W): W'^T and W,
+//                                                   or the caller's Y on the last step
+template <int PHASE>
+__global__ void __launch_bounds__(256) ns_simt_gemm_kernel(PhaseParams p) {
+  const Tile tl = p.tiles[blockIdx.x];
+  const MatDesc &d = p.mats[tl.mat];
+  const int e0 = p.ext[2 * tl.mat], e1 = p.ext[2 * tl.mat + 1];
+  const int meff = d.transposed ? e1 : e0, neff = d.transposed ? e0 : e1;
+  const int m = d.m, n = d.n, pm = d.pm, pn = d.pn;
+  const int rows_eff = PHASE == 2 ? neff : meff;
+  if (tl.row0 >= rows_eff || tl.col0 >= meff) return;
+  const int K = PHASE == 0 ? neff : meff;
+  const int rows = PHASE == 2 ? n : m;
+  const int cols = m;
+  const int cur = p.step & 1;
+  const float *P = static_cast<const float *>(PHASE == 0 ? d.x : PHASE == 1 ? d.a : d.xt[cur]);
+  const float *Q = static_cast<const float *>(PHASE == 0 ? d.x : PHASE == 1 ? d.a : d.b);
+  const int pitch_p = PHASE == 0 ? pn : pm;
+  const int pitch_q = PHASE == 0 ? pn : pm;
+
+  __shared__ float Ps[16][kSimtBM + 4];
+  __shared__ float Qs[16][kSimtBN + 4];
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < K; k0 += 16) {
+    for (int e = tid; e < kSimtBM * 16; e += 256) {
+      const int rr = e >> 4, kk = e & 15;
+      const int r = tl.row0 + rr, k = k0 + kk;
+      Ps[kk][rr] = (r < rows && k < K) ? P[static_cast<size_t>(r) * pitch_p + k] : 0.f;
+      const int c = tl.col0 + rr;
+      Qs[kk][rr] = (c < cols && k < K) ? Q[static_cast<size_t>(c) * pitch_q + k] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        a[u] = Ps[kk][ty * 4 + u];
+        b[u] = Qs[kk][tx * 4 + u];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int v = 0; v < 4; ++v) acc[u][v] = fmaf(a[u], b[v], acc[u][v]);
+    }
+    __syncthreads();
+  }
+
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const int r = tl.row0 + ty * 4 + u, c = tl.col0 + tx * 4 + v;
+      const float val = acc[u][v];
+      if (PHASE == 0 || PHASE == 1) {
+        if (r < m && c < m && r <= c) {
+          float out = val;
+          float *dst = static_cast<float *>(PHASE == 0 ? d.a : d.b);
+          if (PHASE == 1) out = p.cb * static_cast<const float *>(d.a)[static_cast<size_t>(r) * pm + c] + p.cc * val;
+          dst[static_cast<size_t>(r) * pm + c] = out;
+          dst[static_cast<size_t>(c) * pm + r] = out;
+        }
+      } else {
+        if (r < n && c < m) {
+          const float *xt = static_cast<const float *>(d.xt[cur]);
+          const float out = p.ca * xt[static_cast<size_t>(r) * pm + c] + val;
+          if (!p.final_step) {
+            static_cast<float *>(d.xt[cur ^ 1])[static_cast<size_t>(r) * pm + c] = out;
+            static_cast<float *>(d.x)[static_cast<size_t>(c) * pn + r] = out;
+          } else {
+            float *u = static_cast<float *>(d.user);
+            if (d.transposed) u[static_cast<size_t>(r) * d.N + c] = out;
+            else u[static_cast<size_t>(c) * d.N + r] = out;
+          }
+        }
+      }
+    }
+  }
+}
+
+int launch_simt_phase(int phase, const PhaseParams &p, cudaStream_t s) {
+  if (p.ntiles <= 0) return 0;
+  if (phase == 0) ns_simt_gemm_kernel<0><<<p.ntiles, 256, 0, s>>>(p);
+  else if (phase == 1) ns_simt_gemm_kernel<1><<<p.ntiles, 256, 0, s>>>(p);
+  else ns_simt_gemm_kernel<2><<<p.ntiles, 256, 0, s>>>(p);
+  count_launch();
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace ns

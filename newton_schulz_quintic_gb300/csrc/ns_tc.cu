@@ -1,0 +1,385 @@
+// ns_tc.cu -- bf16 tensor-core GEMM phases of libns on sm_103a (tcgen05).
+//
+// One persistent, warp-specialised kernel per phase, over a cost-ordered
+// list of 128 x 256 output tiles drawn from every matrix of the batch:
+//   warp 0      TMA producer: 128x64 tile of the first operand and 256x64 of
+//               the second per k-block into a 4-stage shared-memory ring
+//               (128-byte swizzle), mbarrier full/empty handshake;
+//   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators)
+//               and, from one thread, issues tcgen05.mma (M=128, N=256,
+//               K=16, bf16 in, fp32 accumulate) and tcgen05.commit;
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator, the fused
+//               element-wise step in fp32, round-to-nearest-even to bf16 and
+//               the stores; the second accumulator lets the next tile's
+//               main loop overlap this epilogue.
+// Phases (all operands K-major, see ns_internal.h for the layout):
+//   0 gram    A = W W^T             upper-triangle tiles; stores tile + mirror
+//   1 square  B = b A + c (A A)     upper-triangle tiles; stores tile + mirror
+//   2 apply   W' = a W + B W        computed as (B W)^T tiles over W^T; stores
+//                                   W'^T and W' (or the caller's Y on the last step)
+// Tiles wholly outside a matrix's non-zero extent are skipped, and k-loops
+// stop at the extent: zero rows and columns stay zero through every step.
+// Every wait is bounded (see mbar_wait); a timeout sets the status word and
+// the CTA drains its in-flight copies and MMAs, frees TMEM and exits.
+#include <cuda_runtime.h>
+
+#include "ns_device.cuh"
+
+namespace ns {
+
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kABytes = kTcBM * kTcBK * 2;  // 16 KB
+constexpr int kBBytes = kTcBN * kTcBK * 2;  // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kTmemCols = 2 * kTcBN;        // two accumulators
+constexpr int kThreads = 192;
+constexpr int kEpiThreads = 128;
+
+struct Barriers {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+struct TileInfo {
+  const MatDesc *d;
+  int row0, col0;
+  int nk;
+  bool skip;
+};
+
+template <int PHASE>
+__device__ __forceinline__ TileInfo tile_info(const PhaseParams &p, int t) {
+  const Tile tl = p.tiles[t];
+  TileInfo ti;
+  ti.d = p.mats + tl.mat;
+  ti.row0 = tl.row0;
+  ti.col0 = tl.col0;
+  const int e0 = p.ext[2 * tl.mat], e1 = p.ext[2 * tl.mat + 1];
+  const int tr = ti.d->transposed;
+  const int meff = tr ? e1 : e0, neff = tr ? e0 : e1;
+  const int rows_eff = PHASE == 2 ? neff : meff;
+  const int k_eff = PHASE == 0 ? neff : meff;
+  ti.skip = (tl.row0 >= rows_eff) || (tl.col0 >= meff);
+  ti.nk = (k_eff + kTcBK - 1) / kTcBK;
+  return ti;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+__device__ __forceinline__ void store_row32(__nv_bfloat16 *dst, const float (&v)[32]) {
+  uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 w;
+    w.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+    w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+    w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+    w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+    d4[q] = w;
+  }
+}
+
+__device__ __forceinline__ void load_row32(const __nv_bfloat16 *src, float (&v)[32]) {
+  const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 w = s4[q];
+    const __nv_bfloat16 *e = reinterpret_cast<const __nv_bfloat16 *>(&w);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[8 * q + u] = __bfloat162float(e[u]);
+  }
+}
+
+// Epilogue of one 32-column chunk held by one thread: tile row r, columns
+// chunk*32 .. chunk*32+31 of the tile.
+template <int PHASE>
+__device__ __forceinline__ void epilogue_chunk(const PhaseParams &p, const TileInfo &ti, int r, int chunk,
+                                               const uint32_t (&raw)[32]) {
+  const MatDesc &d = *ti.d;
+  float f[32];
+#pragma unroll
+  for (int t = 0; t < 32; ++t) f[t] = __uint_as_float(raw[t]);
+
+  if (PHASE == 0 || PHASE == 1) {
+    const int m = d.m, pm = d.pm;
+    const int i = ti.row0 + r;
+    const int jb = ti.col0 + chunk * 32;
+    if (i >= m || jb + 31 < i) return;
+    const bool full = (jb >= i) && (jb + 32 <= m);
+    if (PHASE == 1) {
+      const __nv_bfloat16 *A = static_cast<const __nv_bfloat16 *>(d.a) + static_cast<size_t>(i) * pm + jb;
+      float aold[32];
+      if (full) {
+        load_row32(A, aold);
+      } else {
+#pragma unroll
+        for (int t = 0; t < 32; ++t) {
+          const int j = jb + t;
+          aold[t] = (j >= i && j < m) ? __bfloat162float(A[t]) : 0.f;
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < 32; ++t) f[t] = p.cb * aold[t] + p.cc * f[t];
+    }
+    __nv_bfloat16 *O = static_cast<__nv_bfloat16 *>(PHASE == 0 ? d.a : d.b);
+    if (full) {
+      store_row32(O + static_cast<size_t>(i) * pm + jb, f);
+    } else {
+#pragma unroll
+      for (int t = 0; t < 32; ++t) {
+        const int j = jb + t;
+        if (j >= i && j < m) O[static_cast<size_t>(i) * pm + j] = __float2bfloat16_rn(f[t]);
+      }
+    }
+    // mirror: O[j, i] for j > i (consecutive lanes hold consecutive i)
+#pragma unroll
+    for (int t = 0; t < 32; ++t) {
+      const int j = jb + t;
+      if (j > i && j < m) O[static_cast<size_t>(j) * pm + i] = __float2bfloat16_rn(f[t]);
+    }
+  } else {
+    const int m = d.m, n = d.n, pm = d.pm, pn = d.pn;
+    const int jr = ti.row0 + r;          // row of W^T (index over n)
+    const int ib = ti.col0 + chunk * 32; // column of W^T (index over m)
+    if (jr >= n || ib >= m) return;
+    const int cur = p.step & 1;
+    const bool full = ib + 32 <= m;
+    const __nv_bfloat16 *XT = static_cast<const __nv_bfloat16 *>(d.xt[cur]) + static_cast<size_t>(jr) * pm + ib;
+    float xo[32];
+    if (full) {
+      load_row32(XT, xo);
+    } else {
+#pragma unroll
+      for (int t = 0; t < 32; ++t) xo[t] = (ib + t < m) ? __bfloat162float(XT[t]) : 0.f;
+    }
+#pragma unroll
+    for (int t = 0; t < 32; ++t) f[t] = p.ca * xo[t] + f[t];
+
+    if (!p.final_step) {
+      __nv_bfloat16 *XTn = static_cast<__nv_bfloat16 *>(d.xt[cur ^ 1]) + static_cast<size_t>(jr) * pm + ib;
+      if (full) {
+        store_row32(XTn, f);
+      } else {
+#pragma unroll
+        for (int t = 0; t < 32; ++t)
+          if (ib + t < m) XTn[t] = __float2bfloat16_rn(f[t]);
+      }
+      __nv_bfloat16 *X = static_cast<__nv_bfloat16 *>(d.x);
+#pragma unroll
+      for (int t = 0; t < 32; ++t)
+        if (ib + t < m) X[static_cast<size_t>(ib + t) * pn + jr] = __float2bfloat16_rn(f[t]);
+    } else {
+      __nv_bfloat16 *U = static_cast<__nv_bfloat16 *>(d.user);
+      if (d.transposed) {
+        // caller's Y is n x m: row jr, columns ib..ib+31
+        __nv_bfloat16 *dst = U + static_cast<size_t>(jr) * d.N + ib;
+        if (full && ((reinterpret_cast<uintptr_t>(dst) & 15) == 0)) {
+          store_row32(dst, f);
+        } else {
+#pragma unroll
+          for (int t = 0; t < 32; ++t)
+            if (ib + t < m) dst[t] = __float2bfloat16_rn(f[t]);
+        }
+      } else {
+        // caller's Y is m x n: column jr of rows ib..ib+31
+#pragma unroll
+        for (int t = 0; t < 32; ++t)
+          if (ib + t < m) U[static_cast<size_t>(ib + t) * d.N + jr] = __float2bfloat16_rn(f[t]);
+      }
+    }
+  }
+}
+
+// Bounded wait that ignores the abort flag: used only to drain in-flight
+// asynchronous work before the CTA releases its shared memory and TMEM.
+__device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity, int *status) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      set_status(status, kStatusTimeout);
+      return;
+    }
+  }
+}
+
+template <int PHASE>
+__global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_constant__ PhaseParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *sA = smem;
+  uint8_t *sB = smem + kStages * kABytes;
+  Barriers *bar = reinterpret_cast<Barriers *>(smem + kStages * kStageBytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bar->full[s], 1);
+      mbar_init(&bar->empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&bar->tfull[a], 1);
+      mbar_init(&bar->tempty[a], kEpiThreads);
+    }
+    mbar_init(&bar->drain, 1);
+    bar->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bar->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bar->tmem_base;
+  volatile int *abort = &bar->abort;
+  const int cur = p.step & 1;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------- TMA producer
+      const uint64_t pol = l2_policy_evict_normal();
+      int issued_phase[kStages];
+      for (int s = 0; s < kStages; ++s) issued_phase[s] = -1;
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.ntiles && ok; t += gridDim.x) {
+        const TileInfo ti = tile_info<PHASE>(p, t);
+        if (ti.skip) continue;
+        const void *mapA = PHASE == 0 ? &ti.d->tm_x : PHASE == 1 ? &ti.d->tm_a : &ti.d->tm_xt[cur];
+        const void *mapB = PHASE == 0 ? &ti.d->tm_x : PHASE == 1 ? &ti.d->tm_a : &ti.d->tm_b;
+        for (int kb = 0; kb < ti.nk; ++kb) {
+          if (!mbar_wait(&bar->empty[stage], phase ^ 1u, abort, p.status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bar->full[stage], kStageBytes);
+          const int kx = kb * kTcBK;
+          tma_load_2d(sA + stage * kABytes, mapA, kx, ti.row0, &bar->full[stage], pol);
+          tma_load_2d(sB + stage * kBBytes, mapB, kx, ti.col0, &bar->full[stage], pol);
+          tma_load_2d(sB + stage * kBBytes + kBBytes / 2, mapB, kx, ti.col0 + kTcBM, &bar->full[stage], pol);
+          issued_phase[stage] = static_cast<int>(phase);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // make sure no copy is still landing in shared memory
+        for (int s = 0; s < kStages; ++s)
+          if (issued_phase[s] >= 0) mbar_drain(&bar->full[s], static_cast<uint32_t>(issued_phase[s]), p.status);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------- MMA issuer
+      constexpr uint32_t idesc = umma_idesc_bf16(kTcBM, kTcBN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.ntiles && ok; t += gridDim.x) {
+        const TileInfo ti = tile_info<PHASE>(p, t);
+        if (ti.skip) continue;
+        if (!mbar_wait(&bar->tempty[acc], acc_phase ^ 1u, abort, p.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * kTcBN);
+        for (int kb = 0; kb < ti.nk; ++kb) {
+          if (!mbar_wait(&bar->full[stage], phase, abort, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(sA + stage * kABytes);
+          const uint32_t b_addr = smem_u32(sB + stage * kBBytes);
+#pragma unroll
+          for (int k = 0; k < kTcBK / 16; ++k) {
+            umma_bf16(d_tmem, sw128_kmajor_desc(a_addr + k * 32), sw128_kmajor_desc(b_addr + k * 32), idesc,
+                      (kb | k) != 0 ? 1u : 0u);
+          }
+          umma_commit(&bar->empty[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&bar->tfull[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      // no MMA may still be running when TMEM is released
+      umma_commit(&bar->drain);
+      mbar_drain(&bar->drain, 0, p.status);
+    }
+  } else {
+    // ------------------------------------------------------ epilogue
+    const int q = warp & 3;         // TMEM lane quarter this warp may access
+    const int r = q * 32 + lane;    // tile row held by this thread
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
+      const TileInfo ti = tile_info<PHASE>(p, t);
+      if (ti.skip) continue;
+      if (!mbar_wait(&bar->tfull[acc], acc_phase, abort, p.status)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kTcBN);
+#pragma unroll 1
+      for (int c = 0; c < kTcBN / 32; ++c) {
+        uint32_t v[32];
+        __syncwarp();
+        tmem_ld32(tbase + static_cast<uint32_t>(c * 32), v);
+        tmem_ld_wait(v);
+        epilogue_chunk<PHASE>(p, ti, r, c, v);
+      }
+      tc_fence_before();
+      mbar_arrive(&bar->tempty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int PHASE>
+int launch_phase_t(const PhaseParams &p, int grid, cudaStream_t s) {
+  const int smem = tc_smem_bytes();
+  if (cudaFuncSetAttribute(ns_tc_gemm_kernel<PHASE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+      cudaSuccess)
+    return -1;
+  ns_tc_gemm_kernel<PHASE><<<grid, kThreads, smem, s>>>(p);
+  count_launch();
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace
+
+int tc_smem_bytes() { return 1024 + kStages * kStageBytes + static_cast<int>(sizeof(Barriers)); }
+
+int launch_tc_phase(int phase, const PhaseParams &p, int grid, cudaStream_t s) {
+  if (p.ntiles <= 0) return 0;
+  if (grid > p.ntiles) grid = p.ntiles;
+  if (phase == 0) return launch_phase_t<0>(p, grid, s);
+  if (phase == 1) return launch_phase_t<1>(p, grid, s);
+  return launch_phase_t<2>(p, grid, s);
+}
+
+}  // namespace ns

@@ -12,6 +12,9 @@ Two independent computations live here:
 * ``orthogonalize`` -- the iteration itself, step by step in fp64, in plain C
   (``ns_oracle.c``): s = ||X||_F, X <- X/(s+eps), work on X^T when M > N, then
   ``steps`` times A = X X^T, B = b A + c A^2, X = a X + B X.
+  ``orthogonalize_np`` takes the same steps in the same order with NumPy's
+  fp64 matrix product as the product primitive; it is what the CPU baseline
+  times (the C loops run minutes per step on the largest matrices).
 * ``svd_twin`` -- the closed form of the same map through LAPACK's SVD: every
   step is an odd matrix polynomial, so it keeps the singular vectors and maps
   each singular value through f(s) = a s + b s^3 + c s^5.
@@ -120,6 +123,30 @@ def orthogonalize(X, steps: int = DEFAULT_STEPS, coeffs=DEFAULT_COEFFS,
     if rc != 0:
         raise RuntimeError(f"ns_oracle_orthogonalize failed with {rc}")
     return W
+
+
+def orthogonalize_np(X, steps: int = DEFAULT_STEPS, coeffs=DEFAULT_COEFFS,
+                     eps: float = DEFAULT_EPS, orient: int = 0) -> np.ndarray:
+    """The same steps as ``orthogonalize`` with numpy.matmul (fp64) as the
+    product: s = ||X||_F; X/(s+eps); transpose when M > N (orient as above);
+    then ``steps`` times A = W W^T, B = b A + c A A, W = a W + B W."""
+    W = np.array(to_f64(X), dtype=np.float64, copy=True)
+    if W.ndim != 2:
+        raise ValueError("oracle takes 2-D matrices")
+    if W.size == 0:
+        return W
+    a, b, c = (float(v) for v in coeffs)
+    s = np.sqrt(np.sum(W * W))
+    W = W / (s + float(eps))
+    M, N = W.shape
+    transpose = (M > N) if orient == 0 else (orient == 2)
+    if transpose:
+        W = np.ascontiguousarray(W.T)
+    for _ in range(int(steps)):
+        A = W @ W.T
+        B = b * A + c * (A @ A)
+        W = a * W + B @ W
+    return np.ascontiguousarray(W.T) if transpose else W
 
 
 def orthogonalize_batched(mats, steps: int = DEFAULT_STEPS, coeffs=DEFAULT_COEFFS,

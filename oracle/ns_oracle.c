@@ -69,26 +69,6 @@ double ns_oracle_frobenius(const double *X, int64_t M, int64_t N)
     return sqrt(acc);
 }
 
-/* A = W W^T for W m x n, row-major; A is m x m. */
-static void gram(const double *W, int64_t m, int64_t n, double *A)
-{
-#pragma omp parallel for schedule(static)
-    for (int64_t i = 0; i < m; ++i) {
-        for (int64_t j = 0; j < m; ++j) {
-            double acc = 0.0;
-            for (int64_t k = 0; k < n; ++k) {
-#if NS_ORACLE_MUTATION == 3
-                /* planted: second operand indexed by the wrong row */
-                acc += W[i * n + k] * W[((j + 1) % m) * n + k];
-#else
-                acc += W[i * n + k] * W[j * n + k];
-#endif
-            }
-            A[i * m + j] = acc;
-        }
-    }
-}
-
 /* C = P Q for P (r x q), Q (q x s), all row-major. Each C[i][j] is the sum
  * over k = 0..q-1 of P[i][k]*Q[k][j], accumulated in increasing k. */
 static void matmul(const double *P, const double *Q, int64_t r, int64_t q, int64_t s, double *C)
@@ -103,6 +83,21 @@ static void matmul(const double *P, const double *Q, int64_t r, int64_t q, int64
             for (int64_t j = 0; j < s; ++j) crow[j] += p * qrow[j];
         }
     }
+}
+
+/* A = W W^T for W m x n, row-major; A is m x m: A[i][j] is the sum over
+ * k = 0..n-1 of W[i][k]*W[j][k] in increasing k, computed as W times an
+ * explicit copy of W^T (Wt, n x m) so the same product routine serves. */
+static void gram(const double *W, int64_t m, int64_t n, double *Wt, double *A)
+{
+    for (int64_t i = 0; i < m; ++i)
+        for (int64_t k = 0; k < n; ++k)
+#if NS_ORACLE_MUTATION == 3
+            Wt[k * m + i] = W[((i + 1) % m) * n + k];  /* planted: wrong row of the second operand */
+#else
+            Wt[k * m + i] = W[i * n + k];
+#endif
+    matmul(W, Wt, m, n, m, A);
 }
 
 /*
@@ -136,8 +131,9 @@ int ns_oracle_orthogonalize(double *X, int64_t M, int64_t N, int steps,
     double *W2 = (double *)malloc(sizeof(double) * (size_t)(m * n));
     double *A = (double *)malloc(sizeof(double) * (size_t)(m * m));
     double *AA = (double *)malloc(sizeof(double) * (size_t)(m * m));
-    if (!W || !W2 || !A || !AA) {
-        free(W); free(W2); free(A); free(AA);
+    double *Wt = (double *)malloc(sizeof(double) * (size_t)(m * n));
+    if (!W || !W2 || !A || !AA || !Wt) {
+        free(W); free(W2); free(A); free(AA); free(Wt);
         return -2;
     }
 
@@ -153,7 +149,7 @@ int ns_oracle_orthogonalize(double *X, int64_t M, int64_t N, int steps,
     if (nsteps > 0) nsteps -= 1;                 /* planted: one step short */
 #endif
     for (int it = 0; it < nsteps; ++it) {
-        gram(W, m, n, A);                        /* A = W W^T */
+        gram(W, m, n, Wt, A);                    /* A = W W^T */
         matmul(A, A, m, m, m, AA);               /* AA = A A */
         for (int64_t i = 0; i < m * m; ++i) {    /* B = b A + c A^2, kept in A */
 #if NS_ORACLE_MUTATION == 1
@@ -178,7 +174,7 @@ int ns_oracle_orthogonalize(double *X, int64_t M, int64_t N, int steps,
         for (int64_t j = 0; j < N; ++j)
             X[i * N + j] = transpose ? W[j * n + i] : W[i * n + j];
 
-    free(W); free(W2); free(A); free(AA);
+    free(W); free(W2); free(A); free(AA); free(Wt);
     return 0;
 }
 

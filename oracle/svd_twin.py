@@ -52,3 +52,23 @@ def polar(X: np.ndarray) -> np.ndarray:
 
 def singular_values(X: np.ndarray) -> np.ndarray:
     return np.linalg.svd(np.asarray(X, dtype=np.float64), compute_uv=False)
+
+
+def closed_form_eigh(X: np.ndarray, steps: int, coeffs, eps: float) -> np.ndarray:
+    """The same closed form through the eigen-decomposition of the smaller
+    Gram matrix, for large inputs. With M >= N: X^T X = V diag(s^2) V^T and
+    the result is X V diag(g(s)/s) V^T; with M < N: X X^T = U diag(s^2) U^T
+    and the result is U diag(g(s)/s) U^T X, where g(s) = f^steps(s/(||X||+eps)).
+    Directions with s == 0 contribute nothing (g(0) = 0)."""
+    X = np.asarray(X, dtype=np.float64)
+    if X.size == 0:
+        return X.copy()
+    fro = np.sqrt(np.sum(X * X))
+    tall = X.shape[0] >= X.shape[1]
+    G = X.T @ X if tall else X @ X.T
+    lam, Q = np.linalg.eigh(G)
+    s = np.sqrt(np.clip(lam, 0.0, None))
+    g = quintic_iterate(s / (fro + eps), steps, coeffs)
+    ratio = np.where(s > 0, g / np.where(s > 0, s, 1.0), 0.0)
+    core = (Q * ratio) @ Q.T
+    return X @ core if tall else core @ X

@@ -1,0 +1,93 @@
+"""C ABI checks that need no GPU: the library builds for sm_103a and loads,
+exports every function include/ns.h declares, and rejects bad arguments
+before touching a device (validation runs first and launches nothing)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from newton_schulz_quintic_gb300 import api, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ns.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return api.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ns_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ["ns_orthogonalize_batched", "ns_orthogonalize_batched_ex", "ns_workspace_bytes",
+                 "ns_orthogonalize_batched_host", "ns_cost", "ns_get_status", "ns_strerror",
+                 "ns_release_workspace"]:
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", api.library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\sT\s(ns_\w+)", out))
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_built_for_sm103a(lib):
+    assert build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+    assert build.up_to_date()
+
+
+def test_cost_matches_formula(lib):
+    # second page, "Changes" item 1: max(M,N) * min(M,N)^2
+    for M, N in [(8192, 6144), (6144, 8192), (4096, 14336), (1024, 4096), (18, 2304), (0, 7), (1, 1)]:
+        assert api.cost(M, N) == max(M, N) * min(M, N) ** 2
+    assert api.cost(-1, 4) == -1
+
+
+def test_workspace_bytes(lib):
+    assert api.workspace_bytes([], 1) > 0
+    small = api.workspace_bytes([(64, 128)], api.NS_F32)      # resident path: descriptors only
+    big = api.workspace_bytes([(8192, 6144)], api.NS_BF16)
+    # W, two W^T buffers, A and B of a 6144 x 8192 working matrix, bf16
+    assert big >= 2 * (3 * 6144 * 8192 + 2 * 6144 * 6144)
+    assert small < 1 << 20
+    assert api.workspace_bytes([(-1, 5)], api.NS_BF16) == 0
+    assert api.workspace_bytes([(5, 5)], 7) == 0
+
+
+def _call(lib, ptrs, shapes, count, steps=5, dtype=api.NS_BF16):
+    return lib.ns_orthogonalize_batched(ptrs, shapes, count, steps, None, dtype, None)
+
+
+def test_validation_rejects_before_launch(lib):
+    P = ctypes.c_void_p
+    S = ctypes.c_int64
+    good_ptrs = (P * 1)(0x100000)
+    good_shape = (S * 2)(4, 8)
+    assert _call(lib, good_ptrs, good_shape, 0) == 0                     # empty batch: no-op
+    assert _call(lib, good_ptrs, good_shape, -1) == -1                   # negative count
+    assert _call(lib, good_ptrs, good_shape, 1, steps=-2) == -1          # negative steps
+    assert _call(lib, good_ptrs, good_shape, 1, dtype=5) == -1           # bad dtype
+    assert _call(lib, good_ptrs, (S * 2)(-4, 8), 1) == -1                # negative dim
+    assert _call(lib, None, good_shape, 1) == -1                         # null pointer array
+    assert _call(lib, (P * 1)(0), good_shape, 1) == -1                   # null matrix
+    assert _call(lib, (P * 1)(0x100001), good_shape, 1) == -2            # misaligned bf16
+    assert _call(lib, (P * 1)(0x100002), good_shape, 1, dtype=api.NS_F32) == -2  # misaligned f32
+    assert lib.ns_orthogonalize_batched_ex(good_ptrs, good_shape, 1, 5, None, 1e-7, 1, None, 0, None) == -1
+
+
+def test_strerror(lib):
+    for code in [0, -1, -2, -3, -4, -5, -6]:
+        assert lib.ns_strerror(code)
+    assert b"unknown" in lib.ns_strerror(-99)

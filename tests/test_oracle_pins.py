@@ -28,6 +28,12 @@ CO = oracle.DEFAULT_COEFFS
 EPS = oracle.DEFAULT_EPS
 
 
+@pytest.fixture(params=["c", "numpy"])
+def ns(request):
+    """Both implementations of the oracle's steps face the same pins."""
+    return oracle.orthogonalize if request.param == "c" else oracle.orthogonalize_np
+
+
 def rel(a, b):
     return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
 
@@ -42,42 +48,42 @@ SHAPES = [(1, 7), (7, 1), (1, 1), (5, 5), (12, 40), (40, 12), (64, 128), (128, 6
 
 
 @pytest.mark.parametrize("shape", SHAPES)
-def test_matches_svd_closed_form(shape):
+def test_matches_svd_closed_form(ns, shape):
     X = randn(shape, seed=shape[0] * 1000 + shape[1], std=0.02)
-    got = oracle.orthogonalize(X)
+    got = ns(X)
     ref = svd_twin.closed_form(X, 5, CO, EPS)
     assert rel(got, ref) < 1e-10
 
 
 @pytest.mark.parametrize("steps", [0, 1, 2, 3, 7])
-def test_matches_svd_closed_form_any_steps(steps):
+def test_matches_svd_closed_form_any_steps(ns, steps):
     X = randn((20, 50), seed=steps)
-    assert rel(oracle.orthogonalize(X, steps=steps), svd_twin.closed_form(X, steps, CO, EPS)) < 1e-10
+    assert rel(ns(X, steps=steps), svd_twin.closed_form(X, steps, CO, EPS)) < 1e-10
 
 
-def test_custom_coefficients_closed_form():
+def test_custom_coefficients_closed_form(ns):
     X = randn((16, 30), seed=3)
     co = (2.0, -1.5, 0.5)
-    assert rel(oracle.orthogonalize(X, steps=4, coeffs=co), svd_twin.closed_form(X, 4, co, EPS)) < 1e-10
+    assert rel(ns(X, steps=4, coeffs=co), svd_twin.closed_form(X, 4, co, EPS)) < 1e-10
 
 
-def test_zero_steps_is_normalisation():
+def test_zero_steps_is_normalisation(ns):
     X = randn((9, 13), seed=4)
     s = np.sqrt(np.sum(X ** 2))
-    got = oracle.orthogonalize(X, steps=0)
+    got = ns(X, steps=0)
     assert rel(got, X / (s + EPS)) < 1e-15
 
 
 @pytest.mark.parametrize("shape", [(1, 50), (50, 1), (1, 2304)])
-def test_single_row_or_column_scalar_recurrence(shape):
+def test_single_row_or_column_scalar_recurrence(ns, shape):
     # one singular value sigma = ||x||: result is f^5(sigma/(sigma+eps)) * x/sigma
     x = randn(shape, seed=11)
     s = np.linalg.norm(x)
     g = svd_twin.quintic_iterate(s / (s + EPS), 5, CO)
-    assert rel(oracle.orthogonalize(x), g * x / s) < 1e-13
+    assert rel(ns(x), g * x / s) < 1e-13
 
 
-def test_diagonal_scalar_recurrence():
+def test_diagonal_scalar_recurrence(ns):
     # diagonal input: every entry follows the scalar recurrence on its own
     d = np.array([0.3, -1.7, 0.02, 4.0, -0.5])
     X = np.zeros((5, 9))
@@ -85,53 +91,53 @@ def test_diagonal_scalar_recurrence():
     s = np.linalg.norm(d)
     expect = np.zeros_like(X)
     expect[np.arange(5), np.arange(5)] = svd_twin.quintic_iterate(d / (s + EPS), 5, CO)
-    got = oracle.orthogonalize(X)
+    got = ns(X)
     assert np.max(np.abs(got - expect)) < 1e-14
     assert np.array_equal(got == 0, expect == 0)
 
 
 @pytest.mark.parametrize("m,n", [(1, 16), (8, 32), (24, 64), (64, 128)])
-def test_orthonormal_rows_scale(m, n):
+def test_orthonormal_rows_scale(ns, m, n):
     # X X^T = I: every step keeps X up to the scalar g = f^5(1/(sqrt(m)+eps))
     Q, _ = np.linalg.qr(randn((n, n), seed=m))
     X = Q[:m]
     g = svd_twin.quintic_iterate(1.0 / (np.sqrt(m) + EPS), 5, CO)
-    assert rel(oracle.orthogonalize(X), g * X) < 1e-12
-    assert rel(oracle.orthogonalize(X.T.copy()), g * X.T) < 1e-12
+    assert rel(ns(X), g * X) < 1e-12
+    assert rel(ns(X.T.copy()), g * X.T) < 1e-12
 
 
-def test_orthonormal_scale_values():
+def test_orthonormal_scale_values(ns):
     # spot values of g (m=1, 8, 24, 64), recomputed from the scalar map
     want = {1: 0.6964365, 8: 1.0669680, 24: 0.7072018, 64: 0.6881399}
     for m, g in want.items():
         Q, _ = np.linalg.qr(randn((2 * m + 3, 2 * m + 3), seed=7))
         X = Q[:m]
-        out = oracle.orthogonalize(X)
+        out = ns(X)
         ratio = np.sum(out * X) / np.sum(X * X)
         assert abs(ratio - g) < 1e-6
 
 
-def test_zero_matrix():
+def test_zero_matrix(ns):
     for shape in [(4, 6), (6, 4), (1, 1)]:
-        out = oracle.orthogonalize(np.zeros(shape))
+        out = ns(np.zeros(shape))
         assert np.all(out == 0) and not np.any(np.signbit(out))
 
 
 @pytest.mark.parametrize("shape,zero_rows", [((10, 40), [0, 4, 9]), ((40, 10), [3, 39]),
                                              ((24, 100), list(range(18, 24)))])
-def test_zero_rows_stay_exactly_zero(shape, zero_rows):
+def test_zero_rows_stay_exactly_zero(ns, shape, zero_rows):
     X = randn(shape, seed=5)
     X[zero_rows] = 0.0
-    out = oracle.orthogonalize(X)
+    out = ns(X)
     assert np.all(out[zero_rows] == 0)
     assert not np.any(np.signbit(out[zero_rows]))
     assert np.all(out[[i for i in range(shape[0]) if i not in zero_rows]] != 0)
 
 
-def test_zero_columns_stay_exactly_zero():
+def test_zero_columns_stay_exactly_zero(ns):
     X = randn((12, 30), seed=6)
     X[:, [0, 17, 29]] = 0.0
-    out = oracle.orthogonalize(X)
+    out = ns(X)
     assert np.all(out[:, [0, 17, 29]] == 0)
 
 
@@ -151,45 +157,45 @@ def test_padding_equivalence_bit_exact(real, shards):
 
 
 @pytest.mark.parametrize("shape", [(20, 50), (50, 20), (1, 9), (30, 30)])
-def test_orientations_agree(shape):
+def test_orientations_agree(ns, shape):
     # X p(X^T X) = p(X X^T) X: the iteration on X and on X^T give one result
     X = randn(shape, seed=8)
-    a = oracle.orthogonalize(X, orient=1)
-    b = oracle.orthogonalize(X, orient=2)
+    a = ns(X, orient=1)
+    b = ns(X, orient=2)
     assert rel(a, b) < 1e-12
 
 
-def test_scale_invariance():
+def test_scale_invariance(ns):
     X = randn((16, 48), seed=9)
     for alpha in (1e-3, 7.5, 1e4):
-        assert rel(oracle.orthogonalize(alpha * X, eps=0.0), oracle.orthogonalize(X, eps=0.0)) < 1e-12
+        assert rel(ns(alpha * X, eps=0.0), ns(X, eps=0.0)) < 1e-12
 
 
-def test_orthogonal_equivariance():
+def test_orthogonal_equivariance(ns):
     X = randn((16, 40), seed=10)
     Q, _ = np.linalg.qr(randn((16, 16), seed=12))
     R, _ = np.linalg.qr(randn((40, 40), seed=13))
-    lhs = oracle.orthogonalize(Q @ X @ R)
-    rhs = Q @ oracle.orthogonalize(X) @ R
+    lhs = ns(Q @ X @ R)
+    rhs = Q @ ns(X) @ R
     assert rel(lhs, rhs) < 1e-11
 
 
 @pytest.mark.parametrize("shape", [(8, 16), (16, 32), (16, 9), (5, 5)])
-def test_cubic_iteration_converges_to_polar_factor(shape):
+def test_cubic_iteration_converges_to_polar_factor(ns, shape):
     # (a,b,c) = (1.5, -0.5, 0) is the cubic Newton-Schulz iteration, whose fixed
     # point on full-rank inputs is the orthogonal polar factor U V^T
     X = randn(shape, seed=shape[0] + shape[1])
-    out = oracle.orthogonalize(X, steps=60, coeffs=(1.5, -0.5, 0.0))
+    out = ns(X, steps=60, coeffs=(1.5, -0.5, 0.0))
     assert np.max(np.abs(out - svd_twin.polar(X))) < 1e-8
 
 
-def test_singular_value_band():
+def test_singular_value_band(ns):
     # for sigma/||X|| in [2e-3, 1], f^5 stays in [0.6818, 1.2024]; a
     # Gaussian 64x128 has all its normalised singular values in that range
     X = randn((64, 128), seed=14)
     s_in = svd_twin.singular_values(X) / np.linalg.norm(X)
     assert s_in.min() > 2e-3
-    s_out = svd_twin.singular_values(oracle.orthogonalize(X))
+    s_out = svd_twin.singular_values(ns(X))
     assert s_out.min() >= 0.6818 - 1e-9 and s_out.max() <= 1.2024 + 1e-9
     grid = np.logspace(np.log10(2e-3), 0, 20001)
     g = svd_twin.quintic_iterate(grid, 5, CO)
@@ -220,3 +226,20 @@ def test_mutations_are_caught(mutation):
     got = oracle.orthogonalize(X, mutation=mutation)
     ref = svd_twin.closed_form(X, 5, CO, EPS)
     assert rel(got, ref) > 1e-3
+
+
+@pytest.mark.parametrize("shape", [(40, 12), (12, 40), (64, 64), (130, 300)])
+def test_eigh_closed_form_matches_svd_closed_form(shape):
+    # the large-size form used for sampled full-size parity agrees with the SVD form
+    X = randn(shape, seed=21, std=0.02)
+    a = svd_twin.closed_form_eigh(X, 5, CO, EPS)
+    b = svd_twin.closed_form(X, 5, CO, EPS)
+    assert rel(a, b) < 1e-9
+    assert rel(a, oracle.orthogonalize(X)) < 1e-9
+
+
+def test_eigh_closed_form_keeps_zero_rows():
+    X = randn((30, 80), seed=22)
+    X[25:] = 0.0
+    out = svd_twin.closed_form_eigh(X, 5, CO, EPS)
+    assert np.max(np.abs(out[25:])) < 1e-14

@@ -1,0 +1,276 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU fp64 oracle
+on the same seeded inputs.
+
+Bar (per matrix): relative Frobenius error ||G - O||_F / ||O||_F <= 1e-4 for
+float32 and <= 3e-2 for bfloat16; rows and columns that are zero on input are
+exactly zero on output. Cases span several tiles with ragged tails, both
+orientations, the resident small-matrix kernel, the bf16 tensor-core path and
+the fp32 CUDA-core path, and the degenerate inputs (empty batch, zero-size
+matrices, all-zero matrices, one row / one column, steps = 0, the cubic
+coefficients). Full-size workloads are checked on sampled matrices against
+the oracle's closed form (eigen-decomposition of the Gram matrix), which the
+CPU tests pin to the step-by-step oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import svd_twin
+from newton_schulz_quintic_gb300 import api, inputs
+
+pytestmark = pytest.mark.gpu
+
+CO = oracle.DEFAULT_COEFFS
+TOL = {torch.float32: 1e-4, torch.bfloat16: 3e-2}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from newton_schulz_quintic_gb300 import build
+    build.build()
+    api.load_library()
+    yield
+    torch.cuda.synchronize()
+
+
+def rel(a, b):
+    nb = np.linalg.norm(b)
+    return float(np.linalg.norm(a - b) / nb) if nb > 0 else float(np.linalg.norm(a))
+
+
+def run_gpu(mats, steps=5, coeffs=None, eps=None, calls=None):
+    dev = [m.contiguous().cuda() for m in mats]
+    if calls is None:
+        api.orthogonalize_batched(dev, steps=steps, coeffs=coeffs, eps=eps)
+    else:
+        for sl in calls:
+            api.orthogonalize_batched(dev[sl], steps=steps, coeffs=coeffs, eps=eps)
+    torch.cuda.synchronize()
+    assert api.get_status() == 0
+    return [d.cpu() for d in dev]
+
+
+def zero_lines(x):
+    x = oracle.to_f64(x)
+    return np.where(~x.any(axis=1))[0], np.where(~x.any(axis=0))[0]
+
+
+def check_one(x, y, steps=5, coeffs=CO, eps=oracle.DEFAULT_EPS, ref=None):
+    if ref is None:
+        ref = oracle.orthogonalize(x, steps=steps, coeffs=coeffs, eps=eps)
+    got = oracle.to_f64(y)
+    assert np.all(np.isfinite(got))
+    err = rel(got, ref)
+    assert err <= TOL[x.dtype], f"shape {tuple(x.shape)} rel err {err}"
+    zr, zc = zero_lines(x)
+    assert np.all(got[zr] == 0) and np.all(got[:, zc] == 0)
+    return err
+
+
+def seeded(shape, dtype, seed, std=0.02):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(shape, generator=g) * std).to(dtype)
+
+
+# ------------------------------------------------------------ the small workloads in full
+
+def test_f32_8x64x128_resident():
+    wl = inputs.WORKLOADS["f32-8x64x128"]
+    xs = wl.matrices()
+    ys = run_gpu(xs)
+    for x, y in zip(xs, ys):
+        check_one(x, y)
+
+
+def test_bf16_32x24x2304_padded_rows_stay_zero():
+    wl = inputs.WORKLOADS["bf16-32x24x2304-pad"]
+    xs = wl.matrices()
+    ys = run_gpu(xs)
+    for x, y in zip(xs, ys):
+        check_one(x, y)
+        # padded rows 18..23: exactly +0 (bit pattern 0)
+        assert torch.all(y[18:].view(torch.int16) == 0)
+        # the real rows equal NS of the unpadded 18 x 2304 matrix
+        ref18 = oracle.orthogonalize(x[:18])
+        assert rel(oracle.to_f64(y[:18]), ref18) <= TOL[torch.bfloat16]
+
+
+# ------------------------------------------------------------ tensor-core path (bf16)
+
+TC_SHAPES = [(300, 520), (520, 300), (256, 256), (130, 300), (70, 4000), (129, 1031), (640, 1200),
+             (1200, 640), (65, 65), (384, 2048)]
+
+
+@pytest.mark.parametrize("shape", TC_SHAPES)
+def test_bf16_tensor_core_shapes(shape):
+    x = seeded(shape, torch.bfloat16, seed=shape[0] * 7 + shape[1])
+    (y,) = run_gpu([x])
+    check_one(x, y)
+
+
+def test_bf16_mixed_batch_one_call():
+    xs = [seeded(s, torch.bfloat16, seed=i) for i, s in enumerate(TC_SHAPES + [(24, 100), (1, 300)])]
+    ys = run_gpu(xs)
+    for x, y in zip(xs, ys):
+        check_one(x, y)
+
+
+def test_bf16_zero_rows_and_columns_skipped():
+    x = seeded((300, 1024), torch.bfloat16, seed=5)
+    x[250:] = 0
+    x[:, 900:] = 0
+    x[:, 17] = 0
+    xt = seeded((1024, 300), torch.bfloat16, seed=6)
+    xt[700:] = 0
+    xt[:, 299] = 0
+    ys = run_gpu([x, xt])
+    check_one(x, ys[0])
+    check_one(xt, ys[1])
+    assert torch.all(ys[0][250:].view(torch.int16) == 0)
+    assert torch.all(ys[1][700:].view(torch.int16) == 0)
+
+
+def test_bf16_orientations_bit_identical():
+    # Y (m < n) and Y^T are worked on as the same W, so the results agree bit for bit
+    y = seeded((300, 700), torch.bfloat16, seed=9)
+    a, b = run_gpu([y, y.t().contiguous()])
+    assert torch.equal(a, b.t())
+
+
+def test_bf16_cubic_coefficients_many_steps():
+    x = seeded((200, 400), torch.bfloat16, seed=10)
+    co = (1.5, -0.5, 0.0)
+    (y,) = run_gpu([x], steps=12, coeffs=co)
+    check_one(x, y, steps=12, coeffs=co)
+
+
+@pytest.mark.parametrize("dtype,shape", [(torch.bfloat16, (300, 520)), (torch.float32, (100, 300)),
+                                         (torch.bfloat16, (24, 100)), (torch.float32, (8, 16))])
+def test_steps_zero_is_normalisation(dtype, shape):
+    x = seeded(shape, dtype, seed=11)
+    (y,) = run_gpu([x], steps=0)
+    check_one(x, y, steps=0)
+
+
+# ------------------------------------------------------------ fp32 CUDA-core path
+
+F32_SHAPES = [(100, 300), (300, 100), (200, 200), (65, 1000), (129, 257)]
+
+
+@pytest.mark.parametrize("shape", F32_SHAPES)
+def test_f32_large_shapes(shape):
+    x = seeded(shape, torch.float32, seed=shape[0] + 3 * shape[1], std=1.0)
+    (y,) = run_gpu([x])
+    check_one(x, y)
+
+
+def test_f32_zero_rows_and_custom_eps():
+    x = seeded((150, 400), torch.float32, seed=12, std=1.0)
+    x[140:] = 0
+    (y,) = run_gpu([x], eps=1e-3)
+    check_one(x, y, eps=1e-3)
+
+
+# ------------------------------------------------------------ degenerate inputs
+
+def test_empty_batch_and_zero_size_matrices():
+    api.orthogonalize_batched([])
+    xs = [torch.zeros((0, 5), dtype=torch.bfloat16), seeded((1, 1), torch.bfloat16, 1),
+          seeded((5, 1), torch.bfloat16, 2), seeded((1, 7), torch.bfloat16, 3),
+          torch.zeros((4, 0), dtype=torch.bfloat16)]
+    ys = run_gpu(xs)
+    for x, y in zip(xs, ys):
+        if x.numel():
+            check_one(x, y)
+        else:
+            assert y.shape == x.shape
+
+
+@pytest.mark.parametrize("dtype,shape", [(torch.bfloat16, (200, 300)), (torch.bfloat16, (8, 16)),
+                                         (torch.float32, (100, 300)), (torch.float32, (8, 16))])
+def test_all_zero_matrix(dtype, shape):
+    x = torch.zeros(shape, dtype=dtype)
+    (y,) = run_gpu([x])
+    assert torch.all(y == 0) and not torch.any(torch.isnan(y))
+
+
+@pytest.mark.parametrize("shape", [(1, 100000), (100000, 1), (1, 2)])
+def test_single_row_or_column(shape):
+    x = seeded(shape, torch.bfloat16, seed=13)
+    (y,) = run_gpu([x])
+    check_one(x, y)
+
+
+# ------------------------------------------------------------ reproducibility and entry points
+
+def test_bitwise_reproducible():
+    xs = [seeded((640, 1200), torch.bfloat16, 14), seeded((24, 2304), torch.bfloat16, 15),
+          seeded((1200, 640), torch.bfloat16, 16)]
+    a = run_gpu(xs)
+    b = run_gpu(xs)
+    for u, v in zip(a, b):
+        assert torch.equal(u, v)
+
+
+def test_explicit_workspace_and_host_entry_point_agree():
+    xs = [seeded((300, 520), torch.bfloat16, 17), seeded((24, 100), torch.bfloat16, 18)]
+    ref = run_gpu(xs)
+    dev = [x.cuda() for x in xs]
+    need = api.workspace_bytes([tuple(x.shape) for x in xs], torch.bfloat16)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    api.orthogonalize_batched(dev, workspace=ws)
+    torch.cuda.synchronize()
+    for r, d in zip(ref, dev):
+        assert torch.equal(r, d.cpu())
+    host = [x.clone().pin_memory() for x in xs]
+    api.orthogonalize_batched_host(host)
+    for r, h in zip(ref, host):
+        assert torch.equal(r, h)
+
+
+def test_workspace_too_small_is_rejected():
+    x = seeded((300, 520), torch.bfloat16, 19).cuda()
+    ws = torch.empty(1024, dtype=torch.uint8, device="cuda")
+    with pytest.raises(api.NSError) as e:
+        api.orthogonalize_batched([x], workspace=ws)
+    assert e.value.code == -3
+
+
+# ------------------------------------------------------------ full-size workloads, sampled
+
+def _closed(x):
+    return svd_twin.closed_form_eigh(oracle.to_f64(x), 5, CO, oracle.DEFAULT_EPS)
+
+
+def test_full_bf16_8x8192x6144_sampled():
+    wl = inputs.WORKLOADS["bf16-8x8192x6144"]
+    xs = wl.matrices()
+    ys = run_gpu(xs, calls=wl.call_slices())
+    for y in ys:
+        assert torch.all(torch.isfinite(y.float()))
+    for i in (0, 7):
+        err = check_one(xs[i], ys[i], ref=_closed(xs[i]))
+        print(f"8192x6144 matrix {i}: rel err {err:.4e}")
+
+
+def test_full_bf16_moe_64_plus_12_sampled():
+    wl = inputs.WORKLOADS["bf16-moe-76x2048x6144"]
+    xs = wl.matrices()
+    ys = run_gpu(xs, calls=wl.call_slices())
+    for i in (0, 63, 64, 75):
+        check_one(xs[i], ys[i], ref=_closed(xs[i]))
+
+
+def test_full_bf16_mixed_120_sampled():
+    wl = inputs.WORKLOADS["bf16-mixed-120"]
+    xs = wl.matrices()
+    ys = run_gpu(xs, calls=wl.call_slices())
+    rng = np.random.default_rng(1004)
+    firsts = {}
+    for i, s in enumerate(wl.shapes):
+        firsts.setdefault(s, []).append(i)
+    for s, idx in firsts.items():
+        i = int(rng.choice(idx))
+        err = check_one(xs[i], ys[i], ref=_closed(xs[i]))
+        print(f"{s} matrix {i}: rel err {err:.4e}")

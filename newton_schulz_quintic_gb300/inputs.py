@@ -111,6 +111,13 @@ class Workload:
         return out
 
 
+def subset(wl: Workload, count: int) -> Workload:
+    """The first ``count`` matrices of a workload (same seeds), one call."""
+    count = max(1, min(int(count), wl.count))
+    return Workload(f"{wl.name}[:{count}]", tuple(wl.shapes[:count]), wl.dtype, wl.std, wl.seed,
+                    wl.steps, wl.real_rows, wl.shards, ())
+
+
 def _mixed_shapes():
     return (((4096, 4096),) * 24 + ((4096, 14336),) * 24 + ((14336, 4096),) * 24
             + ((1024, 4096),) * 48)

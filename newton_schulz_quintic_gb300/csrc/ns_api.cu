@@ -164,7 +164,7 @@ void build_layout(const int64_t *shapes, int count, int dtype, Layout &L) {
   std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
     return ns_cost(shapes[2 * a], shapes[2 * a + 1]) > ns_cost(shapes[2 * b], shapes[2 * b + 1]);
   });
-  const int BM = dtype == NS_BF16 ? kTcBM : kSimtBM;
+  const int BM = dtype == NS_BF16 ? kTcPairM : kSimtBM;  // bf16: rows of one CTA pair
   const int BN = dtype == NS_BF16 ? kTcBN : kSimtBN;
   L.prefix.push_back(0);
   for (int idx : order) {

@@ -109,6 +109,29 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const void *map, int
       : "memory");
 }
 
+// The same load delivered to every CTA of the cluster named in cta_mask, at
+// the same shared-memory offsets; each destination's mbarrier at the offset
+// of `bar` receives the transaction bytes.
+__device__ __forceinline__ void tma_load_2d_multicast(void *smem_dst, const void *map, int x, int y, uint64_t *bar,
+                                                      uint16_t cta_mask, uint64_t cache_hint) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(cta_mask), "l"(cache_hint)
+      : "memory");
+}
+
+// ---------------------------------------------------------------- clusters
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Full cluster barrier (every thread of every CTA of the cluster).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // L2 eviction-priority hints (createpolicy encodings computed at run time)
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   uint64_t p;
@@ -156,6 +179,16 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_u32(bar))
                : "memory");
+}
+
+// As umma_commit, arriving once on the mbarrier at the same offset in every
+// CTA of the cluster named in cta_mask.
+__device__ __forceinline__ void umma_commit_multicast(uint64_t *bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
 }
 
 // Shared-memory matrix descriptor: K-major operand written by TMA with

@@ -94,10 +94,15 @@ struct ResParams {
 constexpr int kNormBlocks = 128;  // partial-sum blocks per matrix
 constexpr int kPrepTile = 64;     // Y tile edge of the preparation kernel
 
-// tcgen05 GEMM tile (bf16 path)
+// tcgen05 GEMM tile (bf16 path). Tiles are processed by 2-CTA clusters: a
+// tile list entry covers kTcPairM x kTcBN outputs, CTA rank r of the cluster
+// computes rows [row0 + r*kTcBM, row0 + (r+1)*kTcBM) and the pair shares the
+// kTcBN-row second operand through TMA multicast.
 constexpr int kTcBM = 128;
 constexpr int kTcBN = 256;
 constexpr int kTcBK = 64;
+constexpr int kTcCluster = 2;
+constexpr int kTcPairM = kTcCluster * kTcBM;
 // SIMT GEMM tile (fp32 path)
 constexpr int kSimtBM = 64;
 constexpr int kSimtBN = 64;
@@ -107,7 +112,7 @@ int launch_norm(const PrepParams &p, cudaStream_t s);
 int launch_prep(const PrepParams &p, int total_tiles, cudaStream_t s);
 int launch_resident(const ResParams &p, int maxm, int smem_bytes, cudaStream_t s);
 int launch_simt_phase(int phase, const PhaseParams &p, cudaStream_t s);
-int launch_tc_phase(int phase, const PhaseParams &p, int grid, cudaStream_t s);
+int launch_tc_phase(int phase, const PhaseParams &p, int max_ctas, cudaStream_t s);
 int tc_smem_bytes();
 int resident_smem_bytes(int m, int n, int dtype);
 

@@ -104,10 +104,15 @@ int launch_norm(const PrepParams &p, cudaStream_t s) {
 // One block per 64x64 tile of the caller's Y. Every block sums the
 // matrix's kNormBlocks partials in the same fixed order, so all blocks agree
 // on s = ||Y||_F. It writes y / (s + eps), rounded to the working type, into
-// W and W^T (or back into Y when no step follows).
+// W and W^T (or back into Y when no step follows). When Y's rows are 16-byte
+// aligned the tile moves in 16-byte vectors; the transposed copy goes through
+// shared memory so both writes are row-contiguous.
 template <int DT>
 __global__ void __launch_bounds__(256) ns_prep_kernel(PrepParams p) {
   using T = typename Elem<DT>::T;
+  constexpr int V = 16 / sizeof(T);                 // elements per 16-byte vector
+  constexpr int CPR = kPrepTile / V;                // vectors per tile row
+  constexpr int PER = kPrepTile * kPrepTile / V / 256;  // vectors per thread
   const int bid = blockIdx.x;
   int lo = 0, hi = p.nmats;
   while (hi - lo > 1) {
@@ -120,35 +125,77 @@ __global__ void __launch_bounds__(256) ns_prep_kernel(PrepParams p) {
   const int local = bid - p.tile_prefix[mat];
   const int tcols = (N + kPrepTile - 1) / kPrepTile;
   const int r0 = (local / tcols) * kPrepTile, c0 = (local % tcols) * kPrepTile;
+  const T *y = static_cast<const T *>(d.user);
+  const bool vec = (N % V == 0) && ((reinterpret_cast<uintptr_t>(y) & 15) == 0);
 
   __shared__ float s_denom;
   __shared__ float tile[kPrepTile][kPrepTile + 1];
   const int tid = threadIdx.x;
+
+  // raw loads first: they do not depend on the norm
+  uint4 raw[PER];
+  if (vec) {
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      const int q = tid + k * 256, rr = q / CPR, cv = q % CPR;
+      const int r = r0 + rr, c = c0 + cv * V;
+      raw[k] = make_uint4(0, 0, 0, 0);
+      if (r < M && c < N) raw[k] = __ldg(reinterpret_cast<const uint4 *>(y + static_cast<size_t>(r) * N + c));
+    }
+  }
   if (tid < 32) {
     float v = 0.f;
     for (int i = tid; i < kNormBlocks; i += 32) v += p.partials[mat * kNormBlocks + i];
     v = warp_sum(v);
     if (tid == 0) s_denom = sqrtf(v) + p.eps;
   }
-  const T *y = static_cast<const T *>(d.user);
   __syncthreads();
   const float denom = s_denom;
-  for (int e = tid; e < kPrepTile * kPrepTile; e += 256) {
-    const int rr = e / kPrepTile, cc = e % kPrepTile;
-    const int r = r0 + rr, c = c0 + cc;
-    float v = 0.f;
-    if (r < M && c < N) v = __fdiv_rn(Elem<DT>::load(y + static_cast<size_t>(r) * N + c), denom);
-    tile[rr][cc] = v;
-  }
-  __syncthreads();
-
-  if (p.to_user) {
-    T *u = static_cast<T *>(d.user);
+  if (vec) {
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      const int q = tid + k * 256, rr = q / CPR, cv = q % CPR;
+      const T *e = reinterpret_cast<const T *>(&raw[k]);
+#pragma unroll
+      for (int u = 0; u < V; ++u) tile[rr][cv * V + u] = __fdiv_rn(Elem<DT>::to_f(e[u]), denom);
+    }
+  } else {
     for (int e = tid; e < kPrepTile * kPrepTile; e += 256) {
       const int rr = e / kPrepTile, cc = e % kPrepTile;
       const int r = r0 + rr, c = c0 + cc;
-      if (r < M && c < N) u[static_cast<size_t>(r) * N + c] = Elem<DT>::from_f(tile[rr][cc]);
+      float v = 0.f;
+      if (r < M && c < N) v = __fdiv_rn(Elem<DT>::load(y + static_cast<size_t>(r) * N + c), denom);
+      tile[rr][cc] = v;
     }
+  }
+  __syncthreads();
+
+  // writes: destination rows are 16-byte aligned (workspace pitches are
+  // multiples of 8 elements; the caller's rows when `vec`)
+  auto write_tile = [&](T *dst, int pitch, bool flip, int rows, int cols, bool dst_vec) {
+    // the tile as seen by the destination: rows x cols = (flip ? 64 cols of Y : 64 rows of Y)
+    const int R0 = flip ? c0 : r0, C0 = flip ? r0 : c0;
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      const int q = tid + k * 256, rr = q / CPR, cv = q % CPR;
+      const int R = R0 + rr, C = C0 + cv * V;
+      if (R >= rows || C >= cols) continue;
+      T *out = dst + static_cast<size_t>(R) * pitch + C;
+      if (dst_vec && C + V <= cols) {
+        uint4 w;
+        T *we = reinterpret_cast<T *>(&w);
+#pragma unroll
+        for (int u = 0; u < V; ++u) we[u] = Elem<DT>::from_f(flip ? tile[cv * V + u][rr] : tile[rr][cv * V + u]);
+        *reinterpret_cast<uint4 *>(out) = w;
+      } else {
+        for (int u = 0; u < V && C + u < cols; ++u)
+          out[u] = Elem<DT>::from_f(flip ? tile[cv * V + u][rr] : tile[rr][cv * V + u]);
+      }
+    }
+  };
+
+  if (p.to_user) {
+    write_tile(static_cast<T *>(d.user), N, false, M, N, vec);
     return;
   }
   // same orientation as Y: W when not transposed, W^T when transposed
@@ -157,16 +204,8 @@ __global__ void __launch_bounds__(256) ns_prep_kernel(PrepParams p) {
   // transposed orientation: W^T when not transposed, W when transposed
   T *flip = static_cast<T *>(d.transposed ? d.x : d.xt[0]);
   const int flip_pitch = d.transposed ? d.pn : d.pm;
-  for (int e = tid; e < kPrepTile * kPrepTile; e += 256) {
-    const int rr = e / kPrepTile, cc = e % kPrepTile;
-    const int r = r0 + rr, c = c0 + cc;
-    if (r < M && c < N) same[static_cast<size_t>(r) * same_pitch + c] = Elem<DT>::from_f(tile[rr][cc]);
-  }
-  for (int e = tid; e < kPrepTile * kPrepTile; e += 256) {
-    const int q = e / kPrepTile, pp = e % kPrepTile;  // output row c0+q, column r0+pp
-    const int r = r0 + pp, c = c0 + q;
-    if (r < M && c < N) flip[static_cast<size_t>(c) * flip_pitch + r] = Elem<DT>::from_f(tile[pp][q]);
-  }
+  write_tile(same, same_pitch, false, M, N, true);
+  write_tile(flip, flip_pitch, true, N, M, true);
 }
 
 int launch_prep(const PrepParams &p, int total_tiles, cudaStream_t s) {

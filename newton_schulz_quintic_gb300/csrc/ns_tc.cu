@@ -1,10 +1,14 @@
 // ns_tc.cu -- bf16 tensor-core GEMM phases of libns on sm_103a (tcgen05).
 //
-// One persistent, warp-specialised kernel per phase, over a cost-ordered
-// list of 128 x 256 output tiles drawn from every matrix of the batch:
-//   warp 0      TMA producer: 128x64 tile of the first operand and 256x64 of
-//               the second per k-block into a 4-stage shared-memory ring
-//               (128-byte swizzle), mbarrier full/empty handshake;
+// One persistent, warp-specialised kernel per phase, launched as clusters of
+// two CTAs over a cost-ordered list of 256 x 256 output tiles drawn from
+// every matrix of the batch. CTA rank r of a cluster computes the tile's rows
+// r*128 .. r*128+127; both CTAs need the same 256 rows of the second operand,
+// so each loads one 128-row half and multicasts it to both.
+//   warp 0      TMA producer: its own 128x64 box of the first operand and one
+//               128x64 half of the second (multicast to the pair) per k-block
+//               into a 4-stage shared-memory ring (128-byte swizzle); a stage
+//               is refilled only after both CTAs' MMAs have released it;
 //   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators)
 //               and, from one thread, issues tcgen05.mma (M=128, N=256,
 //               K=16, bf16 in, fp32 accumulate) and tcgen05.commit;
@@ -66,6 +70,7 @@ __device__ __forceinline__ TileInfo tile_info(const PhaseParams &p, int t) {
   const int meff = tr ? e1 : e0, neff = tr ? e0 : e1;
   const int rows_eff = PHASE == 2 ? neff : meff;
   const int k_eff = PHASE == 0 ? neff : meff;
+  // decided per pair tile, so both CTAs of a cluster agree
   ti.skip = (tl.row0 >= rows_eff) || (tl.col0 >= meff);
   ti.nk = (k_eff + kTcBK - 1) / kTcBK;
   return ti;
@@ -220,11 +225,16 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
   uint8_t *sB = smem + kStages * kABytes;
   Barriers *bar = reinterpret_cast<Barriers *>(smem + kStages * kStageBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();             // 0 or 1 within the pair
+  const int cluster = blockIdx.x / kTcCluster;
+  const int nclusters = gridDim.x / kTcCluster;
+  const int my_rows = static_cast<int>(rank) * kTcBM;  // this CTA's offset inside a pair tile
+  constexpr uint16_t kPairMask = (1u << kTcCluster) - 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bar->full[s], 1);
-      mbar_init(&bar->empty[s], 1);
+      mbar_init(&bar->empty[s], kTcCluster);  // released by both CTAs' MMAs
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&bar->tfull[a], 1);
@@ -240,6 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
   }
   tc_fence_before();
   __syncthreads();
+  // the peer may multicast into this CTA's ring only after its barriers exist
+  cluster_sync();
   tc_fence_after();
   const uint32_t tmem = bar->tmem_base;
   volatile int *abort = &bar->abort;
@@ -254,21 +266,24 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < p.ntiles && ok; t += gridDim.x) {
+      for (int t = cluster; t < p.ntiles && ok; t += nclusters) {
         const TileInfo ti = tile_info<PHASE>(p, t);
         if (ti.skip) continue;
         const void *mapA = PHASE == 0 ? &ti.d->tm_x : PHASE == 1 ? &ti.d->tm_a : &ti.d->tm_xt[cur];
         const void *mapB = PHASE == 0 ? &ti.d->tm_x : PHASE == 1 ? &ti.d->tm_a : &ti.d->tm_b;
         for (int kb = 0; kb < ti.nk; ++kb) {
+          // both CTAs' MMAs must be done with this stage: the B half loaded
+          // here also lands in the peer's ring
           if (!mbar_wait(&bar->empty[stage], phase ^ 1u, abort, p.status)) {
             ok = false;
             break;
           }
+          // 16 KB own A box + 16 KB own B half + 16 KB B half from the peer
           mbar_arrive_expect_tx(&bar->full[stage], kStageBytes);
           const int kx = kb * kTcBK;
-          tma_load_2d(sA + stage * kABytes, mapA, kx, ti.row0, &bar->full[stage], pol);
-          tma_load_2d(sB + stage * kBBytes, mapB, kx, ti.col0, &bar->full[stage], pol);
-          tma_load_2d(sB + stage * kBBytes + kBBytes / 2, mapB, kx, ti.col0 + kTcBM, &bar->full[stage], pol);
+          tma_load_2d(sA + stage * kABytes, mapA, kx, ti.row0 + my_rows, &bar->full[stage], pol);
+          tma_load_2d_multicast(sB + stage * kBBytes + rank * (kBBytes / 2), mapB, kx,
+                                ti.col0 + static_cast<int>(rank) * kTcBM, &bar->full[stage], kPairMask, pol);
           issued_phase[stage] = static_cast<int>(phase);
           if (++stage == kStages) {
             stage = 0;
@@ -291,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < p.ntiles && ok; t += gridDim.x) {
+      for (int t = cluster; t < p.ntiles && ok; t += nclusters) {
         const TileInfo ti = tile_info<PHASE>(p, t);
         if (ti.skip) continue;
         if (!mbar_wait(&bar->tempty[acc], acc_phase ^ 1u, abort, p.status)) break;
@@ -310,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
             umma_bf16(d_tmem, sw128_kmajor_desc(a_addr + k * 32), sw128_kmajor_desc(b_addr + k * 32), idesc,
                       (kb | k) != 0 ? 1u : 0u);
           }
-          umma_commit(&bar->empty[stage]);
+          umma_commit_multicast(&bar->empty[stage], kPairMask);  // release the stage in both CTAs
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
@@ -331,9 +346,10 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
     const int r = q * 32 + lane;    // tile row held by this thread
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
-      const TileInfo ti = tile_info<PHASE>(p, t);
+    for (int t = cluster; t < p.ntiles; t += nclusters) {
+      TileInfo ti = tile_info<PHASE>(p, t);
       if (ti.skip) continue;
+      ti.row0 += my_rows;
       if (!mbar_wait(&bar->tfull[acc], acc_phase, abort, p.status)) break;
       tc_fence_after();
       const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kTcBN);
@@ -355,17 +371,46 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  // the peer's multicast copies and MMA commits target this CTA's shared
+  // memory until it is done: leave together
+  cluster_sync();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
 template <int PHASE>
-int launch_phase_t(const PhaseParams &p, int grid, cudaStream_t s) {
+int launch_phase_t(const PhaseParams &p, int max_ctas, cudaStream_t s) {
   const int smem = tc_smem_bytes();
-  if (cudaFuncSetAttribute(ns_tc_gemm_kernel<PHASE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-      cudaSuccess)
-    return -1;
-  ns_tc_gemm_kernel<PHASE><<<grid, kThreads, smem, s>>>(p);
+  auto kernel = ns_tc_gemm_kernel<PHASE>;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -1;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kTcCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // persistent: as many pairs as can be resident at once, at most one per tile
+  static int resident_pairs[16][3] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int &cached = resident_pairs[dev & 15][PHASE];
+  if (cached == 0) {
+    cfg.gridDim = dim3(kTcCluster * (max_ctas / kTcCluster), 1, 1);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = max_ctas / kTcCluster;
+    }
+    cached = n;
+  }
+  const int pairs = cached < p.ntiles ? cached : p.ntiles;
+  cfg.gridDim = dim3(kTcCluster * pairs, 1, 1);
+  if (cudaLaunchKernelEx(&cfg, kernel, p) != cudaSuccess) return -1;
   count_launch();
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
@@ -374,12 +419,11 @@ int launch_phase_t(const PhaseParams &p, int grid, cudaStream_t s) {
 
 int tc_smem_bytes() { return 1024 + kStages * kStageBytes + static_cast<int>(sizeof(Barriers)); }
 
-int launch_tc_phase(int phase, const PhaseParams &p, int grid, cudaStream_t s) {
+int launch_tc_phase(int phase, const PhaseParams &p, int max_ctas, cudaStream_t s) {
   if (p.ntiles <= 0) return 0;
-  if (grid > p.ntiles) grid = p.ntiles;
-  if (phase == 0) return launch_phase_t<0>(p, grid, s);
-  if (phase == 1) return launch_phase_t<1>(p, grid, s);
-  return launch_phase_t<2>(p, grid, s);
+  if (phase == 0) return launch_phase_t<0>(p, max_ctas, s);
+  if (phase == 1) return launch_phase_t<1>(p, max_ctas, s);
+  return launch_phase_t<2>(p, max_ctas, s);
 }
 
 }  // namespace ns

@@ -53,6 +53,7 @@ extern "C" {
 #define NS_ECUDA (-4)    /* a CUDA runtime or driver call failed */
 #define NS_ETIMEOUT (-5) /* a bounded device-side wait gave up (reported by ns_get_status) */
 #define NS_ENODEV (-6)   /* no usable sm_100-family device */
+#define NS_ETOOBIG (-7)  /* batch needs more scratch than ns_orthogonalize_batched_noalloc holds */
 
 /*
  * ns_orthogonalize_batched -- Newton-Schulz of `count` matrices, in place.
@@ -97,6 +98,31 @@ size_t ns_workspace_bytes(const int64_t *shapes, int count, int dtype);
  */
 int ns_orthogonalize_batched_host(void *const *X_host, const int64_t *shapes, int count,
                                   int steps, const float *coeffs, int dtype, void *stream);
+
+/*
+ * ns_orthogonalize_batched_noalloc -- the same operation as
+ * ns_orthogonalize_batched (same arguments, eps = 1e-7) for callers that
+ * cannot allocate device memory: processes whose framework allocator has
+ * already reserved nearly all of HBM, optimizer steps that cannot absorb an
+ * allocator's synchronisation, runtimes that forbid allocation after
+ * start-up. It calls no cudaMalloc, cudaFree or other allocating routine; its
+ * scratch is one fixed 256 MiB device array inside the library, reserved on
+ * every device that loads the library until the process exits.
+ *   - A batch whose ns_workspace_bytes exceeds 256 MiB is rejected with
+ *     NS_ETOOBIG before anything runs (e.g. one 4096 x 4096 bf16 matrix
+ *     fits; one 8192 x 6144 does not).
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call shares the one array and leaves its contents behind; each
+ *     call clears what must start at zero itself. Calls that overlap on the
+ *     GPU (other streams, other host threads) race on the array: serialise
+ *     them.
+ * The pages have no counterpart of this entry point; it exists for callers
+ * of this library that cannot allocate.
+ */
+int ns_orthogonalize_batched_noalloc(void *const *X, const int64_t *shapes, int count, int steps,
+                                     const float *coeffs, int dtype, void *stream);
 
 /*
  * ns_cost -- Newton-Schulz cost of an M x N matrix, max(M,N) * min(M,N)^2

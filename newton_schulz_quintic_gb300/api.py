@@ -15,7 +15,7 @@ NS_F32 = 0
 NS_BF16 = 1
 
 _ERRORS = {0: "NS_OK", -1: "NS_EINVAL", -2: "NS_EALIGN", -3: "NS_ENOMEM", -4: "NS_ECUDA",
-           -5: "NS_ETIMEOUT", -6: "NS_ENODEV"}
+           -5: "NS_ETIMEOUT", -6: "NS_ENODEV", -7: "NS_ETOOBIG"}
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _lock = threading.Lock()
@@ -73,6 +73,8 @@ def load_library() -> ctypes.CDLL:
         lib.ns_release_workspace.argtypes = []
         lib.ns_num_kernel_launches.restype = i64
         lib.ns_num_kernel_launches.argtypes = []
+        lib.ns_orthogonalize_batched_noalloc.restype = i32
+        lib.ns_orthogonalize_batched_noalloc.argtypes = [vp, vp, i32, i32, vp, i32, vp]
         lib.ns_set_kernel_timing.restype = i32
         lib.ns_set_kernel_timing.argtypes = [i32]
         lib.ns_get_kernel_times.restype = i32
@@ -152,6 +154,26 @@ def orthogonalize_batched(mats, steps: int = 5, coeffs=None, eps: float | None =
                                                  workspace.numel(), sp)
     if rc != 0:
         raise NSError(rc, "ns_orthogonalize_batched")
+
+
+def orthogonalize_batched_noalloc(mats, steps: int = 5, coeffs=None, stream=None) -> None:
+    """In-place Newton-Schulz through the entry point that allocates no device
+    memory (for callers that cannot allocate: its scratch is a fixed 256 MiB
+    array inside the library; larger batches raise NSError NS_ETOOBIG)."""
+    import torch
+    lib = load_library()
+    mats = list(mats)
+    code = _check(mats, want_cuda=True)
+    if code is None:
+        return
+    dev = mats[0].device
+    with torch.cuda.device(dev):
+        s = stream if stream is not None else torch.cuda.current_stream(dev)
+        ptrs, shapes, co = _marshal(mats, coeffs)
+        rc = lib.ns_orthogonalize_batched_noalloc(ptrs, shapes, len(mats), int(steps), co, code,
+                                                  ctypes.c_void_p(s.cuda_stream))
+    if rc != 0:
+        raise NSError(rc, "ns_orthogonalize_batched_noalloc")
 
 
 def orthogonalize_batched_host(mats, steps: int = 5, coeffs=None, device=None, stream=None) -> None:

@@ -511,6 +511,7 @@ const char *ns_strerror(int code) {
     case NS_ECUDA: return "CUDA runtime or driver error";
     case NS_ETIMEOUT: return "a bounded device-side wait gave up";
     case NS_ENODEV: return "no sm_100-family device is current";
+    case NS_ETOOBIG: return "batch needs more scratch than the no-allocation entry point's 256 MiB array";
     default: return "unknown status";
   }
 }

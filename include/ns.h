@@ -163,6 +163,17 @@ int64_t ns_num_kernel_launches(void);
  * for k < n (n <= 6). Returns NS_OK or NS_ECUDA.
  */
 int ns_set_kernel_timing(int enable);
+
+/*
+ * ns_selftest_wait_timeout -- failure-detection self-test. Launches one CTA
+ * that waits, with the library's bounded wait and a limit of `limit_us`
+ * microseconds (1 .. 10^7), on an mbarrier nothing will ever arrive on. The
+ * wait gives up, records NS_ETIMEOUT in the device status word (read it with
+ * ns_get_status) and the kernel exits normally: no fault, no trap, no hang,
+ * and the CUDA context stays usable. Synchronises `stream`. Returns NS_OK if
+ * the wait gave up as designed, NS_EINVAL for a bad limit, NS_ECUDA otherwise.
+ */
+int ns_selftest_wait_timeout(int limit_us, void *stream);
 int ns_get_kernel_times(double *ms, int64_t *launches, int n);
 
 #ifdef __cplusplus

@@ -75,6 +75,8 @@ def load_library() -> ctypes.CDLL:
         lib.ns_num_kernel_launches.argtypes = []
         lib.ns_orthogonalize_batched_noalloc.restype = i32
         lib.ns_orthogonalize_batched_noalloc.argtypes = [vp, vp, i32, i32, vp, i32, vp]
+        lib.ns_selftest_wait_timeout.restype = i32
+        lib.ns_selftest_wait_timeout.argtypes = [i32, vp]
         lib.ns_set_kernel_timing.restype = i32
         lib.ns_set_kernel_timing.argtypes = [i32]
         lib.ns_get_kernel_times.restype = i32
@@ -234,3 +236,10 @@ def kernel_times() -> dict:
     if rc != 0:
         raise NSError(rc, "ns_get_kernel_times")
     return {k: (float(ms[i]), int(cnt[i])) for i, k in enumerate(KERNEL_KINDS)}
+
+
+def selftest_wait_timeout(limit_us: int = 20000, stream=None) -> int:
+    """Run the bounded-wait self-test (see include/ns.h); returns its status code."""
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(load_library().ns_selftest_wait_timeout(int(limit_us), ctypes.c_void_p(s.cuda_stream)))

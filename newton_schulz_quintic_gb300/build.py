@@ -17,8 +17,13 @@ from concurrent.futures import ThreadPoolExecutor
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
-BUILD = os.path.join(PKG, "_build")
-LIB = os.path.join(PKG, "libns.so")
+# NS_BUILD_TAG / NS_EXTRA_NVCC_FLAGS build a variant (e.g. a different
+# prefetch depth) next to the default library, as libns_<tag>.so; load it
+# with NS_LIBRARY_PATH.
+_TAG = os.environ.get("NS_BUILD_TAG", "")
+_EXTRA = os.environ.get("NS_EXTRA_NVCC_FLAGS", "").split()
+BUILD = os.path.join(PKG, "_build" + (f"_{_TAG}" if _TAG else ""))
+LIB = os.path.join(PKG, f"libns_{_TAG}.so" if _TAG else "libns.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          f"-I{os.path.join(ROOT, 'include')}", f"-I{CSRC}"]
@@ -53,7 +58,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
 
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.basename(src) + ".o")
-        cmd = [exe, *ARCH, *FLAGS, "-c", src, "-o", obj]
+        cmd = [exe, *ARCH, *FLAGS, *_EXTRA, "-c", src, "-o", obj]
         if ptxas_verbose:
             cmd.insert(1, "-Xptxas=-v")
         r = subprocess.run(cmd, capture_output=True, text=True)

@@ -31,8 +31,10 @@ namespace ns {
 static std::atomic<int64_t> g_launches{0};
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
-// Device status word (one per device, file-scope; see ns_get_status).
+// Device status word (one per device, file-scope; see ns_get_status) and the
+// flag the wait self-test reports through.
 __device__ int g_status_word;
+__device__ int g_probe_word;
 
 namespace {
 
@@ -49,6 +51,7 @@ struct DevInfo {
   bool ok = false;
   int sms = 0;
   int *status = nullptr;
+  int *probe = nullptr;
 };
 std::mutex g_mu;
 std::map<int, DevInfo> g_dev;
@@ -66,6 +69,8 @@ int device_info(DevInfo **out) {
     void *sym = nullptr;
     if (cudaGetSymbolAddress(&sym, g_status_word) != cudaSuccess) return NS_ECUDA;
     di.status = static_cast<int *>(sym);
+    if (cudaGetSymbolAddress(&sym, g_probe_word) != cudaSuccess) return NS_ECUDA;
+    di.probe = static_cast<int *>(sym);
     it = g_dev.emplace(dev, di).first;
   }
   *out = &it->second;
@@ -534,6 +539,24 @@ int ns_release_workspace(void) {
 }
 
 int64_t ns_num_kernel_launches(void) { return g_launches.load(); }
+
+int ns_selftest_wait_timeout(int limit_us, void *stream) {
+  if (limit_us <= 0 || limit_us > 10000000) return NS_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DevInfo *di = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    const int rc = device_info(&di);
+    if (rc) return rc;
+  }
+  int *gave_up = di->probe;
+  if (cudaMemsetAsync(gave_up, 0, sizeof(int), s) != cudaSuccess) return NS_ECUDA;
+  if (launch_wait_probe(di->status, static_cast<uint64_t>(limit_us) * 1000ull, gave_up, s)) return NS_ECUDA;
+  int h = 0;
+  if (cudaMemcpyAsync(&h, gave_up, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return NS_ECUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return NS_ECUDA;
+  return h ? NS_OK : NS_ECUDA;
+}
 
 static void drop_timed() {
   for (auto &t : g_timed) {

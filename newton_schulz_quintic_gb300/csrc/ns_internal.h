@@ -114,6 +114,7 @@ int launch_resident(const ResParams &p, int maxm, int smem_bytes, cudaStream_t s
 int launch_simt_phase(int phase, const PhaseParams &p, cudaStream_t s);
 int launch_tc_phase(int phase, const PhaseParams &p, int max_ctas, cudaStream_t s);
 int tc_smem_bytes();
+int launch_wait_probe(int *status, uint64_t limit_ns, int *gave_up, cudaStream_t s);
 int resident_smem_bytes(int m, int n, int dtype);
 
 void count_launch();

@@ -91,3 +91,9 @@ def test_strerror(lib):
     for code in [0, -1, -2, -3, -4, -5, -6]:
         assert lib.ns_strerror(code)
     assert b"unknown" in lib.ns_strerror(-99)
+
+
+def test_selftest_rejects_bad_limits_before_launch(lib):
+    assert lib.ns_selftest_wait_timeout(0, None) == -1
+    assert lib.ns_selftest_wait_timeout(-5, None) == -1
+    assert lib.ns_selftest_wait_timeout(20000000, None) == -1

@@ -2,20 +2,23 @@
 //
 // One persistent, warp-specialised kernel per phase, launched as clusters of
 // two CTAs over a cost-ordered list of 256 x 256 output tiles drawn from
-// every matrix of the batch. CTA rank r of a cluster computes the tile's rows
-// r*128 .. r*128+127; both CTAs need the same 256 rows of the second operand,
-// so each loads one 128-row half and multicasts it to both.
-//   warp 0      TMA producer: its own 128x64 box of the first operand and one
-//               128x64 half of the second (multicast to the pair) per k-block
-//               into a 4-stage shared-memory ring (128-byte swizzle); a stage
-//               is refilled only after both CTAs' MMAs have released it;
-//   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators)
-//               and, from one thread, issues tcgen05.mma (M=128, N=256,
-//               K=16, bf16 in, fp32 accumulate) and tcgen05.commit;
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator, the fused
-//               element-wise step in fp32, round-to-nearest-even to bf16 and
-//               the stores; the second accumulator lets the next tile's
-//               main loop overlap this epilogue.
+// every matrix of the batch. Each tile is one pair MMA
+// (tcgen05.mma.cta_group::2, M = 256, N = 256, K = 16, bf16 in, fp32
+// accumulate) issued by the pair's leader CTA (rank 0): CTA rank r holds
+// rows r*128 .. r*128+127 of the first operand and rows r*128 .. r*128+127 of
+// the second in its own shared memory, and receives rows r*128 .. of the
+// 256 x 256 accumulator in its own TMEM. No operand byte is loaded twice.
+//   warp 0      TMA producer (both CTAs): its 128x64 box of each operand per
+//               k-block into a 6-stage ring of 32 KB (128-byte swizzle); the
+//               bytes of both CTAs are counted on the leader's full barrier;
+//   warp 1      TMEM allocation (512 columns = two accumulators, cta_group::2)
+//               in both CTAs; in the leader one thread issues the pair MMAs and
+//               the commits that release stages and hand accumulators to both
+//               CTAs' epilogues;
+//   warps 2..5  epilogue (both CTAs): tcgen05.ld of its 128 accumulator rows,
+//               the fused element-wise step in fp32, round-to-nearest-even to
+//               bf16 and the stores; the second accumulator lets the next
+//               tile's main loop overlap this epilogue.
 // Phases (all operands K-major, see ns_internal.h for the layout):
 //   0 gram    A = W W^T             upper-triangle tiles; stores tile + mirror
 //   1 square  B = b A + c (A A)     upper-triangle tiles; stores tile + mirror
@@ -33,19 +36,21 @@ namespace ns {
 
 namespace {
 
-constexpr int kStages = 4;
-constexpr int kABytes = kTcBM * kTcBK * 2;  // 16 KB
-constexpr int kBBytes = kTcBN * kTcBK * 2;  // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kTmemCols = 2 * kTcBN;        // two accumulators
 constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
+constexpr int kStages = 6;
+constexpr int kABytes = kTcBM * kTcBK * 2;          // 16 KB: this CTA's 128 rows of the first operand
+constexpr int kBBytes = (kTcBN / 2) * kTcBK * 2;    // 16 KB: this CTA's half of the second operand
+constexpr int kStageBytes = kABytes + kBBytes;      // 32 KB per CTA
+constexpr int kPairStageBytes = 2 * kStageBytes;    // both CTAs' loads, counted at the leader
+constexpr int kAccs = 2;                            // accumulators (each kTcBN TMEM columns)
+constexpr int kTmemCols = kAccs * kTcBN;
 
 struct Barriers {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
-  uint64_t tfull[2];
-  uint64_t tempty[2];
+  uint64_t full[kStages];   // leader: both CTAs' loads of a stage landed
+  uint64_t empty[kStages];  // each CTA: the leader's MMAs are done with a stage
+  uint64_t tfull[2];        // each CTA: an accumulator is ready
+  uint64_t tempty[2];       // leader: both epilogues are done with an accumulator
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -94,22 +99,47 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16 *dst, const float (&v)
   }
 }
 
-__device__ __forceinline__ void load_row32(const __nv_bfloat16 *src, float (&v)[32]) {
-  const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+__device__ __forceinline__ void unpack_row32(const uint4 (&w4)[4], float (&v)[32]) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const uint4 w = s4[q];
-    const __nv_bfloat16 *e = reinterpret_cast<const __nv_bfloat16 *>(&w);
+    const __nv_bfloat16 *e = reinterpret_cast<const __nv_bfloat16 *>(&w4[q]);
 #pragma unroll
     for (int u = 0; u < 8; ++u) v[8 * q + u] = __bfloat162float(e[u]);
   }
 }
 
+// The global operand an epilogue chunk reads besides the accumulator (A for
+// square, W^T for apply), fetched ahead of time: 32 bf16 of this thread's
+// row when the whole chunk is in range (the common case); edge chunks are
+// read element by element inside epilogue_chunk instead. Both tensors are
+// read-only during the launch.
+template <int PHASE>
+__device__ __forceinline__ void prefetch_chunk(const PhaseParams &p, const TileInfo &ti, int r, int chunk,
+                                               uint4 (&out)[4]) {
+  if (PHASE == 0) return;
+  const MatDesc &d = *ti.d;
+  const uint4 *src = nullptr;
+  if (PHASE == 1) {
+    const int i = ti.row0 + r, jb = ti.col0 + chunk * 32;
+    if (i < d.m && jb >= i && jb + 32 <= d.m)
+      src = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(d.a) + static_cast<size_t>(i) * d.pm + jb);
+  } else {
+    const int jr = ti.row0 + r, ib = ti.col0 + chunk * 32;
+    if (jr < d.n && ib + 32 <= d.m)
+      src = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(d.xt[p.step & 1]) +
+                                            static_cast<size_t>(jr) * d.pm + ib);
+  }
+  if (src) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) out[q] = __ldg(src + q);
+  }
+}
+
 // Epilogue of one 32-column chunk held by one thread: tile row r, columns
-// chunk*32 .. chunk*32+31 of the tile.
+// chunk*32 .. chunk*32+31 of the tile; `pre` is prefetch_chunk's result.
 template <int PHASE>
 __device__ __forceinline__ void epilogue_chunk(const PhaseParams &p, const TileInfo &ti, int r, int chunk,
-                                               const uint32_t (&raw)[32]) {
+                                               const uint32_t (&raw)[32], const uint4 (&pre)[4]) {
   const MatDesc &d = *ti.d;
   float f[32];
 #pragma unroll
@@ -125,7 +155,7 @@ __device__ __forceinline__ void epilogue_chunk(const PhaseParams &p, const TileI
       const __nv_bfloat16 *A = static_cast<const __nv_bfloat16 *>(d.a) + static_cast<size_t>(i) * pm + jb;
       float aold[32];
       if (full) {
-        load_row32(A, aold);
+        unpack_row32(pre, aold);
       } else {
 #pragma unroll
         for (int t = 0; t < 32; ++t) {
@@ -162,7 +192,7 @@ __device__ __forceinline__ void epilogue_chunk(const PhaseParams &p, const TileI
     const __nv_bfloat16 *XT = static_cast<const __nv_bfloat16 *>(d.xt[cur]) + static_cast<size_t>(jr) * pm + ib;
     float xo[32];
     if (full) {
-      load_row32(XT, xo);
+      unpack_row32(pre, xo);
     } else {
 #pragma unroll
       for (int t = 0; t < 32; ++t) xo[t] = (ib + t < m) ? __bfloat162float(XT[t]) : 0.f;
@@ -217,6 +247,8 @@ __device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity, int *
   }
 }
 
+
+
 template <int PHASE>
 __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_constant__ PhaseParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -225,41 +257,46 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
   uint8_t *sB = smem + kStages * kABytes;
   Barriers *bar = reinterpret_cast<Barriers *>(smem + kStages * kStageBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();             // 0 or 1 within the pair
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
   const int cluster = blockIdx.x / kTcCluster;
   const int nclusters = gridDim.x / kTcCluster;
-  const int my_rows = static_cast<int>(rank) * kTcBM;  // this CTA's offset inside a pair tile
+  const int my_rows = static_cast<int>(rank) * kTcBM;
   constexpr uint16_t kPairMask = (1u << kTcCluster) - 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bar->full[s], 1);
-      mbar_init(&bar->empty[s], kTcCluster);  // released by both CTAs' MMAs
+      mbar_init(&bar->empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&bar->tfull[a], 1);
-      mbar_init(&bar->tempty[a], kEpiThreads);
+      mbar_init(&bar->tempty[a], kTcCluster * kEpiThreads);
     }
     mbar_init(&bar->drain, 1);
     bar->abort = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&bar->tmem_base, kTmemCols);
-    tmem_relinquish();
+    tmem_alloc_pair(&bar->tmem_base, kTmemCols);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
-  // the peer may multicast into this CTA's ring only after its barriers exist
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem = bar->tmem_base;
+  // the pair MMA writes the same TMEM columns in both CTAs: check that both
+  // allocations agree before using them
+  const uint32_t peer_tmem = ld_shared_cluster_u32(mapa_shared(smem_u32(&bar->tmem_base), rank ^ 1u));
+  const bool tmem_ok = peer_tmem == tmem;
+  if (!tmem_ok && threadIdx.x == 0) set_status(p.status, kStatusTmemMismatch);
   volatile int *abort = &bar->abort;
   const int cur = p.step & 1;
 
-  if (warp == 0) {
+  if (tmem_ok && warp == 0) {
     if (lane == 0) {
-      // ---------------------------------------------------- TMA producer
+      // ---------------------------------------------------- TMA producer (both CTAs)
       const uint64_t pol = l2_policy_evict_normal();
       int issued_phase[kStages];
       for (int s = 0; s < kStages; ++s) issued_phase[s] = -1;
@@ -272,18 +309,16 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
         const void *mapA = PHASE == 0 ? &ti.d->tm_x : PHASE == 1 ? &ti.d->tm_a : &ti.d->tm_xt[cur];
         const void *mapB = PHASE == 0 ? &ti.d->tm_x : PHASE == 1 ? &ti.d->tm_a : &ti.d->tm_b;
         for (int kb = 0; kb < ti.nk; ++kb) {
-          // both CTAs' MMAs must be done with this stage: the B half loaded
-          // here also lands in the peer's ring
-          if (!mbar_wait(&bar->empty[stage], phase ^ 1u, abort, p.status)) {
+          if (!mbar_wait<true>(&bar->empty[stage], phase ^ 1u, abort, p.status)) {
             ok = false;
             break;
           }
-          // 16 KB own A box + 16 KB own B half + 16 KB B half from the peer
-          mbar_arrive_expect_tx(&bar->full[stage], kStageBytes);
+          if (leader) mbar_arrive_expect_tx(&bar->full[stage], kPairStageBytes);
+          const uint32_t full_leader = mapa_shared(smem_u32(&bar->full[stage]), 0);
           const int kx = kb * kTcBK;
-          tma_load_2d(sA + stage * kABytes, mapA, kx, ti.row0 + my_rows, &bar->full[stage], pol);
-          tma_load_2d_multicast(sB + stage * kBBytes + rank * (kBBytes / 2), mapB, kx,
-                                ti.col0 + static_cast<int>(rank) * kTcBM, &bar->full[stage], kPairMask, pol);
+          tma_load_2d_pair(sA + stage * kABytes, mapA, kx, ti.row0 + my_rows, full_leader, pol);
+          tma_load_2d_pair(sB + stage * kBBytes, mapB, kx, ti.col0 + static_cast<int>(rank) * (kTcBN / 2),
+                           full_leader, pol);
           issued_phase[stage] = static_cast<int>(phase);
           if (++stage == kStages) {
             stage = 0;
@@ -291,16 +326,15 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
           }
         }
       }
-      if (!ok) {
-        // make sure no copy is still landing in shared memory
+      if (!ok && leader) {
         for (int s = 0; s < kStages; ++s)
           if (issued_phase[s] >= 0) mbar_drain(&bar->full[s], static_cast<uint32_t>(issued_phase[s]), p.status);
       }
     }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------------------------------------------- MMA issuer
-      constexpr uint32_t idesc = umma_idesc_bf16(kTcBM, kTcBN);
+  } else if (tmem_ok && warp == 1) {
+    if (lane == 0 && leader) {
+      // ---------------------------------------------------- pair MMA issuer (leader)
+      constexpr uint32_t idesc = umma_idesc_bf16(kTcCluster * kTcBM, kTcBN);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -309,11 +343,11 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
       for (int t = cluster; t < p.ntiles && ok; t += nclusters) {
         const TileInfo ti = tile_info<PHASE>(p, t);
         if (ti.skip) continue;
-        if (!mbar_wait(&bar->tempty[acc], acc_phase ^ 1u, abort, p.status)) break;
+        if (!mbar_wait<true>(&bar->tempty[acc], acc_phase ^ 1u, abort, p.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * kTcBN);
         for (int kb = 0; kb < ti.nk; ++kb) {
-          if (!mbar_wait(&bar->full[stage], phase, abort, p.status)) {
+          if (!mbar_wait<true>(&bar->full[stage], phase, abort, p.status)) {
             ok = false;
             break;
           }
@@ -322,60 +356,81 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
           const uint32_t b_addr = smem_u32(sB + stage * kBBytes);
 #pragma unroll
           for (int k = 0; k < kTcBK / 16; ++k) {
-            umma_bf16(d_tmem, sw128_kmajor_desc(a_addr + k * 32), sw128_kmajor_desc(b_addr + k * 32), idesc,
-                      (kb | k) != 0 ? 1u : 0u);
+            umma_bf16_pair(d_tmem, sw128_kmajor_desc(a_addr + k * 32), sw128_kmajor_desc(b_addr + k * 32), idesc,
+                           (kb | k) != 0 ? 1u : 0u);
           }
-          umma_commit_multicast(&bar->empty[stage], kPairMask);  // release the stage in both CTAs
+          umma_commit_pair_multicast(&bar->empty[stage], kPairMask);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        umma_commit(&bar->tfull[acc]);
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
+        umma_commit_pair_multicast(&bar->tfull[acc], kPairMask);
+        if (++acc == kAccs) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
       }
-      // no MMA may still be running when TMEM is released
-      umma_commit(&bar->drain);
+      umma_commit_pair_multicast(&bar->drain, 1u);
       mbar_drain(&bar->drain, 0, p.status);
     }
-  } else {
-    // ------------------------------------------------------ epilogue
-    const int q = warp & 3;         // TMEM lane quarter this warp may access
-    const int r = q * 32 + lane;    // tile row held by this thread
+  } else if (tmem_ok) {
+    // ------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = cluster; t < p.ntiles; t += nclusters) {
       TileInfo ti = tile_info<PHASE>(p, t);
       if (ti.skip) continue;
       ti.row0 += my_rows;
-      if (!mbar_wait(&bar->tfull[acc], acc_phase, abort, p.status)) break;
+      // the epilogue's global operand does not depend on the accumulator:
+      // start fetching it while this tile's MMAs still run
+      uint4 pre[2][4] = {};
+      prefetch_chunk<PHASE>(p, ti, r, 0, pre[0]);
+      prefetch_chunk<PHASE>(p, ti, r, 1, pre[1]);
+      if (!mbar_wait<true>(&bar->tfull[acc], acc_phase, abort, p.status)) break;
       tc_fence_after();
       const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kTcBN);
-#pragma unroll 1
+      // TMEM loads double-buffered: chunk c+1 is read while chunk c is stored
+      uint32_t va[32], vb[32];
+      __syncwarp();
+      tmem_ld32(tbase, va);
+      tmem_ld_wait(va);
+#pragma unroll
       for (int c = 0; c < kTcBN / 32; ++c) {
-        uint32_t v[32];
-        __syncwarp();
-        tmem_ld32(tbase + static_cast<uint32_t>(c * 32), v);
-        tmem_ld_wait(v);
-        epilogue_chunk<PHASE>(p, ti, r, c, v);
+        uint32_t(&cur_v)[32] = (c & 1) ? vb : va;
+        uint32_t(&next_v)[32] = (c & 1) ? va : vb;
+        if (c + 1 < kTcBN / 32) {
+          __syncwarp();
+          tmem_ld32(tbase + static_cast<uint32_t>((c + 1) * 32), next_v);
+        }
+        uint4 px[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) px[u] = pre[c & 1][u];
+        if (c + 2 < kTcBN / 32) prefetch_chunk<PHASE>(p, ti, r, c + 2, pre[c & 1]);
+        epilogue_chunk<PHASE>(p, ti, r, c, cur_v, px);
+        if (c + 1 < kTcBN / 32) {
+          __syncwarp();
+          tmem_ld_wait(next_v);
+        }
       }
       tc_fence_before();
-      mbar_arrive(&bar->tempty[acc]);
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
+      mbar_arrive_cluster(mapa_shared(smem_u32(&bar->tempty[acc]), 0));
+      if (++acc == kAccs) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
     }
   }
 
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  // the peer's multicast copies and MMA commits target this CTA's shared
-  // memory until it is done: leave together
   cluster_sync();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if (warp == 1) tmem_dealloc_pair(tmem, kTmemCols);
 }
 
 template <int PHASE>
@@ -417,7 +472,9 @@ int launch_phase_t(const PhaseParams &p, int max_ctas, cudaStream_t s) {
 
 }  // namespace
 
-int tc_smem_bytes() { return 1024 + kStages * kStageBytes + static_cast<int>(sizeof(Barriers)); }
+int tc_smem_bytes() {
+  return 1024 + kStages * kStageBytes + static_cast<int>(sizeof(Barriers));
+}
 
 int launch_tc_phase(int phase, const PhaseParams &p, int max_ctas, cudaStream_t s) {
   if (p.ntiles <= 0) return 0;

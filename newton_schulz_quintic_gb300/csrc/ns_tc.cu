@@ -36,8 +36,15 @@ namespace ns {
 
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kEpiThreads = 128;
+constexpr int kEpiWarps = 8;                        // two per TMEM lane quarter
+constexpr int kThreads = 64 + 32 * kEpiWarps;       // producer warp, MMA warp, epilogue warps
+constexpr int kChunksPerWarp = (kTcBN / 32) / (kEpiWarps / 4);
+// per-warp staging tile of the epilogue's coalesced stores: 32 rows of 32 bf16
+// (16 words + 4 pad), or 16 rows of 32 packed bf16 pairs (32 words + 4 pad)
+constexpr int kRowStageWords = 20;
+constexpr int kPairStageWords = 36;
+constexpr int kEpiStageBytes = 32 * kRowStageWords * 4;
+static_assert(16 * kPairStageWords * 4 <= kEpiStageBytes, "staging tile too small");
 constexpr int kStages = 6;
 constexpr int kABytes = kTcBM * kTcBK * 2;          // 16 KB: this CTA's 128 rows of the first operand
 constexpr int kBBytes = (kTcBN / 2) * kTcBK * 2;    // 16 KB: this CTA's half of the second operand
@@ -50,11 +57,13 @@ struct Barriers {
   uint64_t full[kStages];   // leader: both CTAs' loads of a stage landed
   uint64_t empty[kStages];  // each CTA: the leader's MMAs are done with a stage
   uint64_t tfull[2];        // each CTA: an accumulator is ready
-  uint64_t tempty[2];       // leader: both epilogues are done with an accumulator
+  uint64_t tempty[2];       // leader: every epilogue warp of both CTAs is done with an accumulator
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
 };
+
+constexpr int kBarrierBytes = (static_cast<int>(sizeof(Barriers)) + 127) / 128 * 128;
 
 struct TileInfo {
   const MatDesc *d;
@@ -86,19 +95,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t *>(&v);
 }
 
-__device__ __forceinline__ void store_row32(__nv_bfloat16 *dst, const float (&v)[32]) {
-  uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint4 w;
-    w.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
-    w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
-    w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
-    w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
-    d4[q] = w;
-  }
-}
-
 __device__ __forceinline__ void unpack_row32(const uint4 (&w4)[4], float (&v)[32]) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
@@ -106,6 +102,88 @@ __device__ __forceinline__ void unpack_row32(const uint4 (&w4)[4], float (&v)[32
 #pragma unroll
     for (int u = 0; u < 8; ++u) v[8 * q + u] = __bfloat162float(e[u]);
   }
+}
+
+// Writes 8 bf16 (one 16-byte word, `o`) at dst = row R, columns C0..C0+7,
+// keeping only elements with column < col_lim and, when upper, column >= R.
+__device__ __forceinline__ void store_piece8(__nv_bfloat16 *dst, const uint4 &o, int R, int C0, int col_lim,
+                                             bool upper) {
+  const bool all = (C0 + 8 <= col_lim) && (!upper || C0 >= R) && ((reinterpret_cast<uintptr_t>(dst) & 15) == 0);
+  if (all) {
+    *reinterpret_cast<uint4 *>(dst) = o;
+    return;
+  }
+  const uint32_t w[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const int C = C0 + e;
+    if (C < col_lim && (!upper || C >= R))
+      dst[e] = __ushort_as_bfloat16(static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1))));
+  }
+}
+
+// Warp-cooperative store of a 32 x 32 block held one row per lane: lane l
+// holds v[t] = element (row row0 + l, column col0 + t). The rows go through
+// the warp's staging tile so that each store instruction writes 8 rows x 64
+// contiguous bytes (4 lanes per row). Elements are written only where
+// row < row_lim, column < col_lim and, if upper, column >= row.
+__device__ __forceinline__ void warp_store_rows(uint32_t *stage, const float (&v)[32], __nv_bfloat16 *base,
+                                                size_t pitch, int row0, int row_lim, int col0, int col_lim,
+                                                bool upper) {
+  const int lane = threadIdx.x & 31;
+  uint4 *srow = reinterpret_cast<uint4 *>(stage + lane * kRowStageWords);
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    srow[q] = make_uint4(pack_bf16x2(v[8 * q + 0], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                         pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+  __syncwarp();
+  const int piece = lane & 3;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int rl = 8 * k + (lane >> 2);
+    const int R = row0 + rl;
+    if (R < row_lim) {
+      const uint4 o = reinterpret_cast<const uint4 *>(stage + rl * kRowStageWords)[piece];
+      store_piece8(base + static_cast<size_t>(R) * pitch + col0 + 8 * piece, o, R, col0 + 8 * piece, col_lim, upper);
+    }
+  }
+  __syncwarp();
+}
+
+// Warp-cooperative transposed store of a 32 x 32 block: lane l holds v[t] =
+// element (row row0 + t, column col0 + l). The block goes through the staging
+// tile as bf16 pairs so that each store instruction writes 8 output rows x 64
+// contiguous bytes. Elements are written only where row < row_lim,
+// column < col_lim and, if strict_lower, column < row.
+__device__ __forceinline__ void warp_store_transposed(uint32_t *stage, const float (&v)[32], __nv_bfloat16 *base,
+                                                      size_t pitch, int row0, int row_lim, int col0, int col_lim,
+                                                      bool strict_lower) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) stage[k * kPairStageWords + lane] = pack_bf16x2(v[2 * k], v[2 * k + 1]);
+  __syncwarp();
+  const int piece = lane & 3;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int t = 8 * k + (lane >> 2);  // output row row0 + t
+    const int R = row0 + t;
+    if (R < row_lim) {
+      const uint4 *src = reinterpret_cast<const uint4 *>(stage + (t >> 1) * kPairStageWords + 8 * piece);
+      const uint4 a = src[0], b = src[1];
+      const uint32_t sel = (t & 1) ? 0x7632u : 0x5410u;  // high or low bf16 of each pair
+      const uint4 o = make_uint4(__byte_perm(a.x, a.y, sel), __byte_perm(a.z, a.w, sel), __byte_perm(b.x, b.y, sel),
+                                 __byte_perm(b.z, b.w, sel));
+      const int C0 = col0 + 8 * piece;
+      __nv_bfloat16 *dst = base + static_cast<size_t>(R) * pitch + C0;
+      if (!strict_lower) {
+        store_piece8(dst, o, R, C0, col_lim, false);
+      } else {
+        // column < row: same as column <= row - 1
+        store_piece8(dst, o, R, C0, col_lim < R ? col_lim : R, false);
+      }
+    }
+  }
+  __syncwarp();
 }
 
 // The global operand an epilogue chunk reads besides the accumulator (A for
@@ -129,18 +207,17 @@ __device__ __forceinline__ void prefetch_chunk(const PhaseParams &p, const TileI
       src = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(d.xt[p.step & 1]) +
                                             static_cast<size_t>(jr) * d.pm + ib);
   }
-  if (src) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) out[q] = __ldg(src + q);
-  }
+  for (int q = 0; q < 4; ++q) out[q] = src ? __ldg(src + q) : make_uint4(0, 0, 0, 0);
 }
 
 // Epilogue of one 32-column chunk held by one thread: tile row r, columns
 // chunk*32 .. chunk*32+31 of the tile; `pre` is prefetch_chunk's result.
 template <int PHASE>
 __device__ __forceinline__ void epilogue_chunk(const PhaseParams &p, const TileInfo &ti, int r, int chunk,
-                                               const uint32_t (&raw)[32], const uint4 (&pre)[4]) {
+                                               const uint32_t (&raw)[32], const uint4 (&pre)[4], uint32_t *stage) {
   const MatDesc &d = *ti.d;
+  const int r0 = r & ~31;  // the warp's first tile row
   float f[32];
 #pragma unroll
   for (int t = 0; t < 32; ++t) f[t] = __uint_as_float(raw[t]);
@@ -148,8 +225,11 @@ __device__ __forceinline__ void epilogue_chunk(const PhaseParams &p, const TileI
   if (PHASE == 0 || PHASE == 1) {
     const int m = d.m, pm = d.pm;
     const int i = ti.row0 + r;
+    const int i0 = ti.row0 + r0;
     const int jb = ti.col0 + chunk * 32;
-    if (i >= m || jb + 31 < i) return;
+    // warp-uniform: the whole 32x32 block is outside the matrix or below the diagonal
+    if (i0 >= m || jb + 31 < i0) return;
+    const bool mine = i < m && jb + 31 >= i;  // this lane's row has elements with j >= i
     const bool full = (jb >= i) && (jb + 32 <= m);
     if (PHASE == 1) {
       const __nv_bfloat16 *A = static_cast<const __nv_bfloat16 *>(d.a) + static_cast<size_t>(i) * pm + jb;
@@ -160,33 +240,23 @@ __device__ __forceinline__ void epilogue_chunk(const PhaseParams &p, const TileI
 #pragma unroll
         for (int t = 0; t < 32; ++t) {
           const int j = jb + t;
-          aold[t] = (j >= i && j < m) ? __bfloat162float(A[t]) : 0.f;
+          aold[t] = (mine && j >= i && j < m) ? __bfloat162float(A[t]) : 0.f;
         }
       }
 #pragma unroll
       for (int t = 0; t < 32; ++t) f[t] = p.cb * aold[t] + p.cc * f[t];
     }
     __nv_bfloat16 *O = static_cast<__nv_bfloat16 *>(PHASE == 0 ? d.a : d.b);
-    if (full) {
-      store_row32(O + static_cast<size_t>(i) * pm + jb, f);
-    } else {
-#pragma unroll
-      for (int t = 0; t < 32; ++t) {
-        const int j = jb + t;
-        if (j >= i && j < m) O[static_cast<size_t>(i) * pm + j] = __float2bfloat16_rn(f[t]);
-      }
-    }
-    // mirror: O[j, i] for j > i (consecutive lanes hold consecutive i)
-#pragma unroll
-    for (int t = 0; t < 32; ++t) {
-      const int j = jb + t;
-      if (j > i && j < m) O[static_cast<size_t>(j) * pm + i] = __float2bfloat16_rn(f[t]);
-    }
+    // O[i, j] for j >= i, and the mirror O[j, i] for j > i
+    warp_store_rows(stage, f, O, pm, i0, m, jb, m, true);
+    warp_store_transposed(stage, f, O, pm, jb, m, i0, m, true);
   } else {
     const int m = d.m, n = d.n, pm = d.pm, pn = d.pn;
     const int jr = ti.row0 + r;          // row of W^T (index over n)
+    const int jr0 = ti.row0 + r0;        // the warp's first row
     const int ib = ti.col0 + chunk * 32; // column of W^T (index over m)
-    if (jr >= n || ib >= m) return;
+    if (jr0 >= n || ib >= m) return;     // warp-uniform
+    const bool mine = jr < n;
     const int cur = p.step & 1;
     const bool full = ib + 32 <= m;
     const __nv_bfloat16 *XT = static_cast<const __nv_bfloat16 *>(d.xt[cur]) + static_cast<size_t>(jr) * pm + ib;
@@ -195,42 +265,21 @@ __device__ __forceinline__ void epilogue_chunk(const PhaseParams &p, const TileI
       unpack_row32(pre, xo);
     } else {
 #pragma unroll
-      for (int t = 0; t < 32; ++t) xo[t] = (ib + t < m) ? __bfloat162float(XT[t]) : 0.f;
+      for (int t = 0; t < 32; ++t) xo[t] = (mine && ib + t < m) ? __bfloat162float(XT[t]) : 0.f;
     }
 #pragma unroll
     for (int t = 0; t < 32; ++t) f[t] = p.ca * xo[t] + f[t];
 
     if (!p.final_step) {
-      __nv_bfloat16 *XTn = static_cast<__nv_bfloat16 *>(d.xt[cur ^ 1]) + static_cast<size_t>(jr) * pm + ib;
-      if (full) {
-        store_row32(XTn, f);
-      } else {
-#pragma unroll
-        for (int t = 0; t < 32; ++t)
-          if (ib + t < m) XTn[t] = __float2bfloat16_rn(f[t]);
-      }
-      __nv_bfloat16 *X = static_cast<__nv_bfloat16 *>(d.x);
-#pragma unroll
-      for (int t = 0; t < 32; ++t)
-        if (ib + t < m) X[static_cast<size_t>(ib + t) * pn + jr] = __float2bfloat16_rn(f[t]);
+      // W'^T rows jr (this warp's rows) and W' rows ib + t
+      warp_store_rows(stage, f, static_cast<__nv_bfloat16 *>(d.xt[cur ^ 1]), pm, jr0, n, ib, m, false);
+      warp_store_transposed(stage, f, static_cast<__nv_bfloat16 *>(d.x), pn, ib, m, jr0, n, false);
     } else {
       __nv_bfloat16 *U = static_cast<__nv_bfloat16 *>(d.user);
-      if (d.transposed) {
-        // caller's Y is n x m: row jr, columns ib..ib+31
-        __nv_bfloat16 *dst = U + static_cast<size_t>(jr) * d.N + ib;
-        if (full && ((reinterpret_cast<uintptr_t>(dst) & 15) == 0)) {
-          store_row32(dst, f);
-        } else {
-#pragma unroll
-          for (int t = 0; t < 32; ++t)
-            if (ib + t < m) dst[t] = __float2bfloat16_rn(f[t]);
-        }
-      } else {
-        // caller's Y is m x n: column jr of rows ib..ib+31
-#pragma unroll
-        for (int t = 0; t < 32; ++t)
-          if (ib + t < m) U[static_cast<size_t>(ib + t) * d.N + jr] = __float2bfloat16_rn(f[t]);
-      }
+      if (d.transposed)  // caller's Y is n x m: rows jr, columns ib..
+        warp_store_rows(stage, f, U, static_cast<size_t>(d.N), jr0, n, ib, m, false);
+      else               // caller's Y is m x n: rows ib + t, columns jr0..
+        warp_store_transposed(stage, f, U, static_cast<size_t>(d.N), ib, m, jr0, n, false);
     }
   }
 }
@@ -256,6 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
   uint8_t *sA = smem;
   uint8_t *sB = smem + kStages * kABytes;
   Barriers *bar = reinterpret_cast<Barriers *>(smem + kStages * kStageBytes);
+  uint32_t *epi_stage = reinterpret_cast<uint32_t *>(smem + kStages * kStageBytes + kBarrierBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
   const bool leader = rank == 0;
@@ -271,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&bar->tfull[a], 1);
-      mbar_init(&bar->tempty[a], kTcCluster * kEpiThreads);
+      mbar_init(&bar->tempty[a], kTcCluster * kEpiWarps);  // one arrival per epilogue warp
     }
     mbar_init(&bar->drain, 1);
     bar->abort = 0;
@@ -377,8 +427,13 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
     }
   } else if (tmem_ok) {
     // ------------------------------------------------------ epilogue (both CTAs)
+    // warps 2..9: TMEM lane quarter q = warp % 4 (tile rows q*32 .. q*32+31),
+    // column half h: chunks h*kChunksPerWarp .. of the 256 accumulator columns
+    const int e = warp - 2;
     const int q = warp & 3;
     const int r = q * 32 + lane;
+    const int c0 = (e / 4) * kChunksPerWarp;
+    uint32_t *stage = epi_stage + e * (kEpiStageBytes / 4);
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = cluster; t < p.ntiles; t += nclusters) {
@@ -388,36 +443,38 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
       // the epilogue's global operand does not depend on the accumulator:
       // start fetching it while this tile's MMAs still run
       uint4 pre[2][4] = {};
-      prefetch_chunk<PHASE>(p, ti, r, 0, pre[0]);
-      prefetch_chunk<PHASE>(p, ti, r, 1, pre[1]);
+      prefetch_chunk<PHASE>(p, ti, r, c0, pre[0]);
+      prefetch_chunk<PHASE>(p, ti, r, c0 + 1, pre[1]);
       if (!mbar_wait<true>(&bar->tfull[acc], acc_phase, abort, p.status)) break;
       tc_fence_after();
       const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kTcBN);
       // TMEM loads double-buffered: chunk c+1 is read while chunk c is stored
       uint32_t va[32], vb[32];
       __syncwarp();
-      tmem_ld32(tbase, va);
+      tmem_ld32(tbase + static_cast<uint32_t>(c0 * 32), va);
       tmem_ld_wait(va);
 #pragma unroll
-      for (int c = 0; c < kTcBN / 32; ++c) {
-        uint32_t(&cur_v)[32] = (c & 1) ? vb : va;
-        uint32_t(&next_v)[32] = (c & 1) ? va : vb;
-        if (c + 1 < kTcBN / 32) {
+      for (int k = 0; k < kChunksPerWarp; ++k) {
+        const int c = c0 + k;
+        uint32_t(&cur_v)[32] = (k & 1) ? vb : va;
+        uint32_t(&next_v)[32] = (k & 1) ? va : vb;
+        if (k + 1 < kChunksPerWarp) {
           __syncwarp();
           tmem_ld32(tbase + static_cast<uint32_t>((c + 1) * 32), next_v);
         }
         uint4 px[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) px[u] = pre[c & 1][u];
-        if (c + 2 < kTcBN / 32) prefetch_chunk<PHASE>(p, ti, r, c + 2, pre[c & 1]);
-        epilogue_chunk<PHASE>(p, ti, r, c, cur_v, px);
-        if (c + 1 < kTcBN / 32) {
+        for (int u = 0; u < 4; ++u) px[u] = pre[k & 1][u];
+        if (k + 2 < kChunksPerWarp) prefetch_chunk<PHASE>(p, ti, r, c + 2, pre[k & 1]);
+        epilogue_chunk<PHASE>(p, ti, r, c, cur_v, px, stage);
+        if (k + 1 < kChunksPerWarp) {
           __syncwarp();
           tmem_ld_wait(next_v);
         }
       }
       tc_fence_before();
-      mbar_arrive_cluster(mapa_shared(smem_u32(&bar->tempty[acc]), 0));
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&bar->tempty[acc]), 0));
       if (++acc == kAccs) {
         acc = 0;
         acc_phase ^= 1u;
@@ -472,9 +529,7 @@ int launch_phase_t(const PhaseParams &p, int max_ctas, cudaStream_t s) {
 
 }  // namespace
 
-int tc_smem_bytes() {
-  return 1024 + kStages * kStageBytes + static_cast<int>(sizeof(Barriers));
-}
+int tc_smem_bytes() { return 1024 + kStages * kStageBytes + kBarrierBytes + kEpiWarps * kEpiStageBytes; }
 
 int launch_tc_phase(int phase, const PhaseParams &p, int max_ctas, cudaStream_t s) {
   if (p.ntiles <= 0) return 0;

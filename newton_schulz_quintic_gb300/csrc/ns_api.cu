@@ -287,7 +287,20 @@ struct CachedWs {
   size_t bytes = 0;
   std::vector<uint8_t> last_blob;  // blob currently resident at ptr
 };
-std::map<std::pair<int, cudaStream_t>, CachedWs> g_ws;
+// keyed by (device, stream, slot): slot 0 serves the device entry points,
+// slot 1 holds the host entry point's device copies, slot 2 + g the workspace
+// of its g-th pipeline group
+struct WsKey {
+  int dev;
+  cudaStream_t stream;
+  int slot;
+  bool operator<(const WsKey &o) const {
+    if (dev != o.dev) return dev < o.dev;
+    if (stream != o.stream) return stream < o.stream;
+    return slot < o.slot;
+  }
+};
+std::map<WsKey, CachedWs> g_ws;
 
 int ensure_ws(CachedWs &c, size_t bytes, cudaStream_t s) {
   if (c.ptr && c.bytes >= bytes) return NS_OK;
@@ -384,7 +397,7 @@ int execute(const Layout &L, uint8_t *ws, int steps, const float *co, float eps,
 }
 
 int run(void *const *X, const int64_t *shapes, int count, int steps, const float *coeffs, float eps, int dtype,
-        void *user_ws, size_t user_ws_bytes, cudaStream_t s) {
+        void *user_ws, size_t user_ws_bytes, cudaStream_t s, int slot = 0) {
   int rc = validate(X, shapes, count, steps, dtype, true);
   if (rc) return rc;
   if (!(eps >= 0.f)) return NS_EINVAL;
@@ -408,7 +421,7 @@ int run(void *const *X, const int64_t *shapes, int count, int steps, const float
   } else {
     int dev = 0;
     cudaGetDevice(&dev);
-    cache = &g_ws[{dev, s}];
+    cache = &g_ws[WsKey{dev, s, slot}];
     rc = ensure_ws(*cache, L.total, s);
     if (rc) return rc;
     ws = cache->ptr;
@@ -420,6 +433,27 @@ int run(void *const *X, const int64_t *shapes, int count, int steps, const float
     if (cache) cache->last_blob = blob;
   }
   return execute(L, ws, steps, co, eps, di, s);
+}
+
+// ------------------------------------------------------------ host pipeline
+// Streams and events of the host entry point, created once per device.
+struct HostPipe {
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  std::vector<cudaEvent_t> ev;
+};
+std::map<int, HostPipe> g_pipe;
+
+int host_pipe(int dev, size_t nev, HostPipe **out) {
+  HostPipe &hp = g_pipe[dev];
+  if (!hp.h2d && cudaStreamCreateWithFlags(&hp.h2d, cudaStreamNonBlocking) != cudaSuccess) return NS_ECUDA;
+  if (!hp.d2h && cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking) != cudaSuccess) return NS_ECUDA;
+  while (hp.ev.size() < nev) {
+    cudaEvent_t e;
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return NS_ECUDA;
+    hp.ev.push_back(e);
+  }
+  *out = &hp;
+  return NS_OK;
 }
 
 }  // namespace
@@ -461,13 +495,29 @@ int ns_orthogonalize_batched_host(void *const *X_host, const int64_t *shapes, in
   if (count == 0) return NS_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t elt = dtype == NS_BF16 ? 2 : 4;
-  std::vector<size_t> off(count);
+  std::vector<size_t> off(count), bytes(count);
   size_t total = 0;
   for (int i = 0; i < count; ++i) {
+    bytes[i] = static_cast<size_t>(shapes[2 * i] * shapes[2 * i + 1]) * elt;
     off[i] = total;
-    total = align_up(total + static_cast<size_t>(shapes[2 * i] * shapes[2 * i + 1]) * elt, 256);
+    total = align_up(total + bytes[i], 256);
   }
+  // contiguous groups of about total/8 bytes: group g's copies in, its
+  // Newton-Schulz and group g-1's copies out overlap
+  constexpr int kMaxGroups = 8;
+  std::vector<int> gstart{0};
+  size_t acc = 0;
+  for (int i = 0; i < count; ++i) {
+    acc += bytes[i];
+    if (acc * kMaxGroups >= total * gstart.size() && i + 1 < count &&
+        static_cast<int>(gstart.size()) < kMaxGroups)
+      gstart.push_back(i + 1);
+  }
+  gstart.push_back(count);
+  const int ngroups = static_cast<int>(gstart.size()) - 1;
+
   uint8_t *dbuf = nullptr;
+  HostPipe *hp = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_mu);
     DevInfo *di = nullptr;
@@ -475,26 +525,36 @@ int ns_orthogonalize_batched_host(void *const *X_host, const int64_t *shapes, in
     if (rc) return rc;
     int dev = 0;
     cudaGetDevice(&dev);
-    // staging buffers are keyed apart from the compute workspace of this stream
-    CachedWs &c = g_ws[{dev + (1 << 20), s}];
+    CachedWs &c = g_ws[WsKey{dev, s, 1}];
     rc = ensure_ws(c, std::max<size_t>(total, 256), s);
     if (rc) return rc;
     dbuf = c.ptr;
+    rc = host_pipe(dev, 2 * static_cast<size_t>(ngroups) + 1, &hp);
+    if (rc) return rc;
   }
   std::vector<void *> dptr(count);
-  for (int i = 0; i < count; ++i) {
-    const size_t bytes = static_cast<size_t>(shapes[2 * i] * shapes[2 * i + 1]) * elt;
-    dptr[i] = dbuf + off[i];
-    if (bytes && cudaMemcpyAsync(dptr[i], X_host[i], bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+  for (int i = 0; i < count; ++i) dptr[i] = dbuf + off[i];
+  cudaEvent_t ev_start = hp->ev[2 * ngroups];
+  // the copies in start after earlier work on the caller's stream
+  if (cudaEventRecord(ev_start, s) != cudaSuccess || cudaStreamWaitEvent(hp->h2d, ev_start, 0) != cudaSuccess)
+    return NS_ECUDA;
+  for (int g = 0; g < ngroups; ++g) {
+    const int i0 = gstart[g], i1 = gstart[g + 1];
+    cudaEvent_t ev_in = hp->ev[2 * g], ev_out = hp->ev[2 * g + 1];
+    for (int i = i0; i < i1; ++i)
+      if (bytes[i] && cudaMemcpyAsync(dptr[i], X_host[i], bytes[i], cudaMemcpyHostToDevice, hp->h2d) != cudaSuccess)
+        return NS_ECUDA;
+    if (cudaEventRecord(ev_in, hp->h2d) != cudaSuccess || cudaStreamWaitEvent(s, ev_in, 0) != cudaSuccess)
       return NS_ECUDA;
-  }
-  rc = run(dptr.data(), shapes, count, steps, coeffs, 1e-7f, dtype, nullptr, 0, s);
-  if (rc) return rc;
-  for (int i = 0; i < count; ++i) {
-    const size_t bytes = static_cast<size_t>(shapes[2 * i] * shapes[2 * i + 1]) * elt;
-    if (bytes && cudaMemcpyAsync(X_host[i], dptr[i], bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    rc = run(dptr.data() + i0, shapes + 2 * i0, i1 - i0, steps, coeffs, 1e-7f, dtype, nullptr, 0, s, 2 + g);
+    if (rc) return rc;
+    if (cudaEventRecord(ev_out, s) != cudaSuccess || cudaStreamWaitEvent(hp->d2h, ev_out, 0) != cudaSuccess)
       return NS_ECUDA;
+    for (int i = i0; i < i1; ++i)
+      if (bytes[i] && cudaMemcpyAsync(X_host[i], dptr[i], bytes[i], cudaMemcpyDeviceToHost, hp->d2h) != cudaSuccess)
+        return NS_ECUDA;
   }
+  if (cudaStreamSynchronize(hp->d2h) != cudaSuccess) return NS_ECUDA;
   return cudaStreamSynchronize(s) == cudaSuccess ? NS_OK : NS_ECUDA;
 }
 
@@ -527,8 +587,7 @@ int ns_release_workspace(void) {
   if (cudaGetDevice(&dev) != cudaSuccess) return NS_ECUDA;
   if (cudaDeviceSynchronize() != cudaSuccess) return NS_ECUDA;
   for (auto it = g_ws.begin(); it != g_ws.end();) {
-    const int key_dev = it->first.first & ((1 << 20) - 1);
-    if (key_dev == dev) {
+    if (it->first.dev == dev) {
       if (it->second.ptr) cudaFree(it->second.ptr);
       it = g_ws.erase(it);
     } else {

@@ -135,6 +135,38 @@ int ns_orthogonalize_batched_noalloc(void *const *X, const int64_t *shapes, int 
 int64_t ns_cost(int64_t M, int64_t N);
 
 /*
+ * ns_plan_shards -- host-only planner that assigns whole matrices to
+ * `nshards` shards (GPUs, streams or ranks) so that Newton-Schulz work is
+ * balanced. It follows the second page's "Changes" items 1-3: matrices are
+ * taken largest first and each goes to the least-loaded shard; with
+ * order = NS_PLAN_COST "size" and "load" are the ns_cost of the matrices,
+ * with order = NS_PLAN_NUMEL they are element counts (the numel heuristic that
+ * page replaces, kept for comparison).
+ *   shapes     host array of 2*count (M, N) of the matrices Newton-Schulz runs
+ *              on; a 1-D parameter of n elements is passed as (1, n), whose
+ *              cost equals its numel.
+ *   numels     NULL (element counts are M*N), or count element counts a shard
+ *              stores, when they differ from the shape Newton-Schulz sees
+ *              (a tensor-parallel shard is stored locally but orthogonalised
+ *              after an all-gather: the second page's GTP case).
+ *   numel_eps  per-call numel cap: when >= 0, a shard is a candidate for a
+ *              matrix only while the elements placed on it by this call plus
+ *              the matrix's stay within ceil((1 + numel_eps) * total / nshards);
+ *              if no shard qualifies the matrix goes to the shard with the
+ *              fewest elements placed by this call (least-numel fallback).
+ *              The page uses 0.3. A negative value disables the cap.
+ *   loads      NULL, or nshards int64 loads that persist across calls (one
+ *              call per bucket); read as the starting loads and updated.
+ *   assign     out: count shard indices.
+ * Ties go to the shard with fewer elements placed by this call, then to the
+ * lower index. Returns NS_OK or NS_EINVAL. Touches no GPU.
+ */
+#define NS_PLAN_COST 0
+#define NS_PLAN_NUMEL 1
+int ns_plan_shards(const int64_t *shapes, const int64_t *numels, int count, int nshards, double numel_eps,
+                   int order, int64_t *loads, int *assign);
+
+/*
  * ns_get_status -- synchronise `stream`, then return and clear the device
  * status word of the current device: NS_OK, or NS_ETIMEOUT if a kernel's
  * bounded wait gave up (its outputs are then unspecified), or NS_ECUDA if

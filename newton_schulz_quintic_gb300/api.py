@@ -77,6 +77,8 @@ def load_library() -> ctypes.CDLL:
         lib.ns_orthogonalize_batched_noalloc.argtypes = [vp, vp, i32, i32, vp, i32, vp]
         lib.ns_selftest_wait_timeout.restype = i32
         lib.ns_selftest_wait_timeout.argtypes = [i32, vp]
+        lib.ns_plan_shards.restype = i32
+        lib.ns_plan_shards.argtypes = [vp, vp, i32, i32, ctypes.c_double, i32, vp, vp]
         lib.ns_set_kernel_timing.restype = i32
         lib.ns_set_kernel_timing.argtypes = [i32]
         lib.ns_get_kernel_times.restype = i32
@@ -243,3 +245,27 @@ def selftest_wait_timeout(limit_us: int = 20000, stream=None) -> int:
     import torch
     s = stream if stream is not None else torch.cuda.current_stream()
     return int(load_library().ns_selftest_wait_timeout(int(limit_us), ctypes.c_void_p(s.cuda_stream)))
+
+
+PLAN_ORDERS = {"cost": 0, "numel": 1}
+
+
+def plan_shards(shapes, nshards: int, numel_eps: float = 0.3, order: str = "cost", loads=None,
+                numels=None):
+    """Assign matrices (list of (M, N)) to nshards shards; returns (assign, loads).
+
+    Largest first onto the least-loaded shard, sized by ns_cost (order="cost")
+    or by element count (order="numel"), with a per-call numel cap and a
+    least-numel fallback; ``loads`` carries per-shard loads across calls and
+    ``numels`` overrides the stored element counts. Host-only: no GPU is touched."""
+    lib = load_library()
+    shapes = [tuple(int(d) for d in s) for s in shapes]
+    n = len(shapes)
+    arr = (ctypes.c_int64 * max(2 * n, 1))(*[d for s in shapes for d in s])
+    ld = (ctypes.c_int64 * nshards)(*([0] * nshards if loads is None else [int(v) for v in loads]))
+    out = (ctypes.c_int * max(n, 1))()
+    nm = None if numels is None else (ctypes.c_int64 * max(n, 1))(*[int(v) for v in numels])
+    rc = lib.ns_plan_shards(arr, nm, n, int(nshards), float(numel_eps), PLAN_ORDERS[order], ld, out)
+    if rc != 0:
+        raise NSError(rc, "ns_plan_shards")
+    return [int(out[i]) for i in range(n)], [int(v) for v in ld]

@@ -17,6 +17,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <map>
@@ -556,6 +557,50 @@ int ns_orthogonalize_batched_host(void *const *X_host, const int64_t *shapes, in
   }
   if (cudaStreamSynchronize(hp->d2h) != cudaSuccess) return NS_ECUDA;
   return cudaStreamSynchronize(s) == cudaSuccess ? NS_OK : NS_ECUDA;
+}
+
+int ns_plan_shards(const int64_t *shapes, const int64_t *numels, int count, int nshards, double numel_eps,
+                   int order, int64_t *loads, int *assign) {
+  if (count < 0 || nshards <= 0 || (count > 0 && (!shapes || !assign))) return NS_EINVAL;
+  if (order != NS_PLAN_COST && order != NS_PLAN_NUMEL) return NS_EINVAL;
+  std::vector<int64_t> size(count), numel(count);
+  int64_t total = 0;
+  for (int i = 0; i < count; ++i) {
+    const int64_t M = shapes[2 * i], N = shapes[2 * i + 1];
+    if (M < 0 || N < 0 || (numels && numels[i] < 0)) return NS_EINVAL;
+    numel[i] = numels ? numels[i] : M * N;
+    size[i] = order == NS_PLAN_COST ? ns_cost(M, N) : numel[i];
+    total += numel[i];
+  }
+  std::vector<int64_t> load(nshards, 0), placed(nshards, 0);
+  if (loads)
+    for (int s = 0; s < nshards; ++s) load[s] = loads[s];
+  // largest first; ties keep the caller's order
+  std::vector<int> idx(count);
+  for (int i = 0; i < count; ++i) idx[i] = i;
+  std::stable_sort(idx.begin(), idx.end(), [&](int a, int b) { return size[a] > size[b]; });
+  const bool capped = numel_eps >= 0.0;
+  const double cap = capped ? std::ceil((1.0 + numel_eps) * static_cast<double>(total) / nshards) : 0.0;
+  for (int i : idx) {
+    int best = -1;
+    if (capped || order == NS_PLAN_COST) {
+      for (int s = 0; s < nshards; ++s) {
+        if (capped && static_cast<double>(placed[s] + numel[i]) > cap) continue;
+        if (best < 0 || load[s] < load[best] || (load[s] == load[best] && placed[s] < placed[best])) best = s;
+      }
+    }
+    if (best < 0) {  // least-numel fallback
+      best = 0;
+      for (int s = 1; s < nshards; ++s)
+        if (placed[s] < placed[best]) best = s;
+    }
+    assign[i] = best;
+    load[best] += size[i];
+    placed[best] += numel[i];
+  }
+  if (loads)
+    for (int s = 0; s < nshards; ++s) loads[s] = load[s];
+  return NS_OK;
 }
 
 int ns_get_status(void *stream) {

@@ -125,27 +125,46 @@ def orthogonalize(X, steps: int = DEFAULT_STEPS, coeffs=DEFAULT_COEFFS,
     return W
 
 
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """Round fp64 values to the nearest bfloat16 (ties to even), returned as
+    fp64: first to fp32 (nearest even), then to the top 16 bits of the fp32
+    pattern with round-to-nearest-even on the dropped 16 bits."""
+    f = np.asarray(x, dtype=np.float64).astype(np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    u = (u + np.uint64(0x7FFF) + ((u >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16) << np.uint64(16)
+    return u.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
 def orthogonalize_np(X, steps: int = DEFAULT_STEPS, coeffs=DEFAULT_COEFFS,
-                     eps: float = DEFAULT_EPS, orient: int = 0) -> np.ndarray:
+                     eps: float = DEFAULT_EPS, orient: int = 0, emulate: str | None = None) -> np.ndarray:
     """The same steps as ``orthogonalize`` with numpy.matmul (fp64) as the
     product: s = ||X||_F; X/(s+eps); transpose when M > N (orient as above);
-    then ``steps`` times A = W W^T, B = b A + c A A, W = a W + B W."""
+    then ``steps`` times A = W W^T, B = b A + c A A, W = a W + B W.
+
+    emulate="bf16" is a diagnostic, not the oracle: it rounds the normalised
+    W, and after every step A, B and W, to bfloat16 (each product and
+    element-wise combination itself stays fp64), i.e. the storage precision of
+    a bf16 tensor-core implementation that keeps those three matrices in bf16
+    between phases."""
     W = np.array(to_f64(X), dtype=np.float64, copy=True)
     if W.ndim != 2:
         raise ValueError("oracle takes 2-D matrices")
     if W.size == 0:
         return W
+    if emulate not in (None, "bf16"):
+        raise ValueError("emulate must be None or 'bf16'")
+    rnd = round_bf16 if emulate == "bf16" else (lambda v: v)
     a, b, c = (float(v) for v in coeffs)
     s = np.sqrt(np.sum(W * W))
-    W = W / (s + float(eps))
+    W = rnd(W / (s + float(eps)))
     M, N = W.shape
     transpose = (M > N) if orient == 0 else (orient == 2)
     if transpose:
         W = np.ascontiguousarray(W.T)
     for _ in range(int(steps)):
-        A = W @ W.T
-        B = b * A + c * (A @ A)
-        W = a * W + B @ W
+        A = rnd(W @ W.T)
+        B = rnd(b * A + c * (A @ A))
+        W = rnd(a * W + B @ W)
     return np.ascontiguousarray(W.T) if transpose else W
 
 

@@ -243,3 +243,21 @@ def test_eigh_closed_form_keeps_zero_rows():
     X[25:] = 0.0
     out = svd_twin.closed_form_eigh(X, 5, CO, EPS)
     assert np.max(np.abs(out[25:])) < 1e-14
+
+
+def test_round_bf16_matches_torch_cast():
+    x = np.random.default_rng(30).standard_normal(10000) * np.logspace(-6, 6, 10000)
+    got = oracle.round_bf16(x)
+    ref = torch.from_numpy(x).to(torch.float32).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(got, ref)
+
+
+def test_bf16_emulation_is_the_oracle_plus_storage_rounding():
+    # without rounding it is the oracle; with it, it stays within the bf16
+    # error band of the oracle (~1e-2) and is not the oracle
+    X = randn((96, 160), seed=31, std=0.02)
+    exact = oracle.orthogonalize_np(X)
+    emu = oracle.orthogonalize_np(X, emulate="bf16")
+    err = rel(emu, exact)
+    assert 1e-4 < err < 3e-2
+    assert rel(oracle.orthogonalize_np(X, emulate=None), oracle.orthogonalize(X)) < 1e-12

@@ -86,6 +86,17 @@ int ns_orthogonalize_batched_ex(void *const *X, const int64_t *shapes, int count
                                 const float *coeffs, float eps, int dtype, void *workspace,
                                 size_t workspace_bytes, void *stream);
 
+/*
+ * ns_orthogonalize_batched_sched -- as ns_orthogonalize_batched, but step s
+ * uses its own coefficients: coeff_table is a host array of steps x 3 floats,
+ * row s = (a, b, c) of step s, read before return; 1 <= steps <= 32 (0 steps
+ * is normalisation only and reads no table). The pages print no schedule;
+ * this serves coefficient schedules that change from step to step.
+ * Returns NS_EINVAL for a NULL table or more than 32 steps.
+ */
+int ns_orthogonalize_batched_sched(void *const *X, const int64_t *shapes, int count, int steps,
+                                   const float *coeff_table, int dtype, void *stream);
+
 /* Device workspace bytes the _ex call needs for this batch (0 on bad input). */
 size_t ns_workspace_bytes(const int64_t *shapes, int count, int dtype);
 

@@ -73,6 +73,8 @@ def load_library() -> ctypes.CDLL:
         lib.ns_release_workspace.argtypes = []
         lib.ns_num_kernel_launches.restype = i64
         lib.ns_num_kernel_launches.argtypes = []
+        lib.ns_orthogonalize_batched_sched.restype = i32
+        lib.ns_orthogonalize_batched_sched.argtypes = [vp, vp, i32, i32, vp, i32, vp]
         lib.ns_orthogonalize_batched_noalloc.restype = i32
         lib.ns_orthogonalize_batched_noalloc.argtypes = [vp, vp, i32, i32, vp, i32, vp]
         lib.ns_selftest_wait_timeout.restype = i32
@@ -158,6 +160,29 @@ def orthogonalize_batched(mats, steps: int = 5, coeffs=None, eps: float | None =
                                                  workspace.numel(), sp)
     if rc != 0:
         raise NSError(rc, "ns_orthogonalize_batched")
+
+
+def orthogonalize_batched_schedule(mats, table, stream=None) -> None:
+    """In-place Newton-Schulz with a per-step coefficient table: ``table`` is a
+    sequence of (a, b, c) triples, one per step (at most 32 steps)."""
+    import torch
+    lib = load_library()
+    mats = list(mats)
+    rows = [tuple(float(v) for v in r) for r in table]
+    if any(len(r) != 3 for r in rows):
+        raise ValueError("every table row must be (a, b, c)")
+    code = _check(mats, want_cuda=True)
+    if code is None:
+        return
+    dev = mats[0].device
+    with torch.cuda.device(dev):
+        s = stream if stream is not None else torch.cuda.current_stream(dev)
+        ptrs, shapes, _ = _marshal(mats, None)
+        tab = (ctypes.c_float * max(3 * len(rows), 3))(*[v for r in rows for v in r])
+        rc = lib.ns_orthogonalize_batched_sched(ptrs, shapes, len(mats), len(rows), tab, code,
+                                                ctypes.c_void_p(s.cuda_stream))
+    if rc != 0:
+        raise NSError(rc, "ns_orthogonalize_batched_sched")
 
 
 def orthogonalize_batched_noalloc(mats, steps: int = 5, coeffs=None, stream=None) -> None:

@@ -344,7 +344,9 @@ int timed(int kind, cudaStream_t s, F &&fn) {
 }
 
 // ------------------------------------------------------------ execution
-int execute(const Layout &L, uint8_t *ws, int steps, const float *co, float eps, DevInfo *di, cudaStream_t s) {
+// co: one (a, b, c) triple for every step (table == false) or a steps x 3 table
+int execute(const Layout &L, uint8_t *ws, int steps, const float *co, bool table, float eps, DevInfo *di,
+            cudaStream_t s) {
   const MatDesc *mats = reinterpret_cast<const MatDesc *>(ws + L.off_mats);
   if (!L.res.empty()) {
     ResParams rp{};
@@ -352,9 +354,9 @@ int execute(const Layout &L, uint8_t *ws, int steps, const float *co, float eps,
     rp.nmats = static_cast<int>(L.res.size());
     rp.dtype = L.dtype;
     rp.steps = steps;
-    rp.ca = co[0];
-    rp.cb = co[1];
-    rp.cc = co[2];
+    rp.ncoef = table ? steps : 1;
+    for (int k = 0; k < (table ? steps : 1); ++k)
+      for (int u = 0; u < 3; ++u) rp.coef[k][u] = co[3 * k + u];
     rp.eps = eps;
     if (timed(5, s, [&] { return launch_resident(rp, L.res_maxm, L.res_smem, s); })) return NS_ECUDA;
   }
@@ -377,12 +379,14 @@ int execute(const Layout &L, uint8_t *ws, int steps, const float *co, float eps,
   ph.mats = mats;
   ph.ext = ext;
   ph.status = di->status;
-  ph.ca = co[0];
-  ph.cb = co[1];
-  ph.cc = co[2];
+
   const Tile *t01 = reinterpret_cast<const Tile *>(ws + L.off_t01);
   const Tile *t2 = reinterpret_cast<const Tile *>(ws + L.off_t2);
   for (int step = 0; step < steps; ++step) {
+    const float *cs = table ? co + 3 * step : co;
+    ph.ca = cs[0];
+    ph.cb = cs[1];
+    ph.cc = cs[2];
     ph.step = step;
     ph.final_step = step == steps - 1;
     for (int phase = 0; phase < 3; ++phase) {
@@ -398,9 +402,10 @@ int execute(const Layout &L, uint8_t *ws, int steps, const float *co, float eps,
 }
 
 int run(void *const *X, const int64_t *shapes, int count, int steps, const float *coeffs, float eps, int dtype,
-        void *user_ws, size_t user_ws_bytes, cudaStream_t s, int slot = 0) {
+        void *user_ws, size_t user_ws_bytes, cudaStream_t s, int slot = 0, bool table = false) {
   int rc = validate(X, shapes, count, steps, dtype, true);
   if (rc) return rc;
+  if (table && steps > 0 && (!coeffs || steps > kMaxTableSteps)) return NS_EINVAL;
   if (!(eps >= 0.f)) return NS_EINVAL;
   if (count == 0) return NS_OK;
   std::lock_guard<std::mutex> lock(g_mu);
@@ -433,7 +438,7 @@ int run(void *const *X, const int64_t *shapes, int count, int steps, const float
     if (cudaMemcpyAsync(ws, blob.data(), blob.size(), cudaMemcpyHostToDevice, s) != cudaSuccess) return NS_ECUDA;
     if (cache) cache->last_blob = blob;
   }
-  return execute(L, ws, steps, co, eps, di, s);
+  return execute(L, ws, steps, co, table, eps, di, s);
 }
 
 // ------------------------------------------------------------ host pipeline
@@ -480,6 +485,12 @@ int ns_orthogonalize_batched_ex(void *const *X, const int64_t *shapes, int count
   if (!workspace && count > 0) return NS_EINVAL;
   return run(X, shapes, count, steps, coeffs, eps, dtype, workspace, workspace_bytes,
              static_cast<cudaStream_t>(stream));
+}
+
+int ns_orthogonalize_batched_sched(void *const *X, const int64_t *shapes, int count, int steps,
+                                   const float *coeff_table, int dtype, void *stream) {
+  return run(X, shapes, count, steps, coeff_table, 1e-7f, dtype, nullptr, 0, static_cast<cudaStream_t>(stream), 0,
+             true);
 }
 
 size_t ns_workspace_bytes(const int64_t *shapes, int count, int dtype) {

@@ -82,12 +82,15 @@ struct PrepParams {
   int to_user;           // 1: write the normalised matrix back to the caller (steps == 0)
 };
 
+constexpr int kMaxTableSteps = 32;  // longest per-step coefficient table
+
 struct ResParams {
   const ResDesc *mats;
   int nmats;
   int dtype;
   int steps;
-  float ca, cb, cc;
+  int ncoef;                        // 1: coef[0] for every step; else coef[step]
+  float coef[kMaxTableSteps][3];    // (a, b, c)
   float eps;
 };
 

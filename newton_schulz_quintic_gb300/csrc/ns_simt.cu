@@ -347,6 +347,8 @@ __global__ void __launch_bounds__(kResThreads, 1) ns_resident_kernel(ResParams p
   const int kslice = (neff + S - 1) / S;
   const int panel = 4 * (kResThreads / max(mb, 1));  // apply: columns per panel
   for (int step = 0; step < p.steps && meff > 0; ++step) {
+    const float *co = p.coef[p.ncoef == 1 ? 0 : step];
+    const float ca = co[0], cb = co[1], cc = co[2];
     // ---- gram: partial 4x4 blocks over k-slices
     if (tid < nblk * S) {
       const int b = tid / S, sl = tid % S;
@@ -408,7 +410,7 @@ __global__ void __launch_bounds__(kResThreads, 1) ns_resident_kernel(ResParams p
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
           const int i = 4 * bi + u, j = 4 * bj + v;
-          const float val = p.cb * as[i * ap + j] + p.cc * c4[u][v];
+          const float val = cb * as[i * ap + j] + cc * c4[u][v];
           bs[i * ap + j] = val;
           bs[j * ap + i] = val;
         }
@@ -437,7 +439,7 @@ __global__ void __launch_bounds__(kResThreads, 1) ns_resident_kernel(ResParams p
         for (int u = 0; u < 4; ++u)
 #pragma unroll
           for (int v = 0; v < 4; ++v)
-            o4[u][v] = p.ca * Elem<DT>::to_f(xs[(4 * rb + u) * np + j0 + v]) + o4[u][v];
+            o4[u][v] = ca * Elem<DT>::to_f(xs[(4 * rb + u) * np + j0 + v]) + o4[u][v];
       }
       __syncthreads();  // every read of this panel happened
       if (active) {

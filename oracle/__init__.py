@@ -77,6 +77,10 @@ def _lib(mutation: int = 0) -> ctypes.CDLL:
             lib.ns_oracle_orthogonalize.argtypes = [
                 ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
                 ctypes.c_double, ctypes.c_double, ctypes.c_double, ctypes.c_double, ctypes.c_int]
+            lib.ns_oracle_orthogonalize_sched.restype = ctypes.c_int
+            lib.ns_oracle_orthogonalize_sched.argtypes = [
+                ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                ctypes.c_void_p, ctypes.c_double, ctypes.c_int]
             _libs[mutation] = lib
         return _libs[mutation]
 
@@ -107,6 +111,17 @@ def to_f64(x) -> np.ndarray:
     return np.asarray(x, dtype=np.float64)
 
 
+def coeff_table(coeffs, steps):
+    """None for one (a, b, c) triple used by every step; else the per-step
+    table as a contiguous (steps, 3) fp64 array (row s = a, b, c of step s)."""
+    arr = np.asarray(coeffs, dtype=np.float64)
+    if arr.ndim == 1:
+        return None
+    if arr.shape != (int(steps), 3):
+        raise ValueError("a coefficient table must have shape (steps, 3)")
+    return np.ascontiguousarray(arr)
+
+
 def orthogonalize(X, steps: int = DEFAULT_STEPS, coeffs=DEFAULT_COEFFS,
                   eps: float = DEFAULT_EPS, orient: int = 0, mutation: int = 0) -> np.ndarray:
     """Newton-Schulz of one M x N matrix in fp64; returns a new array.
@@ -117,9 +132,14 @@ def orthogonalize(X, steps: int = DEFAULT_STEPS, coeffs=DEFAULT_COEFFS,
     W = np.ascontiguousarray(to_f64(X), dtype=np.float64).copy()
     if W.ndim != 2:
         raise ValueError("oracle takes 2-D matrices")
-    a, b, c = (float(v) for v in coeffs)
-    rc = _lib(mutation).ns_oracle_orthogonalize(
-        W.ctypes.data, W.shape[0], W.shape[1], int(steps), a, b, c, float(eps), int(orient))
+    table = coeff_table(coeffs, steps)
+    if table is None:
+        a, b, c = (float(v) for v in coeffs)
+        rc = _lib(mutation).ns_oracle_orthogonalize(
+            W.ctypes.data, W.shape[0], W.shape[1], int(steps), a, b, c, float(eps), int(orient))
+    else:
+        rc = _lib(mutation).ns_oracle_orthogonalize_sched(
+            W.ctypes.data, W.shape[0], W.shape[1], int(steps), table.ctypes.data, float(eps), int(orient))
     if rc != 0:
         raise RuntimeError(f"ns_oracle_orthogonalize failed with {rc}")
     return W
@@ -154,14 +174,15 @@ def orthogonalize_np(X, steps: int = DEFAULT_STEPS, coeffs=DEFAULT_COEFFS,
     if emulate not in (None, "bf16"):
         raise ValueError("emulate must be None or 'bf16'")
     rnd = round_bf16 if emulate == "bf16" else (lambda v: v)
-    a, b, c = (float(v) for v in coeffs)
+    table = coeff_table(coeffs, steps)
+    rows = [tuple(float(v) for v in coeffs)] * int(steps) if table is None else [tuple(r) for r in table]
     s = np.sqrt(np.sum(W * W))
     W = rnd(W / (s + float(eps)))
     M, N = W.shape
     transpose = (M > N) if orient == 0 else (orient == 2)
     if transpose:
         W = np.ascontiguousarray(W.T)
-    for _ in range(int(steps)):
+    for a, b, c in rows:
         A = rnd(W @ W.T)
         B = rnd(b * A + c * (A @ A))
         W = rnd(a * W + B @ W)

@@ -110,11 +110,33 @@ static void gram(const double *W, int64_t m, int64_t n, double *Wt, double *A)
  *
  * Returns 0, or -1 for bad arguments, -2 if memory ran out.
  */
+int ns_oracle_orthogonalize_sched(double *X, int64_t M, int64_t N, int steps,
+                                  const double *table, double eps, int orient);
+
 int ns_oracle_orthogonalize(double *X, int64_t M, int64_t N, int steps,
                             double a, double b, double c, double eps, int orient)
 {
+    if (steps < 0) return -1;
+    double *table = (double *)malloc(sizeof(double) * 3 * (size_t)(steps > 0 ? steps : 1));
+    if (!table) return -2;
+    for (int it = 0; it < steps; ++it) {
+        table[3 * it] = a; table[3 * it + 1] = b; table[3 * it + 2] = c;
+    }
+    int rc = ns_oracle_orthogonalize_sched(X, M, N, steps, table, eps, orient);
+    free(table);
+    return rc;
+}
+
+/*
+ * As ns_oracle_orthogonalize, with the coefficients of step `it` in
+ * table[3*it .. 3*it+2] = (a, b, c), so every step may use its own triple.
+ */
+int ns_oracle_orthogonalize_sched(double *X, int64_t M, int64_t N, int steps,
+                                  const double *table, double eps, int orient)
+{
     if (!X && M * N > 0) return -1;
     if (M < 0 || N < 0 || steps < 0 || orient < 0 || orient > 2) return -1;
+    if (steps > 0 && !table) return -1;
     if (M == 0 || N == 0) return 0;
 
     const double s = ns_oracle_frobenius(X, M, N);
@@ -149,6 +171,7 @@ int ns_oracle_orthogonalize(double *X, int64_t M, int64_t N, int steps,
     if (nsteps > 0) nsteps -= 1;                 /* planted: one step short */
 #endif
     for (int it = 0; it < nsteps; ++it) {
+        const double a = table[3 * it], b = table[3 * it + 1], c = table[3 * it + 2];
         gram(W, m, n, Wt, A);                    /* A = W W^T */
         matmul(A, A, m, m, m, AA);               /* AA = A A */
         for (int64_t i = 0; i < m * m; ++i) {    /* B = b A + c A^2, kept in A */

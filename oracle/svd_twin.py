@@ -26,10 +26,12 @@ def quintic(s, coeffs):
 
 
 def quintic_iterate(s, steps, coeffs):
-    """f applied ``steps`` times."""
+    """f applied ``steps`` times; ``coeffs`` is one (a, b, c) triple or a
+    (steps, 3) table whose row k is the triple of step k."""
     out = np.asarray(s, dtype=np.float64)
-    for _ in range(int(steps)):
-        out = quintic(out, coeffs)
+    table = np.asarray(coeffs, dtype=np.float64)
+    for k in range(int(steps)):
+        out = quintic(out, table[k] if table.ndim == 2 else table)
     return out
 
 

@@ -97,3 +97,11 @@ def test_selftest_rejects_bad_limits_before_launch(lib):
     assert lib.ns_selftest_wait_timeout(0, None) == -1
     assert lib.ns_selftest_wait_timeout(-5, None) == -1
     assert lib.ns_selftest_wait_timeout(20000000, None) == -1
+
+
+def test_schedule_rejects_bad_tables_before_launch(lib):
+    P, S = ctypes.c_void_p, ctypes.c_int64
+    ptrs, shape = (P * 1)(0x100000), (S * 2)(4, 8)
+    assert lib.ns_orthogonalize_batched_sched(ptrs, shape, 1, 5, None, 1, None) == -1
+    tab = (ctypes.c_float * (3 * 40))()
+    assert lib.ns_orthogonalize_batched_sched(ptrs, shape, 1, 40, tab, 1, None) == -1

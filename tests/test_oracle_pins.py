@@ -261,3 +261,19 @@ def test_bf16_emulation_is_the_oracle_plus_storage_rounding():
     err = rel(emu, exact)
     assert 1e-4 < err < 3e-2
     assert rel(oracle.orthogonalize_np(X, emulate=None), oracle.orthogonalize(X)) < 1e-12
+
+
+SCHEDULE = [(3.4445, -4.7750, 2.0315), (3.0, -3.2, 1.2), (2.2, -1.8, 0.6), (1.5, -0.5, 0.0), (1.5, -0.5, 0.0)]
+
+
+@pytest.mark.parametrize("shape", [(20, 50), (50, 20), (64, 64)])
+def test_per_step_schedule_matches_closed_form(ns, shape):
+    # a different (a, b, c) each step: the singular values follow f_4(...f_0(s))
+    X = randn(shape, seed=40, std=0.02)
+    got = ns(X, steps=5, coeffs=SCHEDULE)
+    assert rel(got, svd_twin.closed_form(X, 5, SCHEDULE, EPS)) < 1e-10
+
+
+def test_constant_schedule_is_the_plain_call(ns):
+    X = randn((30, 70), seed=41)
+    assert np.array_equal(ns(X, steps=3, coeffs=[CO] * 3), ns(X, steps=3, coeffs=CO))

@@ -298,3 +298,29 @@ def test_bf16_tensor_core_matches_storage_rounding_emulation(shape, steps):
     e_ref = rel(got, oracle.orthogonalize(x, steps=steps))
     print(f"{shape} steps={steps}: vs bf16-storage emulation {e_emu:.3e}, vs fp64 oracle {e_ref:.3e}")
     assert e_emu <= EMU_TOL[steps]
+
+
+# ------------------------------------------------------------ per-step coefficient tables
+
+SCHEDULE = [(3.4445, -4.7750, 2.0315), (3.0, -3.2, 1.2), (2.2, -1.8, 0.6), (1.5, -0.5, 0.0), (1.5, -0.5, 0.0)]
+
+
+@pytest.mark.parametrize("dtype,shape", [(torch.bfloat16, (640, 1200)), (torch.bfloat16, (1200, 640)),
+                                         (torch.bfloat16, (24, 2304)), (torch.float32, (64, 128)),
+                                         (torch.float32, (100, 300))])
+def test_per_step_schedule(dtype, shape):
+    x = seeded(shape, dtype, seed=50, std=0.02 if dtype == torch.bfloat16 else 1.0)
+    d = x.cuda()
+    api.orthogonalize_batched_schedule([d], SCHEDULE)
+    torch.cuda.synchronize()
+    assert api.get_status() == 0
+    check_one(x, d.cpu(), steps=5, coeffs=SCHEDULE)
+
+
+def test_constant_schedule_equals_plain_call_bitwise():
+    x = seeded((640, 1200), torch.bfloat16, seed=51)
+    a, b = x.cuda(), x.cuda()
+    api.orthogonalize_batched([a])
+    api.orthogonalize_batched_schedule([b], [CO] * 5)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)

@@ -205,10 +205,28 @@ int64_t ns_num_kernel_launches(void);
  * ns_set_kernel_timing(1) enables and clears the record, (0) disables it.
  * ns_get_kernel_times synchronises on the recorded events and writes, for the
  * kernel classes 0 norm, 1 prep, 2 gram, 3 square, 4 apply, 5 resident,
- * the total milliseconds into ms[k] and the launch count into launches[k]
- * for k < n (n <= 6). Returns NS_OK or NS_ECUDA.
+ * 6 gemm (the tensor-core kernel running every step and phase of a call in
+ * one launch), the total milliseconds into ms[k] and the launch count into
+ * launches[k] for k < n (n <= 7). Returns NS_OK or NS_ECUDA.
  */
 int ns_set_kernel_timing(int enable);
+
+/*
+ * ns_set_gemm_schedule -- how later calls launch the bf16 tensor-core GEMMs
+ * (process-wide):
+ *   NS_SCHED_PHASE   one persistent launch per step and phase (default);
+ *   NS_SCHED_SINGLE  one persistent, cooperative launch per call running every
+ *                    step and phase; an item waits, on a per-matrix completion
+ *                    counter, until the earlier phases of its matrix are done,
+ *                    so phases of different matrices overlap. On GB300 it
+ *                    measured 10-20% slower than NS_SCHED_PHASE on the
+ *                    8 x 8192x6144, 76 x 2048x6144 and mixed 120-matrix
+ *                    batches, so it is not the default.
+ * Results are the same in both. Returns NS_OK or NS_EINVAL.
+ */
+#define NS_SCHED_PHASE 0
+#define NS_SCHED_SINGLE 1
+int ns_set_gemm_schedule(int mode);
 
 /*
  * ns_selftest_wait_timeout -- failure-detection self-test. Launches one CTA

@@ -81,6 +81,8 @@ def load_library() -> ctypes.CDLL:
         lib.ns_selftest_wait_timeout.argtypes = [i32, vp]
         lib.ns_plan_shards.restype = i32
         lib.ns_plan_shards.argtypes = [vp, vp, i32, i32, ctypes.c_double, i32, vp, vp]
+        lib.ns_set_gemm_schedule.restype = i32
+        lib.ns_set_gemm_schedule.argtypes = [i32]
         lib.ns_set_kernel_timing.restype = i32
         lib.ns_set_kernel_timing.argtypes = [i32]
         lib.ns_get_kernel_times.restype = i32
@@ -247,7 +249,7 @@ def num_kernel_launches() -> int:
     return int(load_library().ns_num_kernel_launches())
 
 
-KERNEL_KINDS = ("norm", "prep", "gram", "square", "apply", "resident")
+KERNEL_KINDS = ("norm", "prep", "gram", "square", "apply", "resident", "gemm")
 
 
 def set_kernel_timing(enable: bool) -> None:
@@ -294,3 +296,14 @@ def plan_shards(shapes, nshards: int, numel_eps: float = 0.3, order: str = "cost
     if rc != 0:
         raise NSError(rc, "ns_plan_shards")
     return [int(out[i]) for i in range(n)], [int(v) for v in ld]
+
+
+GEMM_SCHEDULES = {"phase": 0, "single": 1}
+
+
+def set_gemm_schedule(mode: str) -> None:
+    """'phase' (default): one tensor-core launch per step and phase;
+    'single': one launch per call with per-matrix dependency counters."""
+    rc = load_library().ns_set_gemm_schedule(GEMM_SCHEDULES[mode])
+    if rc != 0:
+        raise NSError(rc, "ns_set_gemm_schedule")

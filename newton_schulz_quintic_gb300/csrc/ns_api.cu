@@ -115,6 +115,7 @@ struct BigMat {
   int index;  // caller index
   int64_t M, N, m, n, pm, pn;
   int transposed;
+  int t01, t2;  // tiles of this matrix in the gram/square list and in the apply list
   size_t off_x, off_xt0, off_xt1, off_a, off_b;
 };
 
@@ -127,7 +128,7 @@ struct Layout {
   std::vector<Tile> tiles01, tiles2;
   std::vector<int> prefix;   // prep tile prefix, big.size()+1
   size_t off_mats = 0, off_res = 0, off_t01 = 0, off_t2 = 0, off_prefix = 0, blob_end = 0;
-  size_t off_partials = 0, off_ext = 0, off_buffers = 0, total = 0;
+  size_t off_partials = 0, off_ext = 0, off_done = 0, off_buffers = 0, total = 0;
 };
 
 int validate(void *const *X, const int64_t *shapes, int count, int steps, int dtype, bool check_ptrs) {
@@ -185,6 +186,7 @@ void build_layout(const int64_t *shapes, int count, int dtype, Layout &L) {
     b.pn = round8(b.n);
     const int mi = static_cast<int>(L.big.size());
     // gram / square: tiles with some column index >= some row index
+    const size_t n01_before = L.tiles01.size(), n2_before = L.tiles2.size();
     for (int64_t r0 = 0; r0 < b.m; r0 += BM)
       for (int64_t c0 = 0; c0 < b.m; c0 += BN)
         if (c0 + BN > r0) L.tiles01.push_back(Tile{mi, static_cast<int>(r0), static_cast<int>(c0), 0});
@@ -192,6 +194,8 @@ void build_layout(const int64_t *shapes, int count, int dtype, Layout &L) {
     for (int64_t r0 = 0; r0 < b.n; r0 += BM)
       for (int64_t c0 = 0; c0 < b.m; c0 += BN)
         L.tiles2.push_back(Tile{mi, static_cast<int>(r0), static_cast<int>(c0), 0});
+    b.t01 = static_cast<int>(L.tiles01.size() - n01_before);
+    b.t2 = static_cast<int>(L.tiles2.size() - n2_before);
     const int64_t pt = ((b.M + kPrepTile - 1) / kPrepTile) * ((b.N + kPrepTile - 1) / kPrepTile);
     L.prefix.push_back(L.prefix.back() + static_cast<int>(pt));
     L.big.push_back(b);
@@ -211,7 +215,9 @@ void build_layout(const int64_t *shapes, int count, int dtype, Layout &L) {
   L.off_partials = off;
   off = align_up(off + L.big.size() * kNormBlocks * sizeof(float), 256);
   L.off_ext = off;
-  off = align_up(off + L.big.size() * 2 * sizeof(int), kAlign);
+  off = align_up(off + L.big.size() * 2 * sizeof(int), 256);
+  L.off_done = off;
+  off = align_up(off + L.big.size() * sizeof(int), kAlign);
   L.off_buffers = off;
   for (BigMat &b : L.big) {
     b.off_x = off;
@@ -253,6 +259,8 @@ int build_blob(const Layout &L, void *const *X, const int64_t *shapes, uint8_t *
     d.pn = static_cast<int>(b.pn);
     d.transposed = b.transposed;
     d.index = b.index;
+    d.t01 = b.t01;
+    d.t2 = b.t2;
     if (L.dtype == NS_BF16) {
       int rc = encode_bf16(&d.tm_x, d.x, b.m, b.n, b.pn);
       rc = rc ? rc : encode_bf16(&d.tm_a, d.a, b.m, b.m, b.pm);
@@ -322,7 +330,12 @@ int ensure_ws(CachedWs &c, size_t bytes, cudaStream_t s) {
 }
 
 // ------------------------------------------------------------ kernel timing
-constexpr int kKinds = 6;
+constexpr int kKinds = 7;
+
+// How the tensor-core path is launched (ns_set_gemm_schedule): one launch per
+// step and phase (default) or one launch per call with per-matrix counters.
+std::atomic<int> g_gemm_schedule{NS_SCHED_PHASE};
+bool phase_launches() { return g_gemm_schedule.load() != NS_SCHED_SINGLE; }
 struct TimedLaunch {
   int kind;
   cudaEvent_t start, stop;
@@ -363,7 +376,9 @@ int execute(const Layout &L, uint8_t *ws, int steps, const float *co, bool table
   if (L.big.empty()) return NS_OK;
   const int nbig = static_cast<int>(L.big.size());
   int *ext = reinterpret_cast<int *>(ws + L.off_ext);
-  if (cudaMemsetAsync(ext, 0, nbig * 2 * sizeof(int), s) != cudaSuccess) return NS_ECUDA;
+  int *done = reinterpret_cast<int *>(ws + L.off_done);
+  // extents and completion counters start at zero (they are adjacent)
+  if (cudaMemsetAsync(ext, 0, L.off_done + nbig * sizeof(int) - L.off_ext, s) != cudaSuccess) return NS_ECUDA;
   PrepParams pp{};
   pp.mats = mats;
   pp.nmats = nbig;
@@ -375,13 +390,49 @@ int execute(const Layout &L, uint8_t *ws, int steps, const float *co, bool table
   pp.to_user = steps == 0;
   if (timed(0, s, [&] { return launch_norm(pp, s); })) return NS_ECUDA;
   if (timed(1, s, [&] { return launch_prep(pp, L.prefix.back(), s); })) return NS_ECUDA;
+  const Tile *t01 = reinterpret_cast<const Tile *>(ws + L.off_t01);
+  const Tile *t2 = reinterpret_cast<const Tile *>(ws + L.off_t2);
+  if (steps == 0) return NS_OK;
+  if (L.dtype == NS_BF16) {
+    TcParams tp{};
+    tp.tiles01 = t01;
+    tp.tiles2 = t2;
+    tp.n01 = static_cast<int>(L.tiles01.size());
+    tp.n2 = static_cast<int>(L.tiles2.size());
+    tp.steps = steps;
+    tp.mats = mats;
+    tp.ext = ext;
+    tp.status = di->status;
+    tp.done = done;
+    tp.ncoef = table ? steps : 1;
+    for (int k = 0; k < (table ? steps : 1); ++k)
+      for (int u = 0; u < 3; ++u) tp.coef[k][u] = co[3 * k + u];
+    const int per_step = 2 * tp.n01 + tp.n2;
+    int rc = 1;
+    if (!phase_launches() && static_cast<int64_t>(steps) * per_step < (int64_t(1) << 30)) {
+      // one launch: every step and phase, items ordered by per-matrix counters
+      tp.g_begin = 0;
+      tp.g_end = steps * per_step;
+      tp.wait = 1;
+      rc = timed(6, s, [&] { return launch_tc(tp, di->sms, s); });
+      if (rc < 0) return NS_ECUDA;
+    }
+    if (rc == 1) {  // one launch per step and phase
+      tp.wait = 0;
+      const int begin[3] = {0, tp.n01, 2 * tp.n01}, count[3] = {tp.n01, tp.n01, tp.n2};
+      for (int step = 0; step < steps; ++step)
+        for (int phase = 0; phase < 3; ++phase) {
+          tp.g_begin = step * per_step + begin[phase];
+          tp.g_end = tp.g_begin + count[phase];
+          if (timed(2 + phase, s, [&] { return launch_tc(tp, di->sms, s); })) return NS_ECUDA;
+        }
+    }
+    return NS_OK;
+  }
   PhaseParams ph{};
   ph.mats = mats;
   ph.ext = ext;
   ph.status = di->status;
-
-  const Tile *t01 = reinterpret_cast<const Tile *>(ws + L.off_t01);
-  const Tile *t2 = reinterpret_cast<const Tile *>(ws + L.off_t2);
   for (int step = 0; step < steps; ++step) {
     const float *cs = table ? co + 3 * step : co;
     ph.ca = cs[0];
@@ -392,10 +443,7 @@ int execute(const Layout &L, uint8_t *ws, int steps, const float *co, bool table
     for (int phase = 0; phase < 3; ++phase) {
       ph.tiles = phase < 2 ? t01 : t2;
       ph.ntiles = static_cast<int>(phase < 2 ? L.tiles01.size() : L.tiles2.size());
-      int rc = timed(2 + phase, s, [&] {
-        return L.dtype == NS_BF16 ? launch_tc_phase(phase, ph, di->sms, s) : launch_simt_phase(phase, ph, s);
-      });
-      if (rc) return NS_ECUDA;
+      if (timed(2 + phase, s, [&] { return launch_simt_phase(phase, ph, s); })) return NS_ECUDA;
     }
   }
   return NS_OK;
@@ -654,6 +702,12 @@ int ns_release_workspace(void) {
 }
 
 int64_t ns_num_kernel_launches(void) { return g_launches.load(); }
+
+int ns_set_gemm_schedule(int mode) {
+  if (mode != NS_SCHED_PHASE && mode != NS_SCHED_SINGLE) return NS_EINVAL;
+  g_gemm_schedule.store(mode);
+  return NS_OK;
+}
 
 int ns_selftest_wait_timeout(int limit_us, void *stream) {
   if (limit_us <= 0 || limit_us > 10000000) return NS_EINVAL;

@@ -23,6 +23,8 @@ namespace ns {
 
 enum StoreType : int { kF32 = 0, kBF16 = 1 };
 
+constexpr int kMaxTableSteps = 32;  // longest per-step coefficient table
+
 // Tile of one GEMM phase: tile rows [row0, row0+BM), tile cols [col0, col0+BN)
 // of matrix `mat` (index into the matrix descriptor table).
 struct Tile {
@@ -47,6 +49,7 @@ struct MatDesc {  // CUtensorMap members keep it 64-byte aligned or more
   int pm, pn;            // pitches (elements) of m-wide and n-wide buffers
   int transposed;        // 1 when M > N
   int index;             // position in the caller's batch
+  int t01, t2;           // tensor-core path: pair tiles of this matrix per gram/square and per apply
 };
 
 // Small matrices done entirely in one CTA (shared-memory resident).
@@ -70,6 +73,29 @@ struct PhaseParams {
   int final_step;        // 1 on the last step: write the caller's matrix
 };
 
+// Parameters of the tensor-core GEMM kernel. Its work is the item sequence
+// step-major, then phase (gram, square, apply), then the phase's tile list
+// (all matrices, largest ns_cost first): item g of a step lies in
+// [0, 2*n01 + n2). A launch runs items [g_begin, g_end) of that sequence.
+// With wait != 0 an item first waits until every item of the same matrix in
+// earlier phases is complete (per-matrix completion counters `done`), so one
+// launch can run every step and phase; with wait == 0 the launches themselves
+// order the phases.
+struct TcParams {
+  const Tile *tiles01;  // gram / square pair tiles
+  const Tile *tiles2;   // apply pair tiles
+  int n01, n2;
+  int g_begin, g_end;
+  int steps;            // total steps of the call (the last one writes the caller's matrices)
+  int wait;
+  const MatDesc *mats;
+  const int *ext;       // per matrix {rows_eff, cols_eff} in the caller's orientation
+  int *status;
+  int *done;            // per matrix completion counter (zeroed by the host per call)
+  int ncoef;            // 1: coef[0] for every step; else coef[step]
+  float coef[kMaxTableSteps][3];
+};
+
 // Norm / preparation kernel parameters.
 struct PrepParams {
   const MatDesc *mats;
@@ -81,8 +107,6 @@ struct PrepParams {
   int dtype;             // StoreType of the caller's data == workspace store type
   int to_user;           // 1: write the normalised matrix back to the caller (steps == 0)
 };
-
-constexpr int kMaxTableSteps = 32;  // longest per-step coefficient table
 
 struct ResParams {
   const ResDesc *mats;
@@ -115,7 +139,7 @@ int launch_norm(const PrepParams &p, cudaStream_t s);
 int launch_prep(const PrepParams &p, int total_tiles, cudaStream_t s);
 int launch_resident(const ResParams &p, int maxm, int smem_bytes, cudaStream_t s);
 int launch_simt_phase(int phase, const PhaseParams &p, cudaStream_t s);
-int launch_tc_phase(int phase, const PhaseParams &p, int max_ctas, cudaStream_t s);
+int launch_tc(const TcParams &p, int max_ctas, cudaStream_t s);
 int tc_smem_bytes();
 int launch_wait_probe(int *status, uint64_t limit_ns, int *gave_up, cudaStream_t s);
 int resident_smem_bytes(int m, int n, int dtype);

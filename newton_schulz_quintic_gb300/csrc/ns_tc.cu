@@ -1,8 +1,14 @@
 // ns_tc.cu -- bf16 tensor-core GEMM phases of libns on sm_103a (tcgen05).
 //
-// One persistent, warp-specialised kernel per phase, launched as clusters of
-// two CTAs over a cost-ordered list of 256 x 256 output tiles drawn from
-// every matrix of the batch. Each tile is one pair MMA
+// One persistent, warp-specialised kernel, launched as clusters of two CTAs
+// over a sequence of work items: for every step, the gram tiles of all
+// matrices, then the square tiles, then the apply tiles (each list largest
+// ns_cost first); an item is one 256 x 256 output tile. By default one launch
+// runs every step and phase of the call: before loading an item's operands
+// the producer waits until every item of the same matrix in earlier phases is
+// complete (a per-matrix counter that epilogue warps advance after their
+// stores), so the phases of different matrices overlap and the kernel never
+// drains between phases. Each tile is one pair MMA
 // (tcgen05.mma.cta_group::2, M = 256, N = 256, K = 16, bf16 in, fp32
 // accumulate) issued by the pair's leader CTA (rank 0): CTA rank r holds
 // rows r*128 .. r*128+127 of the first operand and rows r*128 .. r*128+127 of
@@ -15,10 +21,11 @@
 //               in both CTAs; in the leader one thread issues the pair MMAs and
 //               the commits that release stages and hand accumulators to both
 //               CTAs' epilogues;
-//   warps 2..5  epilogue (both CTAs): tcgen05.ld of its 128 accumulator rows,
-//               the fused element-wise step in fp32, round-to-nearest-even to
-//               bf16 and the stores; the second accumulator lets the next
-//               tile's main loop overlap this epilogue.
+//   warps 2..9  epilogue (both CTAs): tcgen05.ld of its 128 accumulator rows
+//               (two warps per TMEM lane quarter), the fused element-wise step
+//               in fp32, round-to-nearest-even to bf16 and the stores; the
+//               second accumulator lets the next tile's main loop overlap it;
+//   warp 10     publishes each stored item on its matrix's completion counter.
 // Phases (all operands K-major, see ns_internal.h for the layout):
 //   0 gram    A = W W^T             upper-triangle tiles; stores tile + mirror
 //   1 square  B = b A + c (A A)     upper-triangle tiles; stores tile + mirror
@@ -37,7 +44,8 @@ namespace ns {
 namespace {
 
 constexpr int kEpiWarps = 8;                        // two per TMEM lane quarter
-constexpr int kThreads = 64 + 32 * kEpiWarps;       // producer warp, MMA warp, epilogue warps
+constexpr int kSignalWarp = 2 + kEpiWarps;          // publishes item completion GPU-wide
+constexpr int kThreads = 32 * (kSignalWarp + 1);    // producer, MMA, epilogue warps, signal warp
 constexpr int kChunksPerWarp = (kTcBN / 32) / (kEpiWarps / 4);
 // per-warp staging tile of the epilogue's coalesced stores: 32 rows of 32 bf16
 // (16 words + 4 pad), or 16 rows of 32 packed bf16 pairs (32 words + 4 pad)
@@ -58,6 +66,7 @@ struct Barriers {
   uint64_t empty[kStages];  // each CTA: the leader's MMAs are done with a stage
   uint64_t tfull[2];        // each CTA: an accumulator is ready
   uint64_t tempty[2];       // leader: every epilogue warp of both CTAs is done with an accumulator
+  uint64_t epi_done[2];     // each CTA: its epilogue warps stored an item (signal warp waits on it)
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -67,27 +76,68 @@ constexpr int kBarrierBytes = (static_cast<int>(sizeof(Barriers)) + 127) / 128 *
 
 struct TileInfo {
   const MatDesc *d;
+  int mat;
   int row0, col0;
   int nk;
   bool skip;
 };
 
-template <int PHASE>
-__device__ __forceinline__ TileInfo tile_info(const PhaseParams &p, int t) {
-  const Tile tl = p.tiles[t];
+// Item g of the launch's sequence: step, phase and tile index in that phase's list.
+__device__ __forceinline__ void decode_item(const TcParams &p, int g, int &step, int &phase, int &t) {
+  const int per_step = 2 * p.n01 + p.n2;
+  step = g / per_step;
+  const int r = g - step * per_step;
+  phase = r < p.n01 ? 0 : (r < 2 * p.n01 ? 1 : 2);
+  t = phase == 0 ? r : (phase == 1 ? r - p.n01 : r - 2 * p.n01);
+}
+
+__device__ __forceinline__ TileInfo tile_info(const TcParams &p, int phase, int t) {
+  const Tile tl = (phase < 2 ? p.tiles01 : p.tiles2)[t];
   TileInfo ti;
+  ti.mat = tl.mat;
   ti.d = p.mats + tl.mat;
   ti.row0 = tl.row0;
   ti.col0 = tl.col0;
   const int e0 = p.ext[2 * tl.mat], e1 = p.ext[2 * tl.mat + 1];
   const int tr = ti.d->transposed;
   const int meff = tr ? e1 : e0, neff = tr ? e0 : e1;
-  const int rows_eff = PHASE == 2 ? neff : meff;
-  const int k_eff = PHASE == 0 ? neff : meff;
+  const int rows_eff = phase == 2 ? neff : meff;
+  const int k_eff = phase == 0 ? neff : meff;
   // decided per pair tile, so both CTAs of a cluster agree
   ti.skip = (tl.row0 >= rows_eff) || (tl.col0 >= meff);
   ti.nk = (k_eff + kTcBK - 1) / kTcBK;
   return ti;
+}
+
+// The signal warp of each CTA advances a matrix's counter by one per item,
+// computed or skipped, and only after the item's own dependencies are met
+// (a computed item after its epilogue stored it); hence
+// counter >= units_before(step, phase) implies that every earlier item of the
+// matrix is complete.
+constexpr int kUnitsPerItem = kTcCluster;
+
+// Counter value at which every item of matrix d in phases before (step, phase) is complete.
+__device__ __forceinline__ int units_before(const MatDesc &d, int step, int phase) {
+  const int items = step * (2 * d.t01 + d.t2) + (phase >= 1 ? d.t01 : 0) + (phase >= 2 ? d.t01 : 0);
+  return kUnitsPerItem * items;
+}
+
+// Per-item constants of the epilogue.
+struct StepCtx {
+  int cur;          // W^T ping-pong buffer read by apply
+  int final_step;   // apply writes the caller's matrix
+  float ca, cb, cc;
+};
+
+__device__ __forceinline__ StepCtx step_ctx(const TcParams &p, int step) {
+  const float *co = p.coef[p.ncoef == 1 ? 0 : step];
+  StepCtx c;
+  c.cur = step & 1;
+  c.final_step = step == p.steps - 1;
+  c.ca = co[0];
+  c.cb = co[1];
+  c.cc = co[2];
+  return c;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -192,7 +242,7 @@ __device__ __forceinline__ void warp_store_transposed(uint32_t *stage, const flo
 // read element by element inside epilogue_chunk instead. Both tensors are
 // read-only during the launch.
 template <int PHASE>
-__device__ __forceinline__ void prefetch_chunk(const PhaseParams &p, const TileInfo &ti, int r, int chunk,
+__device__ __forceinline__ void prefetch_chunk(const StepCtx &p, const TileInfo &ti, int r, int chunk,
                                                uint4 (&out)[4]) {
   if (PHASE == 0) return;
   const MatDesc &d = *ti.d;
@@ -204,7 +254,7 @@ __device__ __forceinline__ void prefetch_chunk(const PhaseParams &p, const TileI
   } else {
     const int jr = ti.row0 + r, ib = ti.col0 + chunk * 32;
     if (jr < d.n && ib + 32 <= d.m)
-      src = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(d.xt[p.step & 1]) +
+      src = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(d.xt[p.cur]) +
                                             static_cast<size_t>(jr) * d.pm + ib);
   }
 #pragma unroll
@@ -214,7 +264,7 @@ __device__ __forceinline__ void prefetch_chunk(const PhaseParams &p, const TileI
 // Epilogue of one 32-column chunk held by one thread: tile row r, columns
 // chunk*32 .. chunk*32+31 of the tile; `pre` is prefetch_chunk's result.
 template <int PHASE>
-__device__ __forceinline__ void epilogue_chunk(const PhaseParams &p, const TileInfo &ti, int r, int chunk,
+__device__ __forceinline__ void epilogue_chunk(const StepCtx &p, const TileInfo &ti, int r, int chunk,
                                                const uint32_t (&raw)[32], const uint4 (&pre)[4], uint32_t *stage) {
   const MatDesc &d = *ti.d;
   const int r0 = r & ~31;  // the warp's first tile row
@@ -257,7 +307,7 @@ __device__ __forceinline__ void epilogue_chunk(const PhaseParams &p, const TileI
     const int ib = ti.col0 + chunk * 32; // column of W^T (index over m)
     if (jr0 >= n || ib >= m) return;     // warp-uniform
     const bool mine = jr < n;
-    const int cur = p.step & 1;
+    const int cur = p.cur;
     const bool full = ib + 32 <= m;
     const __nv_bfloat16 *XT = static_cast<const __nv_bfloat16 *>(d.xt[cur]) + static_cast<size_t>(jr) * pm + ib;
     float xo[32];
@@ -298,8 +348,46 @@ __device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity, int *
 
 
 
+// Epilogue of one item in one epilogue warp: prefetch the operand it
+// reloads, wait for the accumulator, then drain this warp's chunks.
 template <int PHASE>
-__global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_constant__ PhaseParams p) {
+__device__ __forceinline__ bool epilogue_item(const StepCtx &sc, const TileInfo &ti, int r, int c0, uint32_t tbase,
+                                              uint32_t *stage, uint64_t *tfull, uint32_t parity, volatile int *abort,
+                                              int *status) {
+  // the operand does not depend on the accumulator: fetch it while the MMAs run
+  uint4 pre[2][4];
+  prefetch_chunk<PHASE>(sc, ti, r, c0, pre[0]);
+  prefetch_chunk<PHASE>(sc, ti, r, c0 + 1, pre[1]);
+  if (!mbar_wait<true>(tfull, parity, abort, status)) return false;
+  tc_fence_after();
+  // TMEM loads double-buffered: chunk c+1 is read while chunk c is stored
+  uint32_t va[32], vb[32];
+  __syncwarp();
+  tmem_ld32(tbase + static_cast<uint32_t>(c0 * 32), va);
+  tmem_ld_wait(va);
+#pragma unroll
+  for (int k = 0; k < kChunksPerWarp; ++k) {
+    const int c = c0 + k;
+    uint32_t(&cur_v)[32] = (k & 1) ? vb : va;
+    uint32_t(&next_v)[32] = (k & 1) ? va : vb;
+    if (k + 1 < kChunksPerWarp) {
+      __syncwarp();
+      tmem_ld32(tbase + static_cast<uint32_t>((c + 1) * 32), next_v);
+    }
+    uint4 px[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) px[u] = pre[k & 1][u];
+    if (k + 2 < kChunksPerWarp) prefetch_chunk<PHASE>(sc, ti, r, c + 2, pre[k & 1]);
+    epilogue_chunk<PHASE>(sc, ti, r, c, cur_v, px, stage);
+    if (k + 1 < kChunksPerWarp) {
+      __syncwarp();
+      tmem_ld_wait(next_v);
+    }
+  }
+  return true;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *sA = smem;
@@ -322,6 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
     for (int a = 0; a < 2; ++a) {
       mbar_init(&bar->tfull[a], 1);
       mbar_init(&bar->tempty[a], kTcCluster * kEpiWarps);  // one arrival per epilogue warp
+      mbar_init(&bar->epi_done[a], kEpiWarps);
     }
     mbar_init(&bar->drain, 1);
     bar->abort = 0;
@@ -342,7 +431,6 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
   const bool tmem_ok = peer_tmem == tmem;
   if (!tmem_ok && threadIdx.x == 0) set_status(p.status, kStatusTmemMismatch);
   volatile int *abort = &bar->abort;
-  const int cur = p.step & 1;
 
   if (tmem_ok && warp == 0) {
     if (lane == 0) {
@@ -351,15 +439,24 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
       int issued_phase[kStages];
       for (int s = 0; s < kStages; ++s) issued_phase[s] = -1;
       int stage = 0;
-      uint32_t phase = 0;
+      uint32_t phase_bit = 0;
       bool ok = true;
-      for (int t = cluster; t < p.ntiles && ok; t += nclusters) {
-        const TileInfo ti = tile_info<PHASE>(p, t);
+      for (int g = p.g_begin + cluster; g < p.g_end && ok; g += nclusters) {
+        int step, phase, t;
+        decode_item(p, g, step, phase, t);
+        const TileInfo ti = tile_info(p, phase, t);
         if (ti.skip) continue;
-        const void *mapA = PHASE == 0 ? &ti.d->tm_x : PHASE == 1 ? &ti.d->tm_a : &ti.d->tm_xt[cur];
-        const void *mapB = PHASE == 0 ? &ti.d->tm_x : PHASE == 1 ? &ti.d->tm_a : &ti.d->tm_b;
+        if (p.wait) {
+          // operands come from earlier phases of this matrix, written by
+          // epilogues anywhere on the GPU
+          if (!wait_count(p.done + ti.mat, units_before(*ti.d, step, phase), abort, p.status)) break;
+          fence_proxy_async_global();
+        }
+        const int cur = step & 1;
+        const void *mapA = phase == 0 ? &ti.d->tm_x : phase == 1 ? &ti.d->tm_a : &ti.d->tm_xt[cur];
+        const void *mapB = phase == 0 ? &ti.d->tm_x : phase == 1 ? &ti.d->tm_a : &ti.d->tm_b;
         for (int kb = 0; kb < ti.nk; ++kb) {
-          if (!mbar_wait<true>(&bar->empty[stage], phase ^ 1u, abort, p.status)) {
+          if (!mbar_wait<true>(&bar->empty[stage], phase_bit ^ 1u, abort, p.status)) {
             ok = false;
             break;
           }
@@ -369,14 +466,14 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
           tma_load_2d_pair(sA + stage * kABytes, mapA, kx, ti.row0 + my_rows, full_leader, pol);
           tma_load_2d_pair(sB + stage * kBBytes, mapB, kx, ti.col0 + static_cast<int>(rank) * (kTcBN / 2),
                            full_leader, pol);
-          issued_phase[stage] = static_cast<int>(phase);
+          issued_phase[stage] = static_cast<int>(phase_bit);
           if (++stage == kStages) {
             stage = 0;
-            phase ^= 1u;
+            phase_bit ^= 1u;
           }
         }
       }
-      if (!ok && leader) {
+      if (*abort && leader) {
         for (int s = 0; s < kStages; ++s)
           if (issued_phase[s] >= 0) mbar_drain(&bar->full[s], static_cast<uint32_t>(issued_phase[s]), p.status);
       }
@@ -386,18 +483,20 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
       // ---------------------------------------------------- pair MMA issuer (leader)
       constexpr uint32_t idesc = umma_idesc_bf16(kTcCluster * kTcBM, kTcBN);
       int stage = 0;
-      uint32_t phase = 0;
+      uint32_t phase_bit = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int t = cluster; t < p.ntiles && ok; t += nclusters) {
-        const TileInfo ti = tile_info<PHASE>(p, t);
+      for (int g = p.g_begin + cluster; g < p.g_end && ok; g += nclusters) {
+        int step, phase, t;
+        decode_item(p, g, step, phase, t);
+        const TileInfo ti = tile_info(p, phase, t);
         if (ti.skip) continue;
         if (!mbar_wait<true>(&bar->tempty[acc], acc_phase ^ 1u, abort, p.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * kTcBN);
         for (int kb = 0; kb < ti.nk; ++kb) {
-          if (!mbar_wait<true>(&bar->full[stage], phase, abort, p.status)) {
+          if (!mbar_wait<true>(&bar->full[stage], phase_bit, abort, p.status)) {
             ok = false;
             break;
           }
@@ -412,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
           umma_commit_pair_multicast(&bar->empty[stage], kPairMask);
           if (++stage == kStages) {
             stage = 0;
-            phase ^= 1u;
+            phase_bit ^= 1u;
           }
         }
         if (!ok) break;
@@ -425,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
       umma_commit_pair_multicast(&bar->drain, 1u);
       mbar_drain(&bar->drain, 0, p.status);
     }
-  } else if (tmem_ok) {
+  } else if (tmem_ok && warp < kSignalWarp) {
     // ------------------------------------------------------ epilogue (both CTAs)
     // warps 2..9: TMEM lane quarter q = warp % 4 (tile rows q*32 .. q*32+31),
     // column half h: chunks h*kChunksPerWarp .. of the 256 accumulator columns
@@ -436,48 +535,63 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
     uint32_t *stage = epi_stage + e * (kEpiStageBytes / 4);
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = cluster; t < p.ntiles; t += nclusters) {
-      TileInfo ti = tile_info<PHASE>(p, t);
+    for (int g = p.g_begin + cluster; g < p.g_end; g += nclusters) {
+      int step, phase, t;
+      decode_item(p, g, step, phase, t);
+      TileInfo ti = tile_info(p, phase, t);
       if (ti.skip) continue;
-      ti.row0 += my_rows;
-      // the epilogue's global operand does not depend on the accumulator:
-      // start fetching it while this tile's MMAs still run
-      uint4 pre[2][4] = {};
-      prefetch_chunk<PHASE>(p, ti, r, c0, pre[0]);
-      prefetch_chunk<PHASE>(p, ti, r, c0 + 1, pre[1]);
-      if (!mbar_wait<true>(&bar->tfull[acc], acc_phase, abort, p.status)) break;
-      tc_fence_after();
-      const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kTcBN);
-      // TMEM loads double-buffered: chunk c+1 is read while chunk c is stored
-      uint32_t va[32], vb[32];
-      __syncwarp();
-      tmem_ld32(tbase + static_cast<uint32_t>(c0 * 32), va);
-      tmem_ld_wait(va);
-#pragma unroll
-      for (int k = 0; k < kChunksPerWarp; ++k) {
-        const int c = c0 + k;
-        uint32_t(&cur_v)[32] = (k & 1) ? vb : va;
-        uint32_t(&next_v)[32] = (k & 1) ? va : vb;
-        if (k + 1 < kChunksPerWarp) {
-          __syncwarp();
-          tmem_ld32(tbase + static_cast<uint32_t>((c + 1) * 32), next_v);
-        }
-        uint4 px[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) px[u] = pre[k & 1][u];
-        if (k + 2 < kChunksPerWarp) prefetch_chunk<PHASE>(p, ti, r, c + 2, pre[k & 1]);
-        epilogue_chunk<PHASE>(p, ti, r, c, cur_v, px, stage);
-        if (k + 1 < kChunksPerWarp) {
-          __syncwarp();
-          tmem_ld_wait(next_v);
-        }
+      if (p.wait) {
+        // the operand this epilogue reloads (A, W^T) comes from an earlier phase
+        bool ready = true;
+        if (lane == 0) ready = wait_count(p.done + ti.mat, units_before(*ti.d, step, phase), abort, p.status);
+        if (!__shfl_sync(0xffffffffu, ready ? 1 : 0, 0)) break;
       }
+      ti.row0 += my_rows;
+      const StepCtx sc = step_ctx(p, step);
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kTcBN);
+      bool ok;
+      if (phase == 0)
+        ok = epilogue_item<0>(sc, ti, r, c0, tbase, stage, &bar->tfull[acc], acc_phase, abort, p.status);
+      else if (phase == 1)
+        ok = epilogue_item<1>(sc, ti, r, c0, tbase, stage, &bar->tfull[acc], acc_phase, abort, p.status);
+      else
+        ok = epilogue_item<2>(sc, ti, r, c0, tbase, stage, &bar->tfull[acc], acc_phase, abort, p.status);
+      if (!ok) break;
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&bar->tempty[acc]), 0));
+      if (lane == 0) {
+        mbar_arrive_cluster(mapa_shared(smem_u32(&bar->tempty[acc]), 0));  // TMEM reusable
+        mbar_arrive(&bar->epi_done[acc]);                                   // stores issued (release)
+      }
       if (++acc == kAccs) {
         acc = 0;
         acc_phase ^= 1u;
+      }
+    }
+  } else if (tmem_ok && warp == kSignalWarp) {
+    if (lane == 0) {
+      // ---------------------------------------------------- completion signal (both CTAs)
+      // After the CTA's epilogue warps stored an item (their arrivals on
+      // epi_done release the stores to this thread), publish it at GPU scope;
+      // the release is cumulative, so a consumer that acquires the counter
+      // sees every store of the item. Skipped items are published once their
+      // own dependencies are met.
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      for (int g = p.g_begin + cluster; g < p.g_end; g += nclusters) {
+        int step, phase, t;
+        decode_item(p, g, step, phase, t);
+        const TileInfo ti = tile_info(p, phase, t);
+        if (ti.skip) {
+          if (p.wait && !wait_count(p.done + ti.mat, units_before(*ti.d, step, phase), abort, p.status)) break;
+        } else {
+          if (!mbar_wait(&bar->epi_done[acc], acc_phase, abort, p.status)) break;
+          if (++acc == kAccs) {
+            acc = 0;
+            acc_phase ^= 1u;
+          }
+        }
+        red_release_gpu_add(p.done + ti.mat, 1);
       }
     }
   }
@@ -490,39 +604,47 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
   if (warp == 1) tmem_dealloc_pair(tmem, kTmemCols);
 }
 
-template <int PHASE>
-int launch_phase_t(const PhaseParams &p, int max_ctas, cudaStream_t s) {
+int launch_tc_kernel(const TcParams &p, int max_ctas, cudaStream_t s) {
   const int smem = tc_smem_bytes();
-  auto kernel = ns_tc_gemm_kernel<PHASE>;
+  auto kernel = ns_tc_gemm_kernel;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -1;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = kTcCluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // items that wait on other clusters' items need every CTA resident at once
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = 1;
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  // persistent: as many pairs as can be resident at once, at most one per tile
-  static int resident_pairs[16][3] = {};
+  // persistent: as many pairs as can be resident at once (items wait on one
+  // another, so every pair of the grid must be resident), at most one per item
+  static int resident_pairs[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  int &cached = resident_pairs[dev & 15][PHASE];
+  int &cached = resident_pairs[dev & 63];
   if (cached == 0) {
     cfg.gridDim = dim3(kTcCluster * (max_ctas / kTcCluster), 1, 1);
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) {
       cudaGetLastError();
-      n = max_ctas / kTcCluster;
+      return -1;
     }
     cached = n;
   }
-  const int pairs = cached < p.ntiles ? cached : p.ntiles;
+  const int items = p.g_end - p.g_begin;
+  const int pairs = cached < items ? cached : items;
   cfg.gridDim = dim3(kTcCluster * pairs, 1, 1);
-  if (cudaLaunchKernelEx(&cfg, kernel, p) != cudaSuccess) return -1;
+  cfg.numAttrs = p.wait ? 2 : 1;
+  if (cudaLaunchKernelEx(&cfg, kernel, p) != cudaSuccess) {
+    cudaGetLastError();
+    return p.wait ? 1 : -1;  // 1: a co-resident launch was refused; the caller can split by phase
+  }
   count_launch();
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
@@ -531,11 +653,9 @@ int launch_phase_t(const PhaseParams &p, int max_ctas, cudaStream_t s) {
 
 int tc_smem_bytes() { return 1024 + kStages * kStageBytes + kBarrierBytes + kEpiWarps * kEpiStageBytes; }
 
-int launch_tc_phase(int phase, const PhaseParams &p, int max_ctas, cudaStream_t s) {
-  if (p.ntiles <= 0) return 0;
-  if (phase == 0) return launch_phase_t<0>(p, max_ctas, s);
-  if (phase == 1) return launch_phase_t<1>(p, max_ctas, s);
-  return launch_phase_t<2>(p, max_ctas, s);
+int launch_tc(const TcParams &p, int max_ctas, cudaStream_t s) {
+  if (p.g_end <= p.g_begin) return 0;
+  return launch_tc_kernel(p, max_ctas, s);
 }
 
 }  // namespace ns

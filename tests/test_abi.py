@@ -105,3 +105,8 @@ def test_schedule_rejects_bad_tables_before_launch(lib):
     assert lib.ns_orthogonalize_batched_sched(ptrs, shape, 1, 5, None, 1, None) == -1
     tab = (ctypes.c_float * (3 * 40))()
     assert lib.ns_orthogonalize_batched_sched(ptrs, shape, 1, 40, tab, 1, None) == -1
+
+
+def test_gemm_schedule_setter(lib):
+    assert lib.ns_set_gemm_schedule(5) == -1
+    assert lib.ns_set_gemm_schedule(1) == 0 and lib.ns_set_gemm_schedule(0) == 0

@@ -324,3 +324,38 @@ def test_constant_schedule_equals_plain_call_bitwise():
     api.orthogonalize_batched_schedule([b], [CO] * 5)
     torch.cuda.synchronize()
     assert torch.equal(a, b)
+
+
+# ------------------------------------------------------------ single-launch schedule
+
+@pytest.fixture
+def single_launch():
+    api.set_gemm_schedule("single")
+    yield
+    api.set_gemm_schedule("phase")
+
+
+def test_single_launch_schedule_matches_phase_launches(single_launch):
+    # one cooperative launch for every step and phase; items wait on
+    # per-matrix counters. Same arithmetic, so the same bits.
+    xs = [seeded(s, torch.bfloat16, seed=60 + i) for i, s in
+          enumerate([(640, 1200), (1200, 640), (300, 520), (24, 100), (2048, 1024)])]
+    zx = seeded((300, 1024), torch.bfloat16, seed=66)
+    zx[250:] = 0
+    zx[:, 900:] = 0
+    xs.append(zx)
+    got = run_gpu(xs)
+    api.set_gemm_schedule("phase")
+    ref = run_gpu(xs)
+    for x, g, r in zip(xs, got, ref):
+        assert torch.equal(g, r)
+        check_one(x, g)
+
+
+def test_single_launch_schedule_per_step_table(single_launch):
+    x = seeded((640, 1200), torch.bfloat16, seed=67)
+    d = x.cuda()
+    api.orthogonalize_batched_schedule([d], SCHEDULE)
+    torch.cuda.synchronize()
+    assert api.get_status() == 0
+    check_one(x, d.cpu(), steps=5, coeffs=SCHEDULE)

@@ -359,3 +359,45 @@ def test_single_launch_schedule_per_step_table(single_launch):
     torch.cuda.synchronize()
     assert api.get_status() == 0
     check_one(x, d.cpu(), steps=5, coeffs=SCHEDULE)
+
+
+# ------------------------------------------------------------ robustness
+
+@pytest.mark.parametrize("shape", [(300, 520), (520, 300), (24, 2304), (129, 1031), (1000, 17)])
+def test_unaligned_user_pointers(shape):
+    # matrices that start 2 bytes past a 16-byte boundary: every 16-byte
+    # vector path on the caller's memory has to fall back to narrower access
+    x = seeded(shape, torch.bfloat16, seed=70)
+    n = x.numel()
+    buf = torch.zeros(n + 1, dtype=torch.bfloat16, device="cuda")
+    view = buf[1:1 + n].view(shape)
+    assert view.data_ptr() % 16 == 2 and view.is_contiguous()
+    view.copy_(x.cuda())
+    api.orthogonalize_batched([view])
+    torch.cuda.synchronize()
+    assert api.get_status() == 0
+    assert buf[0].item() == 0                  # nothing written before the matrix
+    check_one(x, view.cpu())
+    aligned = run_gpu([x])[0]
+    assert torch.equal(aligned, view.cpu())
+
+
+def test_many_matrices_one_call():
+    rng = np.random.default_rng(71)
+    shapes = [(int(rng.integers(1, 400)), int(rng.integers(1, 700))) for _ in range(300)]
+    xs = [seeded(s, torch.bfloat16, seed=100 + i) for i, s in enumerate(shapes)]
+    ys = run_gpu(xs)
+    for i in range(0, 300, 15):  # the oracle on a sample
+        check_one(xs[i], ys[i])
+    ref = run_gpu(xs)                        # and the whole batch is reproducible
+    assert all(torch.equal(a, b) for a, b in zip(ys, ref))
+
+
+def test_host_entry_point_pageable_buffers():
+    xs = [seeded((640, 1200), torch.bfloat16, 72), seeded((1200, 640), torch.bfloat16, 73),
+          seeded((24, 100), torch.bfloat16, 74)]
+    ref = run_gpu(xs)
+    host = [x.clone() for x in xs]             # pageable
+    api.orthogonalize_batched_host(host)
+    for r, h in zip(ref, host):
+        assert torch.equal(r, h)

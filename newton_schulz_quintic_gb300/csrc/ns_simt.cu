@@ -103,7 +103,7 @@ int launch_norm(const PrepParams &p, cudaStream_t s) {
 // ============================================================== preparation
 // One block per 64x64 tile of the caller's Y. Every block sums the
 // matrix's kNormBlocks partials in the same fixed order, so all blocks agree
-// on s = ||Y||_F. It writes y / (s + eps), rounded to the working type, into
+// on s = ||Y||_F. It writes y * (1 / (s + eps)), rounded to the working type, into
 // W and W^T (or back into Y when no step follows). When Y's rows are 16-byte
 // aligned the tile moves in 16-byte vectors; the transposed copy goes through
 // shared memory so both writes are row-contiguous.
@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(256) ns_prep_kernel(PrepParams p) {
   const T *y = static_cast<const T *>(d.user);
   const bool vec = (N % V == 0) && ((reinterpret_cast<uintptr_t>(y) & 15) == 0);
 
-  __shared__ float s_denom;
+  __shared__ float s_denom;  // reciprocal of ||Y||_F + eps
   __shared__ float tile[kPrepTile][kPrepTile + 1];
   const int tid = threadIdx.x;
 
@@ -147,24 +147,24 @@ __global__ void __launch_bounds__(256) ns_prep_kernel(PrepParams p) {
     float v = 0.f;
     for (int i = tid; i < kNormBlocks; i += 32) v += p.partials[mat * kNormBlocks + i];
     v = warp_sum(v);
-    if (tid == 0) s_denom = sqrtf(v) + p.eps;
+    if (tid == 0) s_denom = 1.0f / (sqrtf(v) + p.eps);  // 1 / (||Y||_F + eps)
   }
   __syncthreads();
-  const float denom = s_denom;
+  const float inv = s_denom;
   if (vec) {
 #pragma unroll
     for (int k = 0; k < PER; ++k) {
       const int q = tid + k * 256, rr = q / CPR, cv = q % CPR;
       const T *e = reinterpret_cast<const T *>(&raw[k]);
 #pragma unroll
-      for (int u = 0; u < V; ++u) tile[rr][cv * V + u] = __fdiv_rn(Elem<DT>::to_f(e[u]), denom);
+      for (int u = 0; u < V; ++u) tile[rr][cv * V + u] = Elem<DT>::to_f(e[u]) * inv;
     }
   } else {
     for (int e = tid; e < kPrepTile * kPrepTile; e += 256) {
       const int rr = e / kPrepTile, cc = e % kPrepTile;
       const int r = r0 + rr, c = c0 + cc;
       float v = 0.f;
-      if (r < M && c < N) v = __fdiv_rn(Elem<DT>::load(y + static_cast<size_t>(r) * N + c), denom);
+      if (r < M && c < N) v = Elem<DT>::load(y + static_cast<size_t>(r) * N + c) * inv;
       tile[rr][cc] = v;
     }
   }
@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(kResThreads, 1) ns_resident_kernel(ResParams p
 
   __shared__ float s_sum[NW];
   __shared__ int s_r[NW], s_c[NW];
-  __shared__ float s_denom;
+  __shared__ float s_denom;  // reciprocal of ||Y||_F + eps
   __shared__ int s_meff, s_neff;
 
   // 1. zero the padded working copy, then load Y into it (oriented as W),
@@ -327,17 +327,17 @@ __global__ void __launch_bounds__(kResThreads, 1) ns_resident_kernel(ResParams p
       rr = max(rr, s_r[w]);
       cc = max(cc, s_c[w]);
     }
-    s_denom = sqrtf(t) + p.eps;
+    s_denom = 1.0f / (sqrtf(t) + p.eps);  // 1 / (||Y||_F + eps)
     s_meff = tr ? cc + 1 : rr + 1;
     s_neff = tr ? rr + 1 : cc + 1;
   }
   __syncthreads();
-  const float denom = s_denom;
+  const float inv = s_denom;
   const int meff = s_meff, neff = s_neff;
 
   // 2. normalise (zeros stay zero)
   for (int e = tid; e < L.mp * np; e += kResThreads)
-    xs[e] = Elem<DT>::from_f(__fdiv_rn(Elem<DT>::to_f(xs[e]), denom));
+    xs[e] = Elem<DT>::from_f(Elem<DT>::to_f(xs[e]) * inv);
   __syncthreads();
 
   // 3. iterate on the non-zero block

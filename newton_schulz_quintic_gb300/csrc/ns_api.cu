@@ -41,6 +41,10 @@ namespace {
 
 constexpr float kDefaultCoeffs[3] = {3.4445f, -4.7750f, 2.0315f};
 constexpr int kResidentMaxM = 64;
+#ifndef NS_RASTER_GROUP
+#define NS_RASTER_GROUP 8
+#endif
+constexpr int kRasterGroup = NS_RASTER_GROUP;  // tile rows per rasterisation group
 constexpr int kResidentSmemMax = 200 * 1024;
 constexpr size_t kAlign = 1024;
 
@@ -185,15 +189,21 @@ void build_layout(const int64_t *shapes, int count, int dtype, Layout &L) {
     b.pm = round8(b.m);
     b.pn = round8(b.n);
     const int mi = static_cast<int>(L.big.size());
-    // gram / square: tiles with some column index >= some row index
+    // Tiles in groups of kRasterGroup tile rows: within a group, column by
+    // column, so the tiles in flight at once share a few operand row blocks
+    // of each side and the working set stays in L2.
     const size_t n01_before = L.tiles01.size(), n2_before = L.tiles2.size();
-    for (int64_t r0 = 0; r0 < b.m; r0 += BM)
+    const int64_t gstep = static_cast<int64_t>(kRasterGroup) * BM;
+    // gram / square: tiles with some column index >= some row index
+    for (int64_t g0 = 0; g0 < b.m; g0 += gstep)
       for (int64_t c0 = 0; c0 < b.m; c0 += BN)
-        if (c0 + BN > r0) L.tiles01.push_back(Tile{mi, static_cast<int>(r0), static_cast<int>(c0), 0});
+        for (int64_t r0 = g0; r0 < std::min(b.m, g0 + gstep); r0 += BM)
+          if (c0 + BN > r0) L.tiles01.push_back(Tile{mi, static_cast<int>(r0), static_cast<int>(c0), 0});
     // apply: rows of W^T (over n) x columns (over m)
-    for (int64_t r0 = 0; r0 < b.n; r0 += BM)
+    for (int64_t g0 = 0; g0 < b.n; g0 += gstep)
       for (int64_t c0 = 0; c0 < b.m; c0 += BN)
-        L.tiles2.push_back(Tile{mi, static_cast<int>(r0), static_cast<int>(c0), 0});
+        for (int64_t r0 = g0; r0 < std::min(b.n, g0 + gstep); r0 += BM)
+          L.tiles2.push_back(Tile{mi, static_cast<int>(r0), static_cast<int>(c0), 0});
     b.t01 = static_cast<int>(L.tiles01.size() - n01_before);
     b.t2 = static_cast<int>(L.tiles2.size() - n2_before);
     const int64_t pt = ((b.M + kPrepTile - 1) / kPrepTile) * ((b.N + kPrepTile - 1) / kPrepTile);

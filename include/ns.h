@@ -30,6 +30,10 @@
  *  - Return value: NS_OK (0) or a negative NS_E* code. Arguments are
  *    validated before anything is launched; on a validation error nothing
  *    runs and the matrices are untouched. No C++ exception crosses the ABI.
+ *  - CUDA graphs: once ns_orthogonalize_batched (or _sched) has run with the
+ *    same matrices, shapes, steps, coefficients and stream, a repeat call
+ *    allocates nothing and uploads nothing, so it may be captured into a
+ *    graph on that stream and replayed.
  */
 #ifndef NS_H_
 #define NS_H_

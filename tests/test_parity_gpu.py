@@ -401,3 +401,31 @@ def test_host_entry_point_pageable_buffers():
     api.orthogonalize_batched_host(host)
     for r, h in zip(ref, host):
         assert torch.equal(r, h)
+
+
+# ------------------------------------------------------------ CUDA graphs
+
+@pytest.mark.parametrize("dtype,shapes", [(torch.bfloat16, [(640, 1200), (1200, 640), (24, 2304)]),
+                                          (torch.float32, [(64, 128), (100, 300)])])
+def test_capture_in_cuda_graph_after_warmup(dtype, shapes):
+    # once a call with the same arguments has run, a call allocates nothing
+    # and uploads nothing, so it can be captured and replayed
+    xs = [seeded(s, dtype, seed=80 + i, std=0.02 if dtype == torch.bfloat16 else 1.0)
+          for i, s in enumerate(shapes)]
+    ref = run_gpu(xs)
+    dev = [x.cuda() for x in xs]
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        api.orthogonalize_batched(dev)          # warm-up on the capture stream
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        api.orthogonalize_batched(dev)
+    for _ in range(2):                          # replays recompute from fresh inputs
+        for d, x in zip(dev, xs):
+            d.copy_(x.cuda())
+        g.replay()
+        torch.cuda.synchronize()
+        assert api.get_status() == 0
+        for r, d in zip(ref, dev):
+            assert torch.equal(r, d.cpu())

@@ -101,17 +101,24 @@ int get_encode() {
 }
 
 // bf16 row-major rows x cols matrix with a pitch of `pitch` elements; box
-// {64 columns, 128 rows} with 128-byte swizzle; out-of-range reads give 0.
-int encode_bf16(CUtensorMap *map, void *base, int64_t rows, int64_t cols, int64_t pitch) {
+// {64 columns, box_rows rows} with 128-byte swizzle; out-of-range reads give 0.
+int encode_bf16(CUtensorMap *map, void *base, int64_t rows, int64_t cols, int64_t pitch, int box_rows) {
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(std::max<int64_t>(cols, 1)),
                         static_cast<cuuint64_t>(std::max<int64_t>(rows, 1))};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch * 2)};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(kTcBK), static_cast<cuuint32_t>(kTcBM)};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? NS_OK : NS_ECUDA;
+}
+
+// The two maps of one iterate-shaped tensor: K-major box {64, 128}, MN-major box {64, 64}.
+int encode_iterate(CUtensorMap *kmajor, CUtensorMap *mnmajor, void *base, int64_t rows, int64_t cols,
+                   int64_t pitch) {
+  int rc = encode_bf16(kmajor, base, rows, cols, pitch, kTcBM);
+  return rc ? rc : encode_bf16(mnmajor, base, rows, cols, pitch, 64);
 }
 
 // ------------------------------------------------------------ layout
@@ -120,7 +127,8 @@ struct BigMat {
   int64_t M, N, m, n, pm, pn;
   int transposed;
   int t01, t2;  // tiles of this matrix in the gram/square list and in the apply list
-  size_t off_x, off_xt0, off_xt1, off_a, off_b;
+  int64_t ps;   // bf16 path: pitch of the iterate buffers (caller's orientation)
+  size_t off_x, off_xt0, off_xt1, off_s0, off_s1, off_a, off_b;
 };
 
 struct Layout {
@@ -132,7 +140,7 @@ struct Layout {
   std::vector<Tile> tiles01, tiles2;
   std::vector<int> prefix;   // prep tile prefix, big.size()+1
   size_t off_mats = 0, off_res = 0, off_t01 = 0, off_t2 = 0, off_prefix = 0, blob_end = 0;
-  size_t off_partials = 0, off_ext = 0, off_done = 0, off_buffers = 0, total = 0;
+  size_t off_partials = 0, off_tilepart = 0, off_rscale = 0, off_ext = 0, off_done = 0, off_buffers = 0, total = 0;
 };
 
 int validate(void *const *X, const int64_t *shapes, int count, int steps, int dtype, bool check_ptrs) {
@@ -188,6 +196,7 @@ void build_layout(const int64_t *shapes, int count, int dtype, Layout &L) {
     b.n = std::max(b.M, b.N);
     b.pm = round8(b.m);
     b.pn = round8(b.n);
+    b.ps = round8(b.N);
     const int mi = static_cast<int>(L.big.size());
     // Tiles in groups of kRasterGroup tile rows: within a group, column by
     // column, so the tiles in flight at once share a few operand row blocks
@@ -199,10 +208,12 @@ void build_layout(const int64_t *shapes, int count, int dtype, Layout &L) {
       for (int64_t c0 = 0; c0 < b.m; c0 += BN)
         for (int64_t r0 = g0; r0 < std::min(b.m, g0 + gstep); r0 += BM)
           if (c0 + BN > r0) L.tiles01.push_back(Tile{mi, static_cast<int>(r0), static_cast<int>(c0), 0});
-    // apply: rows of W^T (over n) x columns (over m)
-    for (int64_t g0 = 0; g0 < b.n; g0 += gstep)
-      for (int64_t c0 = 0; c0 < b.m; c0 += BN)
-        for (int64_t r0 = g0; r0 < std::min(b.n, g0 + gstep); r0 += BM)
+    // apply: bf16, tiles of the next iterate in the caller's orientation
+    // (M x N); fp32, tiles of W'^T (n x m)
+    const int64_t arows = dtype == NS_BF16 ? b.M : b.n, acols = dtype == NS_BF16 ? b.N : b.m;
+    for (int64_t g0 = 0; g0 < arows; g0 += gstep)
+      for (int64_t c0 = 0; c0 < acols; c0 += BN)
+        for (int64_t r0 = g0; r0 < std::min(arows, g0 + gstep); r0 += BM)
           L.tiles2.push_back(Tile{mi, static_cast<int>(r0), static_cast<int>(c0), 0});
     b.t01 = static_cast<int>(L.tiles01.size() - n01_before);
     b.t2 = static_cast<int>(L.tiles2.size() - n2_before);
@@ -224,18 +235,29 @@ void build_layout(const int64_t *shapes, int count, int dtype, Layout &L) {
   L.blob_end = off;
   L.off_partials = off;
   off = align_up(off + L.big.size() * kNormBlocks * sizeof(float), 256);
+  L.off_tilepart = off;
+  off = align_up(off + static_cast<size_t>(L.prefix.back()) * sizeof(float), 256);
+  L.off_rscale = off;
+  off = align_up(off + L.big.size() * sizeof(float), 256);
   L.off_ext = off;
   off = align_up(off + L.big.size() * 2 * sizeof(int), 256);
   L.off_done = off;
   off = align_up(off + L.big.size() * sizeof(int), kAlign);
   L.off_buffers = off;
   for (BigMat &b : L.big) {
-    b.off_x = off;
-    off = align_up(off + static_cast<size_t>(b.m * b.pn) * L.elt, kAlign);
-    b.off_xt0 = off;
-    off = align_up(off + static_cast<size_t>(b.n * b.pm) * L.elt, kAlign);
-    b.off_xt1 = off;
-    off = align_up(off + static_cast<size_t>(b.n * b.pm) * L.elt, kAlign);
+    if (dtype == NS_BF16) {  // two iterate buffers in the caller's orientation
+      b.off_s0 = off;
+      off = align_up(off + static_cast<size_t>(b.M * b.ps) * L.elt, kAlign);
+      b.off_s1 = off;
+      off = align_up(off + static_cast<size_t>(b.M * b.ps) * L.elt, kAlign);
+    } else {  // W and two W^T buffers
+      b.off_x = off;
+      off = align_up(off + static_cast<size_t>(b.m * b.pn) * L.elt, kAlign);
+      b.off_xt0 = off;
+      off = align_up(off + static_cast<size_t>(b.n * b.pm) * L.elt, kAlign);
+      b.off_xt1 = off;
+      off = align_up(off + static_cast<size_t>(b.n * b.pm) * L.elt, kAlign);
+    }
     b.off_a = off;
     off = align_up(off + static_cast<size_t>(b.m * b.pm) * L.elt, kAlign);
     b.off_b = off;
@@ -244,7 +266,15 @@ void build_layout(const int64_t *shapes, int count, int dtype, Layout &L) {
   L.total = std::max<size_t>(off, 256);
 }
 
-int build_blob(const Layout &L, void *const *X, const int64_t *shapes, uint8_t *ws, std::vector<uint8_t> &blob) {
+// Step 0 of the bf16 path reads the caller's Y through TMA when its base and
+// row pitch are 16-byte aligned, and when a later step (not step 0 itself)
+// is the one that overwrites it.
+bool reads_y_directly(const void *y, int64_t N, int steps) {
+  return steps >= 2 && (reinterpret_cast<uintptr_t>(y) & 15) == 0 && (N * 2) % 16 == 0;
+}
+
+int build_blob(const Layout &L, void *const *X, const int64_t *shapes, int steps, uint8_t *ws,
+               std::vector<uint8_t> &blob) {
   blob.assign(L.blob_end, 0);
   if (L.dtype == NS_BF16 && !L.big.empty()) {
     int rc = get_encode();
@@ -255,9 +285,14 @@ int build_blob(const Layout &L, void *const *X, const int64_t *shapes, uint8_t *
     const BigMat &b = L.big[k];
     MatDesc d;
     std::memset(&d, 0, sizeof(d));
-    d.x = ws + b.off_x;
-    d.xt[0] = ws + b.off_xt0;
-    d.xt[1] = ws + b.off_xt1;
+    if (L.dtype == NS_BF16) {
+      d.s[0] = ws + b.off_s0;
+      d.s[1] = ws + b.off_s1;
+    } else {
+      d.x = ws + b.off_x;
+      d.xt[0] = ws + b.off_xt0;
+      d.xt[1] = ws + b.off_xt1;
+    }
     d.a = ws + b.off_a;
     d.b = ws + b.off_b;
     d.user = X[b.index];
@@ -267,16 +302,18 @@ int build_blob(const Layout &L, void *const *X, const int64_t *shapes, uint8_t *
     d.n = static_cast<int>(b.n);
     d.pm = static_cast<int>(b.pm);
     d.pn = static_cast<int>(b.pn);
+    d.ps = static_cast<int>(b.ps);
     d.transposed = b.transposed;
     d.index = b.index;
     d.t01 = b.t01;
     d.t2 = b.t2;
     if (L.dtype == NS_BF16) {
-      int rc = encode_bf16(&d.tm_x, d.x, b.m, b.n, b.pn);
-      rc = rc ? rc : encode_bf16(&d.tm_a, d.a, b.m, b.m, b.pm);
-      rc = rc ? rc : encode_bf16(&d.tm_b, d.b, b.m, b.m, b.pm);
-      rc = rc ? rc : encode_bf16(&d.tm_xt[0], d.xt[0], b.n, b.m, b.pm);
-      rc = rc ? rc : encode_bf16(&d.tm_xt[1], d.xt[1], b.n, b.m, b.pm);
+      d.direct = reads_y_directly(d.user, b.N, steps);
+      int rc = encode_bf16(&d.tm_a, d.a, b.m, b.m, b.pm, kTcBM);
+      rc = rc ? rc : encode_bf16(&d.tm_b, d.b, b.m, b.m, b.pm, kTcBM);
+      rc = rc ? rc : encode_iterate(&d.tm_s[0], &d.tm_s_mn[0], d.s[0], b.M, b.N, b.ps);
+      rc = rc ? rc : encode_iterate(&d.tm_s[1], &d.tm_s_mn[1], d.s[1], b.M, b.N, b.ps);
+      if (!rc && d.direct) rc = encode_iterate(&d.tm_y, &d.tm_y_mn, d.user, b.M, b.N, b.N);
       if (rc) return rc;
     }
     std::memcpy(mats + k * sizeof(MatDesc), &d, sizeof(d));
@@ -398,8 +435,19 @@ int execute(const Layout &L, uint8_t *ws, int steps, const float *co, bool table
   pp.eps = eps;
   pp.dtype = L.dtype;
   pp.to_user = steps == 0;
-  if (timed(0, s, [&] { return launch_norm(pp, s); })) return NS_ECUDA;
-  if (timed(1, s, [&] { return launch_prep(pp, L.prefix.back(), s); })) return NS_ECUDA;
+  pp.tile_partials = reinterpret_cast<float *>(ws + L.off_tilepart);
+  pp.rscale = reinterpret_cast<float *>(ws + L.off_rscale);
+  // bf16 with steps: one pass sums Y (and copies it unscaled into the first
+  // iterate buffer where step 0 cannot read Y itself); the first step's
+  // epilogues apply 1/(||Y|| + eps). Otherwise: norm, then a scaled copy.
+  const bool fused = L.dtype == NS_BF16 && steps > 0;
+  if (fused) {
+    if (timed(1, s, [&] { return launch_norm_tiles(pp, L.prefix.back(), 2 * di->sms, s); })) return NS_ECUDA;
+    if (timed(0, s, [&] { return launch_norm_finish(pp, s); })) return NS_ECUDA;
+  } else {
+    if (timed(0, s, [&] { return launch_norm(pp, s); })) return NS_ECUDA;
+    if (timed(1, s, [&] { return launch_prep(pp, L.prefix.back(), s); })) return NS_ECUDA;
+  }
   const Tile *t01 = reinterpret_cast<const Tile *>(ws + L.off_t01);
   const Tile *t2 = reinterpret_cast<const Tile *>(ws + L.off_t2);
   if (steps == 0) return NS_OK;
@@ -414,6 +462,7 @@ int execute(const Layout &L, uint8_t *ws, int steps, const float *co, bool table
     tp.ext = ext;
     tp.status = di->status;
     tp.done = done;
+    tp.rscale = pp.rscale;
     tp.ncoef = table ? steps : 1;
     for (int k = 0; k < (table ? steps : 1); ++k)
       for (int u = 0; u < 3; ++u) tp.coef[k][u] = co[3 * k + u];
@@ -490,7 +539,7 @@ int run(void *const *X, const int64_t *shapes, int count, int steps, const float
     if (rc) return rc;
     ws = cache->ptr;
   }
-  rc = build_blob(L, X, shapes, ws, blob);
+  rc = build_blob(L, X, shapes, steps, ws, blob);
   if (rc) return rc;
   if (!cache || cache->last_blob != blob) {
     if (cudaMemcpyAsync(ws, blob.data(), blob.size(), cudaMemcpyHostToDevice, s) != cudaSuccess) return NS_ECUDA;

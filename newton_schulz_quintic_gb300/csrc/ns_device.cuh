@@ -314,11 +314,30 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
   return d;
 }
 
-// Instruction descriptor of kind::f16: D fp32, A and B bf16, both K-major.
-__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N) {
+// Shared-memory descriptor of an MN-major operand tile with 128-byte swizzle:
+// the MN index runs along the 128-byte rows (64 bf16), one row per K index.
+// The tile is stored as 64-element MN chunks of 64 K rows each (8 KB, one
+// TMA box), so chunks are 8192 B apart (leading byte offset) and groups of 8
+// K rows 1024 B apart (stride byte offset); a K step of 16 advances the start
+// by 2048 B.
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr >> 4) & 0x3FFFu);  // start address
+  d |= static_cast<uint64_t>(8192u >> 4) << 16;            // leading byte offset: next 64 MN elements
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;            // stride byte offset: next 8 K rows
+  d |= static_cast<uint64_t>(1u) << 46;                    // descriptor version
+  d |= static_cast<uint64_t>(2u) << 61;                    // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor of kind::f16: D fp32, A and B bf16; a_mn / b_mn
+// select an MN-major ("transposed") A or B operand, else K-major.
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N, int a_mn = 0, int b_mn = 0) {
   return (1u << 4)                                   // D format: f32
          | (1u << 7)                                 // A format: bf16
          | (1u << 10)                                // B format: bf16
+         | (static_cast<uint32_t>(a_mn & 1) << 15)   // A major-ness
+         | (static_cast<uint32_t>(b_mn & 1) << 16)   // B major-ness
          | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }

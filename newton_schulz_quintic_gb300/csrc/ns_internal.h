@@ -1,18 +1,26 @@
 // ns_internal.h -- structures shared by the host planner and the kernels of
 // libns (batched quintic Newton-Schulz on sm_103a). Not part of the C ABI.
 //
-// Working layout of one matrix on the large-matrix path. The caller's matrix
-// Y is M x N row-major. The iteration works on W (m x n, m = min(M,N)),
-// W = Y^T when M > N ("transposed"). The workspace holds, per matrix:
-//   x      W      m x n   row pitch pn = round_up(n, 8) elements
-//   xt[2]  W^T    n x m   row pitch pm = round_up(m, 8); ping-pong across steps
-//   a      A      m x m   row pitch pm  (A = W W^T, symmetric)
-//   b      B      m x m   row pitch pm  (B = b A + c A^2, symmetric)
-// All five are row-major with the contraction index contiguous for the way
-// they are consumed, so every GEMM reads both operands K-major:
-//   gram    A[i,j]  = sum_k x[i,k]  x[j,k]        (K = n)
-//   square  C[i,j]  = sum_k a[i,k]  a[j,k]        (K = m; A symmetric so A A = A A^T)
-//   apply   D[j,i]  = sum_k xt[j,k] b[i,k]        (K = m; D = (B W)^T)
+// Working layout of one matrix on the large-matrix paths. The caller's
+// matrix Y is M x N row-major. The iteration works on W (m x n,
+// m = min(M,N)), W = Y^T when M > N ("transposed").
+//
+// bf16 tensor-core path: every iterate is kept in the caller's orientation
+// (Y-shaped, so W^T when transposed) and the GEMMs read whichever operand
+// order that gives, K-major or MN-major (tcgen05 reads both):
+//   s[2]   iterates  M x N   row pitch ps = round_up(N, 8); ping-pong across
+//                            steps (step 0 reads Y itself when TMA can address it)
+//   a      A         m x m   row pitch pm = round_up(m, 8)  (A = W W^T, symmetric)
+//   b      B         m x m   row pitch pm  (B = b A + c A^2, symmetric)
+//   gram    A[i,j] = sum_k W[i,k] W[j,k]    (K = n; MN-major operands when transposed)
+//   square  C[i,j] = sum_k A[i,k] A[j,k]    (K = m; A symmetric so A A = A A^T)
+//   apply   not transposed: D = B W   (W read MN-major), D[i,j] over m x n
+//           transposed:     D = W^T B (W^T = the iterate, K-major), D over n x m
+//           either way D is the next iterate in the caller's orientation.
+// fp32 CUDA-core path: both orientations are kept, all reads K-major:
+//   x      W      m x n   row pitch pn = round_up(n, 8)
+//   xt[2]  W^T    n x m   row pitch pm; ping-pong across steps
+//   a, b   as above
 // Pitches are multiples of 16 bytes so TMA can address every row.
 #pragma once
 
@@ -35,19 +43,26 @@ struct Tile {
 };
 
 struct MatDesc {  // CUtensorMap members keep it 64-byte aligned or more
-  CUtensorMap tm_x;      // x,  box {64, 128}
-  CUtensorMap tm_a;      // a,  box {64, 128}
-  CUtensorMap tm_b;      // b,  box {64, 128}
-  CUtensorMap tm_xt[2];  // xt, box {64, 128}
-  void *x;
+  // bf16 path, 128-byte swizzle. K-major loads take one box of 64 columns x
+  // 128 rows; MN-major loads two boxes of 64 x 64 (the swizzle span limits
+  // a box row to 128 bytes, i.e. 64 elements of the MN index)
+  CUtensorMap tm_a;       // a, box {64, 128}
+  CUtensorMap tm_b;       // b, box {64, 128}
+  CUtensorMap tm_s[2];    // s[0], s[1], box {64, 128}
+  CUtensorMap tm_s_mn[2]; // s[0], s[1], box {64, 64}
+  CUtensorMap tm_y;       // the caller's Y (used when `direct`), box {64, 128}
+  CUtensorMap tm_y_mn;    // the caller's Y, box {64, 64}
+  void *x;               // fp32 path: W
+  void *xt[2];           // fp32 path: W^T ping-pong
+  void *s[2];            // bf16 path: iterates in the caller's orientation
   void *a;
   void *b;
-  void *xt[2];
   void *user;            // caller's Y (M x N row-major)
   int M, N;              // caller's shape
   int m, n;              // working shape
-  int pm, pn;            // pitches (elements) of m-wide and n-wide buffers
+  int pm, pn, ps;        // pitches (elements) of m-wide, n-wide and N-wide buffers
   int transposed;        // 1 when M > N
+  int direct;            // bf16 path: step 0 reads Y itself (else an exact copy in s[0])
   int index;             // position in the caller's batch
   int t01, t2;           // tensor-core path: pair tiles of this matrix per gram/square and per apply
 };
@@ -92,6 +107,7 @@ struct TcParams {
   const int *ext;       // per matrix {rows_eff, cols_eff} in the caller's orientation
   int *status;
   int *done;            // per matrix completion counter (zeroed by the host per call)
+  const float *rscale;  // per matrix 1 / (||Y||_F + eps): step 0 scales gram by its square and apply by it
   int ncoef;            // 1: coef[0] for every step; else coef[step]
   float coef[kMaxTableSteps][3];
 };
@@ -106,6 +122,8 @@ struct PrepParams {
   float eps;
   int dtype;             // StoreType of the caller's data == workspace store type
   int to_user;           // 1: write the normalised matrix back to the caller (steps == 0)
+  float *tile_partials;  // bf16 path: one sum of squares per 64x64 tile of W
+  float *rscale;         // bf16 path: per matrix 1 / (||Y||_F + eps)
 };
 
 struct ResParams {
@@ -137,6 +155,8 @@ constexpr int kSimtBN = 64;
 // host-side launchers (defined in the .cu files)
 int launch_norm(const PrepParams &p, cudaStream_t s);
 int launch_prep(const PrepParams &p, int total_tiles, cudaStream_t s);
+int launch_norm_tiles(const PrepParams &p, int total_tiles, int max_blocks, cudaStream_t s);
+int launch_norm_finish(const PrepParams &p, cudaStream_t s);
 int launch_resident(const ResParams &p, int maxm, int smem_bytes, cudaStream_t s);
 int launch_simt_phase(int phase, const PhaseParams &p, cudaStream_t s);
 int launch_tc(const TcParams &p, int max_ctas, cudaStream_t s);

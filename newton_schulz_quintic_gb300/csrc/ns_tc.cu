@@ -14,9 +14,10 @@
 // rows r*128 .. r*128+127 of the first operand and rows r*128 .. r*128+127 of
 // the second in its own shared memory, and receives rows r*128 .. of the
 // 256 x 256 accumulator in its own TMEM. No operand byte is loaded twice.
-//   warp 0      TMA producer (both CTAs): its 128x64 box of each operand per
-//               k-block into a 6-stage ring of 32 KB (128-byte swizzle); the
-//               bytes of both CTAs are counted on the leader's full barrier;
+//   warp 0      TMA producer (both CTAs): its 128 x 64 share of each operand
+//               per k-block (two 64 x 64 boxes, K-major or MN-major) into a
+//               6-stage ring of 32 KB (128-byte swizzle); the bytes of both
+//               CTAs are counted on the leader's full barrier;
 //   warp 1      TMEM allocation (512 columns = two accumulators, cta_group::2)
 //               in both CTAs; in the leader one thread issues the pair MMAs and
 //               the commits that release stages and hand accumulators to both
@@ -26,11 +27,14 @@
 //               in fp32, round-to-nearest-even to bf16 and the stores; the
 //               second accumulator lets the next tile's main loop overlap it;
 //   warp 10     publishes each stored item on its matrix's completion counter.
-// Phases (all operands K-major, see ns_internal.h for the layout):
-//   0 gram    A = W W^T             upper-triangle tiles; stores tile + mirror
+// Phases (see ns_internal.h for the layout). Iterates stay in the caller's
+// orientation; step 0 reads the caller's Y directly when TMA can address it.
+//   0 gram    A = W W^T             upper-triangle tiles; stores tile + mirror;
+//                                   operands MN-major when the matrix is transposed
 //   1 square  B = b A + c (A A)     upper-triangle tiles; stores tile + mirror
-//   2 apply   W' = a W + B W        computed as (B W)^T tiles over W^T; stores
-//                                   W'^T and W' (or the caller's Y on the last step)
+//   2 apply   W' = a W + B W        tiles of the next iterate in the caller's
+//                                   orientation (B W, or W^T B when transposed),
+//                                   one straight store (the caller's Y on the last step)
 // Tiles wholly outside a matrix's non-zero extent are skipped, and k-loops
 // stop at the extent: zero rows and columns stay zero through every step.
 // Every wait is bounded (see mbar_wait); a timeout sets the status word and
@@ -58,6 +62,8 @@ constexpr int kABytes = kTcBM * kTcBK * 2;          // 16 KB: this CTA's 128 row
 constexpr int kBBytes = (kTcBN / 2) * kTcBK * 2;    // 16 KB: this CTA's half of the second operand
 constexpr int kStageBytes = kABytes + kBBytes;      // 32 KB per CTA
 constexpr int kPairStageBytes = 2 * kStageBytes;    // both CTAs' loads, counted at the leader
+constexpr int kBoxBytes = 64 * 64 * 2;             // one TMA box: 64 x 64 bf16
+static_assert(kABytes == 2 * kBoxBytes && kBBytes == 2 * kBoxBytes, "operand share = two boxes");
 constexpr int kAccs = 2;                            // accumulators (each kTcBN TMEM columns)
 constexpr int kTmemCols = kAccs * kTcBN;
 
@@ -101,12 +107,77 @@ __device__ __forceinline__ TileInfo tile_info(const TcParams &p, int phase, int 
   const int e0 = p.ext[2 * tl.mat], e1 = p.ext[2 * tl.mat + 1];
   const int tr = ti.d->transposed;
   const int meff = tr ? e1 : e0, neff = tr ? e0 : e1;
-  const int rows_eff = phase == 2 ? neff : meff;
   const int k_eff = phase == 0 ? neff : meff;
-  // decided per pair tile, so both CTAs of a cluster agree
-  ti.skip = (tl.row0 >= rows_eff) || (tl.col0 >= meff);
+  // decided per pair tile, so both CTAs of a cluster agree; gram and square
+  // tiles are over m x m, apply tiles over the caller's M x N
+  ti.skip = phase == 2 ? (tl.row0 >= e0) || (tl.col0 >= e1) : (tl.row0 >= meff) || (tl.col0 >= meff);
   ti.nk = (k_eff + kTcBK - 1) / kTcBK;
   return ti;
+}
+
+// Where an item's operands come from: tensor map and major-ness of the first
+// (A, rows of the tile) and second (B, columns of the tile) operand.
+struct Operands {
+  const void *map_a, *map_b;
+  int a_mn, b_mn;  // 1: MN-major (the tile's index runs along memory rows), else K-major
+};
+
+__device__ __forceinline__ Operands operands(const MatDesc &d, int step, int phase) {
+  // the iterate read at this step: Y itself or its copy on step 0, then the
+  // ping-pong buffers; each has a K-major and an MN-major map
+  const bool y = step == 0 && d.direct;
+  const void *src_k = y ? &d.tm_y : &d.tm_s[step & 1];
+  const void *src_mn = y ? &d.tm_y_mn : &d.tm_s_mn[step & 1];
+  Operands o;
+  if (phase == 0) {  // W W^T: W's rows are the iterate's columns when transposed
+    o.map_a = o.map_b = d.transposed ? src_mn : src_k;
+    o.a_mn = o.b_mn = d.transposed;
+  } else if (phase == 1) {
+    o.map_a = o.map_b = &d.tm_a;
+    o.a_mn = o.b_mn = 0;
+  } else if (d.transposed) {  // W^T B: iterate rows (K-major) times B
+    o.map_a = src_k;
+    o.map_b = &d.tm_b;
+    o.a_mn = o.b_mn = 0;
+  } else {  // B W: B rows times the iterate's columns (MN-major)
+    o.map_a = &d.tm_b;
+    o.map_b = src_mn;
+    o.a_mn = 0;
+    o.b_mn = 1;
+  }
+  return o;
+}
+
+// TMA of one operand share: 128 tile rows [mn0, mn0 + 128) by K [k0, k0 + 64).
+// K-major: one box of 128 rows. MN-major: box rows are K indices and the tile
+// index runs along them, 64 per box row, so two 64 x 64 boxes 8 KB apart.
+// MN is a template parameter so the producer issues only the copies it needs.
+template <int MN>
+__device__ __forceinline__ void load_operand(uint8_t *dst, const void *map, int mn0, int k0, uint32_t bar_cluster,
+                                             uint64_t pol) {
+  if (MN) {
+    tma_load_2d_pair(dst, map, mn0, k0, bar_cluster, pol);
+    tma_load_2d_pair(dst + kBoxBytes, map, mn0 + 64, k0, bar_cluster, pol);
+  } else {
+    tma_load_2d_pair(dst, map, k0, mn0, bar_cluster, pol);
+  }
+}
+
+// Operand descriptor of the share at `addr` for K sub-step kk (16 K each).
+template <int MN>
+__device__ __forceinline__ uint64_t operand_desc(uint32_t addr, int kk) {
+  return MN ? sw128_mnmajor_desc(addr + static_cast<uint32_t>(kk) * 2048u)
+            : sw128_kmajor_desc(addr + static_cast<uint32_t>(kk) * 32u);
+}
+
+// The iterate read at `step` (the caller's Y or a workspace buffer) and its pitch.
+__device__ __forceinline__ const __nv_bfloat16 *iterate_src(const MatDesc &d, int step, int &pitch) {
+  if (step == 0 && d.direct) {
+    pitch = d.N;
+    return static_cast<const __nv_bfloat16 *>(d.user);
+  }
+  pitch = d.ps;
+  return static_cast<const __nv_bfloat16 *>(d.s[step & 1]);
 }
 
 // The signal warp of each CTA advances a matrix's counter by one per item,
@@ -124,19 +195,23 @@ __device__ __forceinline__ int units_before(const MatDesc &d, int step, int phas
 
 // Per-item constants of the epilogue.
 struct StepCtx {
-  int cur;          // W^T ping-pong buffer read by apply
+  int step;
   int final_step;   // apply writes the caller's matrix
   float ca, cb, cc;
+  float gs, as;     // step 0 folds the normalisation in: A *= r^2, W' *= r (else 1)
 };
 
-__device__ __forceinline__ StepCtx step_ctx(const TcParams &p, int step) {
+__device__ __forceinline__ StepCtx step_ctx(const TcParams &p, int step, int mat) {
   const float *co = p.coef[p.ncoef == 1 ? 0 : step];
   StepCtx c;
-  c.cur = step & 1;
+  c.step = step;
   c.final_step = step == p.steps - 1;
   c.ca = co[0];
   c.cb = co[1];
   c.cc = co[2];
+  const float r = (step == 0 && p.rscale) ? p.rscale[mat] : 1.0f;
+  c.gs = r * r;
+  c.as = r;
   return c;
 }
 
@@ -237,7 +312,7 @@ __device__ __forceinline__ void warp_store_transposed(uint32_t *stage, const flo
 }
 
 // The global operand an epilogue chunk reads besides the accumulator (A for
-// square, W^T for apply), fetched ahead of time: 32 bf16 of this thread's
+// square, the current iterate for apply), fetched ahead of time: 32 bf16 of this thread's
 // row when the whole chunk is in range (the common case); edge chunks are
 // read element by element inside epilogue_chunk instead. Both tensors are
 // read-only during the launch.
@@ -252,10 +327,10 @@ __device__ __forceinline__ void prefetch_chunk(const StepCtx &p, const TileInfo 
     if (i < d.m && jb >= i && jb + 32 <= d.m)
       src = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(d.a) + static_cast<size_t>(i) * d.pm + jb);
   } else {
-    const int jr = ti.row0 + r, ib = ti.col0 + chunk * 32;
-    if (jr < d.n && ib + 32 <= d.m)
-      src = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(d.xt[p.cur]) +
-                                            static_cast<size_t>(jr) * d.pm + ib);
+    const int R = ti.row0 + r, C = ti.col0 + chunk * 32;
+    int sp;
+    const __nv_bfloat16 *S = iterate_src(d, p.step, sp);
+    if (R < d.M && C + 32 <= d.N) src = reinterpret_cast<const uint4 *>(S + static_cast<size_t>(R) * sp + C);
   }
 #pragma unroll
   for (int q = 0; q < 4; ++q) out[q] = src ? __ldg(src + q) : make_uint4(0, 0, 0, 0);
@@ -279,6 +354,10 @@ __device__ __forceinline__ void epilogue_chunk(const StepCtx &p, const TileInfo 
     const int jb = ti.col0 + chunk * 32;
     // warp-uniform: the whole 32x32 block is outside the matrix or below the diagonal
     if (i0 >= m || jb + 31 < i0) return;
+    if (PHASE == 0) {
+#pragma unroll
+      for (int t = 0; t < 32; ++t) f[t] *= p.gs;  // A = r^2 Y Y^T on the first step
+    }
     const bool mine = i < m && jb + 31 >= i;  // this lane's row has elements with j >= i
     const bool full = (jb >= i) && (jb + 32 <= m);
     if (PHASE == 1) {
@@ -301,36 +380,31 @@ __device__ __forceinline__ void epilogue_chunk(const StepCtx &p, const TileInfo 
     warp_store_rows(stage, f, O, pm, i0, m, jb, m, true);
     warp_store_transposed(stage, f, O, pm, jb, m, i0, m, true);
   } else {
-    const int m = d.m, n = d.n, pm = d.pm, pn = d.pn;
-    const int jr = ti.row0 + r;          // row of W^T (index over n)
-    const int jr0 = ti.row0 + r0;        // the warp's first row
-    const int ib = ti.col0 + chunk * 32; // column of W^T (index over m)
-    if (jr0 >= n || ib >= m) return;     // warp-uniform
-    const bool mine = jr < n;
-    const int cur = p.cur;
-    const bool full = ib + 32 <= m;
-    const __nv_bfloat16 *XT = static_cast<const __nv_bfloat16 *>(d.xt[cur]) + static_cast<size_t>(jr) * pm + ib;
+    // tile rows R over the caller's M, columns C over N
+    const int M = d.M, N = d.N;
+    const int R = ti.row0 + r;
+    const int R0 = ti.row0 + r0;         // the warp's first row
+    const int C = ti.col0 + chunk * 32;
+    if (R0 >= M || C >= N) return;       // warp-uniform
+    const bool mine = R < M;
+    const bool full = C + 32 <= N;
+    int sp;
+    const __nv_bfloat16 *S = iterate_src(d, p.step, sp);
+    S += static_cast<size_t>(R) * sp + C;
     float xo[32];
     if (full) {
       unpack_row32(pre, xo);
     } else {
 #pragma unroll
-      for (int t = 0; t < 32; ++t) xo[t] = (mine && ib + t < m) ? __bfloat162float(XT[t]) : 0.f;
+      for (int t = 0; t < 32; ++t) xo[t] = (mine && C + t < N) ? __bfloat162float(S[t]) : 0.f;
     }
 #pragma unroll
-    for (int t = 0; t < 32; ++t) f[t] = p.ca * xo[t] + f[t];
-
-    if (!p.final_step) {
-      // W'^T rows jr (this warp's rows) and W' rows ib + t
-      warp_store_rows(stage, f, static_cast<__nv_bfloat16 *>(d.xt[cur ^ 1]), pm, jr0, n, ib, m, false);
-      warp_store_transposed(stage, f, static_cast<__nv_bfloat16 *>(d.x), pn, ib, m, jr0, n, false);
-    } else {
-      __nv_bfloat16 *U = static_cast<__nv_bfloat16 *>(d.user);
-      if (d.transposed)  // caller's Y is n x m: rows jr, columns ib..
-        warp_store_rows(stage, f, U, static_cast<size_t>(d.N), jr0, n, ib, m, false);
-      else               // caller's Y is m x n: rows ib + t, columns jr0..
-        warp_store_transposed(stage, f, U, static_cast<size_t>(d.N), ib, m, jr0, n, false);
-    }
+    for (int t = 0; t < 32; ++t) f[t] = p.as * (p.ca * xo[t] + f[t]);  // r (a Y + B Y) on the first step
+    if (!p.final_step)
+      warp_store_rows(stage, f, static_cast<__nv_bfloat16 *>(d.s[(p.step + 1) & 1]), static_cast<size_t>(d.ps), R0,
+                      M, C, N, false);
+    else
+      warp_store_rows(stage, f, static_cast<__nv_bfloat16 *>(d.user), static_cast<size_t>(N), R0, M, C, N, false);
   }
 }
 
@@ -382,6 +456,55 @@ __device__ __forceinline__ bool epilogue_item(const StepCtx &sc, const TileInfo 
     if (k + 1 < kChunksPerWarp) {
       __syncwarp();
       tmem_ld_wait(next_v);
+    }
+  }
+  return true;
+}
+
+// The producer's copies of one item in one CTA: for each k-block, wait for
+// the stage to be free, and load this CTA's share of both operands (a0, b0:
+// first tile row of each share) onto the leader's full barrier.
+template <int AMN, int BMN>
+__device__ __forceinline__ bool produce_item(const Operands &op, int nk, int a0, int b0, uint8_t *sA, uint8_t *sB,
+                                             Barriers *bar, bool leader, int &stage, uint32_t &phase_bit,
+                                             int *issued_phase, uint64_t pol, volatile int *abort, int *status) {
+  for (int kb = 0; kb < nk; ++kb) {
+    if (!mbar_wait<true>(&bar->empty[stage], phase_bit ^ 1u, abort, status)) return false;
+    if (leader) mbar_arrive_expect_tx(&bar->full[stage], kPairStageBytes);
+    const uint32_t full_leader = mapa_shared(smem_u32(&bar->full[stage]), 0);
+    const int kx = kb * kTcBK;
+    load_operand<AMN>(sA + stage * kABytes, op.map_a, a0, kx, full_leader, pol);
+    load_operand<BMN>(sB + stage * kBBytes, op.map_b, b0, kx, full_leader, pol);
+    issued_phase[stage] = static_cast<int>(phase_bit);
+    if (++stage == kStages) {
+      stage = 0;
+      phase_bit ^= 1u;
+    }
+  }
+  return true;
+}
+
+// The leader's MMAs of one item: for each k-block, wait for both CTAs'
+// operand shares, issue the four K = 16 pair MMAs into `d_tmem` and release
+// the stage to both producers. AMN / BMN: MN-major first / second operand.
+template <int AMN, int BMN>
+__device__ __forceinline__ bool mma_item(uint32_t d_tmem, int nk, uint8_t *sA, uint8_t *sB, Barriers *bar,
+                                         int &stage, uint32_t &phase_bit, volatile int *abort, int *status) {
+  constexpr uint32_t idesc = umma_idesc_bf16(kTcCluster * kTcBM, kTcBN, AMN, BMN);
+  constexpr uint16_t kPairMask = (1u << kTcCluster) - 1;
+  for (int kb = 0; kb < nk; ++kb) {
+    if (!mbar_wait<true>(&bar->full[stage], phase_bit, abort, status)) return false;
+    tc_fence_after();
+    const uint32_t a_addr = smem_u32(sA + stage * kABytes);
+    const uint32_t b_addr = smem_u32(sB + stage * kBBytes);
+#pragma unroll
+    for (int k = 0; k < kTcBK / 16; ++k)
+      umma_bf16_pair(d_tmem, operand_desc<AMN>(a_addr, k), operand_desc<BMN>(b_addr, k), idesc,
+                     (kb | k) != 0 ? 1u : 0u);
+    umma_commit_pair_multicast(&bar->empty[stage], kPairMask);
+    if (++stage == kStages) {
+      stage = 0;
+      phase_bit ^= 1u;
     }
   }
   return true;
@@ -452,26 +575,17 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
           if (!wait_count(p.done + ti.mat, units_before(*ti.d, step, phase), abort, p.status)) break;
           fence_proxy_async_global();
         }
-        const int cur = step & 1;
-        const void *mapA = phase == 0 ? &ti.d->tm_x : phase == 1 ? &ti.d->tm_a : &ti.d->tm_xt[cur];
-        const void *mapB = phase == 0 ? &ti.d->tm_x : phase == 1 ? &ti.d->tm_a : &ti.d->tm_b;
-        for (int kb = 0; kb < ti.nk; ++kb) {
-          if (!mbar_wait<true>(&bar->empty[stage], phase_bit ^ 1u, abort, p.status)) {
-            ok = false;
-            break;
-          }
-          if (leader) mbar_arrive_expect_tx(&bar->full[stage], kPairStageBytes);
-          const uint32_t full_leader = mapa_shared(smem_u32(&bar->full[stage]), 0);
-          const int kx = kb * kTcBK;
-          tma_load_2d_pair(sA + stage * kABytes, mapA, kx, ti.row0 + my_rows, full_leader, pol);
-          tma_load_2d_pair(sB + stage * kBBytes, mapB, kx, ti.col0 + static_cast<int>(rank) * (kTcBN / 2),
-                           full_leader, pol);
-          issued_phase[stage] = static_cast<int>(phase_bit);
-          if (++stage == kStages) {
-            stage = 0;
-            phase_bit ^= 1u;
-          }
-        }
+        const Operands op = operands(*ti.d, step, phase);
+        const int a0 = ti.row0 + my_rows, b0 = ti.col0 + static_cast<int>(rank) * (kTcBN / 2);
+        if (op.a_mn)
+          ok = produce_item<1, 1>(op, ti.nk, a0, b0, sA, sB, bar, leader, stage, phase_bit, issued_phase, pol, abort,
+                                  p.status);
+        else if (op.b_mn)
+          ok = produce_item<0, 1>(op, ti.nk, a0, b0, sA, sB, bar, leader, stage, phase_bit, issued_phase, pol, abort,
+                                  p.status);
+        else
+          ok = produce_item<0, 0>(op, ti.nk, a0, b0, sA, sB, bar, leader, stage, phase_bit, issued_phase, pol, abort,
+                                  p.status);
       }
       if (*abort && leader) {
         for (int s = 0; s < kStages; ++s)
@@ -481,7 +595,6 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
   } else if (tmem_ok && warp == 1) {
     if (lane == 0 && leader) {
       // ---------------------------------------------------- pair MMA issuer (leader)
-      constexpr uint32_t idesc = umma_idesc_bf16(kTcCluster * kTcBM, kTcBN);
       int stage = 0;
       uint32_t phase_bit = 0;
       int acc = 0;
@@ -492,28 +605,17 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
         decode_item(p, g, step, phase, t);
         const TileInfo ti = tile_info(p, phase, t);
         if (ti.skip) continue;
+        const Operands op = operands(*ti.d, step, phase);
         if (!mbar_wait<true>(&bar->tempty[acc], acc_phase ^ 1u, abort, p.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * kTcBN);
-        for (int kb = 0; kb < ti.nk; ++kb) {
-          if (!mbar_wait<true>(&bar->full[stage], phase_bit, abort, p.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a_addr = smem_u32(sA + stage * kABytes);
-          const uint32_t b_addr = smem_u32(sB + stage * kBBytes);
-#pragma unroll
-          for (int k = 0; k < kTcBK / 16; ++k) {
-            umma_bf16_pair(d_tmem, sw128_kmajor_desc(a_addr + k * 32), sw128_kmajor_desc(b_addr + k * 32), idesc,
-                           (kb | k) != 0 ? 1u : 0u);
-          }
-          umma_commit_pair_multicast(&bar->empty[stage], kPairMask);
-          if (++stage == kStages) {
-            stage = 0;
-            phase_bit ^= 1u;
-          }
-        }
+        // one k-loop per operand order, so descriptors stay compile-time
+        if (op.a_mn)
+          ok = mma_item<1, 1>(d_tmem, ti.nk, sA, sB, bar, stage, phase_bit, abort, p.status);
+        else if (op.b_mn)
+          ok = mma_item<0, 1>(d_tmem, ti.nk, sA, sB, bar, stage, phase_bit, abort, p.status);
+        else
+          ok = mma_item<0, 0>(d_tmem, ti.nk, sA, sB, bar, stage, phase_bit, abort, p.status);
         if (!ok) break;
         umma_commit_pair_multicast(&bar->tfull[acc], kPairMask);
         if (++acc == kAccs) {
@@ -547,7 +649,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
         if (!__shfl_sync(0xffffffffu, ready ? 1 : 0, 0)) break;
       }
       ti.row0 += my_rows;
-      const StepCtx sc = step_ctx(p, step);
+      const StepCtx sc = step_ctx(p, step, ti.mat);
       const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kTcBN);
       bool ok;
       if (phase == 0)

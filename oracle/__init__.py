@@ -161,11 +161,12 @@ def orthogonalize_np(X, steps: int = DEFAULT_STEPS, coeffs=DEFAULT_COEFFS,
     product: s = ||X||_F; X/(s+eps); transpose when M > N (orient as above);
     then ``steps`` times A = W W^T, B = b A + c A A, W = a W + B W.
 
-    emulate="bf16" is a diagnostic, not the oracle: it rounds the normalised
-    W, and after every step A, B and W, to bfloat16 (each product and
-    element-wise combination itself stays fp64), i.e. the storage precision of
-    a bf16 tensor-core implementation that keeps those three matrices in bf16
-    between phases."""
+    emulate="bf16" is a diagnostic, not the oracle: after every step it
+    rounds A, B and W to bfloat16 (each product and element-wise combination
+    itself stays fp64), i.e. the storage precision of a bf16 tensor-core
+    implementation that keeps those three matrices in bf16 between phases and
+    folds the normalisation into the first step (W_0 = Y/(s+eps) itself is
+    never stored, so never rounded)."""
     W = np.array(to_f64(X), dtype=np.float64, copy=True)
     if W.ndim != 2:
         raise ValueError("oracle takes 2-D matrices")
@@ -177,7 +178,7 @@ def orthogonalize_np(X, steps: int = DEFAULT_STEPS, coeffs=DEFAULT_COEFFS,
     table = coeff_table(coeffs, steps)
     rows = [tuple(float(v) for v in coeffs)] * int(steps) if table is None else [tuple(r) for r in table]
     s = np.sqrt(np.sum(W * W))
-    W = rnd(W / (s + float(eps)))
+    W = W / (s + float(eps))
     M, N = W.shape
     transpose = (M > N) if orient == 0 else (orient == 2)
     if transpose:

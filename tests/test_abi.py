@@ -59,8 +59,12 @@ def test_workspace_bytes(lib):
     assert api.workspace_bytes([], 1) > 0
     small = api.workspace_bytes([(64, 128)], api.NS_F32)      # resident path: descriptors only
     big = api.workspace_bytes([(8192, 6144)], api.NS_BF16)
-    # W, two W^T buffers, A and B of a 6144 x 8192 working matrix, bf16
-    assert big >= 2 * (3 * 6144 * 8192 + 2 * 6144 * 6144)
+    # bf16: two iterates in the caller's orientation, A and B (6144 x 6144)
+    need = 2 * (2 * 8192 * 6144 + 2 * 6144 * 6144)
+    assert need <= big < need + (1 << 20)
+    # fp32: W, two W^T buffers, A and B
+    big32 = api.workspace_bytes([(8192, 6144)], api.NS_F32)
+    assert big32 >= 4 * (3 * 6144 * 8192 + 2 * 6144 * 6144)
     assert small < 1 << 20
     assert api.workspace_bytes([(-1, 5)], api.NS_BF16) == 0
     assert api.workspace_bytes([(5, 5)], 7) == 0

@@ -108,7 +108,8 @@ size_t ns_workspace_bytes(const int64_t *shapes, int count, int dtype);
  * ns_orthogonalize_batched_host -- the same operation on HOST matrices:
  * copies each X_host[i] to the device, runs the method, copies the results
  * back into X_host[i] and returns once they are there. The batch is split into
- * up to 8 contiguous groups of about equal bytes; the copies in of group g+1,
+ * up to 8 contiguous groups of about equal bytes, each of at least 32 MiB
+ * (a smaller batch is one group); the copies in of group g+1,
  * the Newton-Schulz of group g (on `stream`) and the copies out of group g-1
  * overlap on two library-owned streams ordered by events. Host buffers may be
  * pageable or pinned (only pinned buffers let the copies overlap). Device

@@ -621,15 +621,20 @@ int ns_orthogonalize_batched_host(void *const *X_host, const int64_t *shapes, in
     off[i] = total;
     total = align_up(total + bytes[i], 256);
   }
-  // contiguous groups of about total/8 bytes: group g's copies in, its
-  // Newton-Schulz and group g-1's copies out overlap
+  // contiguous groups of about total/G bytes: group g's copies in, its
+  // Newton-Schulz and group g-1's copies out overlap. G is at most 8 and
+  // groups hold at least 32 MiB: a group's kernels take about as long for one
+  // small matrix as for many (one CTA per small matrix), so splitting a small
+  // batch would only repeat that latency.
   constexpr int kMaxGroups = 8;
+  constexpr size_t kMinGroupBytes = size_t(32) << 20;
+  const int max_groups = static_cast<int>(std::min<size_t>(kMaxGroups, std::max<size_t>(1, total / kMinGroupBytes)));
   std::vector<int> gstart{0};
   size_t acc = 0;
   for (int i = 0; i < count; ++i) {
     acc += bytes[i];
-    if (acc * kMaxGroups >= total * gstart.size() && i + 1 < count &&
-        static_cast<int>(gstart.size()) < kMaxGroups)
+    if (acc * max_groups >= total * gstart.size() && i + 1 < count &&
+        static_cast<int>(gstart.size()) < max_groups)
       gstart.push_back(i + 1);
   }
   gstart.push_back(count);

@@ -85,6 +85,7 @@ struct TileInfo {
   int mat;
   int row0, col0;
   int nk;
+  int tr;  // the matrix is transposed (M > N)
   bool skip;
 };
 
@@ -97,15 +98,15 @@ __device__ __forceinline__ void decode_item(const TcParams &p, int g, int &step,
   t = phase == 0 ? r : (phase == 1 ? r - p.n01 : r - 2 * p.n01);
 }
 
-__device__ __forceinline__ TileInfo tile_info(const TcParams &p, int phase, int t) {
-  const Tile tl = (phase < 2 ? p.tiles01 : p.tiles2)[t];
+// Tile info from the tile record, the matrix's extents and its orientation.
+__device__ __forceinline__ TileInfo make_tile_info(const TcParams &p, int phase, const Tile &tl, int e0, int e1,
+                                                   int tr) {
   TileInfo ti;
   ti.mat = tl.mat;
   ti.d = p.mats + tl.mat;
   ti.row0 = tl.row0;
   ti.col0 = tl.col0;
-  const int e0 = p.ext[2 * tl.mat], e1 = p.ext[2 * tl.mat + 1];
-  const int tr = ti.d->transposed;
+  ti.tr = tr;
   const int meff = tr ? e1 : e0, neff = tr ? e0 : e1;
   const int k_eff = phase == 0 ? neff : meff;
   // decided per pair tile, so both CTAs of a cluster agree; gram and square
@@ -115,6 +116,65 @@ __device__ __forceinline__ TileInfo tile_info(const TcParams &p, int phase, int 
   return ti;
 }
 
+__device__ __forceinline__ TileInfo tile_info(const TcParams &p, int phase, int t) {
+  const Tile tl = (phase < 2 ? p.tiles01 : p.tiles2)[t];
+  return make_tile_info(p, phase, tl, p.ext[2 * tl.mat], p.ext[2 * tl.mat + 1], p.mats[tl.mat].transposed);
+}
+
+// The items of one cluster (g, g + stride, ...) with their global lookups
+// pipelined, for the single-thread roles whose every stall idles the tensor
+// pipe: while an item runs, the tile record of the item after next and the
+// extents and orientation of the next item are already being loaded. Only
+// loaded values are carried; arithmetic on them waits until the item is taken.
+struct ItemPipe {
+  int g;                   // item taken next
+  int step, phase;         // of item g
+  Tile tl;                 // of item g
+  int e0, e1, tr, direct;  // of item g's matrix
+  int step2, phase2;       // of item g + stride
+  Tile tl2;                // of item g + stride
+};
+
+__device__ __forceinline__ Tile fetch_tile(const TcParams &p, int g, int &step, int &phase) {
+  int t;
+  decode_item(p, g, step, phase, t);
+  return (phase < 2 ? p.tiles01 : p.tiles2)[t];
+}
+
+__device__ __forceinline__ void fetch_matrix(const TcParams &p, ItemPipe &q) {
+  const MatDesc &d = p.mats[q.tl.mat];
+  q.e0 = p.ext[2 * q.tl.mat];
+  q.e1 = p.ext[2 * q.tl.mat + 1];
+  q.tr = d.transposed;
+  q.direct = d.direct;
+}
+
+__device__ __forceinline__ void pipe_start(const TcParams &p, int g, int stride, ItemPipe &q) {
+  q.g = g;
+  if (g < p.g_end) {
+    q.tl = fetch_tile(p, g, q.step, q.phase);
+    fetch_matrix(p, q);
+  }
+  if (g + stride < p.g_end) q.tl2 = fetch_tile(p, g + stride, q.step2, q.phase2);
+}
+
+// Take item q.g (returned through step, phase, ti) and start the lookups of the two after it.
+__device__ __forceinline__ void pipe_take(const TcParams &p, int stride, ItemPipe &q, int &step, int &phase,
+                                          TileInfo &ti, int &direct) {
+  step = q.step;
+  phase = q.phase;
+  ti = make_tile_info(p, q.phase, q.tl, q.e0, q.e1, q.tr);
+  direct = q.direct;
+  q.g += stride;
+  if (q.g < p.g_end) {
+    q.step = q.step2;
+    q.phase = q.phase2;
+    q.tl = q.tl2;
+    fetch_matrix(p, q);
+  }
+  if (q.g + stride < p.g_end) q.tl2 = fetch_tile(p, q.g + stride, q.step2, q.phase2);
+}
+
 // Where an item's operands come from: tensor map and major-ness of the first
 // (A, rows of the tile) and second (B, columns of the tile) operand.
 struct Operands {
@@ -122,20 +182,20 @@ struct Operands {
   int a_mn, b_mn;  // 1: MN-major (the tile's index runs along memory rows), else K-major
 };
 
-__device__ __forceinline__ Operands operands(const MatDesc &d, int step, int phase) {
+__device__ __forceinline__ Operands operands(const MatDesc &d, int step, int phase, int transposed, int direct) {
   // the iterate read at this step: Y itself or its copy on step 0, then the
   // ping-pong buffers; each has a K-major and an MN-major map
-  const bool y = step == 0 && d.direct;
+  const bool y = step == 0 && direct;
   const void *src_k = y ? &d.tm_y : &d.tm_s[step & 1];
   const void *src_mn = y ? &d.tm_y_mn : &d.tm_s_mn[step & 1];
   Operands o;
   if (phase == 0) {  // W W^T: W's rows are the iterate's columns when transposed
-    o.map_a = o.map_b = d.transposed ? src_mn : src_k;
-    o.a_mn = o.b_mn = d.transposed;
+    o.map_a = o.map_b = transposed ? src_mn : src_k;
+    o.a_mn = o.b_mn = transposed;
   } else if (phase == 1) {
     o.map_a = o.map_b = &d.tm_a;
     o.a_mn = o.b_mn = 0;
-  } else if (d.transposed) {  // W^T B: iterate rows (K-major) times B
+  } else if (transposed) {  // W^T B: iterate rows (K-major) times B
     o.map_a = src_k;
     o.map_b = &d.tm_b;
     o.a_mn = o.b_mn = 0;
@@ -564,10 +624,12 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
       int stage = 0;
       uint32_t phase_bit = 0;
       bool ok = true;
-      for (int g = p.g_begin + cluster; g < p.g_end && ok; g += nclusters) {
-        int step, phase, t;
-        decode_item(p, g, step, phase, t);
-        const TileInfo ti = tile_info(p, phase, t);
+      ItemPipe q;
+      pipe_start(p, p.g_begin + cluster, nclusters, q);
+      while (q.g < p.g_end && ok) {
+        int step, phase, direct;
+        TileInfo ti;
+        pipe_take(p, nclusters, q, step, phase, ti, direct);
         if (ti.skip) continue;
         if (p.wait) {
           // operands come from earlier phases of this matrix, written by
@@ -575,7 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
           if (!wait_count(p.done + ti.mat, units_before(*ti.d, step, phase), abort, p.status)) break;
           fence_proxy_async_global();
         }
-        const Operands op = operands(*ti.d, step, phase);
+        const Operands op = operands(*ti.d, step, phase, ti.tr, direct);
         const int a0 = ti.row0 + my_rows, b0 = ti.col0 + static_cast<int>(rank) * (kTcBN / 2);
         if (op.a_mn)
           ok = produce_item<1, 1>(op, ti.nk, a0, b0, sA, sB, bar, leader, stage, phase_bit, issued_phase, pol, abort,
@@ -600,12 +662,14 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int g = p.g_begin + cluster; g < p.g_end && ok; g += nclusters) {
-        int step, phase, t;
-        decode_item(p, g, step, phase, t);
-        const TileInfo ti = tile_info(p, phase, t);
+      ItemPipe q;
+      pipe_start(p, p.g_begin + cluster, nclusters, q);
+      while (q.g < p.g_end && ok) {
+        int step, phase, direct;
+        TileInfo ti;
+        pipe_take(p, nclusters, q, step, phase, ti, direct);
         if (ti.skip) continue;
-        const Operands op = operands(*ti.d, step, phase);
+        const Operands op = operands(*ti.d, step, phase, ti.tr, direct);
         if (!mbar_wait<true>(&bar->tempty[acc], acc_phase ^ 1u, abort, p.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * kTcBN);

@@ -7,7 +7,8 @@
 // one device workspace, builds the per-phase tile lists and TMA descriptors,
 // uploads them, and launches:
 //   resident kernel (all small matrices at once)
-//   norm  ->  prep  ->  steps x { gram -> square -> apply }  (all large matrices)
+//   bf16: tile norms -> norm finish -> steps x { gram -> square -> apply }
+//   fp32: norm -> prep -> steps x { gram -> square -> apply }  (all large matrices)
 // The megabatch of the first page's "Concrete repro" is just `count`
 // matrices of one shape; remainder batches (the xtuner PR's ragged
 // all-to-all commit) are calls with a smaller `count`, so no zero matrix is

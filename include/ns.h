@@ -110,8 +110,11 @@ size_t ns_workspace_bytes(const int64_t *shapes, int count, int dtype);
  * back into X_host[i] and returns once they are there. The batch is split into
  * up to 8 contiguous groups of about equal bytes, each of at least 32 MiB
  * (a smaller batch is one group); the copies in of group g+1,
- * the Newton-Schulz of group g (on `stream`) and the copies out of group g-1
- * overlap on two library-owned streams ordered by events. Host buffers may be
+ * the Newton-Schulz of group g and the copies out of group g-1 overlap on
+ * library-owned streams ordered by events (even groups compute on `stream`,
+ * odd groups on a second library stream, so one group's last partial wave of
+ * tiles overlaps the next group's first; under NS_SCHED_SINGLE every group
+ * computes on `stream`). Host buffers may be
  * pageable or pinned (only pinned buffers let the copies overlap). Device
  * copies and workspaces are part of the internal per-(device, stream) cache.
  */
@@ -209,10 +212,12 @@ int64_t ns_num_kernel_launches(void);
  * caller's stream (a few microseconds of overhead per launch).
  * ns_set_kernel_timing(1) enables and clears the record, (0) disables it.
  * ns_get_kernel_times synchronises on the recorded events and writes, for the
- * kernel classes 0 norm, 1 prep, 2 gram, 3 square, 4 apply, 5 resident,
- * 6 gemm (the tensor-core kernel running every step and phase of a call in
- * one launch), the total milliseconds into ms[k] and the launch count into
- * launches[k] for k < n (n <= 7). Returns NS_OK or NS_ECUDA.
+ * kernel classes 0 norm (per-matrix scale), 1 prep (the pass over the caller's
+ * matrices: bf16 tile sums and extents, plus a copy where the first step
+ * cannot read them in place; fp32 the normalising copy), 2 gram, 3 square,
+ * 4 apply, 5 resident, 6 gemm (the tensor-core kernel running every step and
+ * phase of a call in one launch), the total milliseconds into ms[k] and the
+ * launch count into launches[k] for k < n (n <= 7). Returns NS_OK or NS_ECUDA.
  */
 int ns_set_kernel_timing(int enable);
 

@@ -553,6 +553,7 @@ int run(void *const *X, const int64_t *shapes, int count, int steps, const float
 // Streams and events of the host entry point, created once per device.
 struct HostPipe {
   cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaStream_t comp2 = nullptr;  // second compute stream: odd groups run there
   std::vector<cudaEvent_t> ev;
 };
 std::map<int, HostPipe> g_pipe;
@@ -561,6 +562,7 @@ int host_pipe(int dev, size_t nev, HostPipe **out) {
   HostPipe &hp = g_pipe[dev];
   if (!hp.h2d && cudaStreamCreateWithFlags(&hp.h2d, cudaStreamNonBlocking) != cudaSuccess) return NS_ECUDA;
   if (!hp.d2h && cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking) != cudaSuccess) return NS_ECUDA;
+  if (!hp.comp2 && cudaStreamCreateWithFlags(&hp.comp2, cudaStreamNonBlocking) != cudaSuccess) return NS_ECUDA;
   while (hp.ev.size() < nev) {
     cudaEvent_t e;
     if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return NS_ECUDA;
@@ -654,31 +656,42 @@ int ns_orthogonalize_batched_host(void *const *X_host, const int64_t *shapes, in
     rc = ensure_ws(c, std::max<size_t>(total, 256), s);
     if (rc) return rc;
     dbuf = c.ptr;
-    rc = host_pipe(dev, 2 * static_cast<size_t>(ngroups) + 1, &hp);
+    rc = host_pipe(dev, 2 * static_cast<size_t>(ngroups) + 2, &hp);
     if (rc) return rc;
   }
   std::vector<void *> dptr(count);
   for (int i = 0; i < count; ++i) dptr[i] = dbuf + off[i];
-  cudaEvent_t ev_start = hp->ev[2 * ngroups];
-  // the copies in start after earlier work on the caller's stream
-  if (cudaEventRecord(ev_start, s) != cudaSuccess || cudaStreamWaitEvent(hp->h2d, ev_start, 0) != cudaSuccess)
+  cudaEvent_t ev_start = hp->ev[2 * ngroups], ev_comp2 = hp->ev[2 * ngroups + 1];
+  // Odd groups compute on a second stream, so the partial last wave of one
+  // group's launches shares the GPU with the start of the next group's (the
+  // per-phase launches never wait on one another). The single-launch schedule
+  // keeps every group on the caller's stream: its cooperative launch must
+  // have the whole GPU.
+  cudaStream_t comp[2] = {s, phase_launches() ? hp->comp2 : s};
+  // the copies in and the second compute stream start after earlier work on the caller's stream
+  if (cudaEventRecord(ev_start, s) != cudaSuccess || cudaStreamWaitEvent(hp->h2d, ev_start, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(hp->comp2, ev_start, 0) != cudaSuccess)
     return NS_ECUDA;
   for (int g = 0; g < ngroups; ++g) {
     const int i0 = gstart[g], i1 = gstart[g + 1];
+    cudaStream_t cs = comp[g & 1];
     cudaEvent_t ev_in = hp->ev[2 * g], ev_out = hp->ev[2 * g + 1];
     for (int i = i0; i < i1; ++i)
       if (bytes[i] && cudaMemcpyAsync(dptr[i], X_host[i], bytes[i], cudaMemcpyHostToDevice, hp->h2d) != cudaSuccess)
         return NS_ECUDA;
-    if (cudaEventRecord(ev_in, hp->h2d) != cudaSuccess || cudaStreamWaitEvent(s, ev_in, 0) != cudaSuccess)
+    if (cudaEventRecord(ev_in, hp->h2d) != cudaSuccess || cudaStreamWaitEvent(cs, ev_in, 0) != cudaSuccess)
       return NS_ECUDA;
-    rc = run(dptr.data() + i0, shapes + 2 * i0, i1 - i0, steps, coeffs, 1e-7f, dtype, nullptr, 0, s, 2 + g);
+    rc = run(dptr.data() + i0, shapes + 2 * i0, i1 - i0, steps, coeffs, 1e-7f, dtype, nullptr, 0, cs, 2 + g);
     if (rc) return rc;
-    if (cudaEventRecord(ev_out, s) != cudaSuccess || cudaStreamWaitEvent(hp->d2h, ev_out, 0) != cudaSuccess)
+    if (cudaEventRecord(ev_out, cs) != cudaSuccess || cudaStreamWaitEvent(hp->d2h, ev_out, 0) != cudaSuccess)
       return NS_ECUDA;
     for (int i = i0; i < i1; ++i)
       if (bytes[i] && cudaMemcpyAsync(X_host[i], dptr[i], bytes[i], cudaMemcpyDeviceToHost, hp->d2h) != cudaSuccess)
         return NS_ECUDA;
   }
+  // the caller's stream is ordered after the second compute stream's work
+  if (cudaEventRecord(ev_comp2, hp->comp2) != cudaSuccess || cudaStreamWaitEvent(s, ev_comp2, 0) != cudaSuccess)
+    return NS_ECUDA;
   if (cudaStreamSynchronize(hp->d2h) != cudaSuccess) return NS_ECUDA;
   return cudaStreamSynchronize(s) == cudaSuccess ? NS_OK : NS_ECUDA;
 }

@@ -3,21 +3,22 @@
 // One persistent, warp-specialised kernel, launched as clusters of two CTAs
 // over a sequence of work items: for every step, the gram tiles of all
 // matrices, then the square tiles, then the apply tiles (each list largest
-// ns_cost first); an item is one 256 x 256 output tile. By default one launch
-// runs every step and phase of the call: before loading an item's operands
-// the producer waits until every item of the same matrix in earlier phases is
-// complete (a per-matrix counter that epilogue warps advance after their
-// stores), so the phases of different matrices overlap and the kernel never
-// drains between phases. Each tile is one pair MMA
+// ns_cost first); an item is one 256 x 256 output tile. By default the host
+// launches the kernel once per step and phase, over that phase's items. In
+// the single-launch schedule one launch runs every step and phase of the
+// call: before loading an item's operands the producer waits until every item
+// of the same matrix in earlier phases is complete (a per-matrix counter that
+// the signal warp advances after the epilogue's stores), so the phases of
+// different matrices overlap. Each tile is one pair MMA
 // (tcgen05.mma.cta_group::2, M = 256, N = 256, K = 16, bf16 in, fp32
 // accumulate) issued by the pair's leader CTA (rank 0): CTA rank r holds
 // rows r*128 .. r*128+127 of the first operand and rows r*128 .. r*128+127 of
 // the second in its own shared memory, and receives rows r*128 .. of the
 // 256 x 256 accumulator in its own TMEM. No operand byte is loaded twice.
 //   warp 0      TMA producer (both CTAs): its 128 x 64 share of each operand
-//               per k-block (two 64 x 64 boxes, K-major or MN-major) into a
-//               6-stage ring of 32 KB (128-byte swizzle); the bytes of both
-//               CTAs are counted on the leader's full barrier;
+//               per k-block (one 64 x 128 box K-major, or two 64 x 64 boxes
+//               MN-major) into a 6-stage ring of 32 KB (128-byte swizzle);
+//               the bytes of both CTAs are counted on the leader's full barrier;
 //   warp 1      TMEM allocation (512 columns = two accumulators, cta_group::2)
 //               in both CTAs; in the leader one thread issues the pair MMAs and
 //               the commits that release stages and hand accumulators to both
@@ -707,7 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
       TileInfo ti = tile_info(p, phase, t);
       if (ti.skip) continue;
       if (p.wait) {
-        // the operand this epilogue reloads (A, W^T) comes from an earlier phase
+        // the operand this epilogue reloads (A, or the current iterate) comes from an earlier phase
         bool ready = true;
         if (lane == 0) ready = wait_count(p.done + ti.mat, units_before(*ti.d, step, phase), abort, p.status);
         if (!__shfl_sync(0xffffffffu, ready ? 1 : 0, 0)) break;

@@ -144,6 +144,19 @@ __device__ __forceinline__ bool wait_count(const int *counter, int need, volatil
   }
 }
 
+// One lane of the (converged) warp is elected: the lowest active lane. Used
+// to issue a warp's asynchronous copies, MMAs and commits from one thread
+// while the whole warp runs the loop around them.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b32 r;\n\t"
+      "elect.sync r|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

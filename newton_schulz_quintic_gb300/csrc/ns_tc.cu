@@ -522,6 +522,15 @@ __device__ __forceinline__ bool epilogue_item(const StepCtx &sc, const TileInfo 
   return true;
 }
 
+// A wait of a whole warp that only lane 0 polls (the other lanes sleep in
+// the shuffle that broadcasts the outcome), leaving the warp converged.
+template <bool kCluster>
+__device__ __forceinline__ bool warp_mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort, int *status) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait<kCluster>(bar, parity, abort, status) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
 // The producer's copies of one item in one CTA: for each k-block, wait for
 // the stage to be free, and load this CTA's share of both operands (a0, b0:
 // first tile row of each share) onto the leader's full barrier.
@@ -530,12 +539,15 @@ __device__ __forceinline__ bool produce_item(const Operands &op, int nk, int a0,
                                              Barriers *bar, bool leader, int &stage, uint32_t &phase_bit,
                                              int *issued_phase, uint64_t pol, volatile int *abort, int *status) {
   for (int kb = 0; kb < nk; ++kb) {
-    if (!mbar_wait<true>(&bar->empty[stage], phase_bit ^ 1u, abort, status)) return false;
-    if (leader) mbar_arrive_expect_tx(&bar->full[stage], kPairStageBytes);
-    const uint32_t full_leader = mapa_shared(smem_u32(&bar->full[stage]), 0);
-    const int kx = kb * kTcBK;
-    load_operand<AMN>(sA + stage * kABytes, op.map_a, a0, kx, full_leader, pol);
-    load_operand<BMN>(sB + stage * kBBytes, op.map_b, b0, kx, full_leader, pol);
+    if (!warp_mbar_wait<true>(&bar->empty[stage], phase_bit ^ 1u, abort, status)) return false;
+    if (elect_one()) {
+      if (leader) mbar_arrive_expect_tx(&bar->full[stage], kPairStageBytes);
+      const uint32_t full_leader = mapa_shared(smem_u32(&bar->full[stage]), 0);
+      const int kx = kb * kTcBK;
+      load_operand<AMN>(sA + stage * kABytes, op.map_a, a0, kx, full_leader, pol);
+      load_operand<BMN>(sB + stage * kBBytes, op.map_b, b0, kx, full_leader, pol);
+    }
+    __syncwarp();
     issued_phase[stage] = static_cast<int>(phase_bit);
     if (++stage == kStages) {
       stage = 0;
@@ -554,15 +566,18 @@ __device__ __forceinline__ bool mma_item(uint32_t d_tmem, int nk, uint8_t *sA, u
   constexpr uint32_t idesc = umma_idesc_bf16(kTcCluster * kTcBM, kTcBN, AMN, BMN);
   constexpr uint16_t kPairMask = (1u << kTcCluster) - 1;
   for (int kb = 0; kb < nk; ++kb) {
-    if (!mbar_wait<true>(&bar->full[stage], phase_bit, abort, status)) return false;
+    if (!warp_mbar_wait<true>(&bar->full[stage], phase_bit, abort, status)) return false;
     tc_fence_after();
     const uint32_t a_addr = smem_u32(sA + stage * kABytes);
     const uint32_t b_addr = smem_u32(sB + stage * kBBytes);
+    if (elect_one()) {
 #pragma unroll
-    for (int k = 0; k < kTcBK / 16; ++k)
-      umma_bf16_pair(d_tmem, operand_desc<AMN>(a_addr, k), operand_desc<BMN>(b_addr, k), idesc,
-                     (kb | k) != 0 ? 1u : 0u);
-    umma_commit_pair_multicast(&bar->empty[stage], kPairMask);
+      for (int k = 0; k < kTcBK / 16; ++k)
+        umma_bf16_pair(d_tmem, operand_desc<AMN>(a_addr, k), operand_desc<BMN>(b_addr, k), idesc,
+                       (kb | k) != 0 ? 1u : 0u);
+      umma_commit_pair_multicast(&bar->empty[stage], kPairMask);
+    }
+    __syncwarp();
     if (++stage == kStages) {
       stage = 0;
       phase_bit ^= 1u;
@@ -617,8 +632,9 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
   volatile int *abort = &bar->abort;
 
   if (tmem_ok && warp == 0) {
-    if (lane == 0) {
+    {
       // ---------------------------------------------------- TMA producer (both CTAs)
+      // the whole warp runs the loop; one elected lane issues each copy
       const uint64_t pol = l2_policy_evict_normal();
       int issued_phase[kStages];
       for (int s = 0; s < kStages; ++s) issued_phase[s] = -1;
@@ -635,7 +651,9 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
         if (p.wait) {
           // operands come from earlier phases of this matrix, written by
           // epilogues anywhere on the GPU
-          if (!wait_count(p.done + ti.mat, units_before(*ti.d, step, phase), abort, p.status)) break;
+          int ready = 1;
+          if (lane == 0) ready = wait_count(p.done + ti.mat, units_before(*ti.d, step, phase), abort, p.status) ? 1 : 0;
+          if (!__shfl_sync(0xffffffffu, ready, 0)) break;
           fence_proxy_async_global();
         }
         const Operands op = operands(*ti.d, step, phase, ti.tr, direct);
@@ -650,14 +668,15 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
           ok = produce_item<0, 0>(op, ti.nk, a0, b0, sA, sB, bar, leader, stage, phase_bit, issued_phase, pol, abort,
                                   p.status);
       }
-      if (*abort && leader) {
+      if (*abort && leader && lane == 0) {
         for (int s = 0; s < kStages; ++s)
           if (issued_phase[s] >= 0) mbar_drain(&bar->full[s], static_cast<uint32_t>(issued_phase[s]), p.status);
       }
     }
   } else if (tmem_ok && warp == 1) {
-    if (lane == 0 && leader) {
+    if (leader) {
       // ---------------------------------------------------- pair MMA issuer (leader)
+      // the whole warp runs the loop; one elected lane issues the MMAs and commits
       int stage = 0;
       uint32_t phase_bit = 0;
       int acc = 0;
@@ -671,7 +690,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
         pipe_take(p, nclusters, q, step, phase, ti, direct);
         if (ti.skip) continue;
         const Operands op = operands(*ti.d, step, phase, ti.tr, direct);
-        if (!mbar_wait<true>(&bar->tempty[acc], acc_phase ^ 1u, abort, p.status)) break;
+        if (!warp_mbar_wait<true>(&bar->tempty[acc], acc_phase ^ 1u, abort, p.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * kTcBN);
         // one k-loop per operand order, so descriptors stay compile-time
@@ -682,14 +701,18 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
         else
           ok = mma_item<0, 0>(d_tmem, ti.nk, sA, sB, bar, stage, phase_bit, abort, p.status);
         if (!ok) break;
-        umma_commit_pair_multicast(&bar->tfull[acc], kPairMask);
+        if (elect_one()) umma_commit_pair_multicast(&bar->tfull[acc], kPairMask);
+        __syncwarp();
         if (++acc == kAccs) {
           acc = 0;
           acc_phase ^= 1u;
         }
       }
-      umma_commit_pair_multicast(&bar->drain, 1u);
-      mbar_drain(&bar->drain, 0, p.status);
+      if (elect_one()) {
+        umma_commit_pair_multicast(&bar->drain, 1u);
+        mbar_drain(&bar->drain, 0, p.status);
+      }
+      __syncwarp();
     }
   } else if (tmem_ok && warp < kSignalWarp) {
     // ------------------------------------------------------ epilogue (both CTAs)

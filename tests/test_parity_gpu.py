@@ -410,6 +410,28 @@ def test_host_entry_point_pageable_buffers():
         assert torch.equal(r, h)
 
 
+@pytest.mark.parametrize("schedule", ["phase", "single"])
+def test_host_entry_point_many_groups_matches_device_call(schedule):
+    # ~134 MiB of inputs: the host entry point splits them into several
+    # groups of at least 32 MiB, odd groups computing on a second stream under
+    # the per-phase schedule (one stream under the single-launch one). Every
+    # matrix is computed independently, so each result has the same bits as
+    # the one-call device entry point's.
+    shapes = [(2048, 2048)] * 16 + [(1500, 3000), (3000, 1500), (24, 100)]
+    xs = [seeded(s, torch.bfloat16, seed=90 + i) for i, s in enumerate(shapes)]
+    ref = run_gpu(xs)
+    api.set_gemm_schedule(schedule)
+    try:
+        host = [x.clone().pin_memory() for x in xs]
+        api.orthogonalize_batched_host(host)
+        assert api.get_status() == 0
+    finally:
+        api.set_gemm_schedule("phase")
+    for r, h in zip(ref, host):
+        assert torch.equal(r, h)
+    check_one(xs[18], host[18])
+
+
 # ------------------------------------------------------------ CUDA graphs
 
 @pytest.mark.parametrize("dtype,shapes", [(torch.bfloat16, [(640, 1200), (1200, 640), (24, 2304)]),

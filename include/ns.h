@@ -64,7 +64,8 @@ extern "C" {
  *   X       host array of `count` device pointers; X[i] points at a
  *           contiguous row-major matrix of shapes[2i] x shapes[2i+1]
  *           elements of `dtype`. Matrices may differ in shape; a zero
- *           dimension makes that matrix a no-op. Matrices must not overlap.
+ *           dimension makes that matrix a no-op. Matrices must not overlap
+ *           (checked: overlapping ranges give NS_EINVAL).
  *   shapes  host array of 2*count int64 (M, N) pairs, read before return.
  *   count   number of matrices (0 is valid and does nothing).
  *   steps   number of iterations (>= 0; 0 = normalisation only).

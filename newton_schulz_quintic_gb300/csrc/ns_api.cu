@@ -160,6 +160,21 @@ int validate(void *const *X, const int64_t *shapes, int count, int steps, int dt
       if (reinterpret_cast<uintptr_t>(X[i]) % elt) return NS_EALIGN;
     }
   }
+  if (check_ptrs) {
+    // matrices must not overlap: the last step of one writes its matrix in
+    // place while another may still be reading its own
+    std::vector<std::pair<uintptr_t, uintptr_t>> r;
+    r.reserve(count);
+    for (int i = 0; i < count; ++i) {
+      const int64_t M = shapes[2 * i], N = shapes[2 * i + 1];
+      if (M * N == 0) continue;
+      const uintptr_t b = reinterpret_cast<uintptr_t>(X[i]);
+      r.emplace_back(b, b + static_cast<uintptr_t>(M * N) * elt);
+    }
+    std::sort(r.begin(), r.end());
+    for (size_t k = 1; k < r.size(); ++k)
+      if (r[k].first < r[k - 1].second) return NS_EINVAL;
+  }
   return NS_OK;
 }
 

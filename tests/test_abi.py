@@ -20,6 +20,14 @@ def lib():
     return api.load_library()
 
 
+def _has_gpu():
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
@@ -89,6 +97,17 @@ def test_validation_rejects_before_launch(lib):
     assert _call(lib, (P * 1)(0x100001), good_shape, 1) == -2            # misaligned bf16
     assert _call(lib, (P * 1)(0x100002), good_shape, 1, dtype=api.NS_F32) == -2  # misaligned f32
     assert lib.ns_orthogonalize_batched_ex(good_ptrs, good_shape, 1, 5, None, 1e-7, 1, None, 0, None) == -1
+
+
+@pytest.mark.skipif(_has_gpu(), reason="uses fake device pointers: only run where nothing can launch")
+def test_validation_rejects_overlapping_matrices(lib):
+    # every case here must be refused by validation, before any launch
+    P, S = ctypes.c_void_p, ctypes.c_int64
+    shapes = (S * 4)(4, 8, 4, 8)                                        # 64 bytes each in bf16
+    assert _call(lib, (P * 2)(0x100000, 0x100000), shapes, 2) == -1    # the same matrix twice
+    assert _call(lib, (P * 2)(0x100000, 0x100030), shapes, 2) == -1    # overlapping by 16 bytes
+    assert _call(lib, (P * 2)(0x100030, 0x100000), shapes, 2) == -1    # either order
+    assert _call(lib, (P * 3)(0x200000, 0x100000, 0x10003e), (S * 6)(4, 8, 4, 8, 1, 1), 3) == -1
 
 
 def test_strerror(lib):

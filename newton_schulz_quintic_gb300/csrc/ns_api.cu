@@ -115,7 +115,7 @@ int encode_bf16(CUtensorMap *map, void *base, int64_t rows, int64_t cols, int64_
   return r == CUDA_SUCCESS ? NS_OK : NS_ECUDA;
 }
 
-// The two maps of one iterate-shaped tensor: K-major box {64, 128}, MN-major box {64, 64}.
+// The two maps of one tensor read both ways: K-major box {64, 128}, MN-major box {64, 64}.
 int encode_iterate(CUtensorMap *kmajor, CUtensorMap *mnmajor, void *base, int64_t rows, int64_t cols,
                    int64_t pitch) {
   int rc = encode_bf16(kmajor, base, rows, cols, pitch, kTcBM);
@@ -325,8 +325,8 @@ int build_blob(const Layout &L, void *const *X, const int64_t *shapes, int steps
     d.t2 = b.t2;
     if (L.dtype == NS_BF16) {
       d.direct = reads_y_directly(d.user, b.N, steps);
-      int rc = encode_bf16(&d.tm_a, d.a, b.m, b.m, b.pm, kTcBM);
-      rc = rc ? rc : encode_bf16(&d.tm_b, d.b, b.m, b.m, b.pm, kTcBM);
+      int rc = encode_iterate(&d.tm_a, &d.tm_a_mn, d.a, b.m, b.m, b.pm);
+      rc = rc ? rc : encode_iterate(&d.tm_b, &d.tm_b_mn, d.b, b.m, b.m, b.pm);
       rc = rc ? rc : encode_iterate(&d.tm_s[0], &d.tm_s_mn[0], d.s[0], b.M, b.N, b.ps);
       rc = rc ? rc : encode_iterate(&d.tm_s[1], &d.tm_s_mn[1], d.s[1], b.M, b.N, b.ps);
       if (!rc && d.direct) rc = encode_iterate(&d.tm_y, &d.tm_y_mn, d.user, b.M, b.N, b.N);

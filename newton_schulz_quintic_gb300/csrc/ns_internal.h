@@ -10,10 +10,13 @@
 // order that gives, K-major or MN-major (tcgen05 reads both):
 //   s[2]   iterates  M x N   row pitch ps = round_up(N, 8); ping-pong across
 //                            steps (step 0 reads Y itself when TMA can address it)
-//   a      A         m x m   row pitch pm = round_up(m, 8)  (A = W W^T, symmetric)
-//   b      B         m x m   row pitch pm  (B = b A + c A^2, symmetric)
+//   a      A         m x m   row pitch pm = round_up(m, 8)  (A = W W^T, symmetric;
+//                            only its upper 256 x 256 tiles are stored, whole)
+//   b      B         m x m   row pitch pm  (B = b A + c A^2, symmetric; upper tiles)
 //   gram    A[i,j] = sum_k W[i,k] W[j,k]    (K = n; MN-major operands when transposed)
-//   square  C[i,j] = sum_k A[i,k] A[j,k]    (K = m; A symmetric so A A = A A^T)
+//   square  C[i,j] = sum_k A[i,k] A[j,k]    (K = m; A symmetric so A A = A A^T;
+//                                            A[i,k] with k left of i's diagonal tile is
+//                                            read MN-major as A[k,i] from an upper tile)
 //   apply   not transposed: D = B W   (W read MN-major), D[i,j] over m x n
 //           transposed:     D = W^T B (W^T = the iterate, K-major), D over n x m
 //           either way D is the next iterate in the caller's orientation.
@@ -48,6 +51,8 @@ struct MatDesc {  // CUtensorMap members keep it 64-byte aligned or more
   // a box row to 128 bytes, i.e. 64 elements of the MN index)
   CUtensorMap tm_a;       // a, box {64, 128}
   CUtensorMap tm_b;       // b, box {64, 128}
+  CUtensorMap tm_a_mn;    // a, box {64, 64} (rows left of the diagonal, read from the mirrored upper tiles)
+  CUtensorMap tm_b_mn;    // b, box {64, 64}
   CUtensorMap tm_s[2];    // s[0], s[1], box {64, 128}
   CUtensorMap tm_s_mn[2]; // s[0], s[1], box {64, 64}
   CUtensorMap tm_y;       // the caller's Y (used when `direct`), box {64, 128}

@@ -30,9 +30,11 @@
 //   warp 10     publishes each stored item on its matrix's completion counter.
 // Phases (see ns_internal.h for the layout). Iterates stay in the caller's
 // orientation; step 0 reads the caller's Y directly when TMA can address it.
-//   0 gram    A = W W^T             upper-triangle tiles; stores tile + mirror;
-//                                   operands MN-major when the matrix is transposed
-//   1 square  B = b A + c (A A)     upper-triangle tiles; stores tile + mirror
+//   0 gram    A = W W^T             upper-triangle tiles, each stored whole (no
+//                                   mirror); operands MN-major when transposed
+//   1 square  B = b A + c (A A)     upper-triangle tiles, each stored whole; A's
+//                                   rows left of the diagonal read MN-major from
+//                                   the mirrored upper tiles
 //   2 apply   W' = a W + B W        tiles of the next iterate in the caller's
 //                                   orientation (B W, or W^T B when transposed),
 //                                   one straight store (the caller's Y on the last step)
@@ -53,11 +55,9 @@ constexpr int kSignalWarp = 2 + kEpiWarps;          // publishes item completion
 constexpr int kThreads = 32 * (kSignalWarp + 1);    // producer, MMA, epilogue warps, signal warp
 constexpr int kChunksPerWarp = (kTcBN / 32) / (kEpiWarps / 4);
 // per-warp staging tile of the epilogue's coalesced stores: 32 rows of 32 bf16
-// (16 words + 4 pad), or 16 rows of 32 packed bf16 pairs (32 words + 4 pad)
+// (16 words + 4 pad)
 constexpr int kRowStageWords = 20;
-constexpr int kPairStageWords = 36;
 constexpr int kEpiStageBytes = 32 * kRowStageWords * 4;
-static_assert(16 * kPairStageWords * 4 <= kEpiStageBytes, "staging tile too small");
 constexpr int kStages = 6;
 constexpr int kABytes = kTcBM * kTcBK * 2;          // 16 KB: this CTA's 128 rows of the first operand
 constexpr int kBBytes = (kTcBN / 2) * kTcBK * 2;    // 16 KB: this CTA's half of the second operand
@@ -176,37 +176,63 @@ __device__ __forceinline__ void pipe_take(const TcParams &p, int stride, ItemPip
   if (q.g + stride < p.g_end) q.tl2 = fetch_tile(p, q.g + stride, q.step2, q.phase2);
 }
 
-// Where an item's operands come from: tensor map and major-ness of the first
-// (A, rows of the tile) and second (B, columns of the tile) operand.
-struct Operands {
-  const void *map_a, *map_b;
-  int a_mn, b_mn;  // 1: MN-major (the tile's index runs along memory rows), else K-major
+// The k-loop of an item as three consecutive k-ranges with a fixed operand
+// order each: [0, e0) both operands MN-major, [e0, e1) the first K-major and
+// the second MN-major, [e1, nk) both K-major (any of them may be empty).
+// map[o][0] / map[o][1] are the tensor maps of the first (A, rows of the
+// tile) and second (B, columns of the tile) operand in range o.
+//
+// The symmetric products A and B are stored as their upper 256 x 256 tiles
+// only (every element of each, diagonal tiles included): an operand's rows
+// in tile row X are read K-major from the stored tiles (X, K) for k-blocks of
+// tile column K >= X, and MN-major from the mirrored stored tiles (K, X) for
+// K < X (A = A^T).
+struct ItemPlan {
+  int e0, e1;
+  const void *map[3][2];
 };
 
-__device__ __forceinline__ Operands operands(const MatDesc &d, int step, int phase, int transposed, int direct) {
+__device__ __forceinline__ ItemPlan plan_item(const MatDesc &d, int step, int phase, int transposed, int direct,
+                                              int row0, int col0, int nk) {
   // the iterate read at this step: Y itself or its copy on step 0, then the
   // ping-pong buffers; each has a K-major and an MN-major map
   const bool y = step == 0 && direct;
   const void *src_k = y ? &d.tm_y : &d.tm_s[step & 1];
   const void *src_mn = y ? &d.tm_y_mn : &d.tm_s_mn[step & 1];
-  Operands o;
-  if (phase == 0) {  // W W^T: W's rows are the iterate's columns when transposed
-    o.map_a = o.map_b = transposed ? src_mn : src_k;
-    o.a_mn = o.b_mn = transposed;
-  } else if (phase == 1) {
-    o.map_a = o.map_b = &d.tm_a;
-    o.a_mn = o.b_mn = 0;
-  } else if (transposed) {  // W^T B: iterate rows (K-major) times B
-    o.map_a = src_k;
-    o.map_b = &d.tm_b;
-    o.a_mn = o.b_mn = 0;
-  } else {  // B W: B rows times the iterate's columns (MN-major)
-    o.map_a = &d.tm_b;
-    o.map_b = src_mn;
-    o.a_mn = 0;
-    o.b_mn = 1;
+  const int kb_row = min(row0 / kTcBK, nk), kb_col = min(col0 / kTcBK, nk);  // the diagonal tile's first k-block
+  ItemPlan pl;
+  if (phase == 0) {  // W W^T from the iterate: W's rows are its columns when transposed
+    pl.e0 = pl.e1 = transposed ? nk : 0;
+    pl.map[0][0] = pl.map[0][1] = src_mn;
+    pl.map[1][0] = pl.map[1][1] = src_mn;
+    pl.map[2][0] = pl.map[2][1] = src_k;
+  } else if (phase == 1) {  // A A: both operands from A's upper tiles (row0 <= col0)
+    pl.e0 = kb_row;
+    pl.e1 = max(kb_row, kb_col);
+    pl.map[0][0] = pl.map[0][1] = &d.tm_a_mn;
+    pl.map[1][0] = &d.tm_a;
+    pl.map[1][1] = &d.tm_a_mn;
+    pl.map[2][0] = pl.map[2][1] = &d.tm_a;
+  } else if (transposed) {  // W^T B: iterate rows (K-major) times B's rows col0..
+    pl.e0 = 0;
+    pl.e1 = kb_col;
+    pl.map[0][0] = src_mn;  // (unused: empty range)
+    pl.map[0][1] = &d.tm_b_mn;
+    pl.map[1][0] = src_k;
+    pl.map[1][1] = &d.tm_b_mn;
+    pl.map[2][0] = src_k;
+    pl.map[2][1] = &d.tm_b;
+  } else {  // B W: B's rows row0.. times the iterate's columns (MN-major)
+    pl.e0 = kb_row;
+    pl.e1 = nk;
+    pl.map[0][0] = &d.tm_b_mn;
+    pl.map[0][1] = src_mn;
+    pl.map[1][0] = &d.tm_b;
+    pl.map[1][1] = src_mn;
+    pl.map[2][0] = &d.tm_b;  // (unused: empty range)
+    pl.map[2][1] = src_mn;
   }
-  return o;
+  return pl;
 }
 
 // TMA of one operand share: 128 tile rows [mn0, mn0 + 128) by K [k0, k0 + 64).
@@ -336,42 +362,6 @@ __device__ __forceinline__ void warp_store_rows(uint32_t *stage, const float (&v
   __syncwarp();
 }
 
-// Warp-cooperative transposed store of a 32 x 32 block: lane l holds v[t] =
-// element (row row0 + t, column col0 + l). The block goes through the staging
-// tile as bf16 pairs so that each store instruction writes 8 output rows x 64
-// contiguous bytes. Elements are written only where row < row_lim,
-// column < col_lim and, if strict_lower, column < row.
-__device__ __forceinline__ void warp_store_transposed(uint32_t *stage, const float (&v)[32], __nv_bfloat16 *base,
-                                                      size_t pitch, int row0, int row_lim, int col0, int col_lim,
-                                                      bool strict_lower) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int k = 0; k < 16; ++k) stage[k * kPairStageWords + lane] = pack_bf16x2(v[2 * k], v[2 * k + 1]);
-  __syncwarp();
-  const int piece = lane & 3;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int t = 8 * k + (lane >> 2);  // output row row0 + t
-    const int R = row0 + t;
-    if (R < row_lim) {
-      const uint4 *src = reinterpret_cast<const uint4 *>(stage + (t >> 1) * kPairStageWords + 8 * piece);
-      const uint4 a = src[0], b = src[1];
-      const uint32_t sel = (t & 1) ? 0x7632u : 0x5410u;  // high or low bf16 of each pair
-      const uint4 o = make_uint4(__byte_perm(a.x, a.y, sel), __byte_perm(a.z, a.w, sel), __byte_perm(b.x, b.y, sel),
-                                 __byte_perm(b.z, b.w, sel));
-      const int C0 = col0 + 8 * piece;
-      __nv_bfloat16 *dst = base + static_cast<size_t>(R) * pitch + C0;
-      if (!strict_lower) {
-        store_piece8(dst, o, R, C0, col_lim, false);
-      } else {
-        // column < row: same as column <= row - 1
-        store_piece8(dst, o, R, C0, col_lim < R ? col_lim : R, false);
-      }
-    }
-  }
-  __syncwarp();
-}
-
 // The global operand an epilogue chunk reads besides the accumulator (A for
 // square, the current iterate for apply), fetched ahead of time: 32 bf16 of this thread's
 // row when the whole chunk is in range (the common case); edge chunks are
@@ -385,7 +375,7 @@ __device__ __forceinline__ void prefetch_chunk(const StepCtx &p, const TileInfo 
   const uint4 *src = nullptr;
   if (PHASE == 1) {
     const int i = ti.row0 + r, jb = ti.col0 + chunk * 32;
-    if (i < d.m && jb >= i && jb + 32 <= d.m)
+    if (i < d.m && jb + 32 <= d.m)
       src = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(d.a) + static_cast<size_t>(i) * d.pm + jb);
   } else {
     const int R = ti.row0 + r, C = ti.col0 + chunk * 32;
@@ -413,14 +403,14 @@ __device__ __forceinline__ void epilogue_chunk(const StepCtx &p, const TileInfo 
     const int i = ti.row0 + r;
     const int i0 = ti.row0 + r0;
     const int jb = ti.col0 + chunk * 32;
-    // warp-uniform: the whole 32x32 block is outside the matrix or below the diagonal
-    if (i0 >= m || jb + 31 < i0) return;
+    // warp-uniform: the whole 32x32 block is outside the matrix
+    if (i0 >= m || jb >= m) return;
     if (PHASE == 0) {
 #pragma unroll
       for (int t = 0; t < 32; ++t) f[t] *= p.gs;  // A = r^2 Y Y^T on the first step
     }
-    const bool mine = i < m && jb + 31 >= i;  // this lane's row has elements with j >= i
-    const bool full = (jb >= i) && (jb + 32 <= m);
+    const bool mine = i < m;
+    const bool full = jb + 32 <= m;
     if (PHASE == 1) {
       const __nv_bfloat16 *A = static_cast<const __nv_bfloat16 *>(d.a) + static_cast<size_t>(i) * pm + jb;
       float aold[32];
@@ -430,16 +420,16 @@ __device__ __forceinline__ void epilogue_chunk(const StepCtx &p, const TileInfo 
 #pragma unroll
         for (int t = 0; t < 32; ++t) {
           const int j = jb + t;
-          aold[t] = (mine && j >= i && j < m) ? __bfloat162float(A[t]) : 0.f;
+          aold[t] = (mine && j < m) ? __bfloat162float(A[t]) : 0.f;
         }
       }
 #pragma unroll
       for (int t = 0; t < 32; ++t) f[t] = p.cb * aold[t] + p.cc * f[t];
     }
+    // the whole upper tile (both halves of a diagonal tile); readers take the
+    // lower triangle from the mirrored upper tiles
     __nv_bfloat16 *O = static_cast<__nv_bfloat16 *>(PHASE == 0 ? d.a : d.b);
-    // O[i, j] for j >= i, and the mirror O[j, i] for j > i
-    warp_store_rows(stage, f, O, pm, i0, m, jb, m, true);
-    warp_store_transposed(stage, f, O, pm, jb, m, i0, m, true);
+    warp_store_rows(stage, f, O, pm, i0, m, jb, m, false);
   } else {
     // tile rows R over the caller's M, columns C over N
     const int M = d.M, N = d.N;
@@ -531,21 +521,23 @@ __device__ __forceinline__ bool warp_mbar_wait(uint64_t *bar, uint32_t parity, v
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-// The producer's copies of one item in one CTA: for each k-block, wait for
-// the stage to be free, and load this CTA's share of both operands (a0, b0:
-// first tile row of each share) onto the leader's full barrier.
+// The producer's copies of one segment of an item in one CTA: for each
+// k-block, wait for the stage to be free, and load this CTA's share of both
+// operands (a0, b0: first tile row of each share) onto the leader's full
+// barrier.
 template <int AMN, int BMN>
-__device__ __forceinline__ bool produce_item(const Operands &op, int nk, int a0, int b0, uint8_t *sA, uint8_t *sB,
-                                             Barriers *bar, bool leader, int &stage, uint32_t &phase_bit,
-                                             int *issued_phase, uint64_t pol, volatile int *abort, int *status) {
-  for (int kb = 0; kb < nk; ++kb) {
+__device__ __forceinline__ bool produce_segment(int kb0, int kb1, const void *map_a, const void *map_b, int a0, int b0,
+                                                uint8_t *sA, uint8_t *sB, Barriers *bar, bool leader, int &stage,
+                                                uint32_t &phase_bit, int *issued_phase, uint64_t pol,
+                                                volatile int *abort, int *status) {
+  for (int kb = kb0; kb < kb1; ++kb) {
     if (!warp_mbar_wait<true>(&bar->empty[stage], phase_bit ^ 1u, abort, status)) return false;
     if (elect_one()) {
       if (leader) mbar_arrive_expect_tx(&bar->full[stage], kPairStageBytes);
       const uint32_t full_leader = mapa_shared(smem_u32(&bar->full[stage]), 0);
       const int kx = kb * kTcBK;
-      load_operand<AMN>(sA + stage * kABytes, op.map_a, a0, kx, full_leader, pol);
-      load_operand<BMN>(sB + stage * kBBytes, op.map_b, b0, kx, full_leader, pol);
+      load_operand<AMN>(sA + stage * kABytes, map_a, a0, kx, full_leader, pol);
+      load_operand<BMN>(sB + stage * kBBytes, map_b, b0, kx, full_leader, pol);
     }
     __syncwarp();
     issued_phase[stage] = static_cast<int>(phase_bit);
@@ -557,15 +549,17 @@ __device__ __forceinline__ bool produce_item(const Operands &op, int nk, int a0,
   return true;
 }
 
-// The leader's MMAs of one item: for each k-block, wait for both CTAs'
-// operand shares, issue the four K = 16 pair MMAs into `d_tmem` and release
-// the stage to both producers. AMN / BMN: MN-major first / second operand.
+// The leader's MMAs of one segment of an item: for each k-block, wait for
+// both CTAs' operand shares, issue the four K = 16 pair MMAs into `d_tmem`
+// (accumulating from the item's first k-block on) and release the stage to
+// both producers. AMN / BMN: MN-major first / second operand.
 template <int AMN, int BMN>
-__device__ __forceinline__ bool mma_item(uint32_t d_tmem, int nk, uint8_t *sA, uint8_t *sB, Barriers *bar,
-                                         int &stage, uint32_t &phase_bit, volatile int *abort, int *status) {
+__device__ __forceinline__ bool mma_segment(uint32_t d_tmem, int kb0, int kb1, uint8_t *sA, uint8_t *sB,
+                                            Barriers *bar, int &stage, uint32_t &phase_bit, volatile int *abort,
+                                            int *status) {
   constexpr uint32_t idesc = umma_idesc_bf16(kTcCluster * kTcBM, kTcBN, AMN, BMN);
   constexpr uint16_t kPairMask = (1u << kTcCluster) - 1;
-  for (int kb = 0; kb < nk; ++kb) {
+  for (int kb = kb0; kb < kb1; ++kb) {
     if (!warp_mbar_wait<true>(&bar->full[stage], phase_bit, abort, status)) return false;
     tc_fence_after();
     const uint32_t a_addr = smem_u32(sA + stage * kABytes);
@@ -656,17 +650,17 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
           if (!__shfl_sync(0xffffffffu, ready, 0)) break;
           fence_proxy_async_global();
         }
-        const Operands op = operands(*ti.d, step, phase, ti.tr, direct);
+        const ItemPlan pl = plan_item(*ti.d, step, phase, ti.tr, direct, ti.row0, ti.col0, ti.nk);
         const int a0 = ti.row0 + my_rows, b0 = ti.col0 + static_cast<int>(rank) * (kTcBN / 2);
-        if (op.a_mn)
-          ok = produce_item<1, 1>(op, ti.nk, a0, b0, sA, sB, bar, leader, stage, phase_bit, issued_phase, pol, abort,
-                                  p.status);
-        else if (op.b_mn)
-          ok = produce_item<0, 1>(op, ti.nk, a0, b0, sA, sB, bar, leader, stage, phase_bit, issued_phase, pol, abort,
-                                  p.status);
-        else
-          ok = produce_item<0, 0>(op, ti.nk, a0, b0, sA, sB, bar, leader, stage, phase_bit, issued_phase, pol, abort,
-                                  p.status);
+        // one k-loop per operand order, so the copies issued are exactly the ones needed
+        ok = produce_segment<1, 1>(0, pl.e0, pl.map[0][0], pl.map[0][1], a0, b0, sA, sB, bar, leader, stage, phase_bit,
+                                   issued_phase, pol, abort, p.status);
+        if (ok)
+          ok = produce_segment<0, 1>(pl.e0, pl.e1, pl.map[1][0], pl.map[1][1], a0, b0, sA, sB, bar, leader, stage,
+                                     phase_bit, issued_phase, pol, abort, p.status);
+        if (ok)
+          ok = produce_segment<0, 0>(pl.e1, ti.nk, pl.map[2][0], pl.map[2][1], a0, b0, sA, sB, bar, leader, stage,
+                                     phase_bit, issued_phase, pol, abort, p.status);
       }
       if (*abort && leader && lane == 0) {
         for (int s = 0; s < kStages; ++s)
@@ -689,17 +683,14 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
         TileInfo ti;
         pipe_take(p, nclusters, q, step, phase, ti, direct);
         if (ti.skip) continue;
-        const Operands op = operands(*ti.d, step, phase, ti.tr, direct);
+        const ItemPlan pl = plan_item(*ti.d, step, phase, ti.tr, direct, ti.row0, ti.col0, ti.nk);
         if (!warp_mbar_wait<true>(&bar->tempty[acc], acc_phase ^ 1u, abort, p.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * kTcBN);
         // one k-loop per operand order, so descriptors stay compile-time
-        if (op.a_mn)
-          ok = mma_item<1, 1>(d_tmem, ti.nk, sA, sB, bar, stage, phase_bit, abort, p.status);
-        else if (op.b_mn)
-          ok = mma_item<0, 1>(d_tmem, ti.nk, sA, sB, bar, stage, phase_bit, abort, p.status);
-        else
-          ok = mma_item<0, 0>(d_tmem, ti.nk, sA, sB, bar, stage, phase_bit, abort, p.status);
+        ok = mma_segment<1, 1>(d_tmem, 0, pl.e0, sA, sB, bar, stage, phase_bit, abort, p.status);
+        if (ok) ok = mma_segment<0, 1>(d_tmem, pl.e0, pl.e1, sA, sB, bar, stage, phase_bit, abort, p.status);
+        if (ok) ok = mma_segment<0, 0>(d_tmem, pl.e1, ti.nk, sA, sB, bar, stage, phase_bit, abort, p.status);
         if (!ok) break;
         if (elect_one()) umma_commit_pair_multicast(&bar->tfull[acc], kPairMask);
         __syncwarp();

@@ -18,11 +18,12 @@
 //   warp 0      TMA producer (both CTAs): its 128 x 64 share of each operand
 //               per k-block (one 64 x 128 box K-major, or two 64 x 64 boxes
 //               MN-major) into a 6-stage ring of 32 KB (128-byte swizzle);
-//               the bytes of both CTAs are counted on the leader's full barrier;
+//               the bytes of both CTAs are counted on the leader's full
+//               barrier; the whole warp runs the loop, one elected lane issues;
 //   warp 1      TMEM allocation (512 columns = two accumulators, cta_group::2)
-//               in both CTAs; in the leader one thread issues the pair MMAs and
-//               the commits that release stages and hand accumulators to both
-//               CTAs' epilogues;
+//               in both CTAs; in the leader the warp runs the MMA loop and one
+//               elected lane issues the pair MMAs and the commits that release
+//               stages and hand accumulators to both CTAs' epilogues;
 //   warps 2..9  epilogue (both CTAs): tcgen05.ld of its 128 accumulator rows
 //               (two warps per TMEM lane quarter), the fused element-wise step
 //               in fp32, round-to-nearest-even to bf16 and the stores; the
@@ -36,7 +37,8 @@
 //                                   rows left of the diagonal read MN-major from
 //                                   the mirrored upper tiles
 //   2 apply   W' = a W + B W        tiles of the next iterate in the caller's
-//                                   orientation (B W, or W^T B when transposed),
+//                                   orientation (B W, or W^T B when transposed;
+//                                   B's rows left of the diagonal read MN-major),
 //                                   one straight store (the caller's Y on the last step)
 // Tiles wholly outside a matrix's non-zero extent are skipped, and k-loops
 // stop at the extent: zero rows and columns stay zero through every step.

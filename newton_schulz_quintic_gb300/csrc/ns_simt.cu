@@ -247,6 +247,9 @@ __global__ void __launch_bounds__(256) ns_norm_tiles_kernel(PrepParams p, int to
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = gridDim.x * 8;
   const int bc = lane & 7;
+  // extents are kept per warp while it stays in one matrix and published
+  // (two atomics) when it moves on or finishes, not once per tile
+  int ext_mat = -1, ext_r = -1, ext_c = -1;
   for (int tile = blockIdx.x * 8 + warp; tile < total_tiles; tile += nwarps) {
     int lo = 0, hi = p.nmats;
     while (hi - lo > 1) {
@@ -254,6 +257,14 @@ __global__ void __launch_bounds__(256) ns_norm_tiles_kernel(PrepParams p, int to
       if (p.tile_prefix[mid] <= tile) lo = mid; else hi = mid;
     }
     const int mat = lo;
+    if (mat != ext_mat) {
+      if (lane == 0 && ext_mat >= 0) {
+        if (ext_r >= 0) atomicMax(&p.ext[2 * ext_mat + 0], ext_r + 1);
+        if (ext_c >= 0) atomicMax(&p.ext[2 * ext_mat + 1], ext_c + 1);
+      }
+      ext_mat = mat;
+      ext_r = ext_c = -1;
+    }
     const MatDesc &d = p.mats[mat];
     const int M = d.M, N = d.N;
     const int local = tile - p.tile_prefix[mat];
@@ -342,10 +353,14 @@ __global__ void __launch_bounds__(256) ns_norm_tiles_kernel(PrepParams p, int to
       // stored at the tile's index in W's tile grid (W = Y^T when transposed)
       const int wtile = d.transposed ? (local % tcols) * ((M + kPrepTile - 1) / kPrepTile) + local / tcols : local;
       p.tile_partials[p.tile_prefix[mat] + wtile] = t;
-      if (rmax >= 0) atomicMax(&p.ext[2 * mat + 0], rmax + 1);
-      if (cmax >= 0) atomicMax(&p.ext[2 * mat + 1], cmax + 1);
     }
+    ext_r = max(ext_r, rmax);
+    ext_c = max(ext_c, cmax);
     __syncwarp();
+  }
+  if (lane == 0 && ext_mat >= 0) {
+    if (ext_r >= 0) atomicMax(&p.ext[2 * ext_mat + 0], ext_r + 1);
+    if (ext_c >= 0) atomicMax(&p.ext[2 * ext_mat + 1], ext_c + 1);
   }
 }
 

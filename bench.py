@@ -163,16 +163,17 @@ def workload_flops(shapes, steps):
     return nominal, executed, apply
 
 
-def traffic_record(kernel: str):
-    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if it
-    was captured from the current kernel source (sha256 prefix matches)."""
+def traffic_record(kernel: str, workload: str):
+    """Per-launch DRAM bytes of `kernel` on `workload` from the committed ncu
+    summary, if it was captured from the current kernel source (sha256 prefix
+    matches) for this workload."""
     src = os.path.join(ROOT, "newton_schulz_quintic_gb300", "csrc", "ns_tc.cu")
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     try:
         sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
         for line in open(path):
             f = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
-            if f.get("kernel") == kernel and f.get("source_sha") == sha and f.get("workload"):
+            if f.get("kernel") == kernel and f.get("source_sha") == sha and f.get("workload") == workload:
                 return f
     except Exception:
         return None
@@ -284,7 +285,7 @@ def run_ours(args, world, rank, local, pg):
     apply_per_launch = kflops * args.steps / max(klaunch, 1)
     achieved = apply_per_launch / (kms / max(klaunch, 1) / 1e3) / 1e12 if klaunch else None
     peak = peaks.get("bf16_tflops_sustained", 1700.0)
-    tr = traffic_record("gemm" if glaunch else "apply")
+    tr = traffic_record("gemm" if glaunch else "apply", wl.name)
     gemm_ms = sum(ktimes[k][0] for k in ("gram", "square", "apply", "gemm"))
     out = {
         "metric": "NS-orthogonalized matrices/s (bf16 tensor-core TFLOP/s and fraction of peak alongside)",

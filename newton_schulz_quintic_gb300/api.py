@@ -157,6 +157,9 @@ def orthogonalize_batched(mats, steps: int = 5, coeffs=None, eps: float | None =
             if workspace is None:
                 need = workspace_bytes([tuple(t.shape) for t in mats], mats[0].dtype)
                 workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+                # the caching allocator must not hand this block out again
+                # before the work queued on `s` has finished with it
+                workspace.record_stream(s)
             rc = lib.ns_orthogonalize_batched_ex(ptrs, shapes, len(mats), int(steps), co, e, code,
                                                  ctypes.c_void_p(workspace.data_ptr()),
                                                  workspace.numel(), sp)

@@ -1,0 +1,68 @@
+"""Host-side helpers of bench.py (no GPU): the DRAM-traffic record is taken
+only for the kernel source, kernel and workload it was captured from; the
+flop counts follow the definitions the bench reports (nominal 4m^2n + 2m^3
+and executed 3m^2n + m^3 per step, apply 2m^2n); the GPU index honours
+CUDA_VISIBLE_DEVICES."""
+import hashlib
+import importlib.util
+import os
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture()
+def bench():
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def _fake_tree(tmp_path, source: bytes, record: str):
+    src = tmp_path / "newton_schulz_quintic_gb300" / "csrc"
+    src.mkdir(parents=True)
+    (src / "ns_tc.cu").write_bytes(source)
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "traffic.txt").write_text(record)
+    return hashlib.sha256(source).hexdigest()[:16]
+
+
+def test_traffic_record_matches_source_kernel_and_workload(bench, tmp_path):
+    sha = hashlib.sha256(b"kernel v1").hexdigest()[:16]
+    _fake_tree(tmp_path, b"kernel v1",
+               f"kernel=apply workload=w1 source_sha={sha} bytes_per_launch=123\n"
+               f"kernel=gemm workload=w1 source_sha={sha} bytes_per_launch=456\n")
+    bench.ROOT = str(tmp_path)
+    assert bench.traffic_record("apply", "w1")["bytes_per_launch"] == "123"
+    assert bench.traffic_record("gemm", "w1")["bytes_per_launch"] == "456"
+    assert bench.traffic_record("apply", "w2") is None          # another workload
+    assert bench.traffic_record("apply", "w1[:2]") is None      # a subset of it
+    assert bench.traffic_record("square", "w1") is None         # another kernel
+
+
+def test_traffic_record_is_dropped_when_the_kernel_source_changes(bench, tmp_path):
+    old = hashlib.sha256(b"kernel v1").hexdigest()[:16]
+    _fake_tree(tmp_path, b"kernel v2", f"kernel=apply workload=w1 source_sha={old} bytes_per_launch=123\n")
+    bench.ROOT = str(tmp_path)
+    assert bench.traffic_record("apply", "w1") is None
+
+
+def test_workload_flops(bench):
+    nominal, executed, apply = bench.workload_flops([(8192, 6144)], 5)
+    m, n = 6144, 8192
+    assert nominal == 5 * (4 * m * m * n + 2 * m ** 3)
+    assert executed == 5 * (3 * m * m * n + m ** 3)
+    assert apply == 5 * 2 * m * m * n
+    # orientation does not matter: the iteration runs on the short side
+    assert bench.workload_flops([(6144, 8192)], 5) == (nominal, executed, apply)
+
+
+def test_physical_gpu_index(bench, monkeypatch):
+    monkeypatch.setenv("CUDA_VISIBLE_DEVICES", "3,5")
+    assert bench.physical_gpu_index(0) == 3
+    assert bench.physical_gpu_index(1) == 5
+    monkeypatch.delenv("CUDA_VISIBLE_DEVICES")
+    assert bench.physical_gpu_index(2) == 2

@@ -170,13 +170,16 @@ def traffic_record(kernel: str, workload: str):
     src = os.path.join(ROOT, "newton_schulz_quintic_gb300", "csrc", "ns_tc.cu")
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     try:
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        for line in open(path):
-            f = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
-            if f.get("kernel") == kernel and f.get("source_sha") == sha and f.get("workload") == workload:
-                return f
+        with open(src, "rb") as fh:
+            sha = hashlib.sha256(fh.read()).hexdigest()[:16]
+        with open(path) as fh:
+            lines = fh.readlines()
     except Exception:
         return None
+    for line in lines:
+        f = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
+        if f.get("kernel") == kernel and f.get("source_sha") == sha and f.get("workload") == workload:
+            return f
     return None
 
 

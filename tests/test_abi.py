@@ -29,7 +29,8 @@ def _has_gpu():
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    with open(HEADER) as f:
+        text = f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(ns_[a-z_0-9]+)\s*\(", text)))
 

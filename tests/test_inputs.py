@@ -11,7 +11,8 @@ GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "chunk_split.json")
 
 
 def test_chunk_sizes_match_pages():
-    g = json.load(open(GOLDEN))
+    with open(GOLDEN) as f:
+        g = json.load(f)
     for case in g["splits"]:
         assert inputs.chunk_sizes(case["size"], case["shards"]) == case["sizes"]
         # the same split torch.chunk produces, padded with empty shards
@@ -23,7 +24,8 @@ def test_chunk_sizes_match_pages():
 def test_watchdog_numel_matches_padded_layout():
     # every rank's padded shard of the 18-row weight holds 3 rows; per_rank = 4
     # such matrices go to each of 8 ranks: 8 x 4 x 3 x 2304 elements
-    w = json.load(open(GOLDEN))["watchdog_numel"]
+    with open(GOLDEN) as f:
+        w = json.load(f)["watchdog_numel"]
     x = torch.randn(18, w["cols"])
     p = inputs.pad_shards(x, w["world_size"])
     rows_per_shard = p.shape[0] // w["world_size"]

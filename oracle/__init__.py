@@ -155,6 +155,51 @@ def round_bf16(x: np.ndarray) -> np.ndarray:
     return u.astype(np.uint32).view(np.float32).astype(np.float64)
 
 
+E4M3_MAX = 448.0  # largest finite e4m3 value (1.75 * 2^8; the format has no infinities)
+
+
+def round_e4m3(x: np.ndarray) -> np.ndarray:
+    """Round fp64 values to the nearest 8-bit e4m3 value (1 sign, 4 exponent
+    bits with bias 7, 3 mantissa bits; ties to even; subnormals below 2^-6 in
+    steps of 2^-9), saturating at +-448, returned as fp64."""
+    x = np.asarray(x, dtype=np.float64)
+    ax = np.abs(x)
+    _, e2 = np.frexp(ax)               # ax = f * 2^e2, f in [0.5, 1)
+    e = np.maximum(e2 - 1, -6)         # binade exponent; subnormals share 2^-6's spacing
+    step = np.ldexp(1.0, e - 3)        # 3 mantissa bits
+    q = np.rint(ax / step) * step      # np.rint rounds halves to even
+    q = np.minimum(q, E4M3_MAX)
+    return np.where(ax == 0.0, 0.0, np.copysign(q, x))
+
+
+def quantise_e4m3_tensor(x: np.ndarray) -> np.ndarray:
+    """fp8 operand with one scale per tensor: x/s rounded to e4m3, times s,
+    s = max|x| / 448 (values exactly representable after scaling back)."""
+    amax = float(np.max(np.abs(x))) if x.size else 0.0
+    if amax == 0.0:
+        return np.zeros_like(x)
+    s = amax / E4M3_MAX
+    return round_e4m3(x / s) * s
+
+
+def quantise_mxfp8(x: np.ndarray, axis: int) -> np.ndarray:
+    """fp8 operand with block scaling: blocks of 32 consecutive elements along
+    `axis` (the contraction index) share the power-of-two scale
+    2^ceil(log2(amax / 448)), the smallest that keeps the block's largest
+    magnitude within e4m3's range, and each element is rounded to e4m3 after
+    dividing by it (MX-style block scaling with e4m3 elements)."""
+    x = np.moveaxis(np.asarray(x, dtype=np.float64), axis, -1)
+    k = x.shape[-1]
+    pad = (-k) % 32
+    xp = np.concatenate([x, np.zeros(x.shape[:-1] + (pad,))], axis=-1) if pad else x
+    blocks = xp.reshape(xp.shape[:-1] + (-1, 32))
+    amax = np.max(np.abs(blocks), axis=-1, keepdims=True)
+    scale = np.exp2(np.ceil(np.log2(np.where(amax > 0, amax, 1.0) / E4M3_MAX)))
+    q = round_e4m3(blocks / scale) * scale
+    q = np.where(amax > 0, q, 0.0).reshape(xp.shape)[..., :k]
+    return np.moveaxis(q, -1, axis)
+
+
 def orthogonalize_np(X, steps: int = DEFAULT_STEPS, coeffs=DEFAULT_COEFFS,
                      eps: float = DEFAULT_EPS, orient: int = 0, emulate: str | None = None) -> np.ndarray:
     """The same steps as ``orthogonalize`` with numpy.matmul (fp64) as the
@@ -166,15 +211,28 @@ def orthogonalize_np(X, steps: int = DEFAULT_STEPS, coeffs=DEFAULT_COEFFS,
     itself stays fp64), i.e. the storage precision of a bf16 tensor-core
     implementation that keeps those three matrices in bf16 between phases and
     folds the normalisation into the first step (W_0 = Y/(s+eps) itself is
-    never stored, so never rounded)."""
+    never stored, so never rounded).
+
+    emulate="e4m3" and emulate="mxfp8" are diagnostics of an fp8 tensor-core
+    variant (not built): W, A and B are stored as bfloat16 as above, and every
+    matrix product takes its two operands rounded to e4m3 -- with one scale
+    per tensor ("e4m3") or one power-of-two scale per 32 elements along the
+    contraction index ("mxfp8") -- while the element-wise terms a W and b A
+    use the bf16 values and every sum stays fp64."""
     W = np.array(to_f64(X), dtype=np.float64, copy=True)
     if W.ndim != 2:
         raise ValueError("oracle takes 2-D matrices")
     if W.size == 0:
         return W
-    if emulate not in (None, "bf16"):
-        raise ValueError("emulate must be None or 'bf16'")
-    rnd = round_bf16 if emulate == "bf16" else (lambda v: v)
+    if emulate not in (None, "bf16", "e4m3", "mxfp8"):
+        raise ValueError("emulate must be None, 'bf16', 'e4m3' or 'mxfp8'")
+    rnd = round_bf16 if emulate is not None else (lambda v: v)
+    if emulate == "e4m3":
+        qa = qb = lambda v, axis: quantise_e4m3_tensor(v)
+    elif emulate == "mxfp8":
+        qa = qb = quantise_mxfp8
+    else:
+        qa = qb = lambda v, axis: v
     table = coeff_table(coeffs, steps)
     rows = [tuple(float(v) for v in coeffs)] * int(steps) if table is None else [tuple(r) for r in table]
     s = np.sqrt(np.sum(W * W))
@@ -184,9 +242,12 @@ def orthogonalize_np(X, steps: int = DEFAULT_STEPS, coeffs=DEFAULT_COEFFS,
     if transpose:
         W = np.ascontiguousarray(W.T)
     for a, b, c in rows:
-        A = rnd(W @ W.T)
-        B = rnd(b * A + c * (A @ A))
-        W = rnd(a * W + B @ W)
+        # contraction index: columns of the first operand, rows of the second
+        Wq = qa(W, 1)
+        A = rnd(Wq @ Wq.T)
+        Aq = qa(A, 1)
+        B = rnd(b * A + c * (Aq @ Aq))
+        W = rnd(a * W + qa(B, 1) @ qb(W, 0))
     return np.ascontiguousarray(W.T) if transpose else W
 
 

@@ -283,3 +283,40 @@ def test_per_step_schedule_matches_closed_form(ns, shape):
 def test_constant_schedule_is_the_plain_call(ns):
     X = randn((30, 70), seed=41)
     assert np.array_equal(ns(X, steps=3, coeffs=[CO] * 3), ns(X, steps=3, coeffs=CO))
+
+
+def test_round_e4m3_matches_torch_float8_cast():
+    # the fp8 emulation's rounding against torch's float8_e4m3fn cast (nearest,
+    # ties to even, subnormals), over values spanning the format's range
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8_e4m3fn")
+    rng = np.random.default_rng(31)
+    x = rng.standard_normal(100000) * np.exp(rng.uniform(-12, 6, 100000))
+    x = np.concatenate([x, [0.0, 448.0, -448.0, 2.0 ** -9, 2.0 ** -10, 3 * 2.0 ** -10, 1.0625, 1.1875]])
+    x = x[np.abs(x) <= 448.0].astype(np.float32).astype(np.float64)
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(oracle.round_e4m3(x), want)
+    assert oracle.round_e4m3(np.array([1e6, -1e6])).tolist() == [448.0, -448.0]   # saturates
+
+
+def test_fp8_operand_quantisers():
+    rng = np.random.default_rng(32)
+    x = rng.standard_normal((40, 70)) * np.exp(rng.uniform(-3, 3, (40, 70)))
+    x[3] = 0.0
+    for q in (oracle.quantise_e4m3_tensor, lambda v: oracle.quantise_mxfp8(v, 1),
+              lambda v: oracle.quantise_mxfp8(v, 0)):
+        y = q(x)
+        assert np.array_equal(q(y), y)                  # idempotent: already on the grid
+        assert np.all(y[3] == 0)                        # zero rows stay zero
+    # block scaling: within a 32-element block along the axis, the error of an
+    # element is at most half an e4m3 step at its block's scale
+    y = oracle.quantise_mxfp8(x, 1)
+    for r in range(40):
+        for b0 in range(0, 70, 32):
+            blk, qb = x[r, b0:b0 + 32], y[r, b0:b0 + 32]
+            amax = np.max(np.abs(blk))
+            if amax == 0:
+                continue
+            scale = 2.0 ** np.ceil(np.log2(amax / 448.0))
+            assert np.max(np.abs(qb)) <= 448.0 * scale
+            assert np.all(np.abs(qb - blk) <= np.maximum(np.abs(blk) * 2.0 ** -4, scale * 2.0 ** -10) + 1e-300)

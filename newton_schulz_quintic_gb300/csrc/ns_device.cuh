@@ -158,36 +158,10 @@ __device__ __forceinline__ bool elect_one() {
 }
 
 // ---------------------------------------------------------------- TMA
-__device__ __forceinline__ void tma_prefetch_desc(const void *map) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-
-// 2-D tiled load of box {64 elems, rows} at (x, y) into shared memory,
-// completing `bytes` of transaction count on `bar`.
-__device__ __forceinline__ void tma_load_2d(void *smem_dst, const void *map, int x, int y, uint64_t *bar,
-                                            uint64_t cache_hint) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(cache_hint)
-      : "memory");
-}
-
-// The same load delivered to every CTA of the cluster named in cta_mask, at
-// the same shared-memory offsets; each destination's mbarrier at the offset
-// of `bar` receives the transaction bytes.
-__device__ __forceinline__ void tma_load_2d_multicast(void *smem_dst, const void *map, int x, int y, uint64_t *bar,
-                                                      uint16_t cta_mask, uint64_t cache_hint) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(cta_mask), "l"(cache_hint)
-      : "memory");
-}
-
-// As tma_load_2d, for a CTA pair running cta_group::2 MMAs: the data lands in
-// this CTA's shared memory, the transaction bytes are counted on the mbarrier
-// at shared::cluster address `bar_cluster` (the pair leader's barrier).
+// 2-D tiled TMA load of one box at (x, y) for a CTA pair running cta_group::2
+// MMAs: the data lands in this CTA's shared memory, the transaction bytes are
+// counted on the mbarrier at shared::cluster address `bar_cluster` (the pair
+// leader's barrier).
 __device__ __forceinline__ void tma_load_2d_pair(void *smem_dst, const void *map, int x, int y,
                                                  uint32_t bar_cluster, uint64_t cache_hint) {
   asm volatile(
@@ -223,12 +197,7 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// L2 eviction-priority hints (createpolicy encodings computed at run time)
-__device__ __forceinline__ uint64_t l2_policy_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
+// L2 eviction-priority hint (createpolicy encoding computed at run time)
 __device__ __forceinline__ uint64_t l2_policy_evict_normal() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
@@ -236,17 +205,6 @@ __device__ __forceinline__ uint64_t l2_policy_evict_normal() {
 }
 
 // ---------------------------------------------------------------- tcgen05
-__device__ __forceinline__ void tmem_alloc(uint32_t *smem_slot, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(smem_slot)),
-               "r"(ncols)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
 // cta_group::2 forms: executed by one warp in each CTA of the pair
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t *smem_slot, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(smem_slot)),
@@ -266,17 +224,6 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem desc] * B[smem desc]^T, bf16 inputs, fp32 accumulate.
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 // Pair MMA, issued by the leader CTA: D (256 rows, half in each CTA's TMEM) (+)=
 // A (128 rows from each CTA's shared memory) * B^T (half of B's rows in each CTA).
 __device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
@@ -293,23 +240,6 @@ __device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t a_desc,
 __device__ __forceinline__ void umma_commit_pair_multicast(uint64_t *bar, uint16_t cta_mask) {
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_u32(bar)),
-      "h"(cta_mask)
-      : "memory");
-}
-
-// Arrive once on `bar` when every tcgen05.mma issued so far by this thread completes.
-__device__ __forceinline__ void umma_commit(uint64_t *bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   smem_u32(bar))
-               : "memory");
-}
-
-// As umma_commit, arriving once on the mbarrier at the same offset in every
-// CTA of the cluster named in cta_mask.
-__device__ __forceinline__ void umma_commit_multicast(uint64_t *bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
           smem_u32(bar)),
       "h"(cta_mask)
       : "memory");

@@ -16,6 +16,9 @@ test_mutations plants a numbered mistake in the oracle's C source (a dropped
 term, a wrong sign, a wrong index, a wrong norm, one step short) and checks
 that the pins fail on it.
 """
+import json
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -205,6 +208,16 @@ def test_singular_value_band(ns):
 def test_bf16_widening_exact():
     x = (torch.randn(100) * 3).to(torch.bfloat16)
     assert np.array_equal(oracle.to_f64(x), x.to(torch.float64).numpy())
+
+
+def test_cost_of_the_pages_printed_figures():
+    # second page: the expensive and dense matrices' costs as printed there
+    with open(os.path.join(os.path.dirname(__file__), "golden", "ns_cost.json")) as f:
+        g = json.load(f)
+    for c in g["costs"]:
+        assert oracle.cost(*c["shape"]) == c["cost"]
+    hi, dense = g["costs"][0]["cost"], g["costs"][2]["cost"]
+    assert hi == g["ratio_expensive_to_dense"] * dense
 
 
 def test_cost_formula():

@@ -221,6 +221,7 @@ int64_t ns_num_kernel_launches(void);
  * launch count into launches[k] for k < n (n <= 7). Returns NS_OK or NS_ECUDA.
  */
 int ns_set_kernel_timing(int enable);
+int ns_get_kernel_times(double *ms, int64_t *launches, int n);
 
 /*
  * ns_set_gemm_schedule -- how later calls launch the bf16 tensor-core GEMMs
@@ -249,7 +250,6 @@ int ns_set_gemm_schedule(int mode);
  * the wait gave up as designed, NS_EINVAL for a bad limit, NS_ECUDA otherwise.
  */
 int ns_selftest_wait_timeout(int limit_us, void *stream);
-int ns_get_kernel_times(double *ms, int64_t *launches, int n);
 
 #ifdef __cplusplus
 }

@@ -56,7 +56,7 @@ extern "C" {
 #define NS_ENOMEM (-3)   /* workspace allocation failed / caller workspace too small */
 #define NS_ECUDA (-4)    /* a CUDA runtime or driver call failed */
 #define NS_ETIMEOUT (-5) /* a bounded device-side wait gave up (reported by ns_get_status) */
-#define NS_ENODEV (-6)   /* no usable sm_100-family device */
+#define NS_ENODEV (-6)   /* no CUDA driver or device, or the current device is not sm_100-family */
 #define NS_ETOOBIG (-7)  /* batch needs more scratch than ns_orthogonalize_batched_noalloc holds */
 
 /*

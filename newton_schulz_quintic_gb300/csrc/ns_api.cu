@@ -62,9 +62,18 @@ struct DevInfo {
 std::mutex g_mu;
 std::map<int, DevInfo> g_dev;
 
+// cudaGetDevice, with "no CUDA driver or device" reported as NS_ENODEV and
+// any other failure as NS_ECUDA
+int current_device(int *dev) {
+  const cudaError_t e = cudaGetDevice(dev);
+  if (e == cudaSuccess) return NS_OK;
+  cudaGetLastError();
+  return e == cudaErrorNoDevice || e == cudaErrorInsufficientDriver ? NS_ENODEV : NS_ECUDA;
+}
+
 int device_info(DevInfo **out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return NS_ECUDA;
+  if (const int rc = current_device(&dev)) return rc;
   auto it = g_dev.find(dev);
   if (it == g_dev.end()) {
     DevInfo di;
@@ -756,6 +765,8 @@ int ns_plan_shards(const int64_t *shapes, const int64_t *numels, int count, int 
 }
 
 int ns_get_status(void *stream) {
+  int dev = 0;
+  if (const int rc = current_device(&dev)) return rc;
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return NS_ECUDA;
   int v = 0;
   if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(int)) != cudaSuccess) return NS_ECUDA;
@@ -772,7 +783,7 @@ const char *ns_strerror(int code) {
     case NS_ENOMEM: return "workspace allocation failed or caller workspace too small";
     case NS_ECUDA: return "CUDA runtime or driver error";
     case NS_ETIMEOUT: return "a bounded device-side wait gave up";
-    case NS_ENODEV: return "no sm_100-family device is current";
+    case NS_ENODEV: return "no CUDA device or driver, or the current device is not sm_100-family";
     case NS_ETOOBIG: return "batch needs more scratch than the no-allocation entry point's 256 MiB array";
     default: return "unknown status";
   }
@@ -781,7 +792,7 @@ const char *ns_strerror(int code) {
 int ns_release_workspace(void) {
   std::lock_guard<std::mutex> lock(g_mu);
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return NS_ECUDA;
+  if (const int rc = current_device(&dev)) return rc;
   if (cudaDeviceSynchronize() != cudaSuccess) return NS_ECUDA;
   for (auto it = g_ws.begin(); it != g_ws.end();) {
     if (it->first.dev == dev) {

@@ -146,8 +146,9 @@ constexpr int kPrepTile = 64;     // Y tile edge of the preparation kernel
 
 // tcgen05 GEMM tile (bf16 path). Tiles are processed by 2-CTA clusters: a
 // tile list entry covers kTcPairM x kTcBN outputs, CTA rank r of the cluster
-// computes rows [row0 + r*kTcBM, row0 + (r+1)*kTcBM) and the pair shares the
-// kTcBN-row second operand through TMA multicast.
+// computes rows [row0 + r*kTcBM, row0 + (r+1)*kTcBM) and loads half of the
+// kTcBN-row second operand; the pair MMA reads both halves, so no operand
+// byte is loaded twice.
 constexpr int kTcBM = 128;
 constexpr int kTcBN = 256;
 constexpr int kTcBK = 64;

@@ -36,7 +36,12 @@ void *g_addr[kMaxDevices] = {};
 
 int scratch_address(void **out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NS_ECUDA;
+  const cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return e == cudaErrorNoDevice || e == cudaErrorInsufficientDriver ? NS_ENODEV : NS_ECUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return NS_ECUDA;
   std::lock_guard<std::mutex> lock(g_mu);
   if (!g_addr[dev]) {
     void *p = nullptr;

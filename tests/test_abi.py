@@ -111,8 +111,34 @@ def test_validation_rejects_overlapping_matrices(lib):
     assert _call(lib, (P * 3)(0x200000, 0x100000, 0x10003e), (S * 6)(4, 8, 4, 8, 1, 1), 3) == -1
 
 
+@pytest.mark.skipif(_has_gpu(), reason="checks the error path of a machine with no CUDA device")
+def test_no_device_is_reported_as_enodev(lib):
+    # valid arguments on a machine without a CUDA driver or device: every entry
+    # point that needs the GPU says so with NS_ENODEV and touches nothing
+    import numpy as np
+    P, S = ctypes.c_void_p, ctypes.c_int64
+    x = np.arange(64 * 128, dtype=np.float32).reshape(64, 128)
+    before = x.copy()
+    ptrs, shapes = (P * 1)(x.ctypes.data), (S * 2)(64, 128)
+    f32 = api.NS_F32
+    tab = (ctypes.c_float * 3)(3.4445, -4.7750, 2.0315)
+    ws = np.zeros(1 << 20, dtype=np.uint8)
+    assert lib.ns_orthogonalize_batched(ptrs, shapes, 1, 5, None, f32, None) == -6
+    assert lib.ns_orthogonalize_batched_host(ptrs, shapes, 1, 5, None, f32, None) == -6
+    assert lib.ns_orthogonalize_batched_noalloc(ptrs, shapes, 1, 5, None, f32, None) == -6
+    assert lib.ns_orthogonalize_batched_sched(ptrs, shapes, 1, 1, tab, f32, None) == -6
+    ws_ptr = P(ws.ctypes.data + (-ws.ctypes.data) % 256)
+    assert lib.ns_orthogonalize_batched_ex(ptrs, shapes, 1, 5, None, 1e-7, f32, ws_ptr, 1 << 19, None) == -6
+    assert lib.ns_get_status(None) == -6
+    assert lib.ns_release_workspace() == -6
+    assert lib.ns_selftest_wait_timeout(1000, None) == -6
+    assert np.array_equal(x, before)
+    # validation still comes first
+    assert lib.ns_orthogonalize_batched(ptrs, shapes, 1, -1, None, f32, None) == -1
+
+
 def test_strerror(lib):
-    for code in [0, -1, -2, -3, -4, -5, -6]:
+    for code in [0, -1, -2, -3, -4, -5, -6, -7]:
         assert lib.ns_strerror(code)
     assert b"unknown" in lib.ns_strerror(-99)
 

@@ -359,6 +359,19 @@ def cores():
         return os.cpu_count() or 1
 
 
+def blas_threads():
+    """Threads NumPy's OpenBLAS runs with: its thread variables as read when
+    NumPy loaded (OPENBLAS_NUM_THREADS before OMP_NUM_THREADS), else every
+    core this process may run on."""
+    n = cores()
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        try:
+            return max(1, min(n, int(os.environ[var])))
+        except (KeyError, ValueError):
+            continue
+    return n
+
+
 def run_reference(args, world, rank):
     from newton_schulz_quintic_gb300 import inputs
     if rank != 0:
@@ -389,7 +402,7 @@ def run_reference(args, world, rank):
         "data": "synthetic (seeded N(0,0.02) bf16 inputs widened exactly to fp64)",
         "config": {"workload": wl.name, "matrices": wl.count,
                    "shapes": [list(t) for t in sorted({tuple(x) for x in wl.shapes})], "ns_steps": wl.steps},
-        "cpu_baseline": {"value": round(value, 6), "unit": "matrices/s", "cores": cores(), "kind": "oracle",
+        "cpu_baseline": {"value": round(value, 6), "unit": "matrices/s", "cores": blas_threads(), "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": round(value, 6), "unit": "matrices/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -399,6 +412,13 @@ def run_reference(args, world, rank):
 
 def main():
     args = parse_args()
+    if args.impl == "reference" and os.environ.get("RANK", "0") == "0":
+        # rank 0 alone times the oracle and the other ranks do no work, so it
+        # takes every host core: torchrun's default of one OpenMP thread per
+        # rank would otherwise hold NumPy's BLAS to one thread. Set before
+        # NumPy is first imported.
+        for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+            os.environ[var] = str(cores())
     world, rank, local, pg = dist_setup(args)
     if args.impl == "reference":
         out = run_reference(args, world, rank)
@@ -414,7 +434,7 @@ def main():
         if world == 1 and not args.no_cpu_baseline:
             dt, desc = cpu_oracle_sample(wl)
             v = 1.0 / (wl.steps * dt)
-            out["cpu_baseline"] = {"value": round(v, 6), "unit": "matrices/s", "cores": cores(),
+            out["cpu_baseline"] = {"value": round(v, 6), "unit": "matrices/s", "cores": blas_threads(),
                                    "kind": "oracle", "sample": desc}
         print(json.dumps(out), flush=True)
     if pg:

@@ -2,7 +2,8 @@
 only for the kernel source, kernel and workload it was captured from; the
 flop counts follow the definitions the bench reports (nominal 4m^2n + 2m^3
 and executed 3m^2n + m^3 per step, apply 2m^2n); the GPU index honours
-CUDA_VISIBLE_DEVICES."""
+CUDA_VISIBLE_DEVICES; the CPU baseline reports the BLAS threads it ran with;
+and the reference arm runs as two torchrun ranks on the CPU (gloo)."""
 import hashlib
 import importlib.util
 import os
@@ -66,3 +67,40 @@ def test_physical_gpu_index(bench, monkeypatch):
     assert bench.physical_gpu_index(1) == 5
     monkeypatch.delenv("CUDA_VISIBLE_DEVICES")
     assert bench.physical_gpu_index(2) == 2
+
+
+def test_blas_threads_reports_the_thread_variables(bench, monkeypatch):
+    n = bench.cores()
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        monkeypatch.delenv(var, raising=False)
+    assert bench.blas_threads() == n
+    monkeypatch.setenv("OMP_NUM_THREADS", "1")
+    assert bench.blas_threads() == 1
+    monkeypatch.setenv("OPENBLAS_NUM_THREADS", str(n + 100))   # capped at the usable cores
+    assert bench.blas_threads() == n
+
+
+def test_reference_arm_under_torchrun_two_ranks():
+    # the reference arm as launched for N > 1: rank 0 alone times the oracle
+    # (on every host core) and prints one line; the other rank exits 0
+    import json
+    import socket
+    import subprocess
+    import sys
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py", "--impl", "reference",
+           "--gpus", "2", "--steps", "2", "--warmup", "1", "--workload", "f32-8x64x128"]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [json.loads(x) for x in r.stdout.splitlines() if x.startswith("{")]
+    assert len(lines) == 1
+    out = lines[0]
+    assert out["impl"] == "reference" and out["n_gpus"] == 2 and out["steps"] == 2
+    assert out["value"] > 0 and out["e2e"]["value"] == out["value"]
+    assert out["e2e"]["h2d_bytes_per_step"] == 0 and out["e2e"]["d2h_bytes_per_step"] == 0
+    cb = out["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == out["value"] and cb["cores"] == len(os.sched_getaffinity(0))

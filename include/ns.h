@@ -51,7 +51,8 @@ extern "C" {
 
 /* status codes */
 #define NS_OK 0
-#define NS_EINVAL (-1)   /* null pointer, negative dims/count/steps, bad dtype */
+#define NS_EINVAL (-1)   /* null pointer, negative dims/count/steps, bad dtype, a side above
+                            2^30 - 1 or a matrix above 2^40 elements, overlapping matrices */
 #define NS_EALIGN (-2)   /* a matrix pointer is not aligned to its element size */
 #define NS_ENOMEM (-3)   /* workspace allocation failed / caller workspace too small */
 #define NS_ECUDA (-4)    /* a CUDA runtime or driver call failed */

@@ -98,6 +98,12 @@ def test_validation_rejects_before_launch(lib):
     assert _call(lib, (P * 1)(0x100001), good_shape, 1) == -2            # misaligned bf16
     assert _call(lib, (P * 1)(0x100002), good_shape, 1, dtype=api.NS_F32) == -2  # misaligned f32
     assert lib.ns_orthogonalize_batched_ex(good_ptrs, good_shape, 1, 5, None, 1e-7, 1, None, 0, None) == -1
+    # size limits: a side above 2^30 - 1 or more than 2^40 elements is refused
+    assert _call(lib, good_ptrs, (S * 2)(1 << 30, 1), 1) == -1
+    assert _call(lib, good_ptrs, (S * 2)(1, 1 << 30), 1) == -1
+    assert _call(lib, good_ptrs, (S * 2)(1 << 21, 1 << 20), 1) == -1
+    assert lib.ns_workspace_bytes((S * 2)(1 << 21, 1 << 20), 1, 1) == 0
+    assert lib.ns_workspace_bytes((S * 2)(1 << 20, 1 << 20), 1, 1) > 0
 
 
 @pytest.mark.skipif(_has_gpu(), reason="uses fake device pointers: only run where nothing can launch")

@@ -359,6 +359,26 @@ def cores():
         return os.cpu_count() or 1
 
 
+def host_cpu():
+    """Architecture and model of the host CPU, as /proc/cpuinfo names it (Arm
+    cores give only their part number there)."""
+    import platform
+    name = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key, _, val = line.partition(":")
+                key = key.strip().lower()
+                if key == "model name":
+                    name = val.strip()
+                    break
+                if key == "cpu part" and not name:
+                    name = "cpu part " + val.strip()
+    except OSError:
+        pass
+    return f"{platform.machine()} {name}".strip()
+
+
 def blas_threads():
     """Threads NumPy's OpenBLAS runs with: its thread variables as read when
     NumPy loaded (OPENBLAS_NUM_THREADS before OMP_NUM_THREADS), else every
@@ -403,7 +423,7 @@ def run_reference(args, world, rank):
         "config": {"workload": wl.name, "matrices": wl.count,
                    "shapes": [list(t) for t in sorted({tuple(x) for x in wl.shapes})], "ns_steps": wl.steps},
         "cpu_baseline": {"value": round(value, 6), "unit": "matrices/s", "cores": blas_threads(), "kind": "oracle",
-                         "sample": desc},
+                         "cpu": host_cpu(), "sample": desc},
         "e2e": {"value": round(value, 6), "unit": "matrices/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -435,7 +455,7 @@ def main():
             dt, desc = cpu_oracle_sample(wl)
             v = 1.0 / (wl.steps * dt)
             out["cpu_baseline"] = {"value": round(v, 6), "unit": "matrices/s", "cores": blas_threads(),
-                                   "kind": "oracle", "sample": desc}
+                                   "kind": "oracle", "cpu": host_cpu(), "sample": desc}
         print(json.dumps(out), flush=True)
     if pg:
         pg.barrier()

@@ -104,3 +104,4 @@ def test_reference_arm_under_torchrun_two_ranks():
     assert out["e2e"]["h2d_bytes_per_step"] == 0 and out["e2e"]["d2h_bytes_per_step"] == 0
     cb = out["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == out["value"] and cb["cores"] == len(os.sched_getaffinity(0))
+    assert cb["cpu"].startswith(os.uname().machine)

@@ -163,6 +163,33 @@ def workload_flops(shapes, steps):
     return nominal, executed, apply
 
 
+def input_digest(mats):
+    """SHA-256 over the inputs' bytes, matrix after matrix (bf16 as its 16-bit
+    patterns), so that a run names exactly the data it measured."""
+    import torch
+    h = hashlib.sha256()
+    for t in mats:
+        v = t.detach().cpu().contiguous()
+        if v.dtype == torch.bfloat16:
+            v = v.view(torch.int16)
+        h.update(v.numpy().tobytes())
+    return h.hexdigest()
+
+
+def norm_pass_record(ktimes, bytes_per_step, steps, hbm_peak):
+    """Achieved HBM bandwidth of the pass over the caller's matrices (bf16: the
+    Frobenius sums and extents; it reads every input byte once per call) from
+    its CUDA-event times, or None when the workload never launched it."""
+    ms, launches = ktimes.get("prep", (0.0, 0))
+    if not launches or ms <= 0:
+        return None
+    gbs = bytes_per_step * steps / (ms / 1e3) / 1e9
+    return {"kernel": "ns_norm_tiles_kernel (Frobenius sums and extents)", "bound": "hbm",
+            "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+            "frac": round(gbs / hbm_peak, 4) if hbm_peak else None,
+            "bytes_per_step": int(bytes_per_step), "launches": int(launches), "ms_total": round(ms, 4)}
+
+
 def traffic_record(kernel: str, workload: str):
     """Per-launch DRAM bytes of `kernel` on `workload` from the committed ncu
     summary, if it was captured from the current kernel source (sha256 prefix
@@ -196,6 +223,7 @@ def run_ours(args, world, rank, local, pg):
         wl = inputs.subset(wl, args.matrices)
     dev = torch.device("cuda", local)
     host = [wl.matrix(i) for i in range(wl.count)]
+    digest = input_digest(host)
     pristine = [h.to(dev) for h in host]
     work = [torch.empty_like(p) for p in pristine]
     slices = wl.call_slices()
@@ -274,6 +302,7 @@ def run_ours(args, world, rank, local, pg):
 
     count = wl.count
     ms_per_step = total_ms / args.steps
+    ws_bytes = max(api.workspace_bytes([tuple(h.shape) for h in host[sl]], host[0].dtype) for sl in slices)
     value = world * count * args.steps / (total_ms / 1e3)
     nominal, executed, apply_flops = workload_flops(wl.shapes, wl.steps)
     peaks, peak_kind = measured_peaks()
@@ -322,6 +351,9 @@ def run_ours(args, world, rank, local, pg):
             "traffic": (int(float(tr["bytes_per_launch"])) if tr else None),
             "algorithmic_flops_per_launch": apply_per_launch,
         },
+        "norm_pass": norm_pass_record(ktimes, e2e_bytes, args.steps, peaks.get("hbm_gbs")),
+        "workspace_bytes": int(ws_bytes),
+        "input_sha256": digest,
         "kernels": {k: {"ms_total": round(v[0], 3), "launches": v[1],
                         "share": round(v[0] / max(sum(x[0] for x in ktimes.values()), 1e-9), 4)}
                     for k, v in ktimes.items() if v[1]},

@@ -105,3 +105,26 @@ def test_reference_arm_under_torchrun_two_ranks():
     cb = out["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == out["value"] and cb["cores"] == len(os.sched_getaffinity(0))
     assert cb["cpu"].startswith(os.uname().machine)
+
+
+def test_input_digest_covers_every_byte(bench):
+    import torch
+    a = (torch.arange(12, dtype=torch.float32).reshape(3, 4) / 7).to(torch.bfloat16)
+    b = torch.ones(2, 5, dtype=torch.bfloat16)
+    want = hashlib.sha256(a.view(torch.int16).numpy().tobytes() + b.view(torch.int16).numpy().tobytes())
+    assert bench.input_digest([a, b]) == want.hexdigest()
+    c = a.clone()
+    c[2, 3] = -c[2, 3]
+    assert bench.input_digest([c, b]) != want.hexdigest()
+    f = torch.zeros(4, 4)
+    assert bench.input_digest([f]) == hashlib.sha256(bytes(64)).hexdigest()
+
+
+def test_norm_pass_record(bench):
+    # 768 MiB read once per step, 10 steps in 1.2 ms of kernel time
+    kt = {"prep": (1.2, 10)}
+    r = bench.norm_pass_record(kt, 805306368, 10, 6789.3)
+    assert r["achieved"] == round(805306368 * 10 / 1.2e-3 / 1e9, 1)
+    assert r["frac"] == round(r["achieved"] / 6789.3, 4) and r["unit"] == "GB/s" and r["launches"] == 10
+    assert bench.norm_pass_record({"prep": (0.0, 0)}, 1, 1, 1.0) is None
+    assert bench.norm_pass_record({}, 1, 1, 1.0) is None

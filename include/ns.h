@@ -208,18 +208,26 @@ int ns_release_workspace(void);
  * since load (for launch accounting in benchmarks). */
 int64_t ns_num_kernel_launches(void);
 
+/* ns_num_workspace_allocations -- device allocations (workspace cache growth)
+ * this library has requested in this process since load; calls that reuse the
+ * cached workspace, calls given a caller workspace and
+ * ns_orthogonalize_batched_noalloc leave it unchanged. */
+int64_t ns_num_workspace_allocations(void);
+
 /*
  * Per-kernel timing for measurement tools. While enabled, every kernel
  * launch of later calls is bracketed by a pair of CUDA events recorded on the
  * caller's stream (a few microseconds of overhead per launch).
  * ns_set_kernel_timing(1) enables and clears the record, (0) disables it.
  * ns_get_kernel_times synchronises on the recorded events and writes, for the
- * kernel classes 0 norm (per-matrix scale), 1 prep (the pass over the caller's
- * matrices: bf16 tile sums and extents, plus a copy where the first step
- * cannot read them in place; fp32 the normalising copy), 2 gram, 3 square,
- * 4 apply, 5 resident, 6 gemm (the tensor-core kernel running every step and
- * phase of a call in one launch), the total milliseconds into ms[k] and the
- * launch count into launches[k] for k < n (n <= 7). Returns NS_OK or NS_ECUDA.
+ * kernel classes 0 norm pass (the one read of the caller's matrices: bf16 tile
+ * sums of squares and extents, plus a copy where the first step cannot read
+ * them in place; fp32 the sums and extents), 1 norm finish (bf16: the
+ * per-matrix scale from the tile sums), 2 gram, 3 square, 4 apply,
+ * 5 resident, 6 gemm (the tensor-core kernel running every step and phase of
+ * a call in one launch), 7 prep (fp32: the normalising copy), the total
+ * milliseconds into ms[k] and the launch count into launches[k] for k < n
+ * (n <= 8). Returns NS_OK or NS_EINVAL / NS_ECUDA.
  */
 int ns_set_kernel_timing(int enable);
 int ns_get_kernel_times(double *ms, int64_t *launches, int n);
@@ -251,6 +259,22 @@ int ns_set_gemm_schedule(int mode);
  * the wait gave up as designed, NS_EINVAL for a bad limit, NS_ECUDA otherwise.
  */
 int ns_selftest_wait_timeout(int limit_us, void *stream);
+
+/*
+ * ns_selftest_dependency_timeout -- failure-detection self-test of the
+ * tensor-core kernel's dependency waits (the per-matrix completion counters of
+ * the NS_SCHED_SINGLE schedule). Runs a two-step call on two 512 x 768 bf16
+ * matrices (allocated, filled and released by the call itself) in one
+ * cooperative launch whose completion signals are held back, with every
+ * bounded wait limited to `limit_us` microseconds (1 .. 10^7): the items that
+ * depend on earlier phases wait on counters that never advance, give up,
+ * record NS_ETIMEOUT in the device status word (read it with ns_get_status),
+ * drain their in-flight copies and MMAs, free their TMEM and exit. No fault,
+ * no trap, no hang; the context stays usable. Synchronises `stream`. Returns
+ * NS_OK if the waits gave up as designed, NS_EINVAL for a bad limit, NS_ENOMEM
+ * if the buffers could not be allocated, NS_ECUDA otherwise.
+ */
+int ns_selftest_dependency_timeout(int limit_us, void *stream);
 
 #ifdef __cplusplus
 }

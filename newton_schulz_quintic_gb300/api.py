@@ -79,6 +79,10 @@ def load_library() -> ctypes.CDLL:
         lib.ns_orthogonalize_batched_noalloc.argtypes = [vp, vp, i32, i32, vp, i32, vp]
         lib.ns_selftest_wait_timeout.restype = i32
         lib.ns_selftest_wait_timeout.argtypes = [i32, vp]
+        lib.ns_selftest_dependency_timeout.restype = i32
+        lib.ns_selftest_dependency_timeout.argtypes = [i32, vp]
+        lib.ns_num_workspace_allocations.restype = i64
+        lib.ns_num_workspace_allocations.argtypes = []
         lib.ns_plan_shards.restype = i32
         lib.ns_plan_shards.argtypes = [vp, vp, i32, i32, ctypes.c_double, i32, vp, vp]
         lib.ns_set_gemm_schedule.restype = i32
@@ -248,11 +252,18 @@ def get_status(stream=None) -> int:
     return int(load_library().ns_get_status(ctypes.c_void_p(s.cuda_stream)))
 
 
+def release_workspace() -> None:
+    """Synchronise the current device and free the library's cached workspaces there."""
+    rc = load_library().ns_release_workspace()
+    if rc != 0:
+        raise NSError(rc, "ns_release_workspace")
+
+
 def num_kernel_launches() -> int:
     return int(load_library().ns_num_kernel_launches())
 
 
-KERNEL_KINDS = ("norm", "prep", "gram", "square", "apply", "resident", "gemm")
+KERNEL_KINDS = ("norm_pass", "norm_finish", "gram", "square", "apply", "resident", "gemm", "prep")
 
 
 def set_kernel_timing(enable: bool) -> None:
@@ -275,6 +286,20 @@ def selftest_wait_timeout(limit_us: int = 20000, stream=None) -> int:
     import torch
     s = stream if stream is not None else torch.cuda.current_stream()
     return int(load_library().ns_selftest_wait_timeout(int(limit_us), ctypes.c_void_p(s.cuda_stream)))
+
+
+def selftest_dependency_timeout(limit_us: int = 20000, stream=None) -> int:
+    """Run the dependency-counter timeout self-test (see include/ns.h); returns
+    its status code."""
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(load_library().ns_selftest_dependency_timeout(int(limit_us),
+                                                             ctypes.c_void_p(s.cuda_stream)))
+
+
+def num_workspace_allocations() -> int:
+    """Device workspace allocations the library has requested since load."""
+    return int(load_library().ns_num_workspace_allocations())
 
 
 PLAN_ORDERS = {"cost": 0, "numel": 1}

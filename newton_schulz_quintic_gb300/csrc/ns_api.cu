@@ -32,6 +32,7 @@ namespace ns {
 
 static std::atomic<int64_t> g_launches{0};
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+static std::atomic<int64_t> g_allocations{0};
 
 // Device status word (one per device, file-scope; see ns_get_status) and the
 // flag the wait self-test reports through.
@@ -392,6 +393,7 @@ int ensure_ws(CachedWs &c, size_t bytes, cudaStream_t s) {
   }
   c.last_blob.clear();
   void *p = nullptr;
+  g_allocations.fetch_add(1, std::memory_order_relaxed);
   if (cudaMallocAsync(&p, bytes, s) != cudaSuccess) {
     cudaGetLastError();
     return NS_ENOMEM;
@@ -402,7 +404,10 @@ int ensure_ws(CachedWs &c, size_t bytes, cudaStream_t s) {
 }
 
 // ------------------------------------------------------------ kernel timing
-constexpr int kKinds = 7;
+// kinds: 0 norm pass (the read of the caller's matrices), 1 norm finish (bf16:
+// per-matrix scale), 2 gram, 3 square, 4 apply, 5 resident, 6 gemm (one
+// launch running every step and phase), 7 prep (fp32: the normalising copy)
+constexpr int kKinds = 8;
 
 // How the tensor-core path is launched (ns_set_gemm_schedule): one launch per
 // step and phase (default) or one launch per call with per-matrix counters.
@@ -429,9 +434,17 @@ int timed(int kind, cudaStream_t s, F &&fn) {
 }
 
 // ------------------------------------------------------------ execution
+// Options of one call that tests use: the limit of the kernels' bounded waits,
+// and the dependency-timeout self-test (the single-launch schedule with every
+// completion signal held back).
+struct RunOpts {
+  uint64_t wait_limit_ns = kWaitLimitNs;
+  bool hold_signals = false;
+};
+
 // co: one (a, b, c) triple for every step (table == false) or a steps x 3 table
 int execute(const Layout &L, uint8_t *ws, int steps, const float *co, bool table, float eps, DevInfo *di,
-            cudaStream_t s) {
+            cudaStream_t s, const RunOpts &opt) {
   const MatDesc *mats = reinterpret_cast<const MatDesc *>(ws + L.off_mats);
   if (!L.res.empty()) {
     ResParams rp{};
@@ -467,11 +480,11 @@ int execute(const Layout &L, uint8_t *ws, int steps, const float *co, bool table
   // epilogues apply 1/(||Y|| + eps). Otherwise: norm, then a scaled copy.
   const bool fused = L.dtype == NS_BF16 && steps > 0;
   if (fused) {
-    if (timed(1, s, [&] { return launch_norm_tiles(pp, L.prefix.back(), 2 * di->sms, s); })) return NS_ECUDA;
-    if (timed(0, s, [&] { return launch_norm_finish(pp, s); })) return NS_ECUDA;
+    if (timed(0, s, [&] { return launch_norm_tiles(pp, L.prefix.back(), 2 * di->sms, s); })) return NS_ECUDA;
+    if (timed(1, s, [&] { return launch_norm_finish(pp, s); })) return NS_ECUDA;
   } else {
     if (timed(0, s, [&] { return launch_norm(pp, s); })) return NS_ECUDA;
-    if (timed(1, s, [&] { return launch_prep(pp, L.prefix.back(), s); })) return NS_ECUDA;
+    if (timed(7, s, [&] { return launch_prep(pp, L.prefix.back(), s); })) return NS_ECUDA;
   }
   const Tile *t01 = reinterpret_cast<const Tile *>(ws + L.off_t01);
   const Tile *t2 = reinterpret_cast<const Tile *>(ws + L.off_t2);
@@ -488,12 +501,14 @@ int execute(const Layout &L, uint8_t *ws, int steps, const float *co, bool table
     tp.status = di->status;
     tp.done = done;
     tp.rscale = pp.rscale;
+    tp.wait_limit_ns = opt.wait_limit_ns;
+    tp.hold_signals = opt.hold_signals ? 1 : 0;
     tp.ncoef = table ? steps : 1;
     for (int k = 0; k < (table ? steps : 1); ++k)
       for (int u = 0; u < 3; ++u) tp.coef[k][u] = co[3 * k + u];
     const int per_step = 2 * tp.n01 + tp.n2;
     int rc = 1;
-    if (!phase_launches() && static_cast<int64_t>(steps) * per_step < (int64_t(1) << 30)) {
+    if ((opt.hold_signals || !phase_launches()) && static_cast<int64_t>(steps) * per_step < (int64_t(1) << 30)) {
       // one launch: every step and phase, items ordered by per-matrix counters
       tp.g_begin = 0;
       tp.g_end = steps * per_step;
@@ -501,6 +516,7 @@ int execute(const Layout &L, uint8_t *ws, int steps, const float *co, bool table
       rc = timed(6, s, [&] { return launch_tc(tp, di->sms, s); });
       if (rc < 0) return NS_ECUDA;
     }
+    if (rc == 1 && opt.hold_signals) return NS_ECUDA;  // the self-test needs the single launch
     if (rc == 1) {  // one launch per step and phase
       tp.wait = 0;
       const int begin[3] = {0, tp.n01, 2 * tp.n01}, count[3] = {tp.n01, tp.n01, tp.n2};
@@ -534,7 +550,8 @@ int execute(const Layout &L, uint8_t *ws, int steps, const float *co, bool table
 }
 
 int run(void *const *X, const int64_t *shapes, int count, int steps, const float *coeffs, float eps, int dtype,
-        void *user_ws, size_t user_ws_bytes, cudaStream_t s, int slot = 0, bool table = false) {
+        void *user_ws, size_t user_ws_bytes, cudaStream_t s, int slot = 0, bool table = false,
+        const RunOpts &opt = RunOpts()) {
   int rc = validate(X, shapes, count, steps, dtype, true);
   if (rc) return rc;
   if (table && steps > 0 && (!coeffs || steps > kMaxTableSteps)) return NS_EINVAL;
@@ -570,7 +587,7 @@ int run(void *const *X, const int64_t *shapes, int count, int steps, const float
     if (cudaMemcpyAsync(ws, blob.data(), blob.size(), cudaMemcpyHostToDevice, s) != cudaSuccess) return NS_ECUDA;
     if (cache) cache->last_blob = blob;
   }
-  return execute(L, ws, steps, co, table, eps, di, s);
+  return execute(L, ws, steps, co, table, eps, di, s, opt);
 }
 
 // ------------------------------------------------------------ host pipeline
@@ -597,6 +614,17 @@ int host_pipe(int dev, size_t nev, HostPipe **out) {
 }
 
 }  // namespace
+
+// Every check a call makes before it touches the GPU: the arguments, then the
+// current device (see ns_internal.h).
+int check_call(void *const *X, const int64_t *shapes, int count, int steps, int dtype) {
+  const int rc = validate(X, shapes, count, steps, dtype, true);
+  if (rc || count == 0) return rc;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DevInfo *di = nullptr;
+  return device_info(&di);
+}
+
 }  // namespace ns
 
 using namespace ns;
@@ -807,6 +835,8 @@ int ns_release_workspace(void) {
 
 int64_t ns_num_kernel_launches(void) { return g_launches.load(); }
 
+int64_t ns_num_workspace_allocations(void) { return g_allocations.load(); }
+
 int ns_set_gemm_schedule(int mode) {
   if (mode != NS_SCHED_PHASE && mode != NS_SCHED_SINGLE) return NS_EINVAL;
   g_gemm_schedule.store(mode);
@@ -829,6 +859,41 @@ int ns_selftest_wait_timeout(int limit_us, void *stream) {
   if (cudaMemcpyAsync(&h, gave_up, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return NS_ECUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return NS_ECUDA;
   return h ? NS_OK : NS_ECUDA;
+}
+
+int ns_selftest_dependency_timeout(int limit_us, void *stream) {
+  if (limit_us <= 0 || limit_us > 10000000) return NS_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    DevInfo *di = nullptr;
+    const int rc = device_info(&di);
+    if (rc) return rc;
+  }
+  // two small non-zero bf16 matrices (every element 0x3C3C) and their own
+  // workspace, allocated here and released before returning
+  const int64_t shapes[4] = {512, 768, 512, 768};
+  const size_t mat_bytes = 512 * 768 * 2;
+  const size_t ws_bytes = ns_workspace_bytes(shapes, 2, NS_BF16);
+  void *buf = nullptr;
+  if (cudaMallocAsync(&buf, 2 * mat_bytes + ws_bytes, s) != cudaSuccess) {
+    cudaGetLastError();
+    return NS_ENOMEM;
+  }
+  uint8_t *base = static_cast<uint8_t *>(buf);
+  void *X[2] = {base, base + mat_bytes};
+  int rc = cudaMemsetAsync(base, 0x3C, 2 * mat_bytes, s) == cudaSuccess ? NS_OK : NS_ECUDA;
+  RunOpts opt;
+  opt.wait_limit_ns = static_cast<uint64_t>(limit_us) * 1000ull;
+  opt.hold_signals = true;
+  if (rc == NS_OK) rc = run(X, shapes, 2, 2, nullptr, 1e-7f, NS_BF16, base + 2 * mat_bytes, ws_bytes, s, 0, false, opt);
+  const cudaError_t sync = cudaStreamSynchronize(s);
+  cudaFreeAsync(buf, s);
+  if (cudaStreamSynchronize(s) != cudaSuccess || sync != cudaSuccess) return NS_ECUDA;
+  if (rc) return rc;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(int)) != cudaSuccess) return NS_ECUDA;
+  return v != 0 ? NS_OK : NS_ECUDA;
 }
 
 static void drop_timed() {

@@ -39,10 +39,6 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
-// Upper bound of any single wait inside a kernel. A correct kernel never gets
-// near it; if it is reached the kernel records NS_ETIMEOUT and winds down.
-constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s
-
 // ---------------------------------------------------------------- shared memory
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -88,22 +84,31 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t pa
   return ok != 0;
 }
 
+// What a bounded wait needs besides its condition: the CTA's abort flag (any
+// wait that gives up sets it, and every other wait of the CTA then gives up
+// too), the device status word and the wait's time limit in nanoseconds. The
+// limit is a kernel parameter, so a test can make a wait run out quickly.
+struct Waiter {
+  volatile int *abort;
+  int *status;
+  uint64_t limit_ns;
+};
+
 // Wait for the phase of `bar` with parity `parity` to complete. Gives up
-// after kWaitLimitNs or once *abort is set; on giving up it sets *abort and
+// after w.limit_ns or once *w.abort is set; on giving up it sets *w.abort and
 // records the timeout in the status word. Returns true if the phase completed.
 template <bool kCluster = false>
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                          int *status, uint64_t limit_ns = kWaitLimitNs) {
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const Waiter &w) {
   auto test = [&] { return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
   if (test()) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (test()) return true;
     if ((it & 255u) == 0) {
-      if (*abort) return false;
-      if (globaltimer_ns() - t0 > limit_ns) {
-        *abort = 1;
-        set_status(status, kStatusTimeout);
+      if (*w.abort) return false;
+      if (globaltimer_ns() - t0 > w.limit_ns) {
+        *w.abort = 1;
+        set_status(w.status, kStatusTimeout);
         return false;
       }
     }
@@ -126,18 +131,18 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 }
 
 // Bounded wait until *counter >= need (acquire, GPU scope). Gives up like
-// mbar_wait: after kWaitLimitNs or once *abort is set.
-__device__ __forceinline__ bool wait_count(const int *counter, int need, volatile int *abort, int *status) {
+// mbar_wait: after w.limit_ns or once *w.abort is set.
+__device__ __forceinline__ bool wait_count(const int *counter, int need, const Waiter &w) {
   if (ld_acquire_gpu(counter) >= need) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     __nanosleep(128);
     if (ld_acquire_gpu(counter) >= need) return true;
     if ((it & 63u) == 0) {
-      if (*abort) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
-        *abort = 1;
-        set_status(status, kStatusTimeout);
+      if (*w.abort) return false;
+      if (globaltimer_ns() - t0 > w.limit_ns) {
+        *w.abort = 1;
+        set_status(w.status, kStatusTimeout);
         return false;
       }
     }

@@ -36,6 +36,11 @@ enum StoreType : int { kF32 = 0, kBF16 = 1 };
 
 constexpr int kMaxTableSteps = 32;  // longest per-step coefficient table
 
+// Default upper bound of any single bounded wait inside a kernel (passed to
+// the kernels as a parameter). A correct kernel never gets near it; if it is
+// reached the kernel records NS_ETIMEOUT and winds down.
+constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s
+
 // Tile of one GEMM phase: tile rows [row0, row0+BM), tile cols [col0, col0+BN)
 // of matrix `mat` (index into the matrix descriptor table).
 struct Tile {
@@ -113,6 +118,8 @@ struct TcParams {
   int *status;
   int *done;            // per matrix completion counter (zeroed by the host per call)
   const float *rscale;  // per matrix 1 / (||Y||_F + eps): step 0 scales gram by its square and apply by it
+  uint64_t wait_limit_ns;  // limit of every bounded wait in the kernel
+  int hold_signals;     // self-test only: never publish completions, so dependent items time out
   int ncoef;            // 1: coef[0] for every step; else coef[step]
   float coef[kMaxTableSteps][3];
 };
@@ -171,5 +178,10 @@ int launch_wait_probe(int *status, uint64_t limit_ns, int *gave_up, cudaStream_t
 int resident_smem_bytes(int m, int n, int dtype);
 
 void count_launch();
+
+// Validation of a device-pointer call (the same checks, in the same order, as
+// ns_orthogonalize_batched makes before launching) and the current-device
+// check: NS_OK, or the status code such a call would return.
+int check_call(void *const *X, const int64_t *shapes, int count, int steps, int dtype);
 
 }  // namespace ns

@@ -18,6 +18,7 @@
 #include <mutex>
 
 #include "../../include/ns.h"
+#include "ns_internal.h"
 
 namespace {
 
@@ -59,13 +60,15 @@ int scratch_address(void **out) {
 
 extern "C" int ns_orthogonalize_batched_noalloc(void *const *X, const int64_t *shapes, int count, int steps,
                                                 const float *coeffs, int dtype, void *stream) {
-  if (count < 0 || steps < 0 || (dtype != NS_F32 && dtype != NS_BF16)) return NS_EINVAL;
-  if (count == 0) return NS_OK;
+  // the arguments and the device first, with the codes every entry point
+  // returns for them; only a valid batch is measured against the array
+  int rc = ns::check_call(X, shapes, count, steps, dtype);
+  if (rc != NS_OK || count == 0) return rc;
   const size_t need = ns_workspace_bytes(shapes, count, dtype);
   if (need == 0) return NS_EINVAL;
   if (need > kNoAllocScratchBytes) return NS_ETOOBIG;
   void *ws = nullptr;
-  const int rc = scratch_address(&ws);
+  rc = scratch_address(&ws);
   if (rc != NS_OK) return rc;
   // the caller-workspace path: it launches into `ws` and allocates nothing
   return ns_orthogonalize_batched_ex(X, shapes, count, steps, coeffs, 1e-7f, dtype, ws, kNoAllocScratchBytes,

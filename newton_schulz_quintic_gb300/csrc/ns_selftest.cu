@@ -21,7 +21,8 @@ __global__ void __launch_bounds__(32) ns_wait_probe_kernel(int *status, uint64_t
   }
   __syncwarp();
   if (threadIdx.x == 0) {
-    const bool done = mbar_wait(&bar, 0, &abort_flag, status, limit_ns);
+    const Waiter w{&abort_flag, status, limit_ns};
+    const bool done = mbar_wait(&bar, 0, w);
     *gave_up = done ? 0 : 1;
   }
 }

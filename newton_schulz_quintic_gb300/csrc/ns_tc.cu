@@ -463,11 +463,11 @@ __device__ __forceinline__ void epilogue_chunk(const StepCtx &p, const TileInfo 
 
 // Bounded wait that ignores the abort flag: used only to drain in-flight
 // asynchronous work before the CTA releases its shared memory and TMEM.
-__device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity, int *status) {
+__device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity, const Waiter &w) {
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
-      set_status(status, kStatusTimeout);
+    if (globaltimer_ns() - t0 > w.limit_ns) {
+      set_status(w.status, kStatusTimeout);
       return;
     }
   }
@@ -479,13 +479,12 @@ __device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity, int *
 // reloads, wait for the accumulator, then drain this warp's chunks.
 template <int PHASE>
 __device__ __forceinline__ bool epilogue_item(const StepCtx &sc, const TileInfo &ti, int r, int c0, uint32_t tbase,
-                                              uint32_t *stage, uint64_t *tfull, uint32_t parity, volatile int *abort,
-                                              int *status) {
+                                              uint32_t *stage, uint64_t *tfull, uint32_t parity, const Waiter &w) {
   // the operand does not depend on the accumulator: fetch it while the MMAs run
   uint4 pre[2][4];
   prefetch_chunk<PHASE>(sc, ti, r, c0, pre[0]);
   prefetch_chunk<PHASE>(sc, ti, r, c0 + 1, pre[1]);
-  if (!mbar_wait<true>(tfull, parity, abort, status)) return false;
+  if (!mbar_wait<true>(tfull, parity, w)) return false;
   tc_fence_after();
   // TMEM loads double-buffered: chunk c+1 is read while chunk c is stored
   uint32_t va[32], vb[32];
@@ -517,9 +516,9 @@ __device__ __forceinline__ bool epilogue_item(const StepCtx &sc, const TileInfo 
 // A wait of a whole warp that only lane 0 polls (the other lanes sleep in
 // the shuffle that broadcasts the outcome), leaving the warp converged.
 template <bool kCluster>
-__device__ __forceinline__ bool warp_mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort, int *status) {
+__device__ __forceinline__ bool warp_mbar_wait(uint64_t *bar, uint32_t parity, const Waiter &w) {
   int ok = 1;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait<kCluster>(bar, parity, abort, status) ? 1 : 0;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait<kCluster>(bar, parity, w) ? 1 : 0;
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
@@ -531,9 +530,9 @@ template <int AMN, int BMN>
 __device__ __forceinline__ bool produce_segment(int kb0, int kb1, const void *map_a, const void *map_b, int a0, int b0,
                                                 uint8_t *sA, uint8_t *sB, Barriers *bar, bool leader, int &stage,
                                                 uint32_t &phase_bit, int *issued_phase, uint64_t pol,
-                                                volatile int *abort, int *status) {
+                                                const Waiter &w) {
   for (int kb = kb0; kb < kb1; ++kb) {
-    if (!warp_mbar_wait<true>(&bar->empty[stage], phase_bit ^ 1u, abort, status)) return false;
+    if (!warp_mbar_wait<true>(&bar->empty[stage], phase_bit ^ 1u, w)) return false;
     if (elect_one()) {
       if (leader) mbar_arrive_expect_tx(&bar->full[stage], kPairStageBytes);
       const uint32_t full_leader = mapa_shared(smem_u32(&bar->full[stage]), 0);
@@ -557,12 +556,11 @@ __device__ __forceinline__ bool produce_segment(int kb0, int kb1, const void *ma
 // both producers. AMN / BMN: MN-major first / second operand.
 template <int AMN, int BMN>
 __device__ __forceinline__ bool mma_segment(uint32_t d_tmem, int kb0, int kb1, uint8_t *sA, uint8_t *sB,
-                                            Barriers *bar, int &stage, uint32_t &phase_bit, volatile int *abort,
-                                            int *status) {
+                                            Barriers *bar, int &stage, uint32_t &phase_bit, const Waiter &w) {
   constexpr uint32_t idesc = umma_idesc_bf16(kTcCluster * kTcBM, kTcBN, AMN, BMN);
   constexpr uint16_t kPairMask = (1u << kTcCluster) - 1;
   for (int kb = kb0; kb < kb1; ++kb) {
-    if (!warp_mbar_wait<true>(&bar->full[stage], phase_bit, abort, status)) return false;
+    if (!warp_mbar_wait<true>(&bar->full[stage], phase_bit, w)) return false;
     tc_fence_after();
     const uint32_t a_addr = smem_u32(sA + stage * kABytes);
     const uint32_t b_addr = smem_u32(sB + stage * kBBytes);
@@ -626,6 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
   const bool tmem_ok = peer_tmem == tmem;
   if (!tmem_ok && threadIdx.x == 0) set_status(p.status, kStatusTmemMismatch);
   volatile int *abort = &bar->abort;
+  const Waiter w{abort, p.status, p.wait_limit_ns};
 
   if (tmem_ok && warp == 0) {
     {
@@ -648,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
           // operands come from earlier phases of this matrix, written by
           // epilogues anywhere on the GPU
           int ready = 1;
-          if (lane == 0) ready = wait_count(p.done + ti.mat, units_before(*ti.d, step, phase), abort, p.status) ? 1 : 0;
+          if (lane == 0) ready = wait_count(p.done + ti.mat, units_before(*ti.d, step, phase), w) ? 1 : 0;
           if (!__shfl_sync(0xffffffffu, ready, 0)) break;
           fence_proxy_async_global();
         }
@@ -656,17 +655,17 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
         const int a0 = ti.row0 + my_rows, b0 = ti.col0 + static_cast<int>(rank) * (kTcBN / 2);
         // one k-loop per operand order, so the copies issued are exactly the ones needed
         ok = produce_segment<1, 1>(0, pl.e0, pl.map[0][0], pl.map[0][1], a0, b0, sA, sB, bar, leader, stage, phase_bit,
-                                   issued_phase, pol, abort, p.status);
+                                   issued_phase, pol, w);
         if (ok)
           ok = produce_segment<0, 1>(pl.e0, pl.e1, pl.map[1][0], pl.map[1][1], a0, b0, sA, sB, bar, leader, stage,
-                                     phase_bit, issued_phase, pol, abort, p.status);
+                                     phase_bit, issued_phase, pol, w);
         if (ok)
           ok = produce_segment<0, 0>(pl.e1, ti.nk, pl.map[2][0], pl.map[2][1], a0, b0, sA, sB, bar, leader, stage,
-                                     phase_bit, issued_phase, pol, abort, p.status);
+                                     phase_bit, issued_phase, pol, w);
       }
       if (*abort && leader && lane == 0) {
         for (int s = 0; s < kStages; ++s)
-          if (issued_phase[s] >= 0) mbar_drain(&bar->full[s], static_cast<uint32_t>(issued_phase[s]), p.status);
+          if (issued_phase[s] >= 0) mbar_drain(&bar->full[s], static_cast<uint32_t>(issued_phase[s]), w);
       }
     }
   } else if (tmem_ok && warp == 1) {
@@ -686,13 +685,13 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
         pipe_take(p, nclusters, q, step, phase, ti, direct);
         if (ti.skip) continue;
         const ItemPlan pl = plan_item(*ti.d, step, phase, ti.tr, direct, ti.row0, ti.col0, ti.nk);
-        if (!warp_mbar_wait<true>(&bar->tempty[acc], acc_phase ^ 1u, abort, p.status)) break;
+        if (!warp_mbar_wait<true>(&bar->tempty[acc], acc_phase ^ 1u, w)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * kTcBN);
         // one k-loop per operand order, so descriptors stay compile-time
-        ok = mma_segment<1, 1>(d_tmem, 0, pl.e0, sA, sB, bar, stage, phase_bit, abort, p.status);
-        if (ok) ok = mma_segment<0, 1>(d_tmem, pl.e0, pl.e1, sA, sB, bar, stage, phase_bit, abort, p.status);
-        if (ok) ok = mma_segment<0, 0>(d_tmem, pl.e1, ti.nk, sA, sB, bar, stage, phase_bit, abort, p.status);
+        ok = mma_segment<1, 1>(d_tmem, 0, pl.e0, sA, sB, bar, stage, phase_bit, w);
+        if (ok) ok = mma_segment<0, 1>(d_tmem, pl.e0, pl.e1, sA, sB, bar, stage, phase_bit, w);
+        if (ok) ok = mma_segment<0, 0>(d_tmem, pl.e1, ti.nk, sA, sB, bar, stage, phase_bit, w);
         if (!ok) break;
         if (elect_one()) umma_commit_pair_multicast(&bar->tfull[acc], kPairMask);
         __syncwarp();
@@ -703,7 +702,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
       }
       if (elect_one()) {
         umma_commit_pair_multicast(&bar->drain, 1u);
-        mbar_drain(&bar->drain, 0, p.status);
+        mbar_drain(&bar->drain, 0, w);
       }
       __syncwarp();
     }
@@ -726,7 +725,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
       if (p.wait) {
         // the operand this epilogue reloads (A, or the current iterate) comes from an earlier phase
         bool ready = true;
-        if (lane == 0) ready = wait_count(p.done + ti.mat, units_before(*ti.d, step, phase), abort, p.status);
+        if (lane == 0) ready = wait_count(p.done + ti.mat, units_before(*ti.d, step, phase), w);
         if (!__shfl_sync(0xffffffffu, ready ? 1 : 0, 0)) break;
       }
       ti.row0 += my_rows;
@@ -734,11 +733,11 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
       const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kTcBN);
       bool ok;
       if (phase == 0)
-        ok = epilogue_item<0>(sc, ti, r, c0, tbase, stage, &bar->tfull[acc], acc_phase, abort, p.status);
+        ok = epilogue_item<0>(sc, ti, r, c0, tbase, stage, &bar->tfull[acc], acc_phase, w);
       else if (phase == 1)
-        ok = epilogue_item<1>(sc, ti, r, c0, tbase, stage, &bar->tfull[acc], acc_phase, abort, p.status);
+        ok = epilogue_item<1>(sc, ti, r, c0, tbase, stage, &bar->tfull[acc], acc_phase, w);
       else
-        ok = epilogue_item<2>(sc, ti, r, c0, tbase, stage, &bar->tfull[acc], acc_phase, abort, p.status);
+        ok = epilogue_item<2>(sc, ti, r, c0, tbase, stage, &bar->tfull[acc], acc_phase, w);
       if (!ok) break;
       tc_fence_before();
       __syncwarp();
@@ -766,15 +765,15 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
         decode_item(p, g, step, phase, t);
         const TileInfo ti = tile_info(p, phase, t);
         if (ti.skip) {
-          if (p.wait && !wait_count(p.done + ti.mat, units_before(*ti.d, step, phase), abort, p.status)) break;
+          if (p.wait && !wait_count(p.done + ti.mat, units_before(*ti.d, step, phase), w)) break;
         } else {
-          if (!mbar_wait(&bar->epi_done[acc], acc_phase, abort, p.status)) break;
+          if (!mbar_wait(&bar->epi_done[acc], acc_phase, w)) break;
           if (++acc == kAccs) {
             acc = 0;
             acc_phase ^= 1u;
           }
         }
-        red_release_gpu_add(p.done + ti.mat, 1);
+        if (!p.hold_signals) red_release_gpu_add(p.done + ti.mat, 1);
       }
     }
   }

@@ -153,6 +153,25 @@ def test_selftest_rejects_bad_limits_before_launch(lib):
     assert lib.ns_selftest_wait_timeout(0, None) == -1
     assert lib.ns_selftest_wait_timeout(-5, None) == -1
     assert lib.ns_selftest_wait_timeout(20000000, None) == -1
+    assert lib.ns_selftest_dependency_timeout(0, None) == -1
+    assert lib.ns_selftest_dependency_timeout(20000001, None) == -1
+
+
+@pytest.mark.skipif(_has_gpu(), reason="uses fake device pointers: only run where nothing can launch")
+def test_noalloc_checks_arguments_and_device_before_its_size_limit(lib):
+    # the no-allocation entry point returns what every entry point returns for
+    # bad arguments and for a missing device, even for a batch that would also
+    # be too large for its scratch array; its own refusal comes last
+    P, S = ctypes.c_void_p, ctypes.c_int64
+    big = (S * 2)(8192, 6144)                     # beyond the 256 MiB scratch
+    f = lib.ns_orthogonalize_batched_noalloc
+    assert f((P * 1)(0), big, 1, 5, None, 1, None) == -1             # null matrix
+    assert f((P * 1)(0x100001), big, 1, 5, None, 1, None) == -2      # misaligned
+    assert f((P * 2)(0x100000, 0x100000), (S * 4)(8192, 6144, 8192, 6144), 2, 5, None, 1, None) == -1
+    assert f((P * 1)(0x100000), big, 1, -1, None, 1, None) == -1     # negative steps
+    assert f((P * 1)(0x100000), big, 1, 5, None, 1, None) == -6      # no device, not "too big"
+    assert f(None, None, 0, 5, None, 1, None) == 0                   # empty batch: no-op
+    assert lib.ns_selftest_dependency_timeout(1000, None) == -6
 
 
 def test_schedule_rejects_bad_tables_before_launch(lib):

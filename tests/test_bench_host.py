@@ -122,9 +122,35 @@ def test_input_digest_covers_every_byte(bench):
 
 def test_norm_pass_record(bench):
     # 768 MiB read once per step, 10 steps in 1.2 ms of kernel time
-    kt = {"prep": (1.2, 10)}
+    kt = {"norm_pass": (1.2, 10), "prep": (5.0, 10)}
     r = bench.norm_pass_record(kt, 805306368, 10, 6789.3)
     assert r["achieved"] == round(805306368 * 10 / 1.2e-3 / 1e9, 1)
     assert r["frac"] == round(r["achieved"] / 6789.3, 4) and r["unit"] == "GB/s" and r["launches"] == 10
-    assert bench.norm_pass_record({"prep": (0.0, 0)}, 1, 1, 1.0) is None
+    assert bench.norm_pass_record({"norm_pass": (0.0, 0)}, 1, 1, 1.0) is None
     assert bench.norm_pass_record({}, 1, 1, 1.0) is None
+
+
+def test_rank_share_is_the_planners_split(bench):
+    # one batch over several GPUs: each rank's share is what the library's
+    # planner assigns it, the shares are disjoint and complete, and one GPU
+    # takes the whole batch
+    from newton_schulz_quintic_gb300 import api, inputs
+    wl = inputs.WORKLOADS["bf16-mixed-120"]
+    assert bench.rank_share(wl, 1, 0) == list(range(wl.count))
+    for world in (2, 4, 8):
+        assign, _ = api.plan_shards(wl.shapes, world, numel_eps=0.3)
+        shares = [bench.rank_share(wl, world, r) for r in range(world)]
+        for r, share in enumerate(shares):
+            assert share == [i for i, a in enumerate(assign) if a == r]
+        assert sorted(sum(shares, [])) == list(range(wl.count))
+        costs = [sum(api.cost(*wl.shapes[i]) for i in sh) for sh in shares]
+        assert max(costs) / (sum(costs) / world) < 1.10
+
+
+def test_rank_calls(bench):
+    from newton_schulz_quintic_gb300 import inputs
+    wl = inputs.WORKLOADS["bf16-moe-76x2048x6144"]
+    # a replica keeps the workload's remainder batches, a split share is one call
+    assert bench.rank_calls(wl, list(range(76)), split=False) == [list(range(64)), list(range(64, 76))]
+    assert bench.rank_calls(wl, [3, 9], split=True) == [[3, 9]]
+    assert bench.rank_calls(wl, [], split=True) == []

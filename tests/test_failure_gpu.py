@@ -1,10 +1,18 @@
 """Failure detection on the device, without faulting anything.
 
-Every wait inside the library's kernels is bounded; when one gives up, the
-kernel records NS_ETIMEOUT in the device status word and returns, so the host
-can read the failure and the CUDA context stays usable. The self-test entry
-point makes one such wait run out (an mbarrier that nothing arrives on, with a
-20 ms limit) and this test checks the status and that work still runs after.
+Every wait inside the library's kernels is bounded, with its limit passed in
+as a kernel parameter; when one gives up, the kernel records NS_ETIMEOUT in the
+device status word, drains its in-flight work and returns, so the host can read
+the failure and the CUDA context stays usable. Two self-tests make a wait run
+out with a 20 ms limit:
+
+* an mbarrier that nothing arrives on (one CTA);
+* the tensor-core kernel's own dependency waits: a cooperative single-launch
+  call whose completion counters are never advanced, so every item that needs
+  an earlier phase of its matrix waits on a counter that never reaches its
+  target (the hang the dion page's "Test plan" catches with a timeout).
+
+After each, the status is read once, then cleared, and a parity call runs.
 """
 import numpy as np
 import pytest
@@ -23,11 +31,7 @@ def _lib():
     api.load_library()
 
 
-def test_bounded_wait_reports_timeout_and_context_survives():
-    assert api.get_status() == 0
-    assert api.selftest_wait_timeout(20000) == 0          # the wait gave up as designed
-    assert api.get_status() == -5                         # NS_ETIMEOUT, read once ...
-    assert api.get_status() == 0                          # ... then cleared
+def _parity_call_still_works():
     g = torch.Generator().manual_seed(3)
     x = (torch.randn((300, 520), generator=g) * 0.02).to(torch.bfloat16)
     d = x.cuda()
@@ -37,3 +41,26 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     ref = oracle.orthogonalize(x)
     got = oracle.to_f64(d.cpu())
     assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 3e-2
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    assert api.get_status() == 0
+    assert api.selftest_wait_timeout(20000) == 0          # the wait gave up as designed
+    assert api.get_status() == -5                         # NS_ETIMEOUT, read once ...
+    assert api.get_status() == 0                          # ... then cleared
+    _parity_call_still_works()
+
+
+def test_dependency_counter_wait_times_out_and_context_survives():
+    assert api.get_status() == 0
+    assert api.selftest_dependency_timeout(20000) == 0    # the counter waits gave up
+    assert api.get_status() == -5
+    assert api.get_status() == 0
+    _parity_call_still_works()
+    # the single-launch schedule itself is unharmed
+    api.set_gemm_schedule("single")
+    try:
+        _parity_call_still_works()
+    finally:
+        api.set_gemm_schedule("phase")
+

@@ -13,6 +13,8 @@ import torch.multiprocessing as mp
 
 from newton_schulz_quintic_gb300 import api, build
 
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
 
 @pytest.fixture(scope="module", autouse=True)
 def _lib():
@@ -127,9 +129,15 @@ def _rank_main(rank, world, port, result_q):
     dist.init_process_group("gloo", rank=rank, world_size=world)
     from newton_schulz_quintic_gb300 import api as a
     from newton_schulz_quintic_gb300 import inputs
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_rank", os.path.join(ROOT, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
     wl = inputs.WORKLOADS["bf16-mixed-120"]
     assign, loads = a.plan_shards(wl.shapes, world)
     mine = [i for i, r in enumerate(assign) if r == rank]
+    # the benchmark's split mode runs exactly the planner's share on this rank
+    assert bench.rank_share(wl, world, rank) == mine
     my_cost = sum(a.cost(*wl.shapes[i]) for i in mine)
     t = torch.tensor([len(mine), my_cost], dtype=torch.float64)
     tot = t.clone()

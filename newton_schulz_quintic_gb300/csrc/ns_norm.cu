@@ -1,0 +1,225 @@
+// ns_norm.cu -- the norm pass of the bf16 path: the one read of every caller
+// matrix Y before the first step.
+//
+// For each matrix it produces the sum of squares of every 64 x 64 tile of W
+// (W = Y, or Y^T when M > N) and the last non-zero row and column of Y, and,
+// when the first step cannot read Y itself through TMA, an exact copy of Y in
+// the first iterate buffer. The scale 1/(||Y||_F + eps) is formed from the
+// tile sums by ns_norm_finish_kernel and applied inside the first step's GEMM
+// epilogues (A = r^2 Y Y^T, W_1 = r (a Y + B Y)), so Y is read once here and
+// the first normalised iterate is never rounded.
+//
+// Every sum is taken in W's orientation: an 8 x 8 sub-block in W-row-major
+// order, the 64 sub-block sums of a tile by a fixed tree over their W index,
+// the tiles in W's tile order (ns_norm_finish_kernel). A matrix and its
+// transpose therefore get bit-identical scales. The squares are exact in fp32
+// (a bf16 has 8 significant bits), so each step of a sub-block sum is one
+// bf16-operand fused multiply-add with fp32 accumulation, which rounds like
+// fmaf on the widened value.
+//
+// Work split: one warp per 64 x 64 tile of Y at a time (tiles strided over
+// all warps of a persistent grid of two 256-thread blocks per SM). A tile is
+// read as two halves of 32 rows; lane l holds the 8 x 8 sub-block
+// (l / 8 + 4 h, l % 8) of half h as eight 16-byte rows (each load instruction
+// of the warp reads 4 rows x 128 contiguous bytes). The loads of the next
+// half are issued before the current half is reduced, so every warp keeps
+// 4 KB in flight while it computes. Zero extents are tested a 16-byte word at
+// a time: a row is non-zero when the OR of its words has a non-zero magnitude
+// bit, a column when the OR over the rows has one in that column's half-word.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "ns_device.cuh"
+
+namespace ns {
+
+namespace {
+
+constexpr uint32_t kMagnitude = 0x7FFF7FFFu;  // both halves' bits except the signs (-0 counts as zero)
+
+// Where tile `tile` of the call's concatenated tile lists lies.
+struct TileLoc {
+  const __nv_bfloat16 *y;  // the caller's matrix
+  __nv_bfloat16 *copy;     // first iterate buffer to copy Y into, or null (step 1 reads Y itself)
+  int mat, M, N;
+  int r0, c0;
+  int wtile;               // the tile's index in W's tile grid, offset by the matrix's first tile
+  int tr;                  // W = Y^T
+  int vec;                 // rows of Y are 16-byte aligned: one 16-byte load per 8 elements
+};
+
+__device__ __forceinline__ TileLoc locate(const PrepParams &p, int tile) {
+  int lo = 0, hi = p.nmats;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (p.tile_prefix[mid] <= tile) lo = mid; else hi = mid;
+  }
+  const MatDesc &d = p.mats[lo];
+  TileLoc t;
+  t.mat = lo;
+  t.M = d.M;
+  t.N = d.N;
+  t.tr = d.transposed;
+  t.y = static_cast<const __nv_bfloat16 *>(d.user);
+  t.copy = d.direct ? nullptr : static_cast<__nv_bfloat16 *>(d.s[0]);
+  t.vec = (t.N % 8 == 0) && ((reinterpret_cast<uintptr_t>(t.y) & 15) == 0);
+  const int base = p.tile_prefix[lo];
+  const int local = tile - base;
+  const int tcols = (t.N + kPrepTile - 1) / kPrepTile;
+  const int tr_ = local / tcols, tc_ = local % tcols;
+  t.r0 = tr_ * kPrepTile;
+  t.c0 = tc_ * kPrepTile;
+  t.wtile = base + (t.tr ? tc_ * ((t.M + kPrepTile - 1) / kPrepTile) + tr_ : local);
+  return t;
+}
+
+// This lane's 8 rows of 8 columns in half h of the tile.
+__device__ __forceinline__ void load_half(const TileLoc &t, int h, int lane, uint4 (&v)[8]) {
+  const int C = t.c0 + (lane & 7) * 8;
+  const int R0 = t.r0 + ((lane >> 3) + 4 * h) * 8;
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    const int R = R0 + r;
+    uint4 w = make_uint4(0, 0, 0, 0);
+    if (R < t.M && C < t.N) {
+      const __nv_bfloat16 *src = t.y + static_cast<size_t>(R) * t.N + C;
+      if (t.vec) {
+        w = __ldg(reinterpret_cast<const uint4 *>(src));
+      } else {
+        uint32_t e[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) e[k] = C + k < t.N ? static_cast<uint32_t>(__bfloat16_as_ushort(src[k])) : 0u;
+        w = make_uint4(e[0] | (e[1] << 16), e[2] | (e[3] << 16), e[4] | (e[5] << 16), e[6] | (e[7] << 16));
+      }
+    }
+    v[r] = w;
+  }
+}
+
+// acc + x * x for the low / high bf16 of a word, rounded once to fp32.
+__device__ __forceinline__ float fma_sq_lo(float acc, uint32_t w) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tfma.rn.f32.bf16 %0, l, l, %0;\n\t}" : "+f"(acc) : "r"(w));
+  return acc;
+}
+__device__ __forceinline__ float fma_sq_hi(float acc, uint32_t w) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tfma.rn.f32.bf16 %0, h, h, %0;\n\t}" : "+f"(acc) : "r"(w));
+  return acc;
+}
+__device__ __forceinline__ uint32_t word(const uint4 &v, int q) { return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w; }
+
+// Sum of squares of the lane's sub-block in W-row-major order.
+__device__ __forceinline__ float subblock_sumsq(const uint4 (&v)[8], int tr) {
+  float acc = 0.f;
+  if (!tr) {  // W rows are Y rows
+#pragma unroll
+    for (int wi = 0; wi < 8; ++wi)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc = fma_sq_lo(acc, word(v[wi], q));
+        acc = fma_sq_hi(acc, word(v[wi], q));
+      }
+  } else {  // W row wi is Y column wi: element (wi, wj) of the sub-block is Y's (wj, wi)
+#pragma unroll
+    for (int wi = 0; wi < 8; ++wi)
+#pragma unroll
+      for (int wj = 0; wj < 8; ++wj)
+        acc = (wi & 1) ? fma_sq_hi(acc, word(v[wj], wi >> 1)) : fma_sq_lo(acc, word(v[wj], wi >> 1));
+  }
+  return acc;
+}
+
+// Reduce half h of a tile held in v: the sub-block sum into the warp's slot
+// table (by W index), the lane's extents, and the copy when there is one.
+__device__ __forceinline__ void reduce_half(const TileLoc &t, int h, int lane, const uint4 (&v)[8], float *slots,
+                                            int &ext_r, int &ext_c) {
+  const int br = (lane >> 3) + 4 * h, bc = lane & 7;
+  const int R0 = t.r0 + br * 8, C = t.c0 + bc * 8;
+  // extents: which of the 8 rows, and which of the 8 columns, hold a non-zero
+  uint32_t rows = 0;
+  uint4 cols = make_uint4(0, 0, 0, 0);
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    rows |= (((v[r].x | v[r].y | v[r].z | v[r].w) & kMagnitude) != 0 ? 1u : 0u) << r;
+    cols.x |= v[r].x;
+    cols.y |= v[r].y;
+    cols.z |= v[r].z;
+    cols.w |= v[r].w;
+  }
+  if (rows) ext_r = max(ext_r, R0 + 31 - __clz(rows));
+  const uint32_t cmask = ((cols.x & 0x7FFFu) ? 1u : 0u) | ((cols.x & 0x7FFF0000u) ? 2u : 0u) |
+                         ((cols.y & 0x7FFFu) ? 4u : 0u) | ((cols.y & 0x7FFF0000u) ? 8u : 0u) |
+                         ((cols.z & 0x7FFFu) ? 16u : 0u) | ((cols.z & 0x7FFF0000u) ? 32u : 0u) |
+                         ((cols.w & 0x7FFFu) ? 64u : 0u) | ((cols.w & 0x7FFF0000u) ? 128u : 0u);
+  if (cmask) ext_c = max(ext_c, C + 31 - __clz(cmask));
+  // exact copy into the first iterate buffer (its pitch: N rounded up to 8 elements)
+  if (t.copy && C < t.N) {
+    const int ps = (t.N + 7) & ~7;
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+      if (R0 + r < t.M) *reinterpret_cast<uint4 *>(t.copy + static_cast<size_t>(R0 + r) * ps + C) = v[r];
+  }
+  slots[t.tr ? bc * 8 + br : br * 8 + bc] = subblock_sumsq(v, t.tr);
+}
+
+// Publish a warp's extents of one matrix (the whole warp calls this).
+__device__ __forceinline__ void publish_extents(const PrepParams &p, int mat, int ext_r, int ext_c, int lane) {
+  ext_r = warp_max(ext_r);
+  ext_c = warp_max(ext_c);
+  if (lane == 0 && mat >= 0) {
+    if (ext_r >= 0) atomicMax(&p.ext[2 * mat + 0], ext_r + 1);
+    if (ext_c >= 0) atomicMax(&p.ext[2 * mat + 1], ext_c + 1);
+  }
+}
+
+__global__ void __launch_bounds__(256, 2) ns_norm_tiles_kernel(PrepParams p, int total_tiles) {
+  __shared__ float s_blk[8][64];  // per warp: sub-block sums of its tile, by W index
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = gridDim.x * 8;
+  float *slots = s_blk[warp];
+  int tile = blockIdx.x * 8 + warp;
+  if (tile >= total_tiles) return;  // whole warps only; no block-wide barrier follows
+  // extents are kept per lane while the warp stays in one matrix and
+  // published (one warp reduction, two atomics) when it moves on or finishes
+  int ext_mat = -1, ext_r = -1, ext_c = -1;
+  TileLoc cur = locate(p, tile);
+  uint4 a[8], b[8];
+  load_half(cur, 0, lane, a);
+  for (;;) {
+    load_half(cur, 1, lane, b);
+    if (cur.mat != ext_mat) {
+      publish_extents(p, ext_mat, ext_r, ext_c, lane);
+      ext_mat = cur.mat;
+      ext_r = ext_c = -1;
+    }
+    reduce_half(cur, 0, lane, a, slots, ext_r, ext_c);
+    const int next = tile + nwarps;
+    TileLoc nxt;
+    if (next < total_tiles) {
+      nxt = locate(p, next);
+      load_half(nxt, 0, lane, a);
+    }
+    reduce_half(cur, 1, lane, b, slots, ext_r, ext_c);
+    __syncwarp();
+    float t = slots[2 * lane] + slots[2 * lane + 1];
+    t = warp_sum(t);  // xor butterfly: every lane ends with the same value
+    if (lane == 0) p.tile_partials[cur.wtile] = t;
+    __syncwarp();
+    if (next >= total_tiles) break;
+    tile = next;
+    cur = nxt;
+  }
+  publish_extents(p, ext_mat, ext_r, ext_c, lane);
+}
+
+}  // namespace
+
+int launch_norm_tiles(const PrepParams &p, int total_tiles, int max_blocks, cudaStream_t s) {
+  if (total_tiles <= 0) return 0;
+  const int blocks = std::min((total_tiles + 7) / 8, std::max(max_blocks, 1));
+  ns_norm_tiles_kernel<<<blocks, 256, 0, s>>>(p, total_tiles);
+  count_launch();
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace ns

@@ -1,12 +1,14 @@
 // ns_simt.cu -- CUDA-core kernels of libns:
-//   * per-matrix Frobenius norm (partial sums) and non-zero extent,
+//   * per-matrix Frobenius norm (partial sums) and non-zero extent (fp32 path),
+//   * the per-matrix scale from the bf16 norm pass's tile sums,
 //   * preparation: normalise by ||Y||_F + eps, round to the working type and
 //     write both orientations W and W^T,
 //   * the shared-memory resident kernel that runs every step of a small
 //     matrix inside one CTA,
 //   * the fp32 tiled GEMM phases (gram / square / apply) for large fp32
 //     matrices.
-// The bf16 tensor-core phases live in ns_tc.cu.
+// The bf16 norm pass lives in ns_norm.cu, the bf16 tensor-core phases in
+// ns_tc.cu.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -216,158 +218,6 @@ int launch_prep(const PrepParams &p, int total_tiles, cudaStream_t s) {
     ns_prep_kernel<kBF16><<<total_tiles, 256, 0, s>>>(p);
   else
     ns_prep_kernel<kF32><<<total_tiles, 256, 0, s>>>(p);
-  count_launch();
-  return cudaGetLastError() == cudaSuccess ? 0 : -1;
-}
-
-// ============================================================== tile norms (bf16 path)
-// One pass over Y. Each warp takes one 64 x 64 tile of Y at a time
-// (persistent, tiles strided over all warps of the grid): lane l loads the
-// two 8 x 8 sub-blocks (l / 8 + 4 j, l % 8), j = 0, 1, as sixteen 16-byte rows
-// (each load instruction of the warp reads 4 rows x 128 contiguous bytes).
-// It stores the tile's sum of squares, advances the non-zero extent and, when
-// step 0 cannot read Y itself, writes the loaded rows unchanged into the first
-// iterate buffer. The scale 1/(||Y||_F + eps) is applied by the first step's
-// GEMM epilogues instead (A = r^2 Y Y^T, W_1 = r (a Y + B Y)), so Y is read
-// once and the first normalised iterate is never rounded.
-// Every sum is taken in W's orientation: a sub-block in W-row-major order,
-// the 64 sub-block sums of a tile by a fixed tree over their W index, the
-// tiles in W's tile order (ns_norm_finish_kernel), so a matrix and its
-// transpose get bit-identical scales.
-__device__ __forceinline__ float bf16_elem(const uint4 &w, int e) {
-  const uint32_t word = e < 2 ? w.x : e < 4 ? w.y : e < 6 ? w.z : w.w;
-  return __uint_as_float(((word >> (16 * (e & 1))) & 0xFFFFu) << 16);
-}
-__device__ __forceinline__ bool bf16_nonzero(uint32_t word, int half) {
-  return ((word >> (16 * half)) & 0x7FFFu) != 0;  // -0 counts as zero
-}
-
-__global__ void __launch_bounds__(256) ns_norm_tiles_kernel(PrepParams p, int total_tiles) {
-  __shared__ float s_blk[8][64];  // per warp: sub-block sums of its tile, by W index
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nwarps = gridDim.x * 8;
-  const int bc = lane & 7;
-  // extents are kept per warp while it stays in one matrix and published
-  // (two atomics) when it moves on or finishes, not once per tile
-  int ext_mat = -1, ext_r = -1, ext_c = -1;
-  for (int tile = blockIdx.x * 8 + warp; tile < total_tiles; tile += nwarps) {
-    int lo = 0, hi = p.nmats;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (p.tile_prefix[mid] <= tile) lo = mid; else hi = mid;
-    }
-    const int mat = lo;
-    if (mat != ext_mat) {
-      if (lane == 0 && ext_mat >= 0) {
-        if (ext_r >= 0) atomicMax(&p.ext[2 * ext_mat + 0], ext_r + 1);
-        if (ext_c >= 0) atomicMax(&p.ext[2 * ext_mat + 1], ext_c + 1);
-      }
-      ext_mat = mat;
-      ext_r = ext_c = -1;
-    }
-    const MatDesc &d = p.mats[mat];
-    const int M = d.M, N = d.N;
-    const int local = tile - p.tile_prefix[mat];
-    const int tcols = (N + kPrepTile - 1) / kPrepTile;
-    const int r0 = (local / tcols) * kPrepTile, c0 = (local % tcols) * kPrepTile;
-    const __nv_bfloat16 *y = static_cast<const __nv_bfloat16 *>(d.user);
-    const bool vec = (N % 8 == 0) && ((reinterpret_cast<uintptr_t>(y) & 15) == 0);
-    const int C = c0 + bc * 8;
-    uint4 v[2][8];
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        const int R = r0 + ((lane >> 3) + 4 * j) * 8 + r;
-        uint4 w = make_uint4(0, 0, 0, 0);
-        if (R < M && C < N) {
-          const __nv_bfloat16 *src = y + static_cast<size_t>(R) * N + C;
-          if (vec) {
-            w = __ldg(reinterpret_cast<const uint4 *>(src));
-          } else {
-            uint32_t h[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-              h[e] = C + e < N ? static_cast<uint32_t>(__bfloat16_as_ushort(src[e])) : 0u;
-            w = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
-          }
-        }
-        v[j][r] = w;
-      }
-    // extents (caller's orientation)
-    int rmax = -1, cmax = -1;
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        const uint32_t ws[4] = {v[j][r].x, v[j][r].y, v[j][r].z, v[j][r].w};
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          if (bf16_nonzero(ws[e >> 1], e & 1)) {
-            rmax = max(rmax, r0 + ((lane >> 3) + 4 * j) * 8 + r);
-            cmax = max(cmax, C + e);
-          }
-      }
-    // exact copy into the first iterate buffer (pitch a multiple of 8 elements)
-    if (!d.direct) {
-      __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(d.s[0]);
-#pragma unroll
-      for (int j = 0; j < 2; ++j)
-#pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          const int R = r0 + ((lane >> 3) + 4 * j) * 8 + r;
-          if (R < M && C < N) *reinterpret_cast<uint4 *>(dst + static_cast<size_t>(R) * d.ps + C) = v[j][r];
-        }
-    }
-    // sub-block sums in W-row-major order, stored at the sub-block's W index
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const int br = (lane >> 3) + 4 * j;
-      float acc = 0.f;
-      if (!d.transposed) {
-#pragma unroll
-        for (int wi = 0; wi < 8; ++wi)
-#pragma unroll
-          for (int wj = 0; wj < 8; ++wj) {
-            const float x = bf16_elem(v[j][wi], wj);
-            acc = fmaf(x, x, acc);
-          }
-        s_blk[warp][br * 8 + bc] = acc;
-      } else {  // W = Y^T: element (wi, wj) of the sub-block is Y's (wj, wi)
-#pragma unroll
-        for (int wi = 0; wi < 8; ++wi)
-#pragma unroll
-          for (int wj = 0; wj < 8; ++wj) {
-            const float x = bf16_elem(v[j][wj], wi);
-            acc = fmaf(x, x, acc);
-          }
-        s_blk[warp][bc * 8 + br] = acc;
-      }
-    }
-    __syncwarp();
-    float t = s_blk[warp][2 * lane] + s_blk[warp][2 * lane + 1];
-    t = warp_sum(t);  // xor butterfly: every lane ends with the same value
-    rmax = warp_max(rmax);
-    cmax = warp_max(cmax);
-    if (lane == 0) {
-      // stored at the tile's index in W's tile grid (W = Y^T when transposed)
-      const int wtile = d.transposed ? (local % tcols) * ((M + kPrepTile - 1) / kPrepTile) + local / tcols : local;
-      p.tile_partials[p.tile_prefix[mat] + wtile] = t;
-    }
-    ext_r = max(ext_r, rmax);
-    ext_c = max(ext_c, cmax);
-    __syncwarp();
-  }
-  if (lane == 0 && ext_mat >= 0) {
-    if (ext_r >= 0) atomicMax(&p.ext[2 * ext_mat + 0], ext_r + 1);
-    if (ext_c >= 0) atomicMax(&p.ext[2 * ext_mat + 1], ext_c + 1);
-  }
-}
-
-int launch_norm_tiles(const PrepParams &p, int total_tiles, int max_blocks, cudaStream_t s) {
-  if (total_tiles <= 0) return 0;
-  const int blocks = std::min((total_tiles + 7) / 8, std::max(max_blocks, 1));
-  ns_norm_tiles_kernel<<<blocks, 256, 0, s>>>(p, total_tiles);
   count_launch();
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }

@@ -20,12 +20,18 @@
 // Work split: one warp per 64 x 64 tile of Y at a time (tiles strided over
 // all warps of a persistent grid of two 256-thread blocks per SM). A tile is
 // read as two halves of 32 rows; lane l holds the 8 x 8 sub-block
-// (l / 8 + 4 h, l % 8) of half h as eight 16-byte rows (each load instruction
-// of the warp reads 4 rows x 128 contiguous bytes). The loads of the next
-// half are issued before the current half is reduced, so every warp keeps
-// 4 KB in flight while it computes. Zero extents are tested a 16-byte word at
-// a time: a row is non-zero when the OR of its words has a non-zero magnitude
-// bit, a column when the OR over the rows has one in that column's half-word.
+// (l / 8 + 4 h, l % 8) of half h as eight 16-byte rows (each copy instruction
+// of the warp reads 4 rows x 128 contiguous bytes). Each lane streams its own
+// rows into its own slots of a three-half-tile ring in shared memory with
+// cp.async (16-byte copies that zero-fill past the matrix), two half-tiles
+// ahead of the one it reduces, so the bytes in flight do not occupy
+// registers: 16 warps per SM keep 128 KB in flight. A lane reads back only
+// what it copied itself, so the ring needs no barrier. Rows that are not
+// 16-byte aligned (N not a multiple of 8, or an unaligned Y) are loaded
+// element by element into the same slots instead. Zero extents are tested a
+// 16-byte word at a time: a row is non-zero when the OR of its words has a
+// non-zero magnitude bit, a column when the OR over the rows has one in that
+// column's half-word.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -74,27 +80,53 @@ __device__ __forceinline__ TileLoc locate(const PrepParams &p, int tile) {
   return t;
 }
 
-// This lane's 8 rows of 8 columns in half h of the tile.
-__device__ __forceinline__ void load_half(const TileLoc &t, int h, int lane, uint4 (&v)[8]) {
+constexpr int kRing = 3;                         // half-tiles per lane in flight or being reduced
+constexpr int kSlotBytes = 8 * 16;               // one lane's rows of one half-tile
+constexpr int kWarpRingBytes = kRing * 32 * kSlotBytes;
+constexpr int kNormSmem = 8 * kWarpRingBytes;    // 96 KB per 256-thread block
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Start this lane's copies of its 8 rows of 8 columns in half h of the tile
+// into its slot (row r at slot + r * 16 * 32: lanes interleaved, so the later
+// 16-byte shared-memory reads of a warp are contiguous).
+__device__ __forceinline__ void issue_half(const TileLoc &t, int h, int lane, uint8_t *slot) {
   const int C = t.c0 + (lane & 7) * 8;
   const int R0 = t.r0 + ((lane >> 3) + 4 * h) * 8;
+  if (t.vec) {
+    const uint32_t dst = smem_u32(slot);
 #pragma unroll
-  for (int r = 0; r < 8; ++r) {
-    const int R = R0 + r;
-    uint4 w = make_uint4(0, 0, 0, 0);
-    if (R < t.M && C < t.N) {
-      const __nv_bfloat16 *src = t.y + static_cast<size_t>(R) * t.N + C;
-      if (t.vec) {
-        w = __ldg(reinterpret_cast<const uint4 *>(src));
-      } else {
+    for (int r = 0; r < 8; ++r) {
+      const int R = R0 + r;
+      const bool in = R < t.M && C < t.N;  // rows are whole 16-byte words when vec
+      const __nv_bfloat16 *src = in ? t.y + static_cast<size_t>(R) * t.N + C : t.y;
+      cp_async16(dst + r * 16 * 32, src, in ? 16u : 0u);
+    }
+  } else {
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const int R = R0 + r;
+      uint4 w = make_uint4(0, 0, 0, 0);
+      if (R < t.M && C < t.N) {
+        const __nv_bfloat16 *src = t.y + static_cast<size_t>(R) * t.N + C;
         uint32_t e[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) e[k] = C + k < t.N ? static_cast<uint32_t>(__bfloat16_as_ushort(src[k])) : 0u;
         w = make_uint4(e[0] | (e[1] << 16), e[2] | (e[3] << 16), e[4] | (e[5] << 16), e[6] | (e[7] << 16));
       }
+      *reinterpret_cast<uint4 *>(slot + r * 16 * 32) = w;
     }
-    v[r] = w;
   }
+}
+
+__device__ __forceinline__ void read_half(const uint8_t *slot, uint4 (&v)[8]) {
+#pragma unroll
+  for (int r = 0; r < 8; ++r) v[r] = *reinterpret_cast<const uint4 *>(slot + r * 16 * 32);
 }
 
 // acc + x * x for the low / high bf16 of a word, rounded once to fp32.
@@ -172,43 +204,74 @@ __device__ __forceinline__ void publish_extents(const PrepParams &p, int mat, in
   }
 }
 
+// The unit sequence of one warp: half-tiles (tile, 0), (tile, 1), (tile +
+// nwarps, 0), ... with the location of the current tile.
+struct UnitIter {
+  int tile, half;
+  TileLoc loc;
+};
+
+__device__ __forceinline__ void unit_next(const PrepParams &p, int nwarps, int total_tiles, UnitIter &u) {
+  if (u.half == 0) {
+    u.half = 1;
+    return;
+  }
+  u.half = 0;
+  u.tile += nwarps;
+  if (u.tile < total_tiles) u.loc = locate(p, u.tile);
+}
+
 __global__ void __launch_bounds__(256, 2) ns_norm_tiles_kernel(PrepParams p, int total_tiles) {
+  extern __shared__ __align__(16) uint8_t norm_smem[];
   __shared__ float s_blk[8][64];  // per warp: sub-block sums of its tile, by W index
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = gridDim.x * 8;
   float *slots = s_blk[warp];
-  int tile = blockIdx.x * 8 + warp;
-  if (tile >= total_tiles) return;  // whole warps only; no block-wide barrier follows
+  uint8_t *ring = norm_smem + warp * kWarpRingBytes + lane * 16;
+  const int first = blockIdx.x * 8 + warp;
+  if (first >= total_tiles) return;  // whole warps only; no block-wide barrier follows
+  // copies run kRing - 1 half-tiles ahead of the reduction; every iteration
+  // commits one copy group (empty past the end) so the group count stays exact
+  UnitIter in{first, 0, locate(p, first)};
+  UnitIter out = in;
+  int in_slot = 0, out_slot = 0;
+#pragma unroll
+  for (int k = 0; k < kRing - 1; ++k) {
+    if (in.tile < total_tiles) issue_half(in.loc, in.half, lane, ring + in_slot * 32 * kSlotBytes);
+    cp_async_commit();
+    unit_next(p, nwarps, total_tiles, in);
+    in_slot = in_slot + 1 == kRing ? 0 : in_slot + 1;
+  }
   // extents are kept per lane while the warp stays in one matrix and
   // published (one warp reduction, two atomics) when it moves on or finishes
   int ext_mat = -1, ext_r = -1, ext_c = -1;
-  TileLoc cur = locate(p, tile);
-  uint4 a[8], b[8];
-  load_half(cur, 0, lane, a);
-  for (;;) {
-    load_half(cur, 1, lane, b);
-    if (cur.mat != ext_mat) {
+  while (out.tile < total_tiles) {
+    if (in.tile < total_tiles) issue_half(in.loc, in.half, lane, ring + in_slot * 32 * kSlotBytes);
+    cp_async_commit();
+    unit_next(p, nwarps, total_tiles, in);
+    in_slot = in_slot + 1 == kRing ? 0 : in_slot + 1;
+
+    cp_async_wait<kRing - 1>();  // this lane's copies of the unit `out` have landed
+    uint4 v[8];
+    read_half(ring + out_slot * 32 * kSlotBytes, v);
+    out_slot = out_slot + 1 == kRing ? 0 : out_slot + 1;
+    const TileLoc &t = out.loc;
+    if (t.mat != ext_mat) {
       publish_extents(p, ext_mat, ext_r, ext_c, lane);
-      ext_mat = cur.mat;
+      ext_mat = t.mat;
       ext_r = ext_c = -1;
     }
-    reduce_half(cur, 0, lane, a, slots, ext_r, ext_c);
-    const int next = tile + nwarps;
-    TileLoc nxt;
-    if (next < total_tiles) {
-      nxt = locate(p, next);
-      load_half(nxt, 0, lane, a);
+    reduce_half(t, out.half, lane, v, slots, ext_r, ext_c);
+    if (out.half == 1) {
+      __syncwarp();
+      float s = slots[2 * lane] + slots[2 * lane + 1];
+      s = warp_sum(s);  // xor butterfly: every lane ends with the same value
+      if (lane == 0) p.tile_partials[t.wtile] = s;
+      __syncwarp();
     }
-    reduce_half(cur, 1, lane, b, slots, ext_r, ext_c);
-    __syncwarp();
-    float t = slots[2 * lane] + slots[2 * lane + 1];
-    t = warp_sum(t);  // xor butterfly: every lane ends with the same value
-    if (lane == 0) p.tile_partials[cur.wtile] = t;
-    __syncwarp();
-    if (next >= total_tiles) break;
-    tile = next;
-    cur = nxt;
+    unit_next(p, nwarps, total_tiles, out);
   }
+  cp_async_wait<0>();
   publish_extents(p, ext_mat, ext_r, ext_c, lane);
 }
 
@@ -217,7 +280,10 @@ __global__ void __launch_bounds__(256, 2) ns_norm_tiles_kernel(PrepParams p, int
 int launch_norm_tiles(const PrepParams &p, int total_tiles, int max_blocks, cudaStream_t s) {
   if (total_tiles <= 0) return 0;
   const int blocks = std::min((total_tiles + 7) / 8, std::max(max_blocks, 1));
-  ns_norm_tiles_kernel<<<blocks, 256, 0, s>>>(p, total_tiles);
+  if (cudaFuncSetAttribute(ns_norm_tiles_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kNormSmem) !=
+      cudaSuccess)
+    return -1;
+  ns_norm_tiles_kernel<<<blocks, 256, kNormSmem, s>>>(p, total_tiles);
   count_launch();
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }

@@ -13,9 +13,8 @@
 // order, the 64 sub-block sums of a tile by a fixed tree over their W index,
 // the tiles in W's tile order (ns_norm_finish_kernel). A matrix and its
 // transpose therefore get bit-identical scales. The squares are exact in fp32
-// (a bf16 has 8 significant bits), so each step of a sub-block sum is one
-// bf16-operand fused multiply-add with fp32 accumulation, which rounds like
-// fmaf on the widened value.
+// (a bf16 has 8 significant bits); a sub-block sum is two fixed chains of
+// fp32 fused multiply-adds (see subblock_sumsq).
 //
 // Work split: one warp per 64 x 64 tile of Y at a time (tiles strided over
 // all warps of a persistent grid of two 256-thread blocks per SM). A tile is
@@ -99,13 +98,17 @@ __device__ __forceinline__ void issue_half(const TileLoc &t, int h, int lane, ui
   const int C = t.c0 + (lane & 7) * 8;
   const int R0 = t.r0 + ((lane >> 3) + 4 * h) * 8;
   if (t.vec) {
+    // rows are whole 16-byte words; rows past the matrix are zero-filled
     const uint32_t dst = smem_u32(slot);
+    const bool col_in = C < t.N;
+    const __nv_bfloat16 *src = t.y + (col_in ? static_cast<size_t>(R0) * t.N + C : 0);
+    const size_t pitch = col_in ? static_cast<size_t>(t.N) : 0;
+    const int rows_in = col_in ? min(8, t.M - R0) : 0;
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
-      const int R = R0 + r;
-      const bool in = R < t.M && C < t.N;  // rows are whole 16-byte words when vec
-      const __nv_bfloat16 *src = in ? t.y + static_cast<size_t>(R) * t.N + C : t.y;
-      cp_async16(dst + r * 16 * 32, src, in ? 16u : 0u);
+      const bool in = r < rows_in;
+      cp_async16(dst + r * 16 * 32, in ? src : t.y, in ? 16u : 0u);
+      src += pitch;
     }
   } else {
 #pragma unroll
@@ -129,36 +132,39 @@ __device__ __forceinline__ void read_half(const uint8_t *slot, uint4 (&v)[8]) {
   for (int r = 0; r < 8; ++r) v[r] = *reinterpret_cast<const uint4 *>(slot + r * 16 * 32);
 }
 
-// acc + x * x for the low / high bf16 of a word, rounded once to fp32.
-__device__ __forceinline__ float fma_sq_lo(float acc, uint32_t w) {
-  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tfma.rn.f32.bf16 %0, l, l, %0;\n\t}" : "+f"(acc) : "r"(w));
-  return acc;
-}
-__device__ __forceinline__ float fma_sq_hi(float acc, uint32_t w) {
-  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tfma.rn.f32.bf16 %0, h, h, %0;\n\t}" : "+f"(acc) : "r"(w));
-  return acc;
-}
 __device__ __forceinline__ uint32_t word(const uint4 &v, int q) { return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w; }
+// fp32 value of the low / high bf16 of a word (exact)
+__device__ __forceinline__ float lo_f(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float hi_f(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// Sum of squares of the lane's sub-block in W-row-major order.
+// Sum of squares of the lane's sub-block in W's orientation: two chains of
+// fused multiply-adds, one over W's even columns and one over its odd
+// columns, each in W-row-major order (one paired fp32 FMA advances both),
+// then even + odd. For W = Y a 16-byte row of Y holds both chains' operands
+// side by side; for W = Y^T, W(i, 2q) and W(i, 2q + 1) are Y(2q, i) and
+// Y(2q + 1, i), the same half of the same word in two adjacent rows.
 __device__ __forceinline__ float subblock_sumsq(const uint4 (&v)[8], int tr) {
-  float acc = 0.f;
-  if (!tr) {  // W rows are Y rows
+  float2 acc = make_float2(0.f, 0.f);
+  if (!tr) {
 #pragma unroll
     for (int wi = 0; wi < 8; ++wi)
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        acc = fma_sq_lo(acc, word(v[wi], q));
-        acc = fma_sq_hi(acc, word(v[wi], q));
+        const uint32_t w = word(v[wi], q);
+        const float2 x = make_float2(lo_f(w), hi_f(w));
+        acc = __ffma2_rn(x, x, acc);
       }
-  } else {  // W row wi is Y column wi: element (wi, wj) of the sub-block is Y's (wj, wi)
+  } else {
 #pragma unroll
     for (int wi = 0; wi < 8; ++wi)
 #pragma unroll
-      for (int wj = 0; wj < 8; ++wj)
-        acc = (wi & 1) ? fma_sq_hi(acc, word(v[wj], wi >> 1)) : fma_sq_lo(acc, word(v[wj], wi >> 1));
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t e = word(v[2 * q], wi >> 1), o = word(v[2 * q + 1], wi >> 1);
+        const float2 x = (wi & 1) ? make_float2(hi_f(e), hi_f(o)) : make_float2(lo_f(e), lo_f(o));
+        acc = __ffma2_rn(x, x, acc);
+      }
   }
-  return acc;
+  return acc.x + acc.y;
 }
 
 // Reduce half h of a tile held in v: the sub-block sum into the warp's slot

@@ -54,6 +54,25 @@ struct TileLoc {
   int vec;                 // rows of Y are 16-byte aligned: one 16-byte load per 8 elements
 };
 
+// q = n / d, r = n % d for 0 <= n, 0 < d: an fp32 estimate corrected by one
+// step (the estimate is within one of q when n < 2^20), else a division.
+__device__ __forceinline__ void divmod(int n, int d, int &q, int &r) {
+  if (n < (1 << 20)) {
+    q = __float2int_rz(__fdividef(static_cast<float>(n), static_cast<float>(d)));
+    r = n - q * d;
+    if (r < 0) {
+      --q;
+      r += d;
+    } else if (r >= d) {
+      ++q;
+      r -= d;
+    }
+  } else {
+    q = n / d;
+    r = n - q * d;
+  }
+}
+
 __device__ __forceinline__ TileLoc locate(const PrepParams &p, int tile) {
   int lo = 0, hi = p.nmats;
   while (hi - lo > 1) {
@@ -72,7 +91,8 @@ __device__ __forceinline__ TileLoc locate(const PrepParams &p, int tile) {
   const int base = p.tile_prefix[lo];
   const int local = tile - base;
   const int tcols = (t.N + kPrepTile - 1) / kPrepTile;
-  const int tr_ = local / tcols, tc_ = local % tcols;
+  int tr_, tc_;
+  divmod(local, tcols, tr_, tc_);
   t.r0 = tr_ * kPrepTile;
   t.c0 = tc_ * kPrepTile;
   t.wtile = base + (t.tr ? tc_ * ((t.M + kPrepTile - 1) / kPrepTile) + tr_ : local);
@@ -81,7 +101,8 @@ __device__ __forceinline__ TileLoc locate(const PrepParams &p, int tile) {
 
 constexpr int kRing = 3;                         // half-tiles per lane in flight or being reduced
 constexpr int kSlotBytes = 8 * 16;               // one lane's rows of one half-tile
-constexpr int kWarpRingBytes = kRing * 32 * kSlotBytes;
+constexpr int kSlot = 32 * kSlotBytes;          // one half-tile of the warp (4 KB)
+constexpr int kWarpRingBytes = kRing * kSlot;
 constexpr int kNormSmem = 8 * kWarpRingBytes;    // 96 KB per 256-thread block
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
@@ -137,14 +158,15 @@ __device__ __forceinline__ uint32_t word(const uint4 &v, int q) { return q == 0 
 __device__ __forceinline__ float lo_f(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float hi_f(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// Sum of squares of the lane's sub-block in W's orientation: two chains of
-// fused multiply-adds, one over W's even columns and one over its odd
-// columns, each in W-row-major order (one paired fp32 FMA advances both),
-// then even + odd. For W = Y a 16-byte row of Y holds both chains' operands
-// side by side; for W = Y^T, W(i, 2q) and W(i, 2q + 1) are Y(2q, i) and
+// Sum of squares of the lane's sub-block in W's orientation: four chains of
+// fused multiply-adds, one per parity of W's row and of W's column, each in
+// W-row-major order (one paired fp32 FMA advances the even- and odd-column
+// chains of a row), then (even row: even + odd column) + (odd row: even +
+// odd column). For W = Y a 16-byte row of Y holds a W row's two chains side
+// by side; for W = Y^T, W(i, 2q) and W(i, 2q + 1) are Y(2q, i) and
 // Y(2q + 1, i), the same half of the same word in two adjacent rows.
 __device__ __forceinline__ float subblock_sumsq(const uint4 (&v)[8], int tr) {
-  float2 acc = make_float2(0.f, 0.f);
+  float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
   if (!tr) {
 #pragma unroll
     for (int wi = 0; wi < 8; ++wi)
@@ -152,7 +174,7 @@ __device__ __forceinline__ float subblock_sumsq(const uint4 (&v)[8], int tr) {
       for (int q = 0; q < 4; ++q) {
         const uint32_t w = word(v[wi], q);
         const float2 x = make_float2(lo_f(w), hi_f(w));
-        acc = __ffma2_rn(x, x, acc);
+        acc[wi & 1] = __ffma2_rn(x, x, acc[wi & 1]);
       }
   } else {
 #pragma unroll
@@ -161,10 +183,10 @@ __device__ __forceinline__ float subblock_sumsq(const uint4 (&v)[8], int tr) {
       for (int q = 0; q < 4; ++q) {
         const uint32_t e = word(v[2 * q], wi >> 1), o = word(v[2 * q + 1], wi >> 1);
         const float2 x = (wi & 1) ? make_float2(hi_f(e), hi_f(o)) : make_float2(lo_f(e), lo_f(o));
-        acc = __ffma2_rn(x, x, acc);
+        acc[wi & 1] = __ffma2_rn(x, x, acc[wi & 1]);
       }
   }
-  return acc.x + acc.y;
+  return (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
 }
 
 // Reduce half h of a tile held in v: the sub-block sum into the warp's slot
@@ -210,23 +232,6 @@ __device__ __forceinline__ void publish_extents(const PrepParams &p, int mat, in
   }
 }
 
-// The unit sequence of one warp: half-tiles (tile, 0), (tile, 1), (tile +
-// nwarps, 0), ... with the location of the current tile.
-struct UnitIter {
-  int tile, half;
-  TileLoc loc;
-};
-
-__device__ __forceinline__ void unit_next(const PrepParams &p, int nwarps, int total_tiles, UnitIter &u) {
-  if (u.half == 0) {
-    u.half = 1;
-    return;
-  }
-  u.half = 0;
-  u.tile += nwarps;
-  if (u.tile < total_tiles) u.loc = locate(p, u.tile);
-}
-
 __global__ void __launch_bounds__(256, 2) ns_norm_tiles_kernel(PrepParams p, int total_tiles) {
   extern __shared__ __align__(16) uint8_t norm_smem[];
   __shared__ float s_blk[8][64];  // per warp: sub-block sums of its tile, by W index
@@ -234,48 +239,52 @@ __global__ void __launch_bounds__(256, 2) ns_norm_tiles_kernel(PrepParams p, int
   const int nwarps = gridDim.x * 8;
   float *slots = s_blk[warp];
   uint8_t *ring = norm_smem + warp * kWarpRingBytes + lane * 16;
-  const int first = blockIdx.x * 8 + warp;
-  if (first >= total_tiles) return;  // whole warps only; no block-wide barrier follows
-  // copies run kRing - 1 half-tiles ahead of the reduction; every iteration
-  // commits one copy group (empty past the end) so the group count stays exact
-  UnitIter in{first, 0, locate(p, first)};
-  UnitIter out = in;
-  int in_slot = 0, out_slot = 0;
-#pragma unroll
-  for (int k = 0; k < kRing - 1; ++k) {
-    if (in.tile < total_tiles) issue_half(in.loc, in.half, lane, ring + in_slot * 32 * kSlotBytes);
-    cp_async_commit();
-    unit_next(p, nwarps, total_tiles, in);
-    in_slot = in_slot + 1 == kRing ? 0 : in_slot + 1;
-  }
+  int tile = blockIdx.x * 8 + warp;
+  if (tile >= total_tiles) return;  // whole warps only; no block-wide barrier follows
+  // The copies run two half-tiles (one tile) ahead of the reduction: while
+  // the halves of `tile` are reduced, the halves of `next` are being copied.
+  // Every half commits one copy group (empty past the end), so waiting until
+  // at most kRing - 1 groups are pending means the half about to be reduced
+  // has landed.
+  TileLoc loc = locate(p, tile);
+  issue_half(loc, 0, lane, ring);
+  cp_async_commit();
+  issue_half(loc, 1, lane, ring + kSlot);
+  cp_async_commit();
+  int next = tile + nwarps;
+  TileLoc nloc = loc;
+  if (next < total_tiles) nloc = locate(p, next);
+  int in_slot = 2, out_slot = 0;
   // extents are kept per lane while the warp stays in one matrix and
   // published (one warp reduction, two atomics) when it moves on or finishes
   int ext_mat = -1, ext_r = -1, ext_c = -1;
-  while (out.tile < total_tiles) {
-    if (in.tile < total_tiles) issue_half(in.loc, in.half, lane, ring + in_slot * 32 * kSlotBytes);
-    cp_async_commit();
-    unit_next(p, nwarps, total_tiles, in);
-    in_slot = in_slot + 1 == kRing ? 0 : in_slot + 1;
-
-    cp_async_wait<kRing - 1>();  // this lane's copies of the unit `out` have landed
-    uint4 v[8];
-    read_half(ring + out_slot * 32 * kSlotBytes, v);
-    out_slot = out_slot + 1 == kRing ? 0 : out_slot + 1;
-    const TileLoc &t = out.loc;
-    if (t.mat != ext_mat) {
+  for (;;) {
+    if (loc.mat != ext_mat) {
       publish_extents(p, ext_mat, ext_r, ext_c, lane);
-      ext_mat = t.mat;
+      ext_mat = loc.mat;
       ext_r = ext_c = -1;
     }
-    reduce_half(t, out.half, lane, v, slots, ext_r, ext_c);
-    if (out.half == 1) {
-      __syncwarp();
-      float s = slots[2 * lane] + slots[2 * lane + 1];
-      s = warp_sum(s);  // xor butterfly: every lane ends with the same value
-      if (lane == 0) p.tile_partials[t.wtile] = s;
-      __syncwarp();
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if (next < total_tiles) issue_half(nloc, h, lane, ring + in_slot * kSlot);
+      cp_async_commit();
+      in_slot = in_slot + 1 == kRing ? 0 : in_slot + 1;
+      cp_async_wait<kRing - 1>();  // this lane's copies of half h of `tile` have landed
+      uint4 v[8];
+      read_half(ring + out_slot * kSlot, v);
+      out_slot = out_slot + 1 == kRing ? 0 : out_slot + 1;
+      reduce_half(loc, h, lane, v, slots, ext_r, ext_c);
     }
-    unit_next(p, nwarps, total_tiles, out);
+    __syncwarp();
+    float s = slots[2 * lane] + slots[2 * lane + 1];
+    s = warp_sum(s);  // xor butterfly: every lane ends with the same value
+    if (lane == 0) p.tile_partials[loc.wtile] = s;
+    __syncwarp();
+    if (next >= total_tiles) break;
+    tile = next;
+    loc = nloc;
+    next += nwarps;
+    if (next < total_tiles) nloc = locate(p, next);
   }
   cp_async_wait<0>();
   publish_extents(p, ext_mat, ext_r, ext_c, lane);

@@ -142,12 +142,19 @@ struct BigMat {
   size_t off_x, off_xt0, off_xt1, off_s0, off_s1, off_a, off_b;
 };
 
+// Resident matrices of one cluster size: entries [start, start + count) of
+// the resident descriptor table, one launch.
+struct ResGroup {
+  int cluster, start, count, smem;
+};
+
 struct Layout {
   int dtype = 0;
   int elt = 2;
   std::vector<BigMat> big;   // cost order
-  std::vector<int> res;      // caller indices on the resident path
-  int res_maxm = 0, res_smem = 0;
+  std::vector<int> res;      // caller indices on the resident path, grouped by cluster size
+  std::vector<int> res_ns;   // their slice widths
+  std::vector<ResGroup> res_groups;
   std::vector<Tile> tiles01, tiles2;
   std::vector<int> prefix;   // prep tile prefix, big.size()+1
   size_t off_mats = 0, off_res = 0, off_t01 = 0, off_t2 = 0, off_prefix = 0, blob_end = 0;
@@ -188,22 +195,48 @@ int validate(void *const *X, const int64_t *shapes, int count, int steps, int dt
   return NS_OK;
 }
 
+// Whether a small matrix takes the shared-memory resident path: m <= 64 and
+// the whole matrix, with its m x m products, would fit one CTA's shared memory.
+bool resident_fits(int64_t m, int64_t n, int dtype) {
+  if (m > kResidentMaxM) return false;
+  const int64_t elt = dtype == NS_BF16 ? 2 : 4;
+  const int64_t mp = (m + 3) / 4 * 4, np = (n + 3) / 4 * 4;
+  return mp * np * elt + 2 * mp * (mp + 1) * 4 + 16 * 1024 <= kResidentSmemMax;
+}
+
 void build_layout(const int64_t *shapes, int count, int dtype, Layout &L) {
   L = Layout();
   L.dtype = dtype;
   L.elt = dtype == NS_BF16 ? 2 : 4;
   std::vector<int> order;
+  std::vector<int> res_cluster;  // indexed by caller index
   for (int i = 0; i < count; ++i) {
     const int64_t M = shapes[2 * i], N = shapes[2 * i + 1];
     if (M == 0 || N == 0) continue;
     const int64_t m = std::min(M, N), n = std::max(M, N);
-    if (m <= kResidentMaxM && resident_smem_bytes(static_cast<int>(m), static_cast<int>(n), dtype) <= kResidentSmemMax) {
+    if (resident_fits(m, n, dtype))
       L.res.push_back(i);
-      L.res_maxm = std::max<int>(L.res_maxm, static_cast<int>(m));
-      L.res_smem = std::max(L.res_smem, resident_smem_bytes(static_cast<int>(m), static_cast<int>(n), dtype));
-    } else {
+    else
       order.push_back(i);
-    }
+  }
+  // resident matrices: one launch per cluster size (largest first), each
+  // matrix's cluster size from its own shape
+  auto cl = [&](int i) {
+    const int64_t M = shapes[2 * i], N = shapes[2 * i + 1];
+    return resident_cluster(static_cast<int>(std::min(M, N)), static_cast<int>(std::max(M, N)));
+  };
+  std::stable_sort(L.res.begin(), L.res.end(), [&](int a, int b) { return cl(a) > cl(b); });
+  for (size_t k = 0; k < L.res.size(); ++k) {
+    const int i = L.res[k];
+    const int64_t M = shapes[2 * i], N = shapes[2 * i + 1];
+    const int m = static_cast<int>(std::min(M, N)), n = static_cast<int>(std::max(M, N));
+    const int c = cl(i), ns = resident_slice(n, c);
+    L.res_ns.push_back(ns);
+    if (L.res_groups.empty() || L.res_groups.back().cluster != c)
+      L.res_groups.push_back(ResGroup{c, static_cast<int>(k), 0, 0});
+    ResGroup &g = L.res_groups.back();
+    ++g.count;
+    g.smem = std::max(g.smem, resident_smem_bytes(m, ns, dtype));
   }
   // largest Newton-Schulz cost first; ties keep the caller's order
   std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
@@ -354,6 +387,7 @@ int build_blob(const Layout &L, void *const *X, const int64_t *shapes, int steps
     r.transposed = r.M > r.N;
     r.m = std::min(r.M, r.N);
     r.n = std::max(r.M, r.N);
+    r.ns = L.res_ns[k];
     std::memcpy(res + k * sizeof(ResDesc), &r, sizeof(r));
   }
   if (!L.tiles01.empty())
@@ -446,17 +480,18 @@ struct RunOpts {
 int execute(const Layout &L, uint8_t *ws, int steps, const float *co, bool table, float eps, DevInfo *di,
             cudaStream_t s, const RunOpts &opt) {
   const MatDesc *mats = reinterpret_cast<const MatDesc *>(ws + L.off_mats);
-  if (!L.res.empty()) {
+  for (const ResGroup &g : L.res_groups) {
     ResParams rp{};
-    rp.mats = reinterpret_cast<const ResDesc *>(ws + L.off_res);
-    rp.nmats = static_cast<int>(L.res.size());
+    rp.mats = reinterpret_cast<const ResDesc *>(ws + L.off_res) + g.start;
+    rp.nmats = g.count;
+    rp.cluster = g.cluster;
     rp.dtype = L.dtype;
     rp.steps = steps;
     rp.ncoef = table ? steps : 1;
     for (int k = 0; k < (table ? steps : 1); ++k)
       for (int u = 0; u < 3; ++u) rp.coef[k][u] = co[3 * k + u];
     rp.eps = eps;
-    if (timed(5, s, [&] { return launch_resident(rp, L.res_maxm, L.res_smem, s); })) return NS_ECUDA;
+    if (timed(5, s, [&] { return launch_resident(rp, g.smem, s); })) return NS_ECUDA;
   }
   if (L.big.empty()) return NS_OK;
   const int nbig = static_cast<int>(L.big.size());

@@ -77,13 +77,14 @@ struct MatDesc {  // CUtensorMap members keep it 64-byte aligned or more
   int t01, t2;           // tensor-core path: pair tiles of this matrix per gram/square and per apply
 };
 
-// Small matrices done entirely in one CTA (shared-memory resident).
+// Small matrices done entirely in shared memory, each by a cluster of CTAs
+// that split W's columns into slices of `ns` columns.
 struct ResDesc {
   void *user;
   int M, N;
   int m, n;
   int transposed;
-  int pad;
+  int ns;
 };
 
 // Kernel parameters shared by the phase kernels.
@@ -141,6 +142,7 @@ struct PrepParams {
 struct ResParams {
   const ResDesc *mats;
   int nmats;
+  int cluster;           // CTAs per matrix (the launch's cluster size)
   int dtype;
   int steps;
   int ncoef;                        // 1: coef[0] for every step; else coef[step]
@@ -170,12 +172,14 @@ int launch_norm(const PrepParams &p, cudaStream_t s);
 int launch_prep(const PrepParams &p, int total_tiles, cudaStream_t s);
 int launch_norm_tiles(const PrepParams &p, int total_tiles, int max_blocks, cudaStream_t s);
 int launch_norm_finish(const PrepParams &p, cudaStream_t s);
-int launch_resident(const ResParams &p, int maxm, int smem_bytes, cudaStream_t s);
+int launch_resident(const ResParams &p, int smem_bytes, cudaStream_t s);
 int launch_simt_phase(int phase, const PhaseParams &p, cudaStream_t s);
 int launch_tc(const TcParams &p, int max_ctas, cudaStream_t s);
 int tc_smem_bytes();
 int launch_wait_probe(int *status, uint64_t limit_ns, int *gave_up, cudaStream_t s);
-int resident_smem_bytes(int m, int n, int dtype);
+int resident_smem_bytes(int m, int ns, int dtype);  // one CTA of a matrix split into ns-column slices
+int resident_cluster(int m, int n);                 // CTAs per matrix of the resident kernel
+int resident_slice(int n, int cluster);             // their slice width
 
 void count_launch();
 

@@ -3,12 +3,11 @@
 //   * the per-matrix scale from the bf16 norm pass's tile sums,
 //   * preparation: normalise by ||Y||_F + eps, round to the working type and
 //     write both orientations W and W^T,
-//   * the shared-memory resident kernel that runs every step of a small
-//     matrix inside one CTA,
 //   * the fp32 tiled GEMM phases (gram / square / apply) for large fp32
 //     matrices.
 // The bf16 norm pass lives in ns_norm.cu, the bf16 tensor-core phases in
-// ns_tc.cu.
+// ns_tc.cu, the shared-memory resident kernel for small matrices in
+// ns_resident.cu.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -245,264 +244,6 @@ int launch_norm_finish(const PrepParams &p, cudaStream_t s) {
   ns_norm_finish_kernel<<<p.nmats, 256, 0, s>>>(p);
   count_launch();
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
-}
-
-// ============================================================== resident
-// One CTA of 256 threads runs the whole method for one small matrix
-// (m <= 64) held in shared memory: W (mp x np, working type, zero padded to
-// multiples of 4), A and B (fp32). Y is read once and written once. All work
-// is on 4 x 4 register blocks with a fixed assignment and fixed reduction
-// order, so results repeat bit for bit:
-//   gram    upper-triangle blocks of A = W W^T; when there are few blocks the
-//           contraction over n is split into S slices whose partial blocks
-//           are summed in slice order;
-//   square  upper-triangle blocks of B = b A + c A A (A, B kept symmetric);
-//   apply   W' = a W + B W in column panels: every thread computes one 4 x 4
-//           block of the panel, then the panel is written back in place.
-// Only the non-zero block [0, meff) x [0, neff) is iterated on.
-namespace {
-constexpr int kResThreads = 256;
-constexpr int kResPartials = kResThreads * 16;  // floats of the split-gram scratch
-
-__host__ __device__ inline size_t res_align16(size_t v) { return (v + 15) & ~size_t(15); }
-
-struct ResLayout {
-  int mp, np, ap;
-  size_t off_a, off_b, off_part, total;
-  __host__ __device__ ResLayout(int m, int n, int elt) {
-    mp = (m + 3) & ~3;
-    np = (n + 3) & ~3;
-    ap = mp + 1;
-    off_a = res_align16(static_cast<size_t>(mp) * np * elt);
-    off_b = res_align16(off_a + static_cast<size_t>(mp) * ap * 4);
-    off_part = res_align16(off_b + static_cast<size_t>(mp) * ap * 4);
-    total = off_part + static_cast<size_t>(kResPartials) * 4;
-  }
-};
-
-// (bi, bj), bi <= bj, of upper-triangle block number b (row-major order)
-__device__ __forceinline__ void upper_block(int b, int mb, int &bi, int &bj) {
-  bi = 0;
-  while (b >= mb - bi) {
-    b -= mb - bi;
-    ++bi;
-  }
-  bj = bi + b;
-}
-}  // namespace
-
-int resident_smem_bytes(int m, int n, int dtype) {
-  const ResLayout L(m, n, dtype == kBF16 ? 2 : 4);
-  return L.total > (size_t(1) << 30) ? (1 << 30) : static_cast<int>(L.total);
-}
-
-template <int DT>
-__global__ void __launch_bounds__(kResThreads, 1) ns_resident_kernel(ResParams p) {
-  using T = typename Elem<DT>::T;
-  extern __shared__ __align__(16) uint8_t smem[];
-  const ResDesc d = p.mats[blockIdx.x];
-  const int M = d.M, N = d.N, m = d.m, n = d.n, tr = d.transposed;
-  const ResLayout L(m, n, sizeof(T));
-  const int np = L.np, ap = L.ap;
-  T *xs = reinterpret_cast<T *>(smem);
-  float *as = reinterpret_cast<float *>(smem + L.off_a);
-  float *bs = reinterpret_cast<float *>(smem + L.off_b);
-  float *part = reinterpret_cast<float *>(smem + L.off_part);
-  T *y = static_cast<T *>(d.user);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  constexpr int NW = kResThreads / 32;
-
-  __shared__ float s_sum[NW];
-  __shared__ int s_r[NW], s_c[NW];
-  __shared__ float s_denom;  // reciprocal of ||Y||_F + eps
-  __shared__ int s_meff, s_neff;
-
-  // 1. zero the padded working copy, then load Y into it (oriented as W),
-  //    with the sum of squares and the non-zero extent
-  for (int e = tid; e < L.mp * np; e += kResThreads) xs[e] = Elem<DT>::from_f(0.f);
-  __syncthreads();
-  float acc = 0.f;
-  int rmax = -1, cmax = -1;
-  for (int r = warp; r < M; r += NW) {
-    const T *row = y + static_cast<size_t>(r) * N;
-    bool any = false;
-#pragma unroll 4
-    for (int c = lane; c < N; c += 32) {
-      const T v = row[c];
-      const float f = Elem<DT>::to_f(v);
-      acc = fmaf(f, f, acc);
-      if (f != 0.f) {
-        any = true;
-        cmax = max(cmax, c);
-      }
-      if (tr) xs[c * np + r] = v; else xs[r * np + c] = v;
-    }
-    if (any) rmax = r;
-  }
-  acc = warp_sum(acc);
-  rmax = warp_max(rmax);
-  cmax = warp_max(cmax);
-  if (lane == 0) {
-    s_sum[warp] = acc;
-    s_r[warp] = rmax;
-    s_c[warp] = cmax;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    float t = 0.f;
-    int rr = -1, cc = -1;
-    for (int w = 0; w < NW; ++w) {
-      t += s_sum[w];
-      rr = max(rr, s_r[w]);
-      cc = max(cc, s_c[w]);
-    }
-    s_denom = 1.0f / (sqrtf(t) + p.eps);  // 1 / (||Y||_F + eps)
-    s_meff = tr ? cc + 1 : rr + 1;
-    s_neff = tr ? rr + 1 : cc + 1;
-  }
-  __syncthreads();
-  const float inv = s_denom;
-  const int meff = s_meff, neff = s_neff;
-
-  // 2. normalise (zeros stay zero)
-  for (int e = tid; e < L.mp * np; e += kResThreads)
-    xs[e] = Elem<DT>::from_f(Elem<DT>::to_f(xs[e]) * inv);
-  __syncthreads();
-
-  // 3. iterate on the non-zero block
-  const int mb = (meff + 3) / 4;          // 4-row blocks holding non-zero rows
-  const int nblk = mb * (mb + 1) / 2;     // upper-triangle blocks
-  const int S = nblk > 0 ? max(1, min(kResThreads / max(nblk, 1), neff)) : 1;  // gram slices
-  const int kslice = (neff + S - 1) / S;
-  const int panel = 4 * (kResThreads / max(mb, 1));  // apply: columns per panel
-  for (int step = 0; step < p.steps && meff > 0; ++step) {
-    const float *co = p.coef[p.ncoef == 1 ? 0 : step];
-    const float ca = co[0], cb = co[1], cc = co[2];
-    // ---- gram: partial 4x4 blocks over k-slices
-    if (tid < nblk * S) {
-      const int b = tid / S, sl = tid % S;
-      int bi, bj;
-      upper_block(b, mb, bi, bj);
-      const int k0 = sl * kslice, k1 = min(neff, k0 + kslice);
-      float c4[4][4] = {};
-      for (int k = k0; k < k1; ++k) {
-        float xa[4], xb[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          xa[u] = Elem<DT>::to_f(xs[(4 * bi + u) * np + k]);
-          xb[u] = Elem<DT>::to_f(xs[(4 * bj + u) * np + k]);
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-#pragma unroll
-          for (int v = 0; v < 4; ++v) c4[u][v] = fmaf(xa[u], xb[v], c4[u][v]);
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-#pragma unroll
-        for (int v = 0; v < 4; ++v) part[(sl * nblk + b) * 16 + u * 4 + v] = c4[u][v];
-    }
-    __syncthreads();
-    // ---- sum the slices in order into A (both triangles)
-    for (int e = tid; e < nblk * 16; e += kResThreads) {
-      const int b = e >> 4, u = (e >> 2) & 3, v = e & 3;
-      int bi, bj;
-      upper_block(b, mb, bi, bj);
-      float sum = 0.f;
-      for (int sl = 0; sl < S; ++sl) sum += part[(sl * nblk + b) * 16 + u * 4 + v];
-      const int i = 4 * bi + u, j = 4 * bj + v;
-      if (bi < bj || u <= v) {
-        as[i * ap + j] = sum;
-        as[j * ap + i] = sum;
-      }
-    }
-    __syncthreads();
-    // ---- square: B = b A + c A A on upper blocks (symmetric, so both triangles)
-    for (int b = tid; b < nblk; b += kResThreads) {
-      int bi, bj;
-      upper_block(b, mb, bi, bj);
-      float c4[4][4] = {};
-      for (int k = 0; k < meff; ++k) {
-        float ar[4], ac[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          ar[u] = as[(4 * bi + u) * ap + k];
-          ac[u] = as[k * ap + 4 * bj + u];
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-#pragma unroll
-          for (int v = 0; v < 4; ++v) c4[u][v] = fmaf(ar[u], ac[v], c4[u][v]);
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const int i = 4 * bi + u, j = 4 * bj + v;
-          const float val = cb * as[i * ap + j] + cc * c4[u][v];
-          bs[i * ap + j] = val;
-          bs[j * ap + i] = val;
-        }
-    }
-    __syncthreads();
-    // ---- apply: W' = a W + B W, one column panel at a time
-    for (int c0 = 0; c0 < neff; c0 += panel) {
-      const int rb = tid % mb, cb = tid / mb;
-      const int j0 = c0 + 4 * cb;
-      const bool active = tid < mb * (panel / 4) && j0 < neff;
-      float o4[4][4] = {};
-      if (active) {
-        for (int k = 0; k < meff; ++k) {
-          float br[4], xr[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            br[u] = bs[(4 * rb + u) * ap + k];
-            xr[u] = Elem<DT>::to_f(xs[k * np + j0 + u]);
-          }
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-#pragma unroll
-            for (int v = 0; v < 4; ++v) o4[u][v] = fmaf(br[u], xr[v], o4[u][v]);
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-#pragma unroll
-          for (int v = 0; v < 4; ++v)
-            o4[u][v] = ca * Elem<DT>::to_f(xs[(4 * rb + u) * np + j0 + v]) + o4[u][v];
-      }
-      __syncthreads();  // every read of this panel happened
-      if (active) {
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-#pragma unroll
-          for (int v = 0; v < 4; ++v) xs[(4 * rb + u) * np + j0 + v] = Elem<DT>::from_f(o4[u][v]);
-      }
-      __syncthreads();
-    }
-  }
-
-  // 4. write back in the caller's orientation
-  for (int r = warp; r < M; r += NW) {
-    T *row = y + static_cast<size_t>(r) * N;
-#pragma unroll 4
-    for (int c = lane; c < N; c += 32) row[c] = tr ? xs[c * np + r] : xs[r * np + c];
-  }
-}
-
-template <int DT>
-static int launch_resident_t(const ResParams &p, int smem, cudaStream_t s) {
-  auto k = ns_resident_kernel<DT>;
-  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -1;
-  k<<<p.nmats, kResThreads, smem, s>>>(p);
-  count_launch();
-  return cudaGetLastError() == cudaSuccess ? 0 : -1;
-}
-
-int launch_resident(const ResParams &p, int maxm, int smem, cudaStream_t s) {
-  (void)maxm;
-  if (p.nmats <= 0) return 0;
-  if (p.dtype == kBF16) return launch_resident_t<kBF16>(p, smem, s);
-  return launch_resident_t<kF32>(p, smem, s);
 }
 
 // ============================================================== fp32 GEMM phases

@@ -8,6 +8,7 @@ fallback: if ``libns.so`` is missing, every call raises.
 from __future__ import annotations
 
 import ctypes
+import itertools
 import os
 import threading
 
@@ -105,9 +106,13 @@ def _dtype_code(dtype) -> int:
 
 
 def _marshal(mats, coeffs):
+    """Device pointers and (M, N) pairs of the matrices as C arrays (numpy
+    buffers, kept alive by the caller for the duration of the call)."""
+    import numpy as np
+    import torch
     n = len(mats)
-    ptrs = (ctypes.c_void_p * max(n, 1))(*[t.data_ptr() for t in mats])
-    shapes = (ctypes.c_int64 * max(2 * n, 1))(*[int(d) for t in mats for d in t.shape])
+    ptrs = np.fromiter(map(torch.Tensor.data_ptr, mats), dtype=np.uint64, count=n)
+    shapes = np.fromiter(itertools.chain.from_iterable(t.shape for t in mats), dtype=np.int64, count=2 * n)
     co = None
     if coeffs is not None:
         if len(coeffs) != 3:
@@ -116,11 +121,15 @@ def _marshal(mats, coeffs):
     return ptrs, shapes, co
 
 
+def _ptr(a) -> ctypes.c_void_p:
+    return ctypes.c_void_p(a.ctypes.data)
+
+
 def _check(mats, want_cuda: bool):
     if not mats:
         return None
-    dt = mats[0].dtype
-    dev = mats[0].device
+    t0 = mats[0]
+    dt, dev = t0.dtype, t0.device
     for t in mats:
         if t.dim() != 2:
             raise ValueError("every matrix must be 2-D")
@@ -128,10 +137,10 @@ def _check(mats, want_cuda: bool):
             raise ValueError("all matrices must share dtype and device")
         if not t.is_contiguous():
             raise ValueError("matrices must be contiguous (row-major)")
-        if want_cuda and not t.is_cuda:
-            raise ValueError("matrices must be CUDA tensors")
-        if not want_cuda and t.is_cuda:
-            raise ValueError("host entry point takes CPU tensors")
+    if want_cuda and dev.type != "cuda":
+        raise ValueError("matrices must be CUDA tensors")
+    if not want_cuda and dev.type == "cuda":
+        raise ValueError("host entry point takes CPU tensors")
     return _dtype_code(dt)
 
 
@@ -155,7 +164,7 @@ def orthogonalize_batched(mats, steps: int = 5, coeffs=None, eps: float | None =
         sp = ctypes.c_void_p(s.cuda_stream)
         ptrs, shapes, co = _marshal(mats, coeffs)
         if eps is None and workspace is None:
-            rc = lib.ns_orthogonalize_batched(ptrs, shapes, len(mats), int(steps), co, code, sp)
+            rc = lib.ns_orthogonalize_batched(_ptr(ptrs), _ptr(shapes), len(mats), int(steps), co, code, sp)
         else:
             e = 1e-7 if eps is None else float(eps)
             if workspace is None:
@@ -164,7 +173,7 @@ def orthogonalize_batched(mats, steps: int = 5, coeffs=None, eps: float | None =
                 # the caching allocator must not hand this block out again
                 # before the work queued on `s` has finished with it
                 workspace.record_stream(s)
-            rc = lib.ns_orthogonalize_batched_ex(ptrs, shapes, len(mats), int(steps), co, e, code,
+            rc = lib.ns_orthogonalize_batched_ex(_ptr(ptrs), _ptr(shapes), len(mats), int(steps), co, e, code,
                                                  ctypes.c_void_p(workspace.data_ptr()),
                                                  workspace.numel(), sp)
     if rc != 0:
@@ -188,7 +197,7 @@ def orthogonalize_batched_schedule(mats, table, stream=None) -> None:
         s = stream if stream is not None else torch.cuda.current_stream(dev)
         ptrs, shapes, _ = _marshal(mats, None)
         tab = (ctypes.c_float * max(3 * len(rows), 3))(*[v for r in rows for v in r])
-        rc = lib.ns_orthogonalize_batched_sched(ptrs, shapes, len(mats), len(rows), tab, code,
+        rc = lib.ns_orthogonalize_batched_sched(_ptr(ptrs), _ptr(shapes), len(mats), len(rows), tab, code,
                                                 ctypes.c_void_p(s.cuda_stream))
     if rc != 0:
         raise NSError(rc, "ns_orthogonalize_batched_sched")
@@ -208,7 +217,7 @@ def orthogonalize_batched_noalloc(mats, steps: int = 5, coeffs=None, stream=None
     with torch.cuda.device(dev):
         s = stream if stream is not None else torch.cuda.current_stream(dev)
         ptrs, shapes, co = _marshal(mats, coeffs)
-        rc = lib.ns_orthogonalize_batched_noalloc(ptrs, shapes, len(mats), int(steps), co, code,
+        rc = lib.ns_orthogonalize_batched_noalloc(_ptr(ptrs), _ptr(shapes), len(mats), int(steps), co, code,
                                                   ctypes.c_void_p(s.cuda_stream))
     if rc != 0:
         raise NSError(rc, "ns_orthogonalize_batched_noalloc")
@@ -227,7 +236,7 @@ def orthogonalize_batched_host(mats, steps: int = 5, coeffs=None, device=None, s
     with torch.cuda.device(dev):
         s = stream if stream is not None else torch.cuda.current_stream(dev)
         ptrs, shapes, co = _marshal(mats, coeffs)
-        rc = lib.ns_orthogonalize_batched_host(ptrs, shapes, len(mats), int(steps), co, code,
+        rc = lib.ns_orthogonalize_batched_host(_ptr(ptrs), _ptr(shapes), len(mats), int(steps), co, code,
                                                ctypes.c_void_p(s.cuda_stream))
     if rc != 0:
         raise NSError(rc, "ns_orthogonalize_batched_host")

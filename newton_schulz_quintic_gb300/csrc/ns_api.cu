@@ -34,6 +34,19 @@ static std::atomic<int64_t> g_launches{0};
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 static std::atomic<int64_t> g_allocations{0};
 
+int SmemOptIn::ensure(const void *kernel, int bytes) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  int &have = allowed[dev & 63];
+  if (bytes <= have) return 0;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  have = bytes;
+  return 0;
+}
+
 // Device status word (one per device, file-scope; see ns_get_status) and the
 // flag the wait self-test reports through.
 __device__ int g_status_word;

@@ -183,6 +183,14 @@ int resident_slice(int n, int cluster);             // their slice width
 
 void count_launch();
 
+// The dynamic shared memory a kernel has been allowed on each device so far,
+// so that the opt-in (cudaFuncSetAttribute) runs once per device and size
+// rather than before every launch.
+struct SmemOptIn {
+  int allowed[64] = {};
+  int ensure(const void *kernel, int bytes);  // 0, or -1 if the attribute could not be set
+};
+
 // Validation of a device-pointer call (the same checks, in the same order, as
 // ns_orthogonalize_batched makes before launching) and the current-device
 // check: NS_OK, or the status code such a call would return.

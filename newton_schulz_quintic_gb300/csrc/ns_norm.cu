@@ -295,9 +295,8 @@ __global__ void __launch_bounds__(256, 2) ns_norm_tiles_kernel(PrepParams p, int
 int launch_norm_tiles(const PrepParams &p, int total_tiles, int max_blocks, cudaStream_t s) {
   if (total_tiles <= 0) return 0;
   const int blocks = std::min((total_tiles + 7) / 8, std::max(max_blocks, 1));
-  if (cudaFuncSetAttribute(ns_norm_tiles_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kNormSmem) !=
-      cudaSuccess)
-    return -1;
+  static SmemOptIn opt_in;
+  if (opt_in.ensure(reinterpret_cast<const void *>(ns_norm_tiles_kernel), kNormSmem)) return -1;
   ns_norm_tiles_kernel<<<blocks, 256, kNormSmem, s>>>(p, total_tiles);
   count_launch();
   return cudaGetLastError() == cudaSuccess ? 0 : -1;

@@ -14,11 +14,14 @@
 //           order) and publishes it in its shared memory; after one cluster
 //           barrier every CTA adds the C partials in rank order through
 //           distributed shared memory (A, both triangles);
-//   square  B = b A + c A A, by every CTA for itself (m <= 64);
-//   apply   W_c' = a W_c + B W_c on the CTA's own columns, in column panels
-//           written back in place.
-// The partials are double-buffered across steps, so one cluster barrier per
-// step orders every exchange. The first step folds the normalisation in
+//   square  B = b A + c A A: every CTA computes the upper 4 x 4 blocks it
+//           owns (block b belongs to rank b % C) and, after a second cluster
+//           barrier, gathers the others' blocks through distributed shared
+//           memory;
+//   apply   W_c' = a W_c + B W_c on the CTA's own columns, in passes of whole
+//           4-column blocks written back in place.
+// The partials are double-buffered across steps, so two cluster barriers per
+// step order every exchange. The first step folds the normalisation in
 // (A = r^2 sum of partials, W_1 = r (a W + B W), r = 1 / (||Y||_F + eps)), so
 // the normalised input is never rounded; every later iterate is stored in the
 // working type (bf16 rounding to nearest even between steps, as on the
@@ -118,13 +121,13 @@ int resident_smem_bytes(int m, int ns, int dtype) {
   return L.total > (size_t(1) << 30) ? (1 << 30) : static_cast<int>(L.total);
 }
 
-// CTAs per matrix: about 2^17 multiply-adds of one step's gram and apply per
+// CTAs per matrix: about 2^16 multiply-adds of one step's gram and apply per
 // CTA, a power of two up to 8, and slices at least 8 columns wide.
 int resident_cluster(int m, int n) {
   const int64_t mp = (m + 3) & ~3;
   const int64_t work = mp * mp * n;
   int c = 1;
-  while (c < 8 && work > (int64_t(1) << 17) * c && n >= 16 * c) c *= 2;
+  while (c < 8 && work > (int64_t(1) << 16) * c && n >= 16 * c) c *= 2;
   return c;
 }
 
@@ -256,7 +259,6 @@ __global__ void __launch_bounds__(kResThreads, 1) ns_resident_kernel(const __gri
   const int kv = (nse + 7) / 8;                   // 8-column groups of the local contraction
   const int S = nblk > 0 ? max(1, min(kResThreads / nblk, kv)) : 1;
   const int kper = (kv + S - 1) / S;
-  const int panel = 4 * (kResThreads / max(mb, 1));  // apply: columns per panel
   for (int step = 0; step < p.steps && meff > 0; ++step) {
     const float *co = p.coef[p.ncoef == 1 ? 0 : step];
     const float ca = co[0], cb = co[1], cc = co[2];
@@ -313,67 +315,109 @@ __global__ void __launch_bounds__(kResThreads, 1) ns_resident_kernel(const __gri
       }
     }
     __syncthreads();
-    // ---- square: B = b A + c A A on upper blocks (symmetric, so both triangles)
-    for (int b = tid; b < nblk; b += kResThreads) {
-      int bi, bj;
-      upper_block(b, mb, bi, bj);
-      float c4[4][4] = {};
-      for (int k = 0; k < 4 * mb; ++k) {
-        float ar[4], ac[4];
+    // ---- square: B = b A + c A A on the upper blocks this CTA owns (block b
+    //      belongs to rank b % C), the contraction split into slices of 4-row
+    //      groups summed in slice order; then every CTA gathers the other
+    //      ranks' blocks (both triangles)
+    {
+      const int own = (nblk - rank + C - 1) / C;
+      const int S2 = own > 0 ? max(1, min(kResThreads / own, mb)) : 1;
+      const int kq = (mb + S2 - 1) / S2;
+      if (tid < own * S2) {
+        const int ob = tid / S2, sl = tid - ob * S2;
+        int bi, bj;
+        upper_block(rank + ob * C, mb, bi, bj);
+        float c4[4][4] = {};
+        for (int k = 4 * sl * kq; k < 4 * min(mb, (sl + 1) * kq); ++k) {
+          float ar[4], ac[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          ar[u] = A[(4 * bi + u) * ap + k];
-          ac[u] = A[k * ap + 4 * bj + u];
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-#pragma unroll
-          for (int v = 0; v < 4; ++v) c4[u][v] = fmaf(ar[u], ac[v], c4[u][v]);
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const int i = 4 * bi + u, j = 4 * bj + v;
-          const float val = cb * A[i * ap + j] + cc * c4[u][v];
-          B[i * ap + j] = val;
-          B[j * ap + i] = val;
-        }
-    }
-    __syncthreads();
-    // ---- apply: W_c' = as (a W_c + B W_c), one column panel at a time
-    for (int pc = 0; pc < nse; pc += panel) {
-      const int rb = tid % mb, cbk = tid / mb;
-      const int j0 = pc + 4 * cbk;
-      const bool active = tid < mb * (panel / 4) && j0 < nse;
-      float o4[4][4] = {};
-      if (active) {
-        for (int k = 0; k < 4 * mb; ++k) {
-          float br[4], xr[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) br[u] = B[(4 * rb + u) * ap + k];
-          ld4(w + k * ld + j0, xr);
+          for (int u = 0; u < 4; ++u) {
+            ar[u] = A[(4 * bi + u) * ap + k];
+            ac[u] = A[k * ap + 4 * bj + u];
+          }
 #pragma unroll
           for (int u = 0; u < 4; ++u)
 #pragma unroll
-            for (int v = 0; v < 4; ++v) o4[u][v] = fmaf(br[u], xr[v], o4[u][v]);
+            for (int v = 0; v < 4; ++v) c4[u][v] = fmaf(ar[u], ac[v], c4[u][v]);
         }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          float xo[4];
-          ld4(w + (4 * rb + u) * ld + j0, xo);
-#pragma unroll
-          for (int v = 0; v < 4; ++v) o4[u][v] = as * (ca * xo[v] + o4[u][v]);
-        }
-      }
-      __syncthreads();  // every read of this panel happened
-      if (active) {
 #pragma unroll
         for (int u = 0; u < 4; ++u)
 #pragma unroll
-          for (int v = 0; v < 4; ++v) w[(4 * rb + u) * ld + j0 + v] = Elem<DT>::from_f(o4[u][v]);
+          for (int v = 0; v < 4; ++v) part[(sl * own + ob) * 16 + u * 4 + v] = c4[u][v];
       }
       __syncthreads();
+      for (int e = tid; e < own * 16; e += kResThreads) {
+        const int ob = e >> 4, u = (e >> 2) & 3, v = e & 3;
+        int bi, bj;
+        upper_block(rank + ob * C, mb, bi, bj);
+        const int i = 4 * bi + u, j = 4 * bj + v;
+        if (bi < bj || u <= v) {
+          float sum = 0.f;
+          for (int sl = 0; sl < S2; ++sl) sum += part[(sl * own + ob) * 16 + u * 4 + v];
+          const float val = cb * A[i * ap + j] + cc * sum;
+          B[i * ap + j] = val;
+          B[j * ap + i] = val;
+        }
+      }
+      res_sync(C);  // every rank's blocks of B are published
+      if (C > 1) {
+        for (int e = tid; e < nblk * 16; e += kResThreads) {
+          const int b = e >> 4, u = (e >> 2) & 3, v = e & 3;
+          const int owner = b % C;
+          if (owner == rank) continue;
+          int bi, bj;
+          upper_block(b, mb, bi, bj);
+          const int i = 4 * bi + u, j = 4 * bj + v;
+          if (bi < bj || u <= v) {
+            const float val = ld_cluster_f32(B + i * ap + j, owner);
+            B[i * ap + j] = val;
+            B[j * ap + i] = val;
+          }
+        }
+      }
+      __syncthreads();
+    }
+    // ---- apply: W_c' = as (a W_c + B W_c) on 4 x 4 output blocks, a pass of
+    //      whole 4-column blocks at a time; when the blocks are few the
+    //      contraction is split into slices of 4-row groups summed in slice order
+    {
+      const int ncb = (nse + 3) / 4;
+      const int S3 = max(1, min(kResThreads / max(mb * ncb, 1), mb));
+      const int kq = (mb + S3 - 1) / S3;
+      const int cpp = max(1, kResThreads / (S3 * mb));  // column blocks per pass
+      for (int cb0 = 0; cb0 < ncb; cb0 += cpp) {
+        const int nb = mb * min(cpp, ncb - cb0);        // output blocks of this pass
+        if (tid < nb * S3) {
+          const int ob = tid / S3, sl = tid - ob * S3;
+          const int rb = ob % mb, j0 = 4 * (cb0 + ob / mb);
+          float o4[4][4] = {};
+          for (int k = 4 * sl * kq; k < 4 * min(mb, (sl + 1) * kq); ++k) {
+            float br[4], xr[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) br[u] = B[(4 * rb + u) * ap + k];
+            ld4(w + k * ld + j0, xr);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+              for (int v = 0; v < 4; ++v) o4[u][v] = fmaf(br[u], xr[v], o4[u][v]);
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int v = 0; v < 4; ++v) part[(sl * nb + ob) * 16 + u * 4 + v] = o4[u][v];
+        }
+        __syncthreads();  // every read of these columns of W happened
+        for (int e = tid; e < nb * 16; e += kResThreads) {
+          const int ob = e >> 4, u = (e >> 2) & 3, v = e & 3;
+          const int i = 4 * (ob % mb) + u, j = 4 * (cb0 + ob / mb) + v;
+          if (i < meff && j < nse) {
+            float sum = 0.f;
+            for (int sl = 0; sl < S3; ++sl) sum += part[(sl * nb + ob) * 16 + u * 4 + v];
+            w[i * ld + j] = Elem<DT>::from_f(as * (ca * Elem<DT>::to_f(w[i * ld + j]) + sum));
+          }
+        }
+        __syncthreads();
+      }
     }
   }
   if (p.steps == 0) {  // normalisation only
@@ -421,7 +465,8 @@ __global__ void __launch_bounds__(kResThreads, 1) ns_resident_kernel(const __gri
 template <int DT>
 int launch_resident_t(const ResParams &p, int smem, cudaStream_t s) {
   auto k = ns_resident_kernel<DT>;
-  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -1;
+  static SmemOptIn opt_in;
+  if (opt_in.ensure(reinterpret_cast<const void *>(k), smem)) return -1;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;

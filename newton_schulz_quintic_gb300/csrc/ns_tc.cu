@@ -789,7 +789,8 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
 int launch_tc_kernel(const TcParams &p, int max_ctas, cudaStream_t s) {
   const int smem = tc_smem_bytes();
   auto kernel = ns_tc_gemm_kernel;
-  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -1;
+  static SmemOptIn opt_in;
+  if (opt_in.ensure(reinterpret_cast<const void *>(kernel), smem)) return -1;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -14,14 +14,15 @@
 //           order) and publishes it in its shared memory; after one cluster
 //           barrier every CTA adds the C partials in rank order through
 //           distributed shared memory (A, both triangles);
-//   square  B = b A + c A A: every CTA computes the upper 4 x 4 blocks it
-//           owns (block b belongs to rank b % C) and, after a second cluster
-//           barrier, gathers the others' blocks through distributed shared
-//           memory;
-//   apply   W_c' = a W_c + B W_c on the CTA's own columns, in passes of whole
-//           4-column blocks written back in place.
-// The partials are double-buffered across steps, so two cluster barriers per
-// step order every exchange. The first step folds the normalisation in
+//   square  B = b A + c A A: by every CTA for itself when it is small; when
+//           it has many 4 x 4 blocks each CTA computes the blocks it owns and
+//           stores them into every CTA of the cluster (a second barrier);
+//   apply   W_c' = a W_c + B W_c on the CTA's own columns, in column panels
+//           written back in place.
+// The partials are double-buffered across steps, so one cluster barrier per
+// step (two with a split square) orders every exchange. Remote shared memory
+// is read with all of a value's C loads in flight at once, and written by
+// plain remote stores. The first step folds the normalisation in
 // (A = r^2 sum of partials, W_1 = r (a W + B W), r = 1 / (||Y||_F + eps)), so
 // the normalised input is never rounded; every later iterate is stored in the
 // working type (bf16 rounding to nearest even between steps, as on the
@@ -108,6 +109,29 @@ __device__ __forceinline__ float ld_cluster_f32(const float *local, int rank) {
 __device__ __forceinline__ int ld_cluster_i32(const int *local, int rank) {
   return static_cast<int>(ld_shared_cluster_u32(mapa_shared(smem_u32(local), static_cast<uint32_t>(rank))));
 }
+__device__ __forceinline__ void st_cluster_f32(float *local, int rank, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(mapa_shared(smem_u32(local), static_cast<uint32_t>(rank))),
+               "f"(v)
+               : "memory");
+}
+
+// Sum over the cluster's ranks, in rank order, of the float at `local`'s
+// offset in each CTA: the C remote loads are issued together, then added.
+template <int C>
+__device__ __forceinline__ float cluster_sum(const float *local) {
+  float v[C];
+#pragma unroll
+  for (int c = 0; c < C; ++c) v[c] = C > 1 ? ld_cluster_f32(local, c) : *local;
+  float t = 0.f;
+#pragma unroll
+  for (int c = 0; c < C; ++c) t += v[c];
+  return t;
+}
+
+// Upper blocks of B at or above this many are split over the cluster's CTAs
+// (each computes the blocks it owns and stores them into every CTA); below
+// it every CTA computes all of B itself.
+constexpr int kSplitSquareBlocks = 32;
 
 // Barrier over the matrix's CTAs: the cluster, or just this CTA when C = 1.
 __device__ __forceinline__ void res_sync(int C) {
@@ -121,13 +145,13 @@ int resident_smem_bytes(int m, int ns, int dtype) {
   return L.total > (size_t(1) << 30) ? (1 << 30) : static_cast<int>(L.total);
 }
 
-// CTAs per matrix: about 2^16 multiply-adds of one step's gram and apply per
+// CTAs per matrix: about 2^17 multiply-adds of one step's gram and apply per
 // CTA, a power of two up to 8, and slices at least 8 columns wide.
 int resident_cluster(int m, int n) {
   const int64_t mp = (m + 3) & ~3;
   const int64_t work = mp * mp * n;
   int c = 1;
-  while (c < 8 && work > (int64_t(1) << 16) * c && n >= 16 * c) c *= 2;
+  while (c < 8 && work > (int64_t(1) << 17) * c && n >= 16 * c) c *= 2;
   return c;
 }
 
@@ -136,7 +160,7 @@ int resident_slice(int n, int c) { return ((n + c - 1) / c + 7) & ~7; }
 
 namespace {
 
-template <int DT>
+template <int DT, int C>
 __global__ void __launch_bounds__(kResThreads, 1) ns_resident_kernel(const __grid_constant__ ResParams p) {
   using T = typename Elem<DT>::T;
   constexpr int V = 16 / static_cast<int>(sizeof(T));
@@ -148,7 +172,6 @@ __global__ void __launch_bounds__(kResThreads, 1) ns_resident_kernel(const __gri
   __shared__ float s_r;
   __shared__ int s_meff, s_nse;
 
-  const int C = p.cluster;
   const int rank = C > 1 ? static_cast<int>(cluster_ctarank()) : 0;
   const ResDesc d = p.mats[blockIdx.x / C];
   const int M = d.M, N = d.N, m = d.m, n = d.n, tr = d.transposed, ns = d.ns;
@@ -239,12 +262,13 @@ __global__ void __launch_bounds__(kResThreads, 1) ns_resident_kernel(const __gri
   }
   res_sync(C);  // every CTA's sum and row extent are published
   if (tid == 0) {
-    float t = 0.f;
+    const float t = cluster_sum<C>(&s_sum);  // rank order
+    int rv[C];
+#pragma unroll
+    for (int c = 0; c < C; ++c) rv[c] = C > 1 ? ld_cluster_i32(&s_rows, c) : s_rows;
     int rows = 0;
-    for (int c = 0; c < C; ++c) {  // rank order
-      t += C > 1 ? ld_cluster_f32(&s_sum, c) : s_sum;
-      rows = max(rows, C > 1 ? ld_cluster_i32(&s_rows, c) : s_rows);
-    }
+#pragma unroll
+    for (int c = 0; c < C; ++c) rows = max(rows, rv[c]);
     s_r = 1.0f / (sqrtf(t) + p.eps);  // 1 / (||Y||_F + eps)
     s_meff = rows;
   }
@@ -259,6 +283,7 @@ __global__ void __launch_bounds__(kResThreads, 1) ns_resident_kernel(const __gri
   const int kv = (nse + 7) / 8;                   // 8-column groups of the local contraction
   const int S = nblk > 0 ? max(1, min(kResThreads / nblk, kv)) : 1;
   const int kper = (kv + S - 1) / S;
+  const int panel = 4 * (kResThreads / max(mb, 1));  // apply: columns per panel
   for (int step = 0; step < p.steps && meff > 0; ++step) {
     const float *co = p.coef[p.ncoef == 1 ? 0 : step];
     const float ca = co[0], cb = co[1], cc = co[2];
@@ -307,21 +332,20 @@ __global__ void __launch_bounds__(kResThreads, 1) ns_resident_kernel(const __gri
       upper_block(b, mb, bi, bj);
       const int i = 4 * bi + u, j = 4 * bj + v;
       if (bi < bj || u <= v) {
-        float sum = 0.f;
-        for (int c = 0; c < C; ++c) sum += C > 1 ? ld_cluster_f32(Pc + i * ap + j, c) : Pc[i * ap + j];
-        sum *= gs;
+        const float sum = gs * cluster_sum<C>(Pc + i * ap + j);
         A[i * ap + j] = sum;
         A[j * ap + i] = sum;
       }
     }
     __syncthreads();
-    // ---- square: B = b A + c A A on the upper blocks this CTA owns (block b
+    // ---- square: B = b A + c A A on upper blocks (symmetric, so both
+    //      triangles). Many blocks: each CTA takes the blocks it owns (block b
     //      belongs to rank b % C), the contraction split into slices of 4-row
-    //      groups summed in slice order; then every CTA gathers the other
-    //      ranks' blocks (both triangles)
-    {
+    //      groups summed in slice order, and stores them into every CTA of
+    //      the cluster; few blocks: every CTA computes all of B itself.
+    if (C > 1 && nblk >= kSplitSquareBlocks) {
       const int own = (nblk - rank + C - 1) / C;
-      const int S2 = own > 0 ? max(1, min(kResThreads / own, mb)) : 1;
+      const int S2 = max(1, min(kResThreads / own, mb));
       const int kq = (mb + S2 - 1) / S2;
       if (tid < own * S2) {
         const int ob = tid / S2, sl = tid - ob * S2;
@@ -355,69 +379,76 @@ __global__ void __launch_bounds__(kResThreads, 1) ns_resident_kernel(const __gri
           float sum = 0.f;
           for (int sl = 0; sl < S2; ++sl) sum += part[(sl * own + ob) * 16 + u * 4 + v];
           const float val = cb * A[i * ap + j] + cc * sum;
-          B[i * ap + j] = val;
-          B[j * ap + i] = val;
-        }
-      }
-      res_sync(C);  // every rank's blocks of B are published
-      if (C > 1) {
-        for (int e = tid; e < nblk * 16; e += kResThreads) {
-          const int b = e >> 4, u = (e >> 2) & 3, v = e & 3;
-          const int owner = b % C;
-          if (owner == rank) continue;
-          int bi, bj;
-          upper_block(b, mb, bi, bj);
-          const int i = 4 * bi + u, j = 4 * bj + v;
-          if (bi < bj || u <= v) {
-            const float val = ld_cluster_f32(B + i * ap + j, owner);
-            B[i * ap + j] = val;
-            B[j * ap + i] = val;
+#pragma unroll
+          for (int c = 0; c < C; ++c) {
+            st_cluster_f32(B + i * ap + j, c, val);
+            st_cluster_f32(B + j * ap + i, c, val);
           }
         }
       }
-      __syncthreads();
-    }
-    // ---- apply: W_c' = as (a W_c + B W_c) on 4 x 4 output blocks, a pass of
-    //      whole 4-column blocks at a time; when the blocks are few the
-    //      contraction is split into slices of 4-row groups summed in slice order
-    {
-      const int ncb = (nse + 3) / 4;
-      const int S3 = max(1, min(kResThreads / max(mb * ncb, 1), mb));
-      const int kq = (mb + S3 - 1) / S3;
-      const int cpp = max(1, kResThreads / (S3 * mb));  // column blocks per pass
-      for (int cb0 = 0; cb0 < ncb; cb0 += cpp) {
-        const int nb = mb * min(cpp, ncb - cb0);        // output blocks of this pass
-        if (tid < nb * S3) {
-          const int ob = tid / S3, sl = tid - ob * S3;
-          const int rb = ob % mb, j0 = 4 * (cb0 + ob / mb);
-          float o4[4][4] = {};
-          for (int k = 4 * sl * kq; k < 4 * min(mb, (sl + 1) * kq); ++k) {
-            float br[4], xr[4];
+      res_sync(C);  // every CTA's blocks of B have landed everywhere
+    } else {
+      for (int b = tid; b < nblk; b += kResThreads) {
+        int bi, bj;
+        upper_block(b, mb, bi, bj);
+        float c4[4][4] = {};
+        for (int k = 0; k < 4 * mb; ++k) {
+          float ar[4], ac[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) br[u] = B[(4 * rb + u) * ap + k];
-            ld4(w + k * ld + j0, xr);
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-#pragma unroll
-              for (int v = 0; v < 4; ++v) o4[u][v] = fmaf(br[u], xr[v], o4[u][v]);
+          for (int u = 0; u < 4; ++u) {
+            ar[u] = A[(4 * bi + u) * ap + k];
+            ac[u] = A[k * ap + 4 * bj + u];
           }
 #pragma unroll
           for (int u = 0; u < 4; ++u)
 #pragma unroll
-            for (int v = 0; v < 4; ++v) part[(sl * nb + ob) * 16 + u * 4 + v] = o4[u][v];
+            for (int v = 0; v < 4; ++v) c4[u][v] = fmaf(ar[u], ac[v], c4[u][v]);
         }
-        __syncthreads();  // every read of these columns of W happened
-        for (int e = tid; e < nb * 16; e += kResThreads) {
-          const int ob = e >> 4, u = (e >> 2) & 3, v = e & 3;
-          const int i = 4 * (ob % mb) + u, j = 4 * (cb0 + ob / mb) + v;
-          if (i < meff && j < nse) {
-            float sum = 0.f;
-            for (int sl = 0; sl < S3; ++sl) sum += part[(sl * nb + ob) * 16 + u * 4 + v];
-            w[i * ld + j] = Elem<DT>::from_f(as * (ca * Elem<DT>::to_f(w[i * ld + j]) + sum));
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const int i = 4 * bi + u, j = 4 * bj + v;
+            const float val = cb * A[i * ap + j] + cc * c4[u][v];
+            B[i * ap + j] = val;
+            B[j * ap + i] = val;
           }
-        }
-        __syncthreads();
       }
+      __syncthreads();
+    }
+    // ---- apply: W_c' = as (a W_c + B W_c), one column panel at a time
+    for (int pc = 0; pc < nse; pc += panel) {
+      const int rb = tid % mb, cbk = tid / mb;
+      const int j0 = pc + 4 * cbk;
+      const bool active = tid < mb * (panel / 4) && j0 < nse;
+      float o4[4][4] = {};
+      if (active) {
+        for (int k = 0; k < 4 * mb; ++k) {
+          float br[4], xr[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) br[u] = B[(4 * rb + u) * ap + k];
+          ld4(w + k * ld + j0, xr);
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int v = 0; v < 4; ++v) o4[u][v] = fmaf(br[u], xr[v], o4[u][v]);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          float xo[4];
+          ld4(w + (4 * rb + u) * ld + j0, xo);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) o4[u][v] = as * (ca * xo[v] + o4[u][v]);
+        }
+      }
+      __syncthreads();  // every read of this panel happened
+      if (active) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int v = 0; v < 4; ++v) w[(4 * rb + u) * ld + j0 + v] = Elem<DT>::from_f(o4[u][v]);
+      }
+      __syncthreads();
     }
   }
   if (p.steps == 0) {  // normalisation only
@@ -462,18 +493,18 @@ __global__ void __launch_bounds__(kResThreads, 1) ns_resident_kernel(const __gri
   }
 }
 
-template <int DT>
+template <int DT, int C>
 int launch_resident_t(const ResParams &p, int smem, cudaStream_t s) {
-  auto k = ns_resident_kernel<DT>;
+  auto k = ns_resident_kernel<DT, C>;
   static SmemOptIn opt_in;
   if (opt_in.ensure(reinterpret_cast<const void *>(k), smem)) return -1;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = p.cluster;
+  attr[0].val.clusterDim.x = C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3(p.nmats * p.cluster, 1, 1);
+  cfg.gridDim = dim3(p.nmats * C, 1, 1);
   cfg.blockDim = dim3(kResThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -487,12 +518,23 @@ int launch_resident_t(const ResParams &p, int smem, cudaStream_t s) {
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
+template <int DT>
+int launch_resident_dt(const ResParams &p, int smem, cudaStream_t s) {
+  switch (p.cluster) {
+    case 1: return launch_resident_t<DT, 1>(p, smem, s);
+    case 2: return launch_resident_t<DT, 2>(p, smem, s);
+    case 4: return launch_resident_t<DT, 4>(p, smem, s);
+    case 8: return launch_resident_t<DT, 8>(p, smem, s);
+    default: return -1;
+  }
+}
+
 }  // namespace
 
 int launch_resident(const ResParams &p, int smem, cudaStream_t s) {
   if (p.nmats <= 0) return 0;
-  if (p.dtype == kBF16) return launch_resident_t<kBF16>(p, smem, s);
-  return launch_resident_t<kF32>(p, smem, s);
+  if (p.dtype == kBF16) return launch_resident_dt<kBF16>(p, smem, s);
+  return launch_resident_dt<kF32>(p, smem, s);
 }
 
 }  // namespace ns

@@ -290,6 +290,20 @@ def measure_workload(wl, dev, steps, warmup, graph=False):
     times = time_steps(steps, restore, one_step, stream)
     if api.get_status() != 0:
         raise RuntimeError(f"device status word reports a timeout on {wl.name}")
+    # host time of a call (argument marshalling, planning, launches), measured
+    # back to back without waiting for the GPU
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(10):
+        one_step()
+    host_us = (time.perf_counter() - t0) / 10 * 1e6
+    torch.cuda.synchronize()
+    # per-kernel times: the same steps with an event pair around every launch
+    api.set_kernel_timing(True)
+    time_steps(steps, restore, one_step, stream)
+    kt = api.kernel_times()
+    api.set_kernel_timing(False)
+    kbytes = sum(M * N for M, N in wl.shapes) * (2 if wl.dtype == "bf16" else 4)
     nominal, executed, _ = workload_flops(wl.shapes, wl.steps)
     peaks, _ = measured_peaks()
     mean = statistics.mean(times)
@@ -300,6 +314,10 @@ def measure_workload(wl, dev, steps, warmup, graph=False):
            "tflops_nominal": round(nominal / (mean / 1e3) / 1e12, 2)}
     rec["executed_frac"] = {"burst": round(rec["tflops_executed"] / peaks["bf16_tflops"], 4),
                             "sustained": round(rec["tflops_executed"] / peaks["bf16_tflops_sustained"], 4)}
+    rec["host_us_per_call"] = round(host_us, 1)
+    rec["kernels"] = {k: {"ms_per_step": round(v[0] / steps, 4), "launches_per_step": round(v[1] / steps, 2)}
+                      for k, v in kt.items() if v[1]}
+    rec["norm_pass"] = norm_pass_record(kt, kbytes, steps, peaks.get("hbm_gbs"))
     if graph:
         g = torch.cuda.CUDAGraph()
         cap = torch.cuda.Stream(dev)

@@ -227,7 +227,12 @@ void build_layout(const int64_t *shapes, int count, int dtype, Layout &L) {
     const int64_t M = shapes[2 * i], N = shapes[2 * i + 1];
     if (M == 0 || N == 0) continue;
     const int64_t m = std::min(M, N), n = std::max(M, N);
-    if (resident_fits(m, n, dtype))
+    bool res = resident_fits(m, n, dtype);
+    if (res) {  // and one CTA's slice of it fits as laid out
+      const int c = resident_cluster(static_cast<int>(m), static_cast<int>(n));
+      res = resident_smem_bytes(static_cast<int>(m), resident_slice(static_cast<int>(n), c), dtype) <= kResidentSmemMax;
+    }
+    if (res)
       L.res.push_back(i);
     else
       order.push_back(i);

@@ -14,15 +14,12 @@
 //           order) and publishes it in its shared memory; after one cluster
 //           barrier every CTA adds the C partials in rank order through
 //           distributed shared memory (A, both triangles);
-//   square  B = b A + c A A: by every CTA for itself when it is small; when
-//           it has many 4 x 4 blocks each CTA computes the blocks it owns and
-//           stores them into every CTA of the cluster (a second barrier);
+//   square  B = b A + c A A, by every CTA for itself (m <= 64);
 //   apply   W_c' = a W_c + B W_c on the CTA's own columns, in column panels
 //           written back in place.
 // The partials are double-buffered across steps, so one cluster barrier per
-// step (two with a split square) orders every exchange. Remote shared memory
-// is read with all of a value's C loads in flight at once, and written by
-// plain remote stores. The first step folds the normalisation in
+// step orders every exchange. Remote shared memory is read with the loads of
+// several values in flight at once. The first step folds the normalisation in
 // (A = r^2 sum of partials, W_1 = r (a W + B W), r = 1 / (||Y||_F + eps)), so
 // the normalised input is never rounded; every later iterate is stored in the
 // working type (bf16 rounding to nearest even between steps, as on the
@@ -55,7 +52,8 @@ struct ResLayout {
     mp = (m + 3) & ~3;
     ld = ns;
     if ((ld / vec) % 2 == 0) ld += vec;  // an odd number of 16-byte units: rows spread over banks
-    ap = mp + 1;
+    ap = mp;  // fp32 rows of A, B, P: 16-byte aligned, an odd number of 16-byte units
+    if ((ap / 4) % 2 == 0) ap += 4;
     off_a = res_align16(static_cast<size_t>(mp) * ld * elt);
     off_b = res_align16(off_a + static_cast<size_t>(mp) * ap * 4);
     off_p0 = res_align16(off_b + static_cast<size_t>(mp) * ap * 4);
@@ -109,12 +107,6 @@ __device__ __forceinline__ float ld_cluster_f32(const float *local, int rank) {
 __device__ __forceinline__ int ld_cluster_i32(const int *local, int rank) {
   return static_cast<int>(ld_shared_cluster_u32(mapa_shared(smem_u32(local), static_cast<uint32_t>(rank))));
 }
-__device__ __forceinline__ void st_cluster_f32(float *local, int rank, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(mapa_shared(smem_u32(local), static_cast<uint32_t>(rank))),
-               "f"(v)
-               : "memory");
-}
-
 // Sum over the cluster's ranks, in rank order, of the float at `local`'s
 // offset in each CTA: the C remote loads are issued together, then added.
 template <int C>
@@ -127,11 +119,6 @@ __device__ __forceinline__ float cluster_sum(const float *local) {
   for (int c = 0; c < C; ++c) t += v[c];
   return t;
 }
-
-// Upper blocks of B at or above this many are split over the cluster's CTAs
-// (each computes the blocks it owns and stores them into every CTA); below
-// it every CTA computes all of B itself.
-constexpr int kSplitSquareBlocks = 32;
 
 // Barrier over the matrix's CTAs: the cluster, or just this CTA when C = 1.
 __device__ __forceinline__ void res_sync(int C) {
@@ -325,97 +312,70 @@ __global__ void __launch_bounds__(kResThreads, 1) ns_resident_kernel(const __gri
       Pc[(4 * bi + u) * ap + 4 * bj + v] = sum;
     }
     res_sync(C);  // every CTA's partial is published
-    // ---- A = gs * (sum of the partials in rank order), both triangles
-    for (int e = tid; e < nblk * 16; e += kResThreads) {
-      const int b = e >> 4, u = (e >> 2) & 3, v = e & 3;
-      int bi, bj;
-      upper_block(b, mb, bi, bj);
-      const int i = 4 * bi + u, j = 4 * bj + v;
-      if (bi < bj || u <= v) {
-        const float sum = gs * cluster_sum<C>(Pc + i * ap + j);
+    // ---- A = gs * (sum of the partials in rank order), both triangles; each
+    //      thread takes four entries at a time with all their remote loads in
+    //      flight together
+    for (int e0 = tid; e0 < nblk * 16; e0 += 4 * kResThreads) {
+      float v[4][C];
+      int at[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int e = e0 + q * kResThreads;
+        at[q] = -1;
+        if (e < nblk * 16) {
+          const int b = e >> 4, u = (e >> 2) & 3, w4 = e & 3;
+          int bi, bj;
+          upper_block(b, mb, bi, bj);
+          if (bi < bj || u <= w4) at[q] = (4 * bi + u) * ap + 4 * bj + w4;
+        }
+        const int src = at[q] < 0 ? 0 : at[q];
+#pragma unroll
+        for (int c = 0; c < C; ++c) v[q][c] = C > 1 ? ld_cluster_f32(Pc + src, c) : Pc[src];
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (at[q] < 0) continue;
+        float sum = 0.f;
+#pragma unroll
+        for (int c = 0; c < C; ++c) sum += v[q][c];
+        sum *= gs;
+        const int i = at[q] / ap, j = at[q] - i * ap;
         A[i * ap + j] = sum;
         A[j * ap + i] = sum;
       }
     }
     __syncthreads();
     // ---- square: B = b A + c A A on upper blocks (symmetric, so both
-    //      triangles). Many blocks: each CTA takes the blocks it owns (block b
-    //      belongs to rank b % C), the contraction split into slices of 4-row
-    //      groups summed in slice order, and stores them into every CTA of
-    //      the cluster; few blocks: every CTA computes all of B itself.
-    if (C > 1 && nblk >= kSplitSquareBlocks) {
-      const int own = (nblk - rank + C - 1) / C;
-      const int S2 = max(1, min(kResThreads / own, mb));
-      const int kq = (mb + S2 - 1) / S2;
-      if (tid < own * S2) {
-        const int ob = tid / S2, sl = tid - ob * S2;
-        int bi, bj;
-        upper_block(rank + ob * C, mb, bi, bj);
-        float c4[4][4] = {};
-        for (int k = 4 * sl * kq; k < 4 * min(mb, (sl + 1) * kq); ++k) {
-          float ar[4], ac[4];
+    //      triangles); (A A)[i, j] = sum_k A[i, k] A[j, k], rows read 4 k at a time
+    for (int b = tid; b < nblk; b += kResThreads) {
+      int bi, bj;
+      upper_block(b, mb, bi, bj);
+      float c4[4][4] = {};
+      for (int k = 0; k < 4 * mb; k += 4) {
+        float ar[4][4], ac[4][4];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            ar[u] = A[(4 * bi + u) * ap + k];
-            ac[u] = A[k * ap + 4 * bj + u];
-          }
+        for (int u = 0; u < 4; ++u) {
+          ld4(A + (4 * bi + u) * ap + k, ar[u]);
+          ld4(A + (4 * bj + u) * ap + k, ac[u]);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
           for (int u = 0; u < 4; ++u)
 #pragma unroll
-            for (int v = 0; v < 4; ++v) c4[u][v] = fmaf(ar[u], ac[v], c4[u][v]);
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-#pragma unroll
-          for (int v = 0; v < 4; ++v) part[(sl * own + ob) * 16 + u * 4 + v] = c4[u][v];
+            for (int v = 0; v < 4; ++v) c4[u][v] = fmaf(ar[u][kk], ac[v][kk], c4[u][v]);
       }
-      __syncthreads();
-      for (int e = tid; e < own * 16; e += kResThreads) {
-        const int ob = e >> 4, u = (e >> 2) & 3, v = e & 3;
-        int bi, bj;
-        upper_block(rank + ob * C, mb, bi, bj);
-        const int i = 4 * bi + u, j = 4 * bj + v;
-        if (bi < bj || u <= v) {
-          float sum = 0.f;
-          for (int sl = 0; sl < S2; ++sl) sum += part[(sl * own + ob) * 16 + u * 4 + v];
-          const float val = cb * A[i * ap + j] + cc * sum;
 #pragma unroll
-          for (int c = 0; c < C; ++c) {
-            st_cluster_f32(B + i * ap + j, c, val);
-            st_cluster_f32(B + j * ap + i, c, val);
-          }
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const int i = 4 * bi + u, j = 4 * bj + v;
+          const float val = cb * A[i * ap + j] + cc * c4[u][v];
+          B[i * ap + j] = val;
+          B[j * ap + i] = val;
         }
-      }
-      res_sync(C);  // every CTA's blocks of B have landed everywhere
-    } else {
-      for (int b = tid; b < nblk; b += kResThreads) {
-        int bi, bj;
-        upper_block(b, mb, bi, bj);
-        float c4[4][4] = {};
-        for (int k = 0; k < 4 * mb; ++k) {
-          float ar[4], ac[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            ar[u] = A[(4 * bi + u) * ap + k];
-            ac[u] = A[k * ap + 4 * bj + u];
-          }
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-#pragma unroll
-            for (int v = 0; v < 4; ++v) c4[u][v] = fmaf(ar[u], ac[v], c4[u][v]);
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const int i = 4 * bi + u, j = 4 * bj + v;
-            const float val = cb * A[i * ap + j] + cc * c4[u][v];
-            B[i * ap + j] = val;
-            B[j * ap + i] = val;
-          }
-      }
-      __syncthreads();
     }
+    __syncthreads();
     // ---- apply: W_c' = as (a W_c + B W_c), one column panel at a time
     for (int pc = 0; pc < nse; pc += panel) {
       const int rb = tid % mb, cbk = tid / mb;
@@ -423,15 +383,19 @@ __global__ void __launch_bounds__(kResThreads, 1) ns_resident_kernel(const __gri
       const bool active = tid < mb * (panel / 4) && j0 < nse;
       float o4[4][4] = {};
       if (active) {
-        for (int k = 0; k < 4 * mb; ++k) {
-          float br[4], xr[4];
+        for (int k = 0; k < 4 * mb; k += 4) {
+          float br[4][4];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) br[u] = B[(4 * rb + u) * ap + k];
-          ld4(w + k * ld + j0, xr);
+          for (int u = 0; u < 4; ++u) ld4(B + (4 * rb + u) * ap + k, br[u]);
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
+          for (int kk = 0; kk < 4; ++kk) {
+            float xr[4];
+            ld4(w + (k + kk) * ld + j0, xr);
 #pragma unroll
-            for (int v = 0; v < 4; ++v) o4[u][v] = fmaf(br[u], xr[v], o4[u][v]);
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+              for (int v = 0; v < 4; ++v) o4[u][v] = fmaf(br[u][kk], xr[v], o4[u][v]);
+          }
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {

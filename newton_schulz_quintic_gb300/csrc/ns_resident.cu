@@ -317,31 +317,34 @@ __global__ void __launch_bounds__(kResThreads, 1) ns_resident_kernel(const __gri
     //      flight together
     for (int e0 = tid; e0 < nblk * 16; e0 += 4 * kResThreads) {
       float v[4][C];
-      int at[4];
+      int ri[4], rj[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int e = e0 + q * kResThreads;
-        at[q] = -1;
+        ri[q] = -1;
+        rj[q] = 0;
         if (e < nblk * 16) {
           const int b = e >> 4, u = (e >> 2) & 3, w4 = e & 3;
           int bi, bj;
           upper_block(b, mb, bi, bj);
-          if (bi < bj || u <= w4) at[q] = (4 * bi + u) * ap + 4 * bj + w4;
+          if (bi < bj || u <= w4) {
+            ri[q] = 4 * bi + u;
+            rj[q] = 4 * bj + w4;
+          }
         }
-        const int src = at[q] < 0 ? 0 : at[q];
+        const int src = ri[q] < 0 ? 0 : ri[q] * ap + rj[q];
 #pragma unroll
         for (int c = 0; c < C; ++c) v[q][c] = C > 1 ? ld_cluster_f32(Pc + src, c) : Pc[src];
       }
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        if (at[q] < 0) continue;
+        if (ri[q] < 0) continue;
         float sum = 0.f;
 #pragma unroll
         for (int c = 0; c < C; ++c) sum += v[q][c];
         sum *= gs;
-        const int i = at[q] / ap, j = at[q] - i * ap;
-        A[i * ap + j] = sum;
-        A[j * ap + i] = sum;
+        A[ri[q] * ap + rj[q]] = sum;
+        A[rj[q] * ap + ri[q]] = sum;
       }
     }
     __syncthreads();
@@ -352,18 +355,18 @@ __global__ void __launch_bounds__(kResThreads, 1) ns_resident_kernel(const __gri
       upper_block(b, mb, bi, bj);
       float c4[4][4] = {};
       for (int k = 0; k < 4 * mb; k += 4) {
-        float ar[4][4], ac[4][4];
+        float ar[4][4];  // A[4 bi + u, k .. k + 3]: the warp's lanes share bi (broadcast)
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          ld4(A + (4 * bi + u) * ap + k, ar[u]);
-          ld4(A + (4 * bj + u) * ap + k, ac[u]);
-        }
+        for (int u = 0; u < 4; ++u) ld4(A + (4 * bi + u) * ap + k, ar[u]);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
+        for (int kk = 0; kk < 4; ++kk) {
+          float ac[4];   // A[k + kk, 4 bj .. 4 bj + 3] = A[4 bj + v, k + kk]: contiguous across lanes
+          ld4(A + (k + kk) * ap + 4 * bj, ac);
 #pragma unroll
           for (int u = 0; u < 4; ++u)
 #pragma unroll
-            for (int v = 0; v < 4; ++v) c4[u][v] = fmaf(ar[u][kk], ac[v][kk], c4[u][v]);
+            for (int v = 0; v < 4; ++v) c4[u][v] = fmaf(ar[u][kk], ac[v], c4[u][v]);
+        }
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u)
@@ -383,19 +386,14 @@ __global__ void __launch_bounds__(kResThreads, 1) ns_resident_kernel(const __gri
       const bool active = tid < mb * (panel / 4) && j0 < nse;
       float o4[4][4] = {};
       if (active) {
-        for (int k = 0; k < 4 * mb; k += 4) {
-          float br[4][4];
+        for (int k = 0; k < 4 * mb; ++k) {
+          float br[4], xr[4];
+          ld4(B + k * ap + 4 * rb, br);  // B[k, 4 rb + u] = B[4 rb + u, k]: contiguous across lanes
+          ld4(w + k * ld + j0, xr);      // the lanes of one column block share it (broadcast)
 #pragma unroll
-          for (int u = 0; u < 4; ++u) ld4(B + (4 * rb + u) * ap + k, br[u]);
+          for (int u = 0; u < 4; ++u)
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            float xr[4];
-            ld4(w + (k + kk) * ld + j0, xr);
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-#pragma unroll
-              for (int v = 0; v < 4; ++v) o4[u][v] = fmaf(br[u][kk], xr[v], o4[u][v]);
-          }
+            for (int v = 0; v < 4; ++v) o4[u][v] = fmaf(br[u], xr[v], o4[u][v]);
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {

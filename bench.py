@@ -290,6 +290,14 @@ def measure_workload(wl, dev, steps, warmup, graph=False):
     times = time_steps(steps, restore, one_step, stream)
     if api.get_status() != 0:
         raise RuntimeError(f"device status word reports a timeout on {wl.name}")
+    # the same calls with their arguments marshalled once (api.PreparedBatch)
+    prepared = [api.PreparedBatch(work[sl], steps=wl.steps) for sl in slices]
+
+    def one_step_prepared():
+        for pb in prepared:
+            pb()
+
+    ptimes = time_steps(steps, restore, one_step_prepared, stream)
     # host time of a call (argument marshalling, planning, launches), measured
     # back to back without waiting for the GPU
     torch.cuda.synchronize()
@@ -314,6 +322,8 @@ def measure_workload(wl, dev, steps, warmup, graph=False):
            "tflops_nominal": round(nominal / (mean / 1e3) / 1e12, 2)}
     rec["executed_frac"] = {"burst": round(rec["tflops_executed"] / peaks["bf16_tflops"], 4),
                             "sustained": round(rec["tflops_executed"] / peaks["bf16_tflops_sustained"], 4)}
+    rec["ms_per_step_prepared"] = round(statistics.mean(ptimes), 4)
+    rec["ms_per_step_prepared_median"] = round(statistics.median(ptimes), 4)
     rec["host_us_per_call"] = round(host_us, 1)
     rec["kernels"] = {k: {"ms_per_step": round(v[0] / steps, 4), "launches_per_step": round(v[1] / steps, 2)}
                       for k, v in kt.items() if v[1]}

@@ -180,6 +180,34 @@ def orthogonalize_batched(mats, steps: int = 5, coeffs=None, eps: float | None =
         raise NSError(rc, "ns_orthogonalize_batched")
 
 
+class PreparedBatch:
+    """A batch whose arguments are marshalled once: calling it runs
+    ns_orthogonalize_batched on the same matrices with the same steps and
+    coefficients, passing on the device pointers and shapes built when it was
+    made. For callers that orthogonalize the same buffers every optimizer step,
+    where per-call argument marshalling would otherwise be a noticeable share
+    of a small batch's time. The tensors must keep their storage (the same
+    data_ptr) for as long as the batch is used; it holds references to them."""
+
+    def __init__(self, mats, steps: int = 5, coeffs=None):
+        import torch
+        self.mats = list(mats)
+        self.code = _check(self.mats, want_cuda=True)
+        self.steps = int(steps)
+        self.device = self.mats[0].device if self.mats else torch.device("cuda")
+        self._ptrs, self._shapes, self._co = _marshal(self.mats, coeffs)
+        self._args = (_ptr(self._ptrs), _ptr(self._shapes), len(self.mats), self.steps, self._co, self.code)
+
+    def __call__(self, stream=None) -> None:
+        import torch
+        if self.code is None:
+            return
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        rc = load_library().ns_orthogonalize_batched(*self._args, ctypes.c_void_p(s.cuda_stream))
+        if rc != 0:
+            raise NSError(rc, "ns_orthogonalize_batched")
+
+
 def orthogonalize_batched_schedule(mats, table, stream=None) -> None:
     """In-place Newton-Schulz with a per-step coefficient table: ``table`` is a
     sequence of (a, b, c) triples, one per step (at most 32 steps)."""

@@ -18,6 +18,8 @@ Two independent computations live here:
 * ``svd_twin`` -- the closed form of the same map through LAPACK's SVD: every
   step is an odd matrix polynomial, so it keeps the singular vectors and maps
   each singular value through f(s) = a s + b s^3 + c s^5.
+* ``muon_update`` -- the momentum step before the orthogonalization and the
+  scaled update after it, with every constant a parameter.
 
 The pages this follows ("Fix megabatch_orthogonalize_async hang on empty FSDP2
 shards", "Balance LayerWise optimizer shards by Newton-Schulz cost, not
@@ -255,6 +257,20 @@ def orthogonalize_batched(mats, steps: int = DEFAULT_STEPS, coeffs=DEFAULT_COEFF
                           eps: float = DEFAULT_EPS) -> list:
     """The batched form: each matrix of the list independently."""
     return [orthogonalize(X, steps, coeffs, eps) for X in mats]
+
+
+def muon_update(G, Mom, mu: float, nesterov: bool, scale: float, steps: int = DEFAULT_STEPS,
+                coeffs=DEFAULT_COEFFS, eps: float = DEFAULT_EPS):
+    """The optimizer step around the orthogonalization, in fp64, every constant
+    a parameter (the dion page's "Summary" names Muon, NorMuon and Dion2 as the
+    callers of the megabatch Newton-Schulz; the pages do not print their
+    updates): the momentum buffer becomes Mom' = mu * Mom + G; the matrix
+    orthogonalized is X = G + mu * Mom' with Nesterov momentum, else X = Mom';
+    the update is scale * NS(X). Returns (Mom', update) as fp64 arrays."""
+    g = to_f64(G)
+    m_new = float(mu) * to_f64(Mom) + g
+    x = g + float(mu) * m_new if nesterov else m_new
+    return m_new, float(scale) * orthogonalize(x, steps, coeffs, eps)
 
 
 def frobenius(X) -> float:

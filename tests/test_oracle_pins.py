@@ -333,3 +333,57 @@ def test_fp8_operand_quantisers():
             scale = 2.0 ** np.ceil(np.log2(amax / 448.0))
             assert np.max(np.abs(qb)) <= 448.0 * scale
             assert np.all(np.abs(qb - blk) <= np.maximum(np.abs(blk) * 2.0 ** -4, scale * 2.0 ** -10) + 1e-300)
+
+
+# ------------------------------------------------------------ the optimizer step around it
+
+def _rel(a, b):
+    return float(np.linalg.norm(a - b) / np.linalg.norm(b))
+
+
+def test_muon_update_without_momentum_is_scaled_newton_schulz():
+    # mu = 0: the momentum buffer becomes the gradient and the update is
+    # scale times the (separately pinned) Newton-Schulz of the gradient
+    g = np.random.default_rng(40).standard_normal((12, 30))
+    m0 = np.random.default_rng(41).standard_normal((12, 30))
+    for nesterov in (False, True):
+        m1, upd = oracle.muon_update(g, m0, 0.0, nesterov, 0.7)
+        assert np.array_equal(m1, g)
+        assert np.allclose(upd, 0.7 * oracle.orthogonalize(g), rtol=0, atol=1e-14)
+
+
+def test_muon_momentum_is_a_geometric_series():
+    # a constant gradient from a zero buffer: after k steps the buffer is
+    # G (1 - mu^k) / (1 - mu); every update is scale * NS(G) because
+    # Newton-Schulz does not see the input's scale (up to eps)
+    g = np.random.default_rng(42).standard_normal((10, 24))
+    mu = 0.9
+    m = np.zeros_like(g)
+    ref = oracle.orthogonalize(g)
+    for k in range(1, 6):
+        m, upd = oracle.muon_update(g, m, mu, False, 1.5)
+        assert np.allclose(m, g * (1 - mu ** k) / (1 - mu), rtol=1e-14, atol=1e-14)
+        assert _rel(upd, 1.5 * ref) < 1e-6
+
+
+def test_muon_nesterov_input():
+    # Nesterov: X = G + mu (mu M + G) = (1 + mu) G + mu^2 M
+    rng = np.random.default_rng(43)
+    g, m0 = rng.standard_normal((16, 40)), rng.standard_normal((16, 40))
+    mu = 0.95
+    m1, upd = oracle.muon_update(g, m0, mu, True, 1.0)
+    assert np.allclose(m1, mu * m0 + g, rtol=1e-15, atol=1e-15)
+    x = (1 + mu) * g + mu * mu * m0
+    assert _rel(upd, oracle.orthogonalize(x)) < 1e-12
+    # without Nesterov the buffer itself is orthogonalized
+    _, plain = oracle.muon_update(g, m0, mu, False, 1.0)
+    assert _rel(plain, oracle.orthogonalize(mu * m0 + g)) < 1e-12
+    assert _rel(plain, upd) > 1e-3           # the two inputs differ, so the updates do
+
+
+def test_muon_update_scale_is_linear():
+    rng = np.random.default_rng(44)
+    g, m0 = rng.standard_normal((8, 20)), rng.standard_normal((8, 20))
+    _, u1 = oracle.muon_update(g, m0, 0.5, True, 1.0)
+    _, u3 = oracle.muon_update(g, m0, 0.5, True, -3.0)
+    assert np.allclose(u3, -3.0 * u1, rtol=1e-15, atol=1e-15)

@@ -149,6 +149,34 @@ int ns_orthogonalize_batched_noalloc(void *const *X, const int64_t *shapes, int 
                                      const float *coeffs, int dtype, void *stream);
 
 /*
+ * ns_muon_update_batched -- one optimizer step around the orthogonalization,
+ * for `count` matrices: the momentum step, Newton-Schulz and a scaled write
+ * of the result. The dion page's "Summary" names Muon, NorMuon and Dion2 as
+ * the optimizers that run the megabatch Newton-Schulz on momentum matrices;
+ * the pages do not print their updates, so every constant here is a
+ * parameter. For each matrix i, with every buffer M x N row-major of `dtype`
+ * on the current device:
+ *     Mom[i] <- mu * Mom[i] + G[i]                       (stored in Mom[i])
+ *     X      <- G[i] + mu * Mom[i]   if nesterov, else Mom[i]
+ *     Out[i] <- scale * NS(X)         (NS as ns_orthogonalize_batched, eps 1e-7)
+ *   G       host array of count device pointers: gradients, read only
+ *   Mom     host array of count device pointers: momentum buffers, updated
+ *   Out     host array of count device pointers: where the update is written;
+ *           Out[i] may be G[i] itself (the gradient buffer is overwritten)
+ *   shapes, count, steps, coeffs, dtype, stream: as ns_orthogonalize_batched
+ *   mu, scale  finite floats; nesterov 0 or 1.
+ * One element-wise kernel does the momentum step and writes X into Out (bf16:
+ * Mom and X rounded to nearest even, arithmetic in fp32); the Newton-Schulz
+ * call then works on Out in place, and `scale` is applied inside its last
+ * step before the final rounding. Buffers of the batch must not overlap,
+ * except Out[i] == G[i] (NS_EINVAL otherwise, before anything runs). Other
+ * returns as ns_orthogonalize_batched.
+ */
+int ns_muon_update_batched(void *const *G, void *const *Mom, void *const *Out, const int64_t *shapes,
+                           int count, int steps, const float *coeffs, float mu, int nesterov,
+                           float scale, int dtype, void *stream);
+
+/*
  * ns_cost -- Newton-Schulz cost of an M x N matrix, max(M,N) * min(M,N)^2
  * (second page, "Changes" item 1: the dominant term of the orthogonalization).
  * Returns -1 if M or N is negative.
@@ -225,9 +253,10 @@ int64_t ns_num_workspace_allocations(void);
  * them in place; fp32 the sums and extents), 1 norm finish (bf16: the
  * per-matrix scale from the tile sums), 2 gram, 3 square, 4 apply,
  * 5 resident, 6 gemm (the tensor-core kernel running every step and phase of
- * a call in one launch), 7 prep (fp32: the normalising copy), the total
- * milliseconds into ms[k] and the launch count into launches[k] for k < n
- * (n <= 8). Returns NS_OK or NS_EINVAL / NS_ECUDA.
+ * a call in one launch), 7 prep (fp32: the normalising copy), 8 momentum
+ * (ns_muon_update_batched's element-wise step), the total milliseconds into
+ * ms[k] and the launch count into launches[k] for k < n (n <= 9). Returns
+ * NS_OK or NS_EINVAL / NS_ECUDA.
  */
 int ns_set_kernel_timing(int enable);
 int ns_get_kernel_times(double *ms, int64_t *launches, int n);

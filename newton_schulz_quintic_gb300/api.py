@@ -82,6 +82,9 @@ def load_library() -> ctypes.CDLL:
         lib.ns_selftest_wait_timeout.argtypes = [i32, vp]
         lib.ns_selftest_dependency_timeout.restype = i32
         lib.ns_selftest_dependency_timeout.argtypes = [i32, vp]
+        lib.ns_muon_update_batched.restype = i32
+        lib.ns_muon_update_batched.argtypes = [vp, vp, vp, vp, i32, i32, vp, ctypes.c_float, i32,
+                                               ctypes.c_float, i32, vp]
         lib.ns_num_workspace_allocations.restype = i64
         lib.ns_num_workspace_allocations.argtypes = []
         lib.ns_plan_shards.restype = i32
@@ -178,6 +181,37 @@ def orthogonalize_batched(mats, steps: int = 5, coeffs=None, eps: float | None =
                                                  workspace.numel(), sp)
     if rc != 0:
         raise NSError(rc, "ns_orthogonalize_batched")
+
+
+def muon_update_batched(grads, moms, outs, mu: float = 0.95, nesterov: bool = True, scale: float = 1.0,
+                        steps: int = 5, coeffs=None, stream=None) -> None:
+    """One optimizer step around the orthogonalization (ns_muon_update_batched):
+    for every matrix, moms[i] <- mu * moms[i] + grads[i] (in place), then
+    outs[i] <- scale * NS(grads[i] + mu * moms[i]) with Nesterov momentum, else
+    scale * NS(moms[i]). outs[i] may be grads[i] itself. Three lists of CUDA
+    tensors of one dtype, matching shapes, contiguous."""
+    import torch
+    lib = load_library()
+    grads, moms, outs = list(grads), list(moms), list(outs)
+    if not (len(grads) == len(moms) == len(outs)):
+        raise ValueError("grads, moms and outs must have the same length")
+    code = _check(grads + moms + outs, want_cuda=True)
+    if code is None:
+        return
+    for g, m, o in zip(grads, moms, outs):
+        if g.shape != m.shape or g.shape != o.shape:
+            raise ValueError("a matrix's gradient, momentum and output must have one shape")
+    dev = grads[0].device
+    with torch.cuda.device(dev):
+        s = stream if stream is not None else torch.cuda.current_stream(dev)
+        pg, shapes, co = _marshal(grads, coeffs)
+        pm, _, _ = _marshal(moms, None)
+        po, _, _ = _marshal(outs, None)
+        rc = lib.ns_muon_update_batched(_ptr(pg), _ptr(pm), _ptr(po), _ptr(shapes), len(grads), int(steps), co,
+                                        float(mu), 1 if nesterov else 0, float(scale), code,
+                                        ctypes.c_void_p(s.cuda_stream))
+    if rc != 0:
+        raise NSError(rc, "ns_muon_update_batched")
 
 
 class PreparedBatch:
@@ -300,7 +334,8 @@ def num_kernel_launches() -> int:
     return int(load_library().ns_num_kernel_launches())
 
 
-KERNEL_KINDS = ("norm_pass", "norm_finish", "gram", "square", "apply", "resident", "gemm", "prep")
+KERNEL_KINDS = ("norm_pass", "norm_finish", "gram", "square", "apply", "resident", "gemm", "prep",
+                "momentum")
 
 
 def set_kernel_timing(enable: bool) -> None:

@@ -458,8 +458,9 @@ int ensure_ws(CachedWs &c, size_t bytes, cudaStream_t s) {
 // ------------------------------------------------------------ kernel timing
 // kinds: 0 norm pass (the read of the caller's matrices), 1 norm finish (bf16:
 // per-matrix scale), 2 gram, 3 square, 4 apply, 5 resident, 6 gemm (one
-// launch running every step and phase), 7 prep (fp32: the normalising copy)
-constexpr int kKinds = 8;
+// launch running every step and phase), 7 prep (fp32: the normalising copy),
+// 8 momentum (ns_muon_update_batched's element-wise step)
+constexpr int kKinds = 9;
 
 // How the tensor-core path is launched (ns_set_gemm_schedule): one launch per
 // step and phase (default) or one launch per call with per-matrix counters.
@@ -492,6 +493,7 @@ int timed(int kind, cudaStream_t s, F &&fn) {
 struct RunOpts {
   uint64_t wait_limit_ns = kWaitLimitNs;
   bool hold_signals = false;
+  float out_scale = 1.0f;  // the result is multiplied by it before it is written
 };
 
 // co: one (a, b, c) triple for every step (table == false) or a steps x 3 table
@@ -509,6 +511,7 @@ int execute(const Layout &L, uint8_t *ws, int steps, const float *co, bool table
     for (int k = 0; k < (table ? steps : 1); ++k)
       for (int u = 0; u < 3; ++u) rp.coef[k][u] = co[3 * k + u];
     rp.eps = eps;
+    rp.out_scale = opt.out_scale;
     if (timed(5, s, [&] { return launch_resident(rp, g.smem, s); })) return NS_ECUDA;
   }
   if (L.big.empty()) return NS_OK;
@@ -528,6 +531,7 @@ int execute(const Layout &L, uint8_t *ws, int steps, const float *co, bool table
   pp.to_user = steps == 0;
   pp.tile_partials = reinterpret_cast<float *>(ws + L.off_tilepart);
   pp.rscale = reinterpret_cast<float *>(ws + L.off_rscale);
+  pp.out_scale = opt.out_scale;
   // bf16 with steps: one pass sums Y (and copies it unscaled into the first
   // iterate buffer where step 0 cannot read Y itself); the first step's
   // epilogues apply 1/(||Y|| + eps). Otherwise: norm, then a scaled copy.
@@ -555,6 +559,7 @@ int execute(const Layout &L, uint8_t *ws, int steps, const float *co, bool table
     tp.done = done;
     tp.rscale = pp.rscale;
     tp.wait_limit_ns = opt.wait_limit_ns;
+    tp.out_scale = opt.out_scale;
     tp.hold_signals = opt.hold_signals ? 1 : 0;
     tp.ncoef = table ? steps : 1;
     for (int k = 0; k < (table ? steps : 1); ++k)
@@ -583,6 +588,7 @@ int execute(const Layout &L, uint8_t *ws, int steps, const float *co, bool table
     return NS_OK;
   }
   PhaseParams ph{};
+  ph.out_scale = opt.out_scale;
   ph.mats = mats;
   ph.ext = ext;
   ph.status = di->status;
@@ -706,6 +712,65 @@ int ns_orthogonalize_batched_sched(void *const *X, const int64_t *shapes, int co
                                    const float *coeff_table, int dtype, void *stream) {
   return run(X, shapes, count, steps, coeff_table, 1e-7f, dtype, nullptr, 0, static_cast<cudaStream_t>(stream), 0,
              true);
+}
+
+int ns_muon_update_batched(void *const *G, void *const *Mom, void *const *Out, const int64_t *shapes, int count,
+                           int steps, const float *coeffs, float mu, int nesterov, float scale, int dtype,
+                           void *stream) {
+  int rc = validate(G, shapes, count, steps, dtype, true);
+  if (!rc) rc = validate(Mom, shapes, count, steps, dtype, true);
+  if (!rc) rc = validate(Out, shapes, count, steps, dtype, true);
+  if (rc) return rc;
+  if (!std::isfinite(mu) || !std::isfinite(scale) || (nesterov != 0 && nesterov != 1)) return NS_EINVAL;
+  if (count == 0) return NS_OK;
+  // the three buffers of every matrix, and of different matrices, must not
+  // overlap; the one exception is an output buffer that is the matrix's own
+  // gradient buffer (the update written over the gradient)
+  {
+    const size_t elt = dtype == NS_BF16 ? 2 : 4;
+    std::vector<std::pair<uintptr_t, uintptr_t>> r;
+    r.reserve(3 * static_cast<size_t>(count));
+    for (int i = 0; i < count; ++i) {
+      const int64_t n = shapes[2 * i] * shapes[2 * i + 1];
+      if (n == 0) continue;
+      const uintptr_t bytes = static_cast<uintptr_t>(n) * elt;
+      for (void *const *arr : {G, Mom, Out}) {
+        if (arr == Out && Out[i] == G[i]) continue;
+        const uintptr_t b = reinterpret_cast<uintptr_t>(arr[i]);
+        r.emplace_back(b, b + bytes);
+      }
+    }
+    std::sort(r.begin(), r.end());
+    for (size_t k = 1; k < r.size(); ++k)
+      if (r[k].first < r[k - 1].second) return NS_EINVAL;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int sms = 0;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    DevInfo *di = nullptr;
+    rc = device_info(&di);
+    if (rc) return rc;
+    sms = di->sms;
+  }
+  for (int k0 = 0; k0 < count; k0 += kMomChunk) {
+    MomentumParams mp{};
+    mp.mu = mu;
+    mp.nesterov = nesterov;
+    for (int i = k0; i < std::min(count, k0 + kMomChunk); ++i) {
+      const int64_t n = shapes[2 * i] * shapes[2 * i + 1];
+      if (n == 0) continue;
+      mp.g[mp.count] = G[i];
+      mp.mom[mp.count] = Mom[i];
+      mp.out[mp.count] = Out[i];
+      mp.numel[mp.count] = n;
+      ++mp.count;
+    }
+    if (timed(8, s, [&] { return launch_momentum(mp, dtype, sms, s); })) return NS_ECUDA;
+  }
+  RunOpts opt;
+  opt.out_scale = scale;
+  return run(Out, shapes, count, steps, coeffs, 1e-7f, dtype, nullptr, 0, s, 0, false, opt);
 }
 
 size_t ns_workspace_bytes(const int64_t *shapes, int count, int dtype) {

@@ -97,6 +97,7 @@ struct PhaseParams {
   float ca, cb, cc;      // coefficients a, b, c
   int step;              // 0-based step (selects xt ping-pong buffer)
   int final_step;        // 1 on the last step: write the caller's matrix
+  float out_scale;       // the last step's result is multiplied by it before the write
 };
 
 // Parameters of the tensor-core GEMM kernel. Its work is the item sequence
@@ -120,6 +121,7 @@ struct TcParams {
   int *done;            // per matrix completion counter (zeroed by the host per call)
   const float *rscale;  // per matrix 1 / (||Y||_F + eps): step 0 scales gram by its square and apply by it
   uint64_t wait_limit_ns;  // limit of every bounded wait in the kernel
+  float out_scale;      // the last step's result is multiplied by it before the write
   int hold_signals;     // self-test only: never publish completions, so dependent items time out
   int ncoef;            // 1: coef[0] for every step; else coef[step]
   float coef[kMaxTableSteps][3];
@@ -137,6 +139,7 @@ struct PrepParams {
   int to_user;           // 1: write the normalised matrix back to the caller (steps == 0)
   float *tile_partials;  // bf16 path: one sum of squares per 64x64 tile of W
   float *rscale;         // bf16 path: per matrix 1 / (||Y||_F + eps)
+  float out_scale;       // to_user: the normalised matrix is multiplied by it
 };
 
 struct ResParams {
@@ -148,6 +151,19 @@ struct ResParams {
   int ncoef;                        // 1: coef[0] for every step; else coef[step]
   float coef[kMaxTableSteps][3];    // (a, b, c)
   float eps;
+  float out_scale;                  // the result is multiplied by it before the write
+};
+
+// Momentum step of ns_muon_update_batched: up to kMomChunk matrices per launch.
+constexpr int kMomChunk = 64;
+struct MomentumParams {
+  const void *g[kMomChunk];
+  void *mom[kMomChunk];
+  void *out[kMomChunk];
+  int64_t numel[kMomChunk];
+  int count;
+  float mu;
+  int nesterov;
 };
 
 constexpr int kNormBlocks = 128;  // partial-sum blocks per matrix
@@ -177,6 +193,7 @@ int launch_simt_phase(int phase, const PhaseParams &p, cudaStream_t s);
 int launch_tc(const TcParams &p, int max_ctas, cudaStream_t s);
 int tc_smem_bytes();
 int launch_wait_probe(int *status, uint64_t limit_ns, int *gave_up, cudaStream_t s);
+int launch_momentum(const MomentumParams &p, int dtype, int sms, cudaStream_t s);
 int resident_smem_bytes(int m, int ns, int dtype);  // one CTA of a matrix split into ns-column slices
 int resident_cluster(int m, int n);                 // CTAs per matrix of the resident kernel
 int resident_slice(int n, int cluster);             // their slice width

@@ -274,7 +274,8 @@ __global__ void __launch_bounds__(kResThreads, 1) ns_resident_kernel(const __gri
   for (int step = 0; step < p.steps && meff > 0; ++step) {
     const float *co = p.coef[p.ncoef == 1 ? 0 : step];
     const float ca = co[0], cb = co[1], cc = co[2];
-    const float gs = step == 0 ? r * r : 1.f, as = step == 0 ? r : 1.f;
+    const float gs = step == 0 ? r * r : 1.f, as0 = step == 0 ? r : 1.f;
+    const float as = step == p.steps - 1 ? as0 * p.out_scale : as0;  // the last step applies the output scale
     float *Pc = (step & 1) ? P1 : P0;
     // ---- gram: partial 4 x 4 blocks of W_c W_c^T over k-slices of this CTA's columns
     if (tid < nblk * S) {
@@ -414,7 +415,8 @@ __global__ void __launch_bounds__(kResThreads, 1) ns_resident_kernel(const __gri
     }
   }
   if (p.steps == 0) {  // normalisation only
-    for (int e = tid; e < meff * ld; e += kResThreads) w[e] = Elem<DT>::from_f(Elem<DT>::to_f(w[e]) * r);
+    const float rs = r * p.out_scale;
+    for (int e = tid; e < meff * ld; e += kResThreads) w[e] = Elem<DT>::from_f(Elem<DT>::to_f(w[e]) * rs);
   }
   res_sync(C);  // no CTA leaves while another may still read its shared memory
   __syncthreads();

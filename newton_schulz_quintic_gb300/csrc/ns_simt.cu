@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(256) ns_prep_kernel(PrepParams p) {
     if (tid == 0) s_denom = 1.0f / (sqrtf(v) + p.eps);  // 1 / (||Y||_F + eps)
   }
   __syncthreads();
-  const float inv = s_denom;
+  const float inv = p.to_user ? s_denom * p.out_scale : s_denom;
   if (vec) {
 #pragma unroll
     for (int k = 0; k < PER; ++k) {
@@ -317,7 +317,8 @@ __global__ void __launch_bounds__(256) ns_simt_gemm_kernel(PhaseParams p) {
       } else {
         if (r < n && c < m) {
           const float *xt = static_cast<const float *>(d.xt[cur]);
-          const float out = p.ca * xt[static_cast<size_t>(r) * pm + c] + val;
+          const float out0 = p.ca * xt[static_cast<size_t>(r) * pm + c] + val;
+          const float out = p.final_step ? out0 * p.out_scale : out0;
           if (!p.final_step) {
             static_cast<float *>(d.xt[cur ^ 1])[static_cast<size_t>(r) * pm + c] = out;
             static_cast<float *>(d.x)[static_cast<size_t>(c) * pn + r] = out;

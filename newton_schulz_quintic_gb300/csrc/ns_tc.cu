@@ -287,7 +287,8 @@ struct StepCtx {
   int step;
   int final_step;   // apply writes the caller's matrix
   float ca, cb, cc;
-  float gs, as;     // step 0 folds the normalisation in: A *= r^2, W' *= r (else 1)
+  float gs, as;     // step 0 folds the normalisation in: A *= r^2, W' *= r (else 1);
+                    // the last step also applies the output scale
 };
 
 __device__ __forceinline__ StepCtx step_ctx(const TcParams &p, int step, int mat) {
@@ -300,7 +301,7 @@ __device__ __forceinline__ StepCtx step_ctx(const TcParams &p, int step, int mat
   c.cc = co[2];
   const float r = (step == 0 && p.rscale) ? p.rscale[mat] : 1.0f;
   c.gs = r * r;
-  c.as = r;
+  c.as = c.final_step ? r * p.out_scale : r;
   return c;
 }
 

@@ -185,3 +185,29 @@ def test_schedule_rejects_bad_tables_before_launch(lib):
 def test_gemm_schedule_setter(lib):
     assert lib.ns_set_gemm_schedule(5) == -1
     assert lib.ns_set_gemm_schedule(1) == 0 and lib.ns_set_gemm_schedule(0) == 0
+
+
+@pytest.mark.skipif(_has_gpu(), reason="uses fake device pointers: only run where nothing can launch")
+def test_muon_update_validation_before_launch(lib):
+    # every refusal below happens before any launch: arguments, then the
+    # overlap of the three buffers, then the device
+    P, S = ctypes.c_void_p, ctypes.c_int64
+    f = lib.ns_muon_update_batched
+    shp = (S * 2)(4, 8)                            # 64 bytes in bf16
+    g, m, o = (P * 1)(0x100000), (P * 1)(0x200000), (P * 1)(0x300000)
+    c = ctypes.c_float
+    assert f(g, m, o, shp, 0, 5, None, c(0.9), 1, c(1.0), 1, None) == 0          # empty batch
+    assert f(None, m, o, shp, 1, 5, None, c(0.9), 1, c(1.0), 1, None) == -1      # null array
+    assert f(g, (P * 1)(0x200001), o, shp, 1, 5, None, c(0.9), 1, c(1.0), 1, None) == -2  # misaligned
+    assert f(g, m, o, shp, 1, 5, None, c(float("nan")), 1, c(1.0), 1, None) == -1
+    assert f(g, m, o, shp, 1, 5, None, c(0.9), 1, c(float("inf")), 1, None) == -1
+    assert f(g, m, o, shp, 1, 5, None, c(0.9), 2, c(1.0), 1, None) == -1         # nesterov not 0/1
+    assert f(g, g, o, shp, 1, 5, None, c(0.9), 1, c(1.0), 1, None) == -1         # momentum is the gradient
+    assert f(g, m, m, shp, 1, 5, None, c(0.9), 1, c(1.0), 1, None) == -1         # output is the momentum
+    assert f(g, m, (P * 1)(0x200020), shp, 1, 5, None, c(0.9), 1, c(1.0), 1, None) == -1  # partial overlap
+    two = (S * 4)(4, 8, 4, 8)
+    assert f((P * 2)(0x100000, 0x110000), (P * 2)(0x200000, 0x210000), (P * 2)(0x110000, 0x100000), two, 2, 5,
+             None, c(0.9), 1, c(1.0), 1, None) == -1                            # output is another gradient
+    # the output written over the gradient is allowed: the call gets as far as the device
+    assert f(g, m, g, shp, 1, 5, None, c(0.9), 1, c(1.0), 1, None) == -6
+    assert f(g, m, o, shp, 1, 5, None, c(0.9), 0, c(1.0), 1, None) == -6

@@ -176,6 +176,12 @@ __device__ __forceinline__ void tma_load_2d_pair(void *smem_dst, const void *map
       : "memory");
 }
 
+// Bring a TMA descriptor (in global memory) into the descriptor cache ahead
+// of the copies that use it.
+__device__ __forceinline__ void prefetch_tensormap(const void *map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
 // ---------------------------------------------------------------- clusters
 // shared::cluster address of the variable at shared::cta address `addr` in CTA `rank`.
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {

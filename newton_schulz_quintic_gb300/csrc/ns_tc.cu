@@ -237,6 +237,26 @@ __device__ __forceinline__ ItemPlan plan_item(const MatDesc &d, int step, int ph
   return pl;
 }
 
+// Prefetch the tensor maps an item of (step, phase) of matrix d reads, so a
+// tile start does not wait for its descriptors (consecutive items of a
+// cluster often belong to different matrices).
+__device__ __forceinline__ void prefetch_item_maps(const MatDesc &d, int step, int phase, int transposed,
+                                                   int direct) {
+  const bool y = step == 0 && direct;
+  const void *src_k = y ? &d.tm_y : &d.tm_s[step & 1];
+  const void *src_mn = y ? &d.tm_y_mn : &d.tm_s_mn[step & 1];
+  if (phase == 0) {
+    prefetch_tensormap(transposed ? src_mn : src_k);
+  } else if (phase == 1) {
+    prefetch_tensormap(&d.tm_a);
+    prefetch_tensormap(&d.tm_a_mn);
+  } else {
+    prefetch_tensormap(&d.tm_b);
+    prefetch_tensormap(&d.tm_b_mn);
+    prefetch_tensormap(transposed ? src_k : src_mn);
+  }
+}
+
 // TMA of one operand share: 128 tile rows [mn0, mn0 + 128) by K [k0, k0 + 64).
 // K-major: one box of 128 rows. MN-major: box rows are K indices and the tile
 // index runs along them, 64 per box row, so two 64 x 64 boxes 8 KB apart.
@@ -643,6 +663,8 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
         int step, phase, direct;
         TileInfo ti;
         pipe_take(p, nclusters, q, step, phase, ti, direct);
+        if (q.g < p.g_end && elect_one()) prefetch_item_maps(p.mats[q.tl.mat], q.step, q.phase, q.tr, q.direct);
+        __syncwarp();
         if (ti.skip) continue;
         if (p.wait) {
           // operands come from earlier phases of this matrix, written by

@@ -33,7 +33,10 @@
  *  - CUDA graphs: once ns_orthogonalize_batched (or _sched) has run with the
  *    same matrices, shapes, steps, coefficients and stream, a repeat call
  *    allocates nothing and uploads nothing, so it may be captured into a
- *    graph on that stream and replayed.
+ *    graph on that stream and replayed. The library keeps the descriptor
+ *    tables of the last 8 distinct batches per stream on the device, so a
+ *    caller alternating between a few batches (e.g. remainder batches) also
+ *    uploads nothing after the first call of each.
  */
 #ifndef NS_H_
 #define NS_H_

@@ -416,11 +416,30 @@ int build_blob(const Layout &L, void *const *X, const int64_t *shapes, int steps
 }
 
 // ------------------------------------------------------------ workspace cache
-struct CachedWs {
+// A descriptor table (matrix descriptors with their TMA maps, tile lists)
+// resident on the device, and the host bytes it was uploaded from.
+struct DevBlob {
   uint8_t *ptr = nullptr;
-  size_t bytes = 0;
-  std::vector<uint8_t> last_blob;  // blob currently resident at ptr
+  std::vector<uint8_t> bytes;
+  uint64_t last_use = 0;
 };
+// Tables kept per workspace: a caller that alternates between a few batches
+// on one stream (remainder batches, several parameter groups) finds each
+// table already on the device, so a call uploads nothing and never waits for
+// a staging copy behind the stream's earlier work.
+constexpr size_t kBlobsPerWs = 8;
+
+struct CachedWs {
+  uint8_t *ptr = nullptr;  // scratch of the largest batch seen (its descriptor-table area unused)
+  size_t bytes = 0;
+  std::vector<DevBlob> blobs;  // tables whose pointers refer to this scratch
+  uint64_t uses = 0;
+};
+
+void drop_blobs(CachedWs &c, cudaStream_t s) {
+  for (DevBlob &b : c.blobs) cudaFreeAsync(b.ptr, s);
+  c.blobs.clear();
+}
 // keyed by (device, stream, slot): slot 0 serves the device entry points,
 // slot 1 holds the host entry point's device copies, slot 2 + g the workspace
 // of its g-th pipeline group
@@ -438,12 +457,12 @@ std::map<WsKey, CachedWs> g_ws;
 
 int ensure_ws(CachedWs &c, size_t bytes, cudaStream_t s) {
   if (c.ptr && c.bytes >= bytes) return NS_OK;
+  drop_blobs(c, s);  // their descriptors point into the old scratch
   if (c.ptr) {
     if (cudaFreeAsync(c.ptr, s) != cudaSuccess) return NS_ECUDA;
     c.ptr = nullptr;
     c.bytes = 0;
   }
-  c.last_blob.clear();
   void *p = nullptr;
   g_allocations.fetch_add(1, std::memory_order_relaxed);
   if (cudaMallocAsync(&p, bytes, s) != cudaSuccess) {
@@ -497,12 +516,14 @@ struct RunOpts {
 };
 
 // co: one (a, b, c) triple for every step (table == false) or a steps x 3 table
-int execute(const Layout &L, uint8_t *ws, int steps, const float *co, bool table, float eps, DevInfo *di,
-            cudaStream_t s, const RunOpts &opt) {
-  const MatDesc *mats = reinterpret_cast<const MatDesc *>(ws + L.off_mats);
+// ws: the scratch (offsets at and past L.blob_end); blob: the device copy of
+// the descriptor table (offsets below L.blob_end), at the front of ws or apart.
+int execute(const Layout &L, uint8_t *ws, const uint8_t *blob, int steps, const float *co, bool table, float eps,
+            DevInfo *di, cudaStream_t s, const RunOpts &opt) {
+  const MatDesc *mats = reinterpret_cast<const MatDesc *>(blob + L.off_mats);
   for (const ResGroup &g : L.res_groups) {
     ResParams rp{};
-    rp.mats = reinterpret_cast<const ResDesc *>(ws + L.off_res) + g.start;
+    rp.mats = reinterpret_cast<const ResDesc *>(blob + L.off_res) + g.start;
     rp.nmats = g.count;
     rp.cluster = g.cluster;
     rp.dtype = L.dtype;
@@ -525,7 +546,7 @@ int execute(const Layout &L, uint8_t *ws, int steps, const float *co, bool table
   pp.nmats = nbig;
   pp.partials = reinterpret_cast<float *>(ws + L.off_partials);
   pp.ext = ext;
-  pp.tile_prefix = reinterpret_cast<const int *>(ws + L.off_prefix);
+  pp.tile_prefix = reinterpret_cast<const int *>(blob + L.off_prefix);
   pp.eps = eps;
   pp.dtype = L.dtype;
   pp.to_user = steps == 0;
@@ -543,8 +564,8 @@ int execute(const Layout &L, uint8_t *ws, int steps, const float *co, bool table
     if (timed(0, s, [&] { return launch_norm(pp, s); })) return NS_ECUDA;
     if (timed(7, s, [&] { return launch_prep(pp, L.prefix.back(), s); })) return NS_ECUDA;
   }
-  const Tile *t01 = reinterpret_cast<const Tile *>(ws + L.off_t01);
-  const Tile *t2 = reinterpret_cast<const Tile *>(ws + L.off_t2);
+  const Tile *t01 = reinterpret_cast<const Tile *>(blob + L.off_t01);
+  const Tile *t2 = reinterpret_cast<const Tile *>(blob + L.off_t2);
   if (steps == 0) return NS_OK;
   if (L.dtype == NS_BF16) {
     TcParams tp{};
@@ -642,11 +663,40 @@ int run(void *const *X, const int64_t *shapes, int count, int steps, const float
   }
   rc = build_blob(L, X, shapes, steps, ws, blob);
   if (rc) return rc;
-  if (!cache || cache->last_blob != blob) {
+  const uint8_t *blob_dev = ws;
+  if (!cache) {  // caller workspace: the table goes at its front, every call
     if (cudaMemcpyAsync(ws, blob.data(), blob.size(), cudaMemcpyHostToDevice, s) != cudaSuccess) return NS_ECUDA;
-    if (cache) cache->last_blob = blob;
+  } else {
+    DevBlob *hit = nullptr;
+    for (DevBlob &b : cache->blobs)
+      if (b.bytes == blob) hit = &b;
+    if (!hit) {
+      if (cache->blobs.size() >= kBlobsPerWs) {  // evict the least recently used table (stream-ordered free)
+        auto lru = std::min_element(cache->blobs.begin(), cache->blobs.end(),
+                                    [](const DevBlob &a, const DevBlob &b) { return a.last_use < b.last_use; });
+        cudaFreeAsync(lru->ptr, s);
+        cache->blobs.erase(lru);
+      }
+      void *p = nullptr;
+      g_allocations.fetch_add(1, std::memory_order_relaxed);
+      if (cudaMallocAsync(&p, std::max<size_t>(blob.size(), 256), s) != cudaSuccess) {
+        cudaGetLastError();
+        return NS_ENOMEM;
+      }
+      if (cudaMemcpyAsync(p, blob.data(), blob.size(), cudaMemcpyHostToDevice, s) != cudaSuccess) {
+        cudaFreeAsync(p, s);
+        return NS_ECUDA;
+      }
+      DevBlob nb;
+      nb.ptr = static_cast<uint8_t *>(p);
+      nb.bytes = std::move(blob);
+      cache->blobs.push_back(std::move(nb));
+      hit = &cache->blobs.back();
+    }
+    hit->last_use = ++cache->uses;
+    blob_dev = hit->ptr;
   }
-  return execute(L, ws, steps, co, table, eps, di, s, opt);
+  return execute(L, ws, blob_dev, steps, co, table, eps, di, s, opt);
 }
 
 // ------------------------------------------------------------ host pipeline
@@ -942,6 +992,7 @@ int ns_release_workspace(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return NS_ECUDA;
   for (auto it = g_ws.begin(); it != g_ws.end();) {
     if (it->first.dev == dev) {
+      for (DevBlob &b : it->second.blobs) cudaFree(b.ptr);
       if (it->second.ptr) cudaFree(it->second.ptr);
       it = g_ws.erase(it);
     } else {

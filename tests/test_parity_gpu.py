@@ -475,3 +475,27 @@ def test_prepared_batch_matches_plain_call():
         assert api.get_status() == 0
         for r, d in zip(ref, dev):
             assert torch.equal(r, d.cpu())
+
+
+def test_alternating_batches_reuse_their_descriptor_tables():
+    # two batches called in turn on one stream (like remainder batches of 64
+    # and 12): after the first call of each, further calls allocate nothing
+    # and give the same bits
+    xa = [seeded((640, 1200), torch.bfloat16, 95), seeded((1200, 640), torch.bfloat16, 96)]
+    xb = [seeded((300, 520), torch.bfloat16, 97)]
+    ra, rb = run_gpu(xa), run_gpu(xb)
+    da, db = [x.cuda() for x in xa], [x.cuda() for x in xb]
+    api.orthogonalize_batched(da)
+    api.orthogonalize_batched(db)
+    torch.cuda.synchronize()
+    allocs = api.num_workspace_allocations()
+    for _ in range(3):
+        for d, x in zip(da + db, xa + xb):
+            d.copy_(x.cuda())
+        api.orthogonalize_batched(da)
+        api.orthogonalize_batched(db)
+        torch.cuda.synchronize()
+        assert api.get_status() == 0
+        assert api.num_workspace_allocations() == allocs
+        for r, d in zip(ra + rb, da + db):
+            assert torch.equal(r, d.cpu())

@@ -318,8 +318,8 @@ void build_layout(const int64_t *shapes, int count, int dtype, Layout &L) {
   off = align_up(off + L.big.size() * sizeof(float), 256);
   L.off_ext = off;
   off = align_up(off + L.big.size() * 2 * sizeof(int), 256);
-  L.off_done = off;
-  off = align_up(off + L.big.size() * sizeof(int), kAlign);
+  L.off_done = off;  // per matrix completion counters, then the ticket counter
+  off = align_up(off + (L.big.size() + 1) * sizeof(int), kAlign);
   L.off_buffers = off;
   for (BigMat &b : L.big) {
     if (dtype == NS_BF16) {  // two iterate buffers in the caller's orientation
@@ -539,8 +539,8 @@ int execute(const Layout &L, uint8_t *ws, const uint8_t *blob, int steps, const 
   const int nbig = static_cast<int>(L.big.size());
   int *ext = reinterpret_cast<int *>(ws + L.off_ext);
   int *done = reinterpret_cast<int *>(ws + L.off_done);
-  // extents and completion counters start at zero (they are adjacent)
-  if (cudaMemsetAsync(ext, 0, L.off_done + nbig * sizeof(int) - L.off_ext, s) != cudaSuccess) return NS_ECUDA;
+  // extents, completion counters and the ticket counter start at zero (they are adjacent)
+  if (cudaMemsetAsync(ext, 0, L.off_done + (nbig + 1) * sizeof(int) - L.off_ext, s) != cudaSuccess) return NS_ECUDA;
   PrepParams pp{};
   pp.mats = mats;
   pp.nmats = nbig;
@@ -578,6 +578,7 @@ int execute(const Layout &L, uint8_t *ws, const uint8_t *blob, int steps, const 
     tp.ext = ext;
     tp.status = di->status;
     tp.done = done;
+    tp.ticket = done + nbig;
     tp.rscale = pp.rscale;
     tp.wait_limit_ns = opt.wait_limit_ns;
     tp.out_scale = opt.out_scale;
@@ -592,12 +593,14 @@ int execute(const Layout &L, uint8_t *ws, const uint8_t *blob, int steps, const 
       tp.g_begin = 0;
       tp.g_end = steps * per_step;
       tp.wait = 1;
+      tp.tickets = 1;
       rc = timed(6, s, [&] { return launch_tc(tp, di->sms, s); });
       if (rc < 0) return NS_ECUDA;
     }
     if (rc == 1 && opt.hold_signals) return NS_ECUDA;  // the self-test needs the single launch
     if (rc == 1) {  // one launch per step and phase
       tp.wait = 0;
+      tp.tickets = 0;
       const int begin[3] = {0, tp.n01, 2 * tp.n01}, count[3] = {tp.n01, tp.n01, tp.n2};
       for (int step = 0; step < steps; ++step)
         for (int phase = 0; phase < 3; ++phase) {

@@ -107,7 +107,9 @@ struct PhaseParams {
 // With wait != 0 an item first waits until every item of the same matrix in
 // earlier phases is complete (per-matrix completion counters `done`), so one
 // launch can run every step and phase; with wait == 0 the launches themselves
-// order the phases.
+// order the phases. With tickets != 0 the CTA pairs take items from the
+// counter `ticket` (zeroed by the host per call) in sequence order, so the
+// items in flight stay contiguous; otherwise pair c takes c, c + #pairs, ...
 struct TcParams {
   const Tile *tiles01;  // gram / square pair tiles
   const Tile *tiles2;   // apply pair tiles
@@ -119,6 +121,8 @@ struct TcParams {
   const int *ext;       // per matrix {rows_eff, cols_eff} in the caller's orientation
   int *status;
   int *done;            // per matrix completion counter (zeroed by the host per call)
+  int *ticket;          // next item to hand out, relative to g_begin (zeroed by the host per call)
+  int tickets;          // 1: items by ticket; 0: static stride
   const float *rscale;  // per matrix 1 / (||Y||_F + eps): step 0 scales gram by its square and apply by it
   uint64_t wait_limit_ns;  // limit of every bounded wait in the kernel
   float out_scale;      // the last step's result is multiplied by it before the write

@@ -70,7 +70,28 @@ static_assert(kABytes == 2 * kBoxBytes && kBBytes == 2 * kBoxBytes, "operand sha
 constexpr int kAccs = 2;                            // accumulators (each kTcBN TMEM columns)
 constexpr int kTmemCols = kAccs * kTcBN;
 
+// One work item as the pair's fetcher decodes it: item index (p.g_end: no
+// more items), step, phase, tile record, and the extents and orientation of
+// its matrix. The fetcher (the leader CTA's producer warp) publishes each
+// item of the pair, in order, into a small queue in both CTAs' shared memory;
+// every other role of both CTAs takes its items from that queue, so all roles
+// see the same sequence and none of them waits on a global lookup.
+struct QItem {
+  int g, step, phase, pad;
+  Tile tl;
+  int e0, e1, tr, direct;
+};
+static_assert(sizeof(QItem) == 48, "three 16-byte words");
+constexpr int kQueue = 8;  // published items a pair may run ahead of its slowest role
+// consumers that release a queue slot: in the leader the MMA warp, the
+// epilogue warps and the signal warp; in the peer its producer warp, epilogue
+// warps and signal warp
+constexpr int kQueueConsumers = 2 * (kEpiWarps + 2);
+
 struct Barriers {
+  QItem queue[kQueue];      // each CTA: the pair's items in order (written by the leader's fetcher)
+  uint64_t qfull[kQueue];   // each CTA: a queue slot holds the next item
+  uint64_t qempty[kQueue];  // leader: every consumer of both CTAs has read a slot
   uint64_t full[kStages];   // leader: both CTAs' loads of a stage landed
   uint64_t empty[kStages];  // each CTA: the leader's MMAs are done with a stage
   uint64_t tfull[2];        // each CTA: an accumulator is ready
@@ -119,23 +140,20 @@ __device__ __forceinline__ TileInfo make_tile_info(const TcParams &p, int phase,
   return ti;
 }
 
-__device__ __forceinline__ TileInfo tile_info(const TcParams &p, int phase, int t) {
-  const Tile tl = (phase < 2 ? p.tiles01 : p.tiles2)[t];
-  return make_tile_info(p, phase, tl, p.ext[2 * tl.mat], p.ext[2 * tl.mat + 1], p.mats[tl.mat].transposed);
-}
 
-// The items of one cluster (g, g + stride, ...) with their global lookups
-// pipelined, for the single-thread roles whose every stall idles the tensor
-// pipe: while an item runs, the tile record of the item after next and the
-// extents and orientation of the next item are already being loaded. Only
-// loaded values are carried; arithmetic on them waits until the item is taken.
-struct ItemPipe {
-  int g;                   // item taken next
-  int step, phase;         // of item g
-  Tile tl;                 // of item g
-  int e0, e1, tr, direct;  // of item g's matrix
-  int step2, phase2;       // of item g + stride
-  Tile tl2;                // of item g + stride
+// The item sequence of one pair as its fetcher produces it: indices from the
+// call's ticket counter (single-launch schedule: every pair takes the lowest
+// item not yet taken, so the items in flight stay contiguous), or the pair's
+// static stride (one launch per phase); the tile record of the next item and
+// its matrix's extents are loaded one item ahead.
+struct Fetcher {
+  int g;                   // the current item
+  int step, phase;
+  Tile tl;
+  int e0, e1, tr, direct;  // of the current item's matrix
+  int g2;                  // the next item
+  int step2, phase2;
+  Tile tl2;
 };
 
 __device__ __forceinline__ Tile fetch_tile(const TcParams &p, int g, int &step, int &phase) {
@@ -144,38 +162,120 @@ __device__ __forceinline__ Tile fetch_tile(const TcParams &p, int g, int &step, 
   return (phase < 2 ? p.tiles01 : p.tiles2)[t];
 }
 
-__device__ __forceinline__ void fetch_matrix(const TcParams &p, ItemPipe &q) {
-  const MatDesc &d = p.mats[q.tl.mat];
-  q.e0 = p.ext[2 * q.tl.mat];
-  q.e1 = p.ext[2 * q.tl.mat + 1];
-  q.tr = d.transposed;
-  q.direct = d.direct;
+__device__ __forceinline__ void fetch_matrix(const TcParams &p, Fetcher &f) {
+  const MatDesc &d = p.mats[f.tl.mat];
+  f.e0 = p.ext[2 * f.tl.mat];
+  f.e1 = p.ext[2 * f.tl.mat + 1];
+  f.tr = d.transposed;
+  f.direct = d.direct;
 }
 
-__device__ __forceinline__ void pipe_start(const TcParams &p, int g, int stride, ItemPipe &q) {
-  q.g = g;
-  if (g < p.g_end) {
-    q.tl = fetch_tile(p, g, q.step, q.phase);
-    fetch_matrix(p, q);
+// The item after `prev` (the whole warp calls this): a ticket, or prev + stride.
+__device__ __forceinline__ int next_item(const TcParams &p, int prev, int stride) {
+  int n;
+  if (p.tickets) {
+    int t = 0;
+    if ((threadIdx.x & 31) == 0) t = atomicAdd(p.ticket, 1);
+    n = p.g_begin + __shfl_sync(0xffffffffu, t, 0);
+  } else {
+    n = prev + stride;
   }
-  if (g + stride < p.g_end) q.tl2 = fetch_tile(p, g + stride, q.step2, q.phase2);
+  return n < p.g_end ? n : p.g_end;
 }
 
-// Take item q.g (returned through step, phase, ti) and start the lookups of the two after it.
-__device__ __forceinline__ void pipe_take(const TcParams &p, int stride, ItemPipe &q, int &step, int &phase,
-                                          TileInfo &ti, int &direct) {
-  step = q.step;
-  phase = q.phase;
-  ti = make_tile_info(p, q.phase, q.tl, q.e0, q.e1, q.tr);
-  direct = q.direct;
-  q.g += stride;
-  if (q.g < p.g_end) {
-    q.step = q.step2;
-    q.phase = q.phase2;
-    q.tl = q.tl2;
-    fetch_matrix(p, q);
+__device__ __forceinline__ void fetcher_start(const TcParams &p, int first, int stride, Fetcher &f) {
+  f.g = p.tickets ? next_item(p, 0, 0) : (first < p.g_end ? first : p.g_end);
+  if (f.g < p.g_end) {
+    f.tl = fetch_tile(p, f.g, f.step, f.phase);
+    fetch_matrix(p, f);
   }
-  if (q.g + stride < p.g_end) q.tl2 = fetch_tile(p, q.g + stride, q.step2, q.phase2);
+  f.g2 = f.g < p.g_end ? next_item(p, f.g, stride) : p.g_end;
+  if (f.g2 < p.g_end) f.tl2 = fetch_tile(p, f.g2, f.step2, f.phase2);
+}
+
+__device__ __forceinline__ QItem fetcher_item(const Fetcher &f) {
+  QItem it;
+  it.g = f.g;
+  it.step = f.step;
+  it.phase = f.phase;
+  it.pad = 0;
+  it.tl = f.tl;
+  it.e0 = f.e0;
+  it.e1 = f.e1;
+  it.tr = f.tr;
+  it.direct = f.direct;
+  return it;
+}
+
+// Move to the next item and start the lookups of the one after it.
+__device__ __forceinline__ void fetcher_advance(const TcParams &p, int stride, Fetcher &f) {
+  f.g = f.g2;
+  if (f.g < p.g_end) {
+    f.step = f.step2;
+    f.phase = f.phase2;
+    f.tl = f.tl2;
+    fetch_matrix(p, f);
+    f.g2 = next_item(p, f.g, stride);
+    if (f.g2 < p.g_end) f.tl2 = fetch_tile(p, f.g2, f.step2, f.phase2);
+  }
+}
+
+// ---- the pair's item queue
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, const uint4 &v) {
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+// The fetcher's lane publishes item number k of the pair into slot k % kQueue
+// of both CTAs, once every consumer has read what the slot held before.
+__device__ __forceinline__ bool queue_put(Barriers *bar, int k, const QItem &it, const Waiter &w) {
+  const int slot = k % kQueue;
+  const uint32_t parity = static_cast<uint32_t>(k / kQueue) & 1u;
+  if (!mbar_wait<true>(&bar->qempty[slot], parity ^ 1u, w)) return false;
+  const uint4 *v = reinterpret_cast<const uint4 *>(&it);
+  uint4 *mine = reinterpret_cast<uint4 *>(&bar->queue[slot]);
+  const uint32_t peer = mapa_shared(smem_u32(&bar->queue[slot]), 1);
+#pragma unroll
+  for (int q = 0; q < 3; ++q) {
+    mine[q] = v[q];
+    st_cluster_v4(peer + 16 * q, v[q]);
+  }
+  mbar_arrive(&bar->qfull[slot]);                                   // release: this CTA's copy
+  mbar_arrive_cluster(mapa_shared(smem_u32(&bar->qfull[slot]), 1));  // release.cluster: the peer's copy
+  return true;
+}
+
+// One lane takes item number k of the pair from its CTA's queue and releases
+// the slot on the leader.
+__device__ __forceinline__ bool queue_get_lane(Barriers *bar, int k, QItem &it, const Waiter &w) {
+  const int slot = k % kQueue;
+  const uint32_t parity = static_cast<uint32_t>(k / kQueue) & 1u;
+  if (!mbar_wait<true>(&bar->qfull[slot], parity, w)) return false;
+  const volatile uint4 *src = reinterpret_cast<const volatile uint4 *>(&bar->queue[slot]);
+  uint4 *dst = reinterpret_cast<uint4 *>(&it);
+#pragma unroll
+  for (int q = 0; q < 3; ++q) {
+    const uint4 v = make_uint4(src[q].x, src[q].y, src[q].z, src[q].w);
+    dst[q] = v;
+  }
+  mbar_arrive_cluster(mapa_shared(smem_u32(&bar->qempty[slot]), 0));
+  return true;
+}
+
+// The same for a whole warp: lane 0 takes the item and broadcasts it.
+__device__ __forceinline__ bool queue_get_warp(Barriers *bar, int k, QItem &it, const Waiter &w) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = queue_get_lane(bar, k, it, w) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  int *v = reinterpret_cast<int *>(&it);
+#pragma unroll
+  for (int q = 0; q < 12; ++q) v[q] = __shfl_sync(0xffffffffu, v[q], 0);
+  return ok != 0;
+}
+
+__device__ __forceinline__ TileInfo item_info(const TcParams &p, const QItem &it) {
+  return make_tile_info(p, it.phase, it.tl, it.e0, it.e1, it.tr);
 }
 
 // The k-loop of an item as three consecutive k-ranges with a fixed operand
@@ -626,6 +726,10 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
       mbar_init(&bar->tempty[a], kTcCluster * kEpiWarps);  // one arrival per epilogue warp
       mbar_init(&bar->epi_done[a], kEpiWarps);
     }
+    for (int q = 0; q < kQueue; ++q) {
+      mbar_init(&bar->qfull[q], 1);
+      mbar_init(&bar->qempty[q], kQueueConsumers);
+    }
     mbar_init(&bar->drain, 1);
     bar->abort = 0;
     fence_mbar_init();
@@ -650,41 +754,57 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
   if (tmem_ok && warp == 0) {
     {
       // ---------------------------------------------------- TMA producer (both CTAs)
-      // the whole warp runs the loop; one elected lane issues each copy
+      // the whole warp runs the loop; one elected lane issues each copy. In
+      // the leader this warp is also the pair's fetcher: it takes the pair's
+      // items (tickets or static stride) and publishes them to both queues.
       const uint64_t pol = l2_policy_evict_normal();
       int issued_phase[kStages];
       for (int s = 0; s < kStages; ++s) issued_phase[s] = -1;
       int stage = 0;
       uint32_t phase_bit = 0;
       bool ok = true;
-      ItemPipe q;
-      pipe_start(p, p.g_begin + cluster, nclusters, q);
-      while (q.g < p.g_end && ok) {
-        int step, phase, direct;
-        TileInfo ti;
-        pipe_take(p, nclusters, q, step, phase, ti, direct);
-        if (q.g < p.g_end && elect_one()) prefetch_item_maps(p.mats[q.tl.mat], q.step, q.phase, q.tr, q.direct);
-        __syncwarp();
-        if (ti.skip) continue;
-        if (p.wait) {
-          // operands come from earlier phases of this matrix, written by
-          // epilogues anywhere on the GPU
-          int ready = 1;
-          if (lane == 0) ready = wait_count(p.done + ti.mat, units_before(*ti.d, step, phase), w) ? 1 : 0;
-          if (!__shfl_sync(0xffffffffu, ready, 0)) break;
-          fence_proxy_async_global();
+      Fetcher f;
+      if (leader) fetcher_start(p, p.g_begin + cluster, nclusters, f);
+      for (int k = 0; ok; ++k) {
+        QItem it;
+        if (leader) {
+          it = fetcher_item(f);
+          int put = 1;
+          if (lane == 0) put = queue_put(bar, k, it, w) ? 1 : 0;
+          if (!__shfl_sync(0xffffffffu, put, 0)) break;
+        } else if (!queue_get_warp(bar, k, it, w)) {
+          break;
         }
-        const ItemPlan pl = plan_item(*ti.d, step, phase, ti.tr, direct, ti.row0, ti.col0, ti.nk);
-        const int a0 = ti.row0 + my_rows, b0 = ti.col0 + static_cast<int>(rank) * (kTcBN / 2);
-        // one k-loop per operand order, so the copies issued are exactly the ones needed
-        ok = produce_segment<1, 1>(0, pl.e0, pl.map[0][0], pl.map[0][1], a0, b0, sA, sB, bar, leader, stage, phase_bit,
-                                   issued_phase, pol, w);
-        if (ok)
-          ok = produce_segment<0, 1>(pl.e0, pl.e1, pl.map[1][0], pl.map[1][1], a0, b0, sA, sB, bar, leader, stage,
+        if (it.g >= p.g_end) break;
+        const TileInfo ti = item_info(p, it);
+        if (!ti.skip) {
+          if (p.wait) {
+            // operands come from earlier phases of this matrix, written by
+            // epilogues anywhere on the GPU
+            int ready = 1;
+            if (lane == 0) ready = wait_count(p.done + ti.mat, units_before(*ti.d, it.step, it.phase), w) ? 1 : 0;
+            if (!__shfl_sync(0xffffffffu, ready, 0)) break;
+            fence_proxy_async_global();
+          }
+          const ItemPlan pl = plan_item(*ti.d, it.step, it.phase, ti.tr, it.direct, ti.row0, ti.col0, ti.nk);
+          const int a0 = ti.row0 + my_rows, b0 = ti.col0 + static_cast<int>(rank) * (kTcBN / 2);
+          // one k-loop per operand order, so the copies issued are exactly the ones needed
+          ok = produce_segment<1, 1>(0, pl.e0, pl.map[0][0], pl.map[0][1], a0, b0, sA, sB, bar, leader, stage,
                                      phase_bit, issued_phase, pol, w);
-        if (ok)
-          ok = produce_segment<0, 0>(pl.e1, ti.nk, pl.map[2][0], pl.map[2][1], a0, b0, sA, sB, bar, leader, stage,
-                                     phase_bit, issued_phase, pol, w);
+          if (ok)
+            ok = produce_segment<0, 1>(pl.e0, pl.e1, pl.map[1][0], pl.map[1][1], a0, b0, sA, sB, bar, leader, stage,
+                                       phase_bit, issued_phase, pol, w);
+          if (ok)
+            ok = produce_segment<0, 0>(pl.e1, ti.nk, pl.map[2][0], pl.map[2][1], a0, b0, sA, sB, bar, leader, stage,
+                                       phase_bit, issued_phase, pol, w);
+        }
+        if (leader) {
+          // the next item (its lookups were started one item ago) and the
+          // lookups of the one after; then its tensor maps into the cache
+          fetcher_advance(p, nclusters, f);
+          if (f.g < p.g_end && elect_one()) prefetch_item_maps(p.mats[f.tl.mat], f.step, f.phase, f.tr, f.direct);
+          __syncwarp();
+        }
       }
       if (*abort && leader && lane == 0) {
         for (int s = 0; s < kStages; ++s)
@@ -700,14 +820,12 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      ItemPipe q;
-      pipe_start(p, p.g_begin + cluster, nclusters, q);
-      while (q.g < p.g_end && ok) {
-        int step, phase, direct;
-        TileInfo ti;
-        pipe_take(p, nclusters, q, step, phase, ti, direct);
+      for (int k = 0; ok; ++k) {
+        QItem it;
+        if (!queue_get_warp(bar, k, it, w) || it.g >= p.g_end) break;
+        const TileInfo ti = item_info(p, it);
         if (ti.skip) continue;
-        const ItemPlan pl = plan_item(*ti.d, step, phase, ti.tr, direct, ti.row0, ti.col0, ti.nk);
+        const ItemPlan pl = plan_item(*ti.d, it.step, it.phase, ti.tr, it.direct, ti.row0, ti.col0, ti.nk);
         if (!warp_mbar_wait<true>(&bar->tempty[acc], acc_phase ^ 1u, w)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * kTcBN);
@@ -740,24 +858,24 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
     uint32_t *stage = epi_stage + e * (kEpiStageBytes / 4);
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int g = p.g_begin + cluster; g < p.g_end; g += nclusters) {
-      int step, phase, t;
-      decode_item(p, g, step, phase, t);
-      TileInfo ti = tile_info(p, phase, t);
+    for (int k = 0;; ++k) {
+      QItem it;
+      if (!queue_get_warp(bar, k, it, w) || it.g >= p.g_end) break;
+      TileInfo ti = item_info(p, it);
       if (ti.skip) continue;
       if (p.wait) {
         // the operand this epilogue reloads (A, or the current iterate) comes from an earlier phase
         bool ready = true;
-        if (lane == 0) ready = wait_count(p.done + ti.mat, units_before(*ti.d, step, phase), w);
+        if (lane == 0) ready = wait_count(p.done + ti.mat, units_before(*ti.d, it.step, it.phase), w);
         if (!__shfl_sync(0xffffffffu, ready ? 1 : 0, 0)) break;
       }
       ti.row0 += my_rows;
-      const StepCtx sc = step_ctx(p, step, ti.mat);
+      const StepCtx sc = step_ctx(p, it.step, ti.mat);
       const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kTcBN);
       bool ok;
-      if (phase == 0)
+      if (it.phase == 0)
         ok = epilogue_item<0>(sc, ti, r, c0, tbase, stage, &bar->tfull[acc], acc_phase, w);
-      else if (phase == 1)
+      else if (it.phase == 1)
         ok = epilogue_item<1>(sc, ti, r, c0, tbase, stage, &bar->tfull[acc], acc_phase, w);
       else
         ok = epilogue_item<2>(sc, ti, r, c0, tbase, stage, &bar->tfull[acc], acc_phase, w);
@@ -783,12 +901,12 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
       // own dependencies are met.
       int acc = 0;
       uint32_t acc_phase = 0;
-      for (int g = p.g_begin + cluster; g < p.g_end; g += nclusters) {
-        int step, phase, t;
-        decode_item(p, g, step, phase, t);
-        const TileInfo ti = tile_info(p, phase, t);
+      for (int k = 0;; ++k) {
+        QItem it;
+        if (!queue_get_lane(bar, k, it, w) || it.g >= p.g_end) break;
+        const TileInfo ti = item_info(p, it);
         if (ti.skip) {
-          if (p.wait && !wait_count(p.done + ti.mat, units_before(*ti.d, step, phase), w)) break;
+          if (p.wait && !wait_count(p.done + ti.mat, units_before(*ti.d, it.step, it.phase), w)) break;
         } else {
           if (!mbar_wait(&bar->epi_done[acc], acc_phase, w)) break;
           if (++acc == kAccs) {

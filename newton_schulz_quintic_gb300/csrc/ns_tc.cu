@@ -71,17 +71,24 @@ constexpr int kAccs = 2;                            // accumulators (each kTcBN 
 constexpr int kTmemCols = kAccs * kTcBN;
 
 // One work item as the pair's fetcher decodes it: item index (p.g_end: no
-// more items), step, phase, tile record, and the extents and orientation of
-// its matrix. The fetcher (the leader CTA's producer warp) publishes each
-// item of the pair, in order, into a small queue in both CTAs' shared memory;
-// every other role of both CTAs takes its items from that queue, so all roles
-// see the same sequence and none of them waits on a global lookup.
+// more items), step, phase and the matrix's orientation (packed), tile
+// record and the matrix's extents. The fetcher (the leader CTA's producer
+// warp) publishes each item of the pair, in order, into a small queue in both
+// CTAs' shared memory; every other role of both CTAs takes its items from
+// that queue, so all roles see the same sequence and none of them waits on a
+// global lookup.
 struct QItem {
-  int g, step, phase, pad;
-  Tile tl;
-  int e0, e1, tr, direct;
+  int g;
+  int spf;               // step * 16 + phase * 4 + transposed * 2 + direct
+  int mat, row0, col0;
+  int e0, e1;
+  int pad;
+  __device__ int step() const { return spf >> 4; }
+  __device__ int phase() const { return (spf >> 2) & 3; }
+  __device__ int tr() const { return (spf >> 1) & 1; }
+  __device__ int direct() const { return spf & 1; }
 };
-static_assert(sizeof(QItem) == 48, "three 16-byte words");
+static_assert(sizeof(QItem) == 32, "two 16-byte words");
 constexpr int kQueue = 8;  // published items a pair may run ahead of its slowest role
 // consumers that release a queue slot: in the leader the MMA warp, the
 // epilogue warps and the signal warp; in the peer its producer warp, epilogue
@@ -144,21 +151,24 @@ __device__ __forceinline__ TileInfo make_tile_info(const TcParams &p, int phase,
 // The item sequence of one pair as its fetcher produces it: indices from the
 // call's ticket counter (single-launch schedule: every pair takes the lowest
 // item not yet taken, so the items in flight stay contiguous), or the pair's
-// static stride (one launch per phase); the tile record of the next item and
-// its matrix's extents are loaded one item ahead.
+// static stride (one launch per phase). The lookups run ahead of use: while
+// an item is produced, the matrix record of the next item, the tile record of
+// the one after and the ticket of the one after that are in flight.
 struct Fetcher {
-  int g;                   // the current item
-  int step, phase;
-  Tile tl;
-  int e0, e1, tr, direct;  // of the current item's matrix
-  int g2;                  // the next item
-  int step2, phase2;
-  Tile tl2;
+  int g, sp;               // the item to publish next: index, step * 16 + phase * 4
+  Tile tl;                 // its tile record
+  int e0, e1, tr, direct;  // its matrix's extents and orientation
+  int g2, sp2;             // the item after it
+  Tile tl2;                // and its tile record
+  int pending;             // lane 0: the raw ticket of the item after g2 (ticket mode)
 };
+// Only loaded values are carried in the fetcher; arithmetic on them waits
+// until the item is published, so no lookup stalls the warp before its use.
 
-__device__ __forceinline__ Tile fetch_tile(const TcParams &p, int g, int &step, int &phase) {
-  int t;
+__device__ __forceinline__ Tile fetch_tile(const TcParams &p, int g, int &sp) {
+  int step, phase, t;
   decode_item(p, g, step, phase, t);
+  sp = step * 16 + phase * 4;
   return (phase < 2 ? p.tiles01 : p.tiles2)[t];
 }
 
@@ -170,54 +180,59 @@ __device__ __forceinline__ void fetch_matrix(const TcParams &p, Fetcher &f) {
   f.direct = d.direct;
 }
 
-// The item after `prev` (the whole warp calls this): a ticket, or prev + stride.
-__device__ __forceinline__ int next_item(const TcParams &p, int prev, int stride) {
-  int n;
-  if (p.tickets) {
-    int t = 0;
-    if ((threadIdx.x & 31) == 0) t = atomicAdd(p.ticket, 1);
-    n = p.g_begin + __shfl_sync(0xffffffffu, t, 0);
-  } else {
-    n = prev + stride;
-  }
-  return n < p.g_end ? n : p.g_end;
+__device__ __forceinline__ int take_ticket(const TcParams &p) {
+  return (threadIdx.x & 31) == 0 ? atomicAdd(p.ticket, 1) : 0;
 }
+__device__ __forceinline__ int clamp_item(const TcParams &p, int g) { return g < p.g_end ? g : p.g_end; }
 
+// Whole warp: the first two items of the pair and the ticket of the third.
 __device__ __forceinline__ void fetcher_start(const TcParams &p, int first, int stride, Fetcher &f) {
-  f.g = p.tickets ? next_item(p, 0, 0) : (first < p.g_end ? first : p.g_end);
+  if (p.tickets) {
+    f.g = clamp_item(p, p.g_begin + __shfl_sync(0xffffffffu, take_ticket(p), 0));
+    f.g2 = clamp_item(p, p.g_begin + __shfl_sync(0xffffffffu, take_ticket(p), 0));
+    f.pending = take_ticket(p);
+  } else {
+    f.g = clamp_item(p, first);
+    f.g2 = f.g < p.g_end ? clamp_item(p, f.g + stride) : p.g_end;
+    f.pending = 0;
+  }
   if (f.g < p.g_end) {
-    f.tl = fetch_tile(p, f.g, f.step, f.phase);
+    f.tl = fetch_tile(p, f.g, f.sp);
     fetch_matrix(p, f);
   }
-  f.g2 = f.g < p.g_end ? next_item(p, f.g, stride) : p.g_end;
-  if (f.g2 < p.g_end) f.tl2 = fetch_tile(p, f.g2, f.step2, f.phase2);
+  if (f.g2 < p.g_end) f.tl2 = fetch_tile(p, f.g2, f.sp2);
 }
 
+// The item to publish, packed.
 __device__ __forceinline__ QItem fetcher_item(const Fetcher &f) {
   QItem it;
   it.g = f.g;
-  it.step = f.step;
-  it.phase = f.phase;
-  it.pad = 0;
-  it.tl = f.tl;
+  it.spf = f.sp | (f.tr << 1) | f.direct;
+  it.mat = f.tl.mat;
+  it.row0 = f.tl.row0;
+  it.col0 = f.tl.col0;
   it.e0 = f.e0;
   it.e1 = f.e1;
-  it.tr = f.tr;
-  it.direct = f.direct;
+  it.pad = 0;
   return it;
 }
 
-// Move to the next item and start the lookups of the one after it.
+// Whole warp, right after the current item was published: the next item
+// becomes current (its matrix record requested now, needed when it is
+// published), the one after gets its index and tile record requested.
 __device__ __forceinline__ void fetcher_advance(const TcParams &p, int stride, Fetcher &f) {
   f.g = f.g2;
-  if (f.g < p.g_end) {
-    f.step = f.step2;
-    f.phase = f.phase2;
-    f.tl = f.tl2;
-    fetch_matrix(p, f);
-    f.g2 = next_item(p, f.g, stride);
-    if (f.g2 < p.g_end) f.tl2 = fetch_tile(p, f.g2, f.step2, f.phase2);
+  if (f.g >= p.g_end) return;
+  f.sp = f.sp2;
+  f.tl = f.tl2;
+  fetch_matrix(p, f);
+  if (p.tickets) {
+    f.g2 = clamp_item(p, p.g_begin + __shfl_sync(0xffffffffu, f.pending, 0));
+    f.pending = take_ticket(p);
+  } else {
+    f.g2 = clamp_item(p, f.g + stride);
   }
+  if (f.g2 < p.g_end) f.tl2 = fetch_tile(p, f.g2, f.sp2);
 }
 
 // ---- the pair's item queue
@@ -237,7 +252,7 @@ __device__ __forceinline__ bool queue_put(Barriers *bar, int k, const QItem &it,
   uint4 *mine = reinterpret_cast<uint4 *>(&bar->queue[slot]);
   const uint32_t peer = mapa_shared(smem_u32(&bar->queue[slot]), 1);
 #pragma unroll
-  for (int q = 0; q < 3; ++q) {
+  for (int q = 0; q < 2; ++q) {
     mine[q] = v[q];
     st_cluster_v4(peer + 16 * q, v[q]);
   }
@@ -255,7 +270,7 @@ __device__ __forceinline__ bool queue_get_lane(Barriers *bar, int k, QItem &it, 
   const volatile uint4 *src = reinterpret_cast<const volatile uint4 *>(&bar->queue[slot]);
   uint4 *dst = reinterpret_cast<uint4 *>(&it);
 #pragma unroll
-  for (int q = 0; q < 3; ++q) {
+  for (int q = 0; q < 2; ++q) {
     const uint4 v = make_uint4(src[q].x, src[q].y, src[q].z, src[q].w);
     dst[q] = v;
   }
@@ -270,12 +285,12 @@ __device__ __forceinline__ bool queue_get_warp(Barriers *bar, int k, QItem &it, 
   ok = __shfl_sync(0xffffffffu, ok, 0);
   int *v = reinterpret_cast<int *>(&it);
 #pragma unroll
-  for (int q = 0; q < 12; ++q) v[q] = __shfl_sync(0xffffffffu, v[q], 0);
+  for (int q = 0; q < 7; ++q) v[q] = __shfl_sync(0xffffffffu, v[q], 0);
   return ok != 0;
 }
 
 __device__ __forceinline__ TileInfo item_info(const TcParams &p, const QItem &it) {
-  return make_tile_info(p, it.phase, it.tl, it.e0, it.e1, it.tr);
+  return make_tile_info(p, it.phase(), Tile{it.mat, it.row0, it.col0, 0}, it.e0, it.e1, it.tr());
 }
 
 // The k-loop of an item as three consecutive k-ranges with a fixed operand
@@ -337,23 +352,25 @@ __device__ __forceinline__ ItemPlan plan_item(const MatDesc &d, int step, int ph
   return pl;
 }
 
-// Prefetch the tensor maps an item of (step, phase) of matrix d reads, so a
-// tile start does not wait for its descriptors (consecutive items of a
-// cluster often belong to different matrices).
-__device__ __forceinline__ void prefetch_item_maps(const MatDesc &d, int step, int phase, int transposed,
-                                                   int direct) {
-  const bool y = step == 0 && direct;
-  const void *src_k = y ? &d.tm_y : &d.tm_s[step & 1];
-  const void *src_mn = y ? &d.tm_y_mn : &d.tm_s_mn[step & 1];
-  if (phase == 0) {
-    prefetch_tensormap(transposed ? src_mn : src_k);
-  } else if (phase == 1) {
+// Prefetch the tensor maps an item of (step, phase) of matrix d may read, so
+// a tile start does not wait for its descriptors (consecutive items of a
+// pair often belong to different matrices). Only the maps' addresses are
+// formed: nothing of d is read, so this does not wait for its record.
+__device__ __forceinline__ void prefetch_item_maps(const MatDesc &d, int step, int phase) {
+  if (phase == 1) {
     prefetch_tensormap(&d.tm_a);
     prefetch_tensormap(&d.tm_a_mn);
-  } else {
+    return;
+  }
+  if (phase == 2) {
     prefetch_tensormap(&d.tm_b);
     prefetch_tensormap(&d.tm_b_mn);
-    prefetch_tensormap(transposed ? src_k : src_mn);
+  }
+  prefetch_tensormap(&d.tm_s[step & 1]);
+  prefetch_tensormap(&d.tm_s_mn[step & 1]);
+  if (step == 0) {
+    prefetch_tensormap(&d.tm_y);
+    prefetch_tensormap(&d.tm_y_mn);
   }
 }
 
@@ -772,39 +789,36 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
           int put = 1;
           if (lane == 0) put = queue_put(bar, k, it, w) ? 1 : 0;
           if (!__shfl_sync(0xffffffffu, put, 0)) break;
+          if (it.g >= p.g_end) break;
+          // the lookups of the items after this one run while it is produced
+          fetcher_advance(p, nclusters, f);
+          if (f.g < p.g_end && elect_one()) prefetch_item_maps(p.mats[f.tl.mat], f.sp >> 4, (f.sp >> 2) & 3);
+          __syncwarp();
         } else if (!queue_get_warp(bar, k, it, w)) {
           break;
         }
         if (it.g >= p.g_end) break;
         const TileInfo ti = item_info(p, it);
-        if (!ti.skip) {
-          if (p.wait) {
-            // operands come from earlier phases of this matrix, written by
-            // epilogues anywhere on the GPU
-            int ready = 1;
-            if (lane == 0) ready = wait_count(p.done + ti.mat, units_before(*ti.d, it.step, it.phase), w) ? 1 : 0;
-            if (!__shfl_sync(0xffffffffu, ready, 0)) break;
-            fence_proxy_async_global();
-          }
-          const ItemPlan pl = plan_item(*ti.d, it.step, it.phase, ti.tr, it.direct, ti.row0, ti.col0, ti.nk);
-          const int a0 = ti.row0 + my_rows, b0 = ti.col0 + static_cast<int>(rank) * (kTcBN / 2);
-          // one k-loop per operand order, so the copies issued are exactly the ones needed
-          ok = produce_segment<1, 1>(0, pl.e0, pl.map[0][0], pl.map[0][1], a0, b0, sA, sB, bar, leader, stage,
+        if (ti.skip) continue;
+        if (p.wait) {
+          // operands come from earlier phases of this matrix, written by
+          // epilogues anywhere on the GPU
+          int ready = 1;
+          if (lane == 0) ready = wait_count(p.done + ti.mat, units_before(*ti.d, it.step(), it.phase()), w) ? 1 : 0;
+          if (!__shfl_sync(0xffffffffu, ready, 0)) break;
+          fence_proxy_async_global();
+        }
+        const ItemPlan pl = plan_item(*ti.d, it.step(), it.phase(), ti.tr, it.direct(), ti.row0, ti.col0, ti.nk);
+        const int a0 = ti.row0 + my_rows, b0 = ti.col0 + static_cast<int>(rank) * (kTcBN / 2);
+        // one k-loop per operand order, so the copies issued are exactly the ones needed
+        ok = produce_segment<1, 1>(0, pl.e0, pl.map[0][0], pl.map[0][1], a0, b0, sA, sB, bar, leader, stage,
+                                   phase_bit, issued_phase, pol, w);
+        if (ok)
+          ok = produce_segment<0, 1>(pl.e0, pl.e1, pl.map[1][0], pl.map[1][1], a0, b0, sA, sB, bar, leader, stage,
                                      phase_bit, issued_phase, pol, w);
-          if (ok)
-            ok = produce_segment<0, 1>(pl.e0, pl.e1, pl.map[1][0], pl.map[1][1], a0, b0, sA, sB, bar, leader, stage,
-                                       phase_bit, issued_phase, pol, w);
-          if (ok)
-            ok = produce_segment<0, 0>(pl.e1, ti.nk, pl.map[2][0], pl.map[2][1], a0, b0, sA, sB, bar, leader, stage,
-                                       phase_bit, issued_phase, pol, w);
-        }
-        if (leader) {
-          // the next item (its lookups were started one item ago) and the
-          // lookups of the one after; then its tensor maps into the cache
-          fetcher_advance(p, nclusters, f);
-          if (f.g < p.g_end && elect_one()) prefetch_item_maps(p.mats[f.tl.mat], f.step, f.phase, f.tr, f.direct);
-          __syncwarp();
-        }
+        if (ok)
+          ok = produce_segment<0, 0>(pl.e1, ti.nk, pl.map[2][0], pl.map[2][1], a0, b0, sA, sB, bar, leader, stage,
+                                     phase_bit, issued_phase, pol, w);
       }
       if (*abort && leader && lane == 0) {
         for (int s = 0; s < kStages; ++s)
@@ -825,7 +839,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
         if (!queue_get_warp(bar, k, it, w) || it.g >= p.g_end) break;
         const TileInfo ti = item_info(p, it);
         if (ti.skip) continue;
-        const ItemPlan pl = plan_item(*ti.d, it.step, it.phase, ti.tr, it.direct, ti.row0, ti.col0, ti.nk);
+        const ItemPlan pl = plan_item(*ti.d, it.step(), it.phase(), ti.tr, it.direct(), ti.row0, ti.col0, ti.nk);
         if (!warp_mbar_wait<true>(&bar->tempty[acc], acc_phase ^ 1u, w)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * kTcBN);
@@ -866,16 +880,17 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
       if (p.wait) {
         // the operand this epilogue reloads (A, or the current iterate) comes from an earlier phase
         bool ready = true;
-        if (lane == 0) ready = wait_count(p.done + ti.mat, units_before(*ti.d, it.step, it.phase), w);
+        if (lane == 0) ready = wait_count(p.done + ti.mat, units_before(*ti.d, it.step(), it.phase()), w);
         if (!__shfl_sync(0xffffffffu, ready ? 1 : 0, 0)) break;
       }
       ti.row0 += my_rows;
-      const StepCtx sc = step_ctx(p, it.step, ti.mat);
+      const StepCtx sc = step_ctx(p, it.step(), ti.mat);
       const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kTcBN);
       bool ok;
-      if (it.phase == 0)
+      const int phase = it.phase();
+      if (phase == 0)
         ok = epilogue_item<0>(sc, ti, r, c0, tbase, stage, &bar->tfull[acc], acc_phase, w);
-      else if (it.phase == 1)
+      else if (phase == 1)
         ok = epilogue_item<1>(sc, ti, r, c0, tbase, stage, &bar->tfull[acc], acc_phase, w);
       else
         ok = epilogue_item<2>(sc, ti, r, c0, tbase, stage, &bar->tfull[acc], acc_phase, w);
@@ -906,7 +921,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
         if (!queue_get_lane(bar, k, it, w) || it.g >= p.g_end) break;
         const TileInfo ti = item_info(p, it);
         if (ti.skip) {
-          if (p.wait && !wait_count(p.done + ti.mat, units_before(*ti.d, it.step, it.phase), w)) break;
+          if (p.wait && !wait_count(p.done + ti.mat, units_before(*ti.d, it.step(), it.phase()), w)) break;
         } else {
           if (!mbar_wait(&bar->epi_done[acc], acc_phase, w)) break;
           if (++acc == kAccs) {

@@ -780,20 +780,36 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
       int stage = 0;
       uint32_t phase_bit = 0;
       bool ok = true;
+      // The fetcher publishes every item one item ahead of its own production
+      // of it, so the peer's producer and the other roles have each item a
+      // whole tile before they need it.
       Fetcher f;
-      if (leader) fetcher_start(p, p.g_begin + cluster, nclusters, f);
+      QItem next;
+      next.g = p.g_end;
+      if (leader) {
+        fetcher_start(p, p.g_begin + cluster, nclusters, f);
+        next = fetcher_item(f);
+        int put = 1;
+        if (lane == 0) put = queue_put(bar, 0, next, w) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, put, 0) != 0;
+        if (ok && next.g < p.g_end) fetcher_advance(p, nclusters, f);
+      }
       for (int k = 0; ok; ++k) {
         QItem it;
         if (leader) {
-          it = fetcher_item(f);
-          int put = 1;
-          if (lane == 0) put = queue_put(bar, k, it, w) ? 1 : 0;
-          if (!__shfl_sync(0xffffffffu, put, 0)) break;
+          it = next;
           if (it.g >= p.g_end) break;
-          // the lookups of the items after this one run while it is produced
-          fetcher_advance(p, nclusters, f);
-          if (f.g < p.g_end && elect_one()) prefetch_item_maps(p.mats[f.tl.mat], f.sp >> 4, (f.sp >> 2) & 3);
-          __syncwarp();
+          // publish item k + 1 now; the lookups of the items after it run
+          // while item k is produced
+          next = fetcher_item(f);
+          int put = 1;
+          if (lane == 0) put = queue_put(bar, k + 1, next, w) ? 1 : 0;
+          if (!__shfl_sync(0xffffffffu, put, 0)) break;
+          if (next.g < p.g_end) {
+            fetcher_advance(p, nclusters, f);
+            if (f.g < p.g_end && elect_one()) prefetch_item_maps(p.mats[f.tl.mat], f.sp >> 4, (f.sp >> 2) & 3);
+            __syncwarp();
+          }
         } else if (!queue_get_warp(bar, k, it, w)) {
           break;
         }

@@ -261,8 +261,17 @@ __device__ __forceinline__ bool queue_put(Barriers *bar, int k, const QItem &it,
   return true;
 }
 
-// One lane takes item number k of the pair from its CTA's queue and releases
-// the slot on the leader.
+// Release slot k % kQueue on the leader: a relaxed arrive (a consumer only
+// read the slot, and calls this after it has used what it read, so no fence
+// has to wait for its own earlier stores).
+__device__ __forceinline__ void queue_release(Barriers *bar, int k) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+                   mapa_shared(smem_u32(&bar->qempty[k % kQueue]), 0))
+               : "memory");
+}
+
+// One lane takes item number k of the pair from its CTA's queue (the caller
+// releases the slot once it has used the item).
 __device__ __forceinline__ bool queue_get_lane(Barriers *bar, int k, QItem &it, const Waiter &w) {
   const int slot = k % kQueue;
   const uint32_t parity = static_cast<uint32_t>(k / kQueue) & 1u;
@@ -274,11 +283,11 @@ __device__ __forceinline__ bool queue_get_lane(Barriers *bar, int k, QItem &it, 
     const uint4 v = make_uint4(src[q].x, src[q].y, src[q].z, src[q].w);
     dst[q] = v;
   }
-  mbar_arrive_cluster(mapa_shared(smem_u32(&bar->qempty[slot]), 0));
   return true;
 }
 
-// The same for a whole warp: lane 0 takes the item and broadcasts it.
+// The same for a whole warp: lane 0 takes the item, broadcasts it (which
+// uses what it read) and releases the slot.
 __device__ __forceinline__ bool queue_get_warp(Barriers *bar, int k, QItem &it, const Waiter &w) {
   int ok = 1;
   if ((threadIdx.x & 31) == 0) ok = queue_get_lane(bar, k, it, w) ? 1 : 0;
@@ -286,6 +295,7 @@ __device__ __forceinline__ bool queue_get_warp(Barriers *bar, int k, QItem &it, 
   int *v = reinterpret_cast<int *>(&it);
 #pragma unroll
   for (int q = 0; q < 7; ++q) v[q] = __shfl_sync(0xffffffffu, v[q], 0);
+  if (ok && (threadIdx.x & 31) == 0) queue_release(bar, k);
   return ok != 0;
 }
 
@@ -934,8 +944,10 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
       uint32_t acc_phase = 0;
       for (int k = 0;; ++k) {
         QItem it;
-        if (!queue_get_lane(bar, k, it, w) || it.g >= p.g_end) break;
+        if (!queue_get_lane(bar, k, it, w)) break;
         const TileInfo ti = item_info(p, it);
+        queue_release(bar, k);  // after the item was used
+        if (it.g >= p.g_end) break;
         if (ti.skip) {
           if (p.wait && !wait_count(p.done + ti.mat, units_before(*ti.d, it.step(), it.phase()), w)) break;
         } else {

@@ -860,9 +860,15 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int k = 0; ok; ++k) {
-        QItem it;
-        if (!queue_get_warp(bar, k, it, w) || it.g >= p.g_end) break;
+      // items are read from the queue one item ahead (each is published
+      // before the item in front of it is produced), so the step from one
+      // item's last MMAs to the next item's first costs no queue access
+      QItem nxt;
+      bool have = queue_get_warp(bar, 0, nxt, w);
+      for (int k = 0; ok && have; ++k) {
+        const QItem it = nxt;
+        if (it.g >= p.g_end) break;
+        have = queue_get_warp(bar, k + 1, nxt, w);
         const TileInfo ti = item_info(p, it);
         if (ti.skip) continue;
         const ItemPlan pl = plan_item(*ti.d, it.step(), it.phase(), ti.tr, it.direct(), ti.row0, ti.col0, ti.nk);

@@ -303,6 +303,65 @@ __device__ __forceinline__ TileInfo item_info(const TcParams &p, const QItem &it
   return make_tile_info(p, it.phase(), Tile{it.mat, it.row0, it.col0, 0}, it.e0, it.e1, it.tr());
 }
 
+__device__ __forceinline__ TileInfo tile_info(const TcParams &p, int phase, int t) {
+  const Tile tl = (phase < 2 ? p.tiles01 : p.tiles2)[t];
+  return make_tile_info(p, phase, tl, p.ext[2 * tl.mat], p.ext[2 * tl.mat + 1], p.mats[tl.mat].transposed);
+}
+
+// Per-phase launches: the items of one pair (g, g + stride, ...), which
+// every role computes for itself, with their global lookups pipelined, for
+// the single-thread roles whose every stall idles the tensor pipe: while an item runs, the tile record of the item after next and the
+// extents and orientation of the next item are already being loaded. Only
+// loaded values are carried; arithmetic on them waits until the item is taken.
+struct ItemPipe {
+  int g;                   // item taken next
+  int step, phase;         // of item g
+  Tile tl;                 // of item g
+  int e0, e1, tr, direct;  // of item g's matrix
+  int step2, phase2;       // of item g + stride
+  Tile tl2;                // of item g + stride
+};
+
+__device__ __forceinline__ Tile fetch_tile_sp(const TcParams &p, int g, int &step, int &phase) {
+  int t;
+  decode_item(p, g, step, phase, t);
+  return (phase < 2 ? p.tiles01 : p.tiles2)[t];
+}
+
+__device__ __forceinline__ void fetch_matrix_sp(const TcParams &p, ItemPipe &q) {
+  const MatDesc &d = p.mats[q.tl.mat];
+  q.e0 = p.ext[2 * q.tl.mat];
+  q.e1 = p.ext[2 * q.tl.mat + 1];
+  q.tr = d.transposed;
+  q.direct = d.direct;
+}
+
+__device__ __forceinline__ void pipe_start(const TcParams &p, int g, int stride, ItemPipe &q) {
+  q.g = g;
+  if (g < p.g_end) {
+    q.tl = fetch_tile_sp(p, g, q.step, q.phase);
+    fetch_matrix_sp(p, q);
+  }
+  if (g + stride < p.g_end) q.tl2 = fetch_tile_sp(p, g + stride, q.step2, q.phase2);
+}
+
+// Take item q.g (returned through step, phase, ti) and start the lookups of the two after it.
+__device__ __forceinline__ void pipe_take(const TcParams &p, int stride, ItemPipe &q, int &step, int &phase,
+                                          TileInfo &ti, int &direct) {
+  step = q.step;
+  phase = q.phase;
+  ti = make_tile_info(p, q.phase, q.tl, q.e0, q.e1, q.tr);
+  direct = q.direct;
+  q.g += stride;
+  if (q.g < p.g_end) {
+    q.step = q.step2;
+    q.phase = q.phase2;
+    q.tl = q.tl2;
+    fetch_matrix_sp(p, q);
+  }
+  if (q.g + stride < p.g_end) q.tl2 = fetch_tile_sp(p, q.g + stride, q.step2, q.phase2);
+}
+
 // The k-loop of an item as three consecutive k-ranges with a fixed operand
 // order each: [0, e0) both operands MN-major, [e0, e1) the first K-major and
 // the second MN-major, [e1, nk) both K-major (any of them may be empty).
@@ -381,6 +440,24 @@ __device__ __forceinline__ void prefetch_item_maps(const MatDesc &d, int step, i
   if (step == 0) {
     prefetch_tensormap(&d.tm_y);
     prefetch_tensormap(&d.tm_y_mn);
+  }
+}
+
+// The same for an item whose matrix record is known: exactly the maps it reads.
+__device__ __forceinline__ void prefetch_item_maps_exact(const MatDesc &d, int step, int phase, int transposed,
+                                                         int direct) {
+  const bool y = step == 0 && direct;
+  const void *src_k = y ? &d.tm_y : &d.tm_s[step & 1];
+  const void *src_mn = y ? &d.tm_y_mn : &d.tm_s_mn[step & 1];
+  if (phase == 0) {
+    prefetch_tensormap(transposed ? src_mn : src_k);
+  } else if (phase == 1) {
+    prefetch_tensormap(&d.tm_a);
+    prefetch_tensormap(&d.tm_a_mn);
+  } else {
+    prefetch_tensormap(&d.tm_b);
+    prefetch_tensormap(&d.tm_b_mn);
+    prefetch_tensormap(transposed ? src_k : src_mn);
   }
 }
 
@@ -728,6 +805,11 @@ __device__ __forceinline__ bool mma_segment(uint32_t d_tmem, int kb0, int kb1, u
   return true;
 }
 
+// kQueued: the pair's items come from the leader's fetcher through the
+// shared-memory queue (tickets or stride; the single-launch schedule);
+// otherwise every role walks the pair's static stride itself (per-phase
+// launches), which keeps that kernel's code and registers to what it needs.
+template <bool kQueued>
 __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -778,6 +860,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
   volatile int *abort = &bar->abort;
   const Waiter w{abort, p.status, p.wait_limit_ns};
 
+  if constexpr (kQueued) {
   if (tmem_ok && warp == 0) {
     {
       // ---------------------------------------------------- TMA producer (both CTAs)
@@ -968,6 +1051,162 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
     }
   }
 
+  } else {
+  if (tmem_ok && warp == 0) {
+    {
+      // ---------------------------------------------------- TMA producer (both CTAs)
+      // the whole warp runs the loop; one elected lane issues each copy
+      const uint64_t pol = l2_policy_evict_normal();
+      int issued_phase[kStages];
+      for (int s = 0; s < kStages; ++s) issued_phase[s] = -1;
+      int stage = 0;
+      uint32_t phase_bit = 0;
+      bool ok = true;
+      ItemPipe q;
+      pipe_start(p, p.g_begin + cluster, nclusters, q);
+      while (q.g < p.g_end && ok) {
+        int step, phase, direct;
+        TileInfo ti;
+        pipe_take(p, nclusters, q, step, phase, ti, direct);
+        if (q.g < p.g_end && elect_one()) prefetch_item_maps_exact(p.mats[q.tl.mat], q.step, q.phase, q.tr, q.direct);
+        __syncwarp();
+        if (ti.skip) continue;
+        if (p.wait) {
+          // operands come from earlier phases of this matrix, written by
+          // epilogues anywhere on the GPU
+          int ready = 1;
+          if (lane == 0) ready = wait_count(p.done + ti.mat, units_before(*ti.d, step, phase), w) ? 1 : 0;
+          if (!__shfl_sync(0xffffffffu, ready, 0)) break;
+          fence_proxy_async_global();
+        }
+        const ItemPlan pl = plan_item(*ti.d, step, phase, ti.tr, direct, ti.row0, ti.col0, ti.nk);
+        const int a0 = ti.row0 + my_rows, b0 = ti.col0 + static_cast<int>(rank) * (kTcBN / 2);
+        // one k-loop per operand order, so the copies issued are exactly the ones needed
+        ok = produce_segment<1, 1>(0, pl.e0, pl.map[0][0], pl.map[0][1], a0, b0, sA, sB, bar, leader, stage, phase_bit,
+                                   issued_phase, pol, w);
+        if (ok)
+          ok = produce_segment<0, 1>(pl.e0, pl.e1, pl.map[1][0], pl.map[1][1], a0, b0, sA, sB, bar, leader, stage,
+                                     phase_bit, issued_phase, pol, w);
+        if (ok)
+          ok = produce_segment<0, 0>(pl.e1, ti.nk, pl.map[2][0], pl.map[2][1], a0, b0, sA, sB, bar, leader, stage,
+                                     phase_bit, issued_phase, pol, w);
+      }
+      if (*abort && leader && lane == 0) {
+        for (int s = 0; s < kStages; ++s)
+          if (issued_phase[s] >= 0) mbar_drain(&bar->full[s], static_cast<uint32_t>(issued_phase[s]), w);
+      }
+    }
+  } else if (tmem_ok && warp == 1) {
+    if (leader) {
+      // ---------------------------------------------------- pair MMA issuer (leader)
+      // the whole warp runs the loop; one elected lane issues the MMAs and commits
+      int stage = 0;
+      uint32_t phase_bit = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      ItemPipe q;
+      pipe_start(p, p.g_begin + cluster, nclusters, q);
+      while (q.g < p.g_end && ok) {
+        int step, phase, direct;
+        TileInfo ti;
+        pipe_take(p, nclusters, q, step, phase, ti, direct);
+        if (ti.skip) continue;
+        const ItemPlan pl = plan_item(*ti.d, step, phase, ti.tr, direct, ti.row0, ti.col0, ti.nk);
+        if (!warp_mbar_wait<true>(&bar->tempty[acc], acc_phase ^ 1u, w)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * kTcBN);
+        // one k-loop per operand order, so descriptors stay compile-time
+        ok = mma_segment<1, 1>(d_tmem, 0, pl.e0, sA, sB, bar, stage, phase_bit, w);
+        if (ok) ok = mma_segment<0, 1>(d_tmem, pl.e0, pl.e1, sA, sB, bar, stage, phase_bit, w);
+        if (ok) ok = mma_segment<0, 0>(d_tmem, pl.e1, ti.nk, sA, sB, bar, stage, phase_bit, w);
+        if (!ok) break;
+        if (elect_one()) umma_commit_pair_multicast(&bar->tfull[acc], kPairMask);
+        __syncwarp();
+        if (++acc == kAccs) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (elect_one()) {
+        umma_commit_pair_multicast(&bar->drain, 1u);
+        mbar_drain(&bar->drain, 0, w);
+      }
+      __syncwarp();
+    }
+  } else if (tmem_ok && warp < kSignalWarp) {
+    // ------------------------------------------------------ epilogue (both CTAs)
+    // warps 2..9: TMEM lane quarter q = warp % 4 (tile rows q*32 .. q*32+31),
+    // column half h: chunks h*kChunksPerWarp .. of the 256 accumulator columns
+    const int e = warp - 2;
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    const int c0 = (e / 4) * kChunksPerWarp;
+    uint32_t *stage = epi_stage + e * (kEpiStageBytes / 4);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int g = p.g_begin + cluster; g < p.g_end; g += nclusters) {
+      int step, phase, t;
+      decode_item(p, g, step, phase, t);
+      TileInfo ti = tile_info(p, phase, t);
+      if (ti.skip) continue;
+      if (p.wait) {
+        // the operand this epilogue reloads (A, or the current iterate) comes from an earlier phase
+        bool ready = true;
+        if (lane == 0) ready = wait_count(p.done + ti.mat, units_before(*ti.d, step, phase), w);
+        if (!__shfl_sync(0xffffffffu, ready ? 1 : 0, 0)) break;
+      }
+      ti.row0 += my_rows;
+      const StepCtx sc = step_ctx(p, step, ti.mat);
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kTcBN);
+      bool ok;
+      if (phase == 0)
+        ok = epilogue_item<0>(sc, ti, r, c0, tbase, stage, &bar->tfull[acc], acc_phase, w);
+      else if (phase == 1)
+        ok = epilogue_item<1>(sc, ti, r, c0, tbase, stage, &bar->tfull[acc], acc_phase, w);
+      else
+        ok = epilogue_item<2>(sc, ti, r, c0, tbase, stage, &bar->tfull[acc], acc_phase, w);
+      if (!ok) break;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_cluster(mapa_shared(smem_u32(&bar->tempty[acc]), 0));  // TMEM reusable
+        mbar_arrive(&bar->epi_done[acc]);                                   // stores issued (release)
+      }
+      if (++acc == kAccs) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  } else if (tmem_ok && warp == kSignalWarp) {
+    if (lane == 0) {
+      // ---------------------------------------------------- completion signal (both CTAs)
+      // After the CTA's epilogue warps stored an item (their arrivals on
+      // epi_done release the stores to this thread), publish it at GPU scope;
+      // the release is cumulative, so a consumer that acquires the counter
+      // sees every store of the item. Skipped items are published once their
+      // own dependencies are met.
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      for (int g = p.g_begin + cluster; g < p.g_end; g += nclusters) {
+        int step, phase, t;
+        decode_item(p, g, step, phase, t);
+        const TileInfo ti = tile_info(p, phase, t);
+        if (ti.skip) {
+          if (p.wait && !wait_count(p.done + ti.mat, units_before(*ti.d, step, phase), w)) break;
+        } else {
+          if (!mbar_wait(&bar->epi_done[acc], acc_phase, w)) break;
+          if (++acc == kAccs) {
+            acc = 0;
+            acc_phase ^= 1u;
+          }
+        }
+        if (!p.hold_signals) red_release_gpu_add(p.done + ti.mat, 1);
+      }
+    }
+  }
+
+  }
   __syncwarp();
   tc_fence_before();
   __syncthreads();
@@ -978,9 +1217,9 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
 
 int launch_tc_kernel(const TcParams &p, int max_ctas, cudaStream_t s) {
   const int smem = tc_smem_bytes();
-  auto kernel = ns_tc_gemm_kernel;
-  static SmemOptIn opt_in;
-  if (opt_in.ensure(reinterpret_cast<const void *>(kernel), smem)) return -1;
+  auto kernel = p.tickets ? ns_tc_gemm_kernel<true> : ns_tc_gemm_kernel<false>;
+  static SmemOptIn opt_in[2];
+  if (opt_in[p.tickets ? 1 : 0].ensure(reinterpret_cast<const void *>(kernel), smem)) return -1;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;

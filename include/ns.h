@@ -239,6 +239,13 @@ int ns_release_workspace(void);
  * since load (for launch accounting in benchmarks). */
 int64_t ns_num_kernel_launches(void);
 
+/* ns_set_nvtx -- NVTX ranges for profilers' timelines: with enable != 0 every
+ * call is bracketed by a range "ns call" and every kernel launch by a range
+ * naming its class ("ns gram", "ns apply", ...). Off by default, unless the
+ * environment variable NS_NVTX=1 was set when the library first looked.
+ * Process-wide; returns NS_OK. */
+int ns_set_nvtx(int enable);
+
 /* ns_num_workspace_allocations -- device allocations (workspace cache growth)
  * this library has requested in this process since load; calls that reuse the
  * cached workspace, calls given a caller workspace and

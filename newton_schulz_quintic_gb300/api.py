@@ -85,6 +85,8 @@ def load_library() -> ctypes.CDLL:
         lib.ns_muon_update_batched.restype = i32
         lib.ns_muon_update_batched.argtypes = [vp, vp, vp, vp, i32, i32, vp, ctypes.c_float, i32,
                                                ctypes.c_float, i32, vp]
+        lib.ns_set_nvtx.restype = i32
+        lib.ns_set_nvtx.argtypes = [i32]
         lib.ns_num_workspace_allocations.restype = i64
         lib.ns_num_workspace_allocations.argtypes = []
         lib.ns_plan_shards.restype = i32
@@ -367,6 +369,11 @@ def selftest_dependency_timeout(limit_us: int = 20000, stream=None) -> int:
     s = stream if stream is not None else torch.cuda.current_stream()
     return int(load_library().ns_selftest_dependency_timeout(int(limit_us),
                                                              ctypes.c_void_p(s.cuda_stream)))
+
+
+def set_nvtx(enable: bool) -> None:
+    """NVTX ranges around every call and launch of the library (for profilers)."""
+    load_library().ns_set_nvtx(1 if enable else 0)
 
 
 def num_workspace_allocations() -> int:

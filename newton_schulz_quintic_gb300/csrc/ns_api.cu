@@ -15,11 +15,13 @@
 // ever orthogonalised.
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -492,9 +494,35 @@ struct TimedLaunch {
 bool g_timing = false;
 std::vector<TimedLaunch> g_timed;
 
-// Launch `fn` bracketed by events when timing is on.
+// NVTX ranges around every launch and every call (for profilers' timelines),
+// off unless ns_set_nvtx(1) or the environment variable NS_NVTX=1.
+std::atomic<int> g_nvtx{-1};
+bool nvtx_on() {
+  int v = g_nvtx.load();
+  if (v < 0) {
+    const char *e = std::getenv("NS_NVTX");
+    v = (e && e[0] == '1') ? 1 : 0;
+    g_nvtx.store(v);
+  }
+  return v != 0;
+}
+const char *const kKindNames[] = {"ns norm pass", "ns norm finish", "ns gram", "ns square", "ns apply",
+                                  "ns resident", "ns gemm (all phases)", "ns prep", "ns momentum"};
+struct NvtxRange {
+  bool on;
+  explicit NvtxRange(const char *name) : on(nvtx_on()) {
+    if (on) nvtxRangePushA(name);
+  }
+  ~NvtxRange() {
+    if (on) nvtxRangePop();
+  }
+};
+
+// Launch `fn` bracketed by events when timing is on (and by an NVTX range
+// when those are on).
 template <typename F>
 int timed(int kind, cudaStream_t s, F &&fn) {
+  NvtxRange range(kKindNames[kind]);
   if (!g_timing) return fn();
   TimedLaunch t{kind, nullptr, nullptr};
   if (cudaEventCreate(&t.start) != cudaSuccess || cudaEventCreate(&t.stop) != cudaSuccess) return -1;
@@ -635,6 +663,7 @@ int execute(const Layout &L, uint8_t *ws, const uint8_t *blob, int steps, const 
 int run(void *const *X, const int64_t *shapes, int count, int steps, const float *coeffs, float eps, int dtype,
         void *user_ws, size_t user_ws_bytes, cudaStream_t s, int slot = 0, bool table = false,
         const RunOpts &opt = RunOpts()) {
+  NvtxRange range("ns call");
   int rc = validate(X, shapes, count, steps, dtype, true);
   if (rc) return rc;
   if (table && steps > 0 && (!coeffs || steps > kMaxTableSteps)) return NS_EINVAL;
@@ -1008,6 +1037,11 @@ int ns_release_workspace(void) {
 int64_t ns_num_kernel_launches(void) { return g_launches.load(); }
 
 int64_t ns_num_workspace_allocations(void) { return g_allocations.load(); }
+
+int ns_set_nvtx(int enable) {
+  g_nvtx.store(enable ? 1 : 0);
+  return NS_OK;
+}
 
 int ns_set_gemm_schedule(int mode) {
   if (mode != NS_SCHED_PHASE && mode != NS_SCHED_SINGLE) return NS_EINVAL;

@@ -499,3 +499,15 @@ def test_alternating_batches_reuse_their_descriptor_tables():
         assert api.num_workspace_allocations() == allocs
         for r, d in zip(ra + rb, da + db):
             assert torch.equal(r, d.cpu())
+
+
+def test_nvtx_ranges_change_nothing():
+    # the profiler ranges are host-side markers only: the same bits with them on
+    xs = [seeded((640, 1200), torch.bfloat16, 98), seeded((24, 2304), torch.bfloat16, 99)]
+    ref = run_gpu(xs)
+    api.set_nvtx(True)
+    try:
+        got = run_gpu(xs)
+    finally:
+        api.set_nvtx(False)
+    assert all(torch.equal(a, b) for a, b in zip(ref, got))

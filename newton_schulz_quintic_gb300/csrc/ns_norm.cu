@@ -30,7 +30,7 @@
 // element by element into the same slots instead. Zero extents are tested a
 // 16-byte word at a time: a row is non-zero when the OR of its words has a
 // non-zero magnitude bit, a column when the OR over the rows has one in that
-// column's half-word.
+// column's half-word; a lane's last row and last column are tested first.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -73,29 +73,62 @@ __device__ __forceinline__ void divmod(int n, int d, int &q, int &r) {
   }
 }
 
-__device__ __forceinline__ TileLoc locate(const PrepParams &p, int tile) {
+// The matrix a warp is in, kept while its tiles (visited in increasing
+// order) stay in that matrix: a tile's location then needs no memory access,
+// and a new matrix's record is read once, when the warp crosses into it.
+struct Locator {
+  int mat, base, end;  // the matrix and its tiles [base, end) in the call's tile numbering
+  const __nv_bfloat16 *y;
+  __nv_bfloat16 *copy;
+  int M, N, tr, vec, tcols, mtiles;
+};
+
+__device__ __forceinline__ void locator_load(const PrepParams &p, Locator &L) {
+  const MatDesc &d = p.mats[L.mat];
+  L.end = p.tile_prefix[L.mat + 1];
+  L.M = d.M;
+  L.N = d.N;
+  L.tr = d.transposed;
+  L.y = static_cast<const __nv_bfloat16 *>(d.user);
+  L.copy = d.direct ? nullptr : static_cast<__nv_bfloat16 *>(d.s[0]);
+  L.vec = (L.N % 8 == 0) && ((reinterpret_cast<uintptr_t>(L.y) & 15) == 0);
+  L.tcols = (L.N + kPrepTile - 1) / kPrepTile;
+  L.mtiles = (L.M + kPrepTile - 1) / kPrepTile;
+}
+
+// The warp's first tile: a binary search over the tile prefix counts.
+__device__ __forceinline__ void locator_start(const PrepParams &p, int tile, Locator &L) {
   int lo = 0, hi = p.nmats;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
     if (p.tile_prefix[mid] <= tile) lo = mid; else hi = mid;
   }
-  const MatDesc &d = p.mats[lo];
+  L.mat = lo;
+  L.base = p.tile_prefix[lo];
+  locator_load(p, L);
+}
+
+// A later tile of the same warp (tile >= every tile located before).
+__device__ __forceinline__ TileLoc locate(const PrepParams &p, int tile, Locator &L) {
+  while (tile >= L.end) {
+    ++L.mat;
+    L.base = L.end;
+    locator_load(p, L);
+  }
   TileLoc t;
-  t.mat = lo;
-  t.M = d.M;
-  t.N = d.N;
-  t.tr = d.transposed;
-  t.y = static_cast<const __nv_bfloat16 *>(d.user);
-  t.copy = d.direct ? nullptr : static_cast<__nv_bfloat16 *>(d.s[0]);
-  t.vec = (t.N % 8 == 0) && ((reinterpret_cast<uintptr_t>(t.y) & 15) == 0);
-  const int base = p.tile_prefix[lo];
-  const int local = tile - base;
-  const int tcols = (t.N + kPrepTile - 1) / kPrepTile;
+  t.mat = L.mat;
+  t.M = L.M;
+  t.N = L.N;
+  t.tr = L.tr;
+  t.y = L.y;
+  t.copy = L.copy;
+  t.vec = L.vec;
+  const int local = tile - L.base;
   int tr_, tc_;
-  divmod(local, tcols, tr_, tc_);
+  divmod(local, L.tcols, tr_, tc_);
   t.r0 = tr_ * kPrepTile;
   t.c0 = tc_ * kPrepTile;
-  t.wtile = base + (t.tr ? tc_ * ((t.M + kPrepTile - 1) / kPrepTile) + tr_ : local);
+  t.wtile = L.base + (t.tr ? tc_ * L.mtiles + tr_ : local);
   return t;
 }
 
@@ -195,23 +228,34 @@ __device__ __forceinline__ void reduce_half(const TileLoc &t, int h, int lane, c
                                             int &ext_r, int &ext_c) {
   const int br = (lane >> 3) + 4 * h, bc = lane & 7;
   const int R0 = t.r0 + br * 8, C = t.c0 + bc * 8;
-  // extents: which of the 8 rows, and which of the 8 columns, hold a non-zero
-  uint32_t rows = 0;
-  uint4 cols = make_uint4(0, 0, 0, 0);
+  // extents: the last of the 8 rows, and the last of the 8 columns, that
+  // holds a non-zero. Dense data has both in the lane's last row and column,
+  // which are tested first; the full scans run only when one of them is zero.
+  if ((v[7].x | v[7].y | v[7].z | v[7].w) & kMagnitude) {
+    ext_r = max(ext_r, R0 + 7);
+  } else {
+    uint32_t rows = 0;
 #pragma unroll
-  for (int r = 0; r < 8; ++r) {
-    rows |= (((v[r].x | v[r].y | v[r].z | v[r].w) & kMagnitude) != 0 ? 1u : 0u) << r;
-    cols.x |= v[r].x;
-    cols.y |= v[r].y;
-    cols.z |= v[r].z;
-    cols.w |= v[r].w;
+    for (int r = 0; r < 7; ++r) rows |= (((v[r].x | v[r].y | v[r].z | v[r].w) & kMagnitude) != 0 ? 1u : 0u) << r;
+    if (rows) ext_r = max(ext_r, R0 + 31 - __clz(rows));
   }
-  if (rows) ext_r = max(ext_r, R0 + 31 - __clz(rows));
-  const uint32_t cmask = ((cols.x & 0x7FFFu) ? 1u : 0u) | ((cols.x & 0x7FFF0000u) ? 2u : 0u) |
-                         ((cols.y & 0x7FFFu) ? 4u : 0u) | ((cols.y & 0x7FFF0000u) ? 8u : 0u) |
-                         ((cols.z & 0x7FFFu) ? 16u : 0u) | ((cols.z & 0x7FFF0000u) ? 32u : 0u) |
-                         ((cols.w & 0x7FFFu) ? 64u : 0u) | ((cols.w & 0x7FFF0000u) ? 128u : 0u);
-  if (cmask) ext_c = max(ext_c, C + 31 - __clz(cmask));
+  const uint32_t last_col = v[0].w | v[1].w | v[2].w | v[3].w | v[4].w | v[5].w | v[6].w | v[7].w;
+  if (last_col & 0x7FFF0000u) {
+    ext_c = max(ext_c, C + 7);
+  } else {
+    uint4 cols = make_uint4(0, 0, 0, last_col);
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      cols.x |= v[r].x;
+      cols.y |= v[r].y;
+      cols.z |= v[r].z;
+    }
+    const uint32_t cmask = ((cols.x & 0x7FFFu) ? 1u : 0u) | ((cols.x & 0x7FFF0000u) ? 2u : 0u) |
+                           ((cols.y & 0x7FFFu) ? 4u : 0u) | ((cols.y & 0x7FFF0000u) ? 8u : 0u) |
+                           ((cols.z & 0x7FFFu) ? 16u : 0u) | ((cols.z & 0x7FFF0000u) ? 32u : 0u) |
+                           ((cols.w & 0x7FFFu) ? 64u : 0u);
+    if (cmask) ext_c = max(ext_c, C + 31 - __clz(cmask));
+  }
   // exact copy into the first iterate buffer (its pitch: N rounded up to 8 elements)
   if (t.copy && C < t.N) {
     const int ps = (t.N + 7) & ~7;
@@ -246,14 +290,16 @@ __global__ void __launch_bounds__(256, 2) ns_norm_tiles_kernel(PrepParams p, int
   // Every half commits one copy group (empty past the end), so waiting until
   // at most kRing - 1 groups are pending means the half about to be reduced
   // has landed.
-  TileLoc loc = locate(p, tile);
+  Locator L;
+  locator_start(p, tile, L);
+  TileLoc loc = locate(p, tile, L);
   issue_half(loc, 0, lane, ring);
   cp_async_commit();
   issue_half(loc, 1, lane, ring + kSlot);
   cp_async_commit();
   int next = tile + nwarps;
   TileLoc nloc = loc;
-  if (next < total_tiles) nloc = locate(p, next);
+  if (next < total_tiles) nloc = locate(p, next, L);
   int in_slot = 2, out_slot = 0;
   // extents are kept per lane while the warp stays in one matrix and
   // published (one warp reduction, two atomics) when it moves on or finishes
@@ -284,7 +330,7 @@ __global__ void __launch_bounds__(256, 2) ns_norm_tiles_kernel(PrepParams p, int
     tile = next;
     loc = nloc;
     next += nwarps;
-    if (next < total_tiles) nloc = locate(p, next);
+    if (next < total_tiles) nloc = locate(p, next, L);
   }
   cp_async_wait<0>();
   publish_extents(p, ext_mat, ext_r, ext_c, lane);

@@ -16,9 +16,8 @@
 // (a bf16 has 8 significant bits); a sub-block sum is two fixed chains of
 // fp32 fused multiply-adds (see subblock_sumsq).
 //
-// Work split: one warp per 64 x 64 tile of Y at a time; each warp of a
-// persistent grid of two 256-thread blocks per SM takes one contiguous run of
-// the call's tiles. A tile is
+// Work split: one warp per 64 x 64 tile of Y at a time (tiles strided over
+// all warps of a persistent grid of two 256-thread blocks per SM). A tile is
 // read as two halves of 32 rows; lane l holds the 8 x 8 sub-block
 // (l / 8 + 4 h, l % 8) of half h as eight 16-byte rows (each copy instruction
 // of the warp reads 4 rows x 128 contiguous bytes). Each lane streams its own
@@ -284,12 +283,8 @@ __global__ void __launch_bounds__(256, 2) ns_norm_tiles_kernel(PrepParams p, int
   const int nwarps = gridDim.x * 8;
   float *slots = s_blk[warp];
   uint8_t *ring = norm_smem + warp * kWarpRingBytes + lane * 16;
-  // each warp takes one contiguous run of tiles, so it stays in one matrix
-  // (and publishes its extents once) for most of its work
-  const int per = (total_tiles + nwarps - 1) / nwarps;
-  int tile = (blockIdx.x * 8 + warp) * per;
-  const int stop = min(total_tiles, tile + per);
-  if (tile >= stop) return;  // whole warps only; no block-wide barrier follows
+  int tile = blockIdx.x * 8 + warp;
+  if (tile >= total_tiles) return;  // whole warps only; no block-wide barrier follows
   // The copies run two half-tiles (one tile) ahead of the reduction: while
   // the halves of `tile` are reduced, the halves of `next` are being copied.
   // Every half commits one copy group (empty past the end), so waiting until
@@ -302,9 +297,9 @@ __global__ void __launch_bounds__(256, 2) ns_norm_tiles_kernel(PrepParams p, int
   cp_async_commit();
   issue_half(loc, 1, lane, ring + kSlot);
   cp_async_commit();
-  int next = tile + 1;
+  int next = tile + nwarps;
   TileLoc nloc = loc;
-  if (next < stop) nloc = locate(p, next, L);
+  if (next < total_tiles) nloc = locate(p, next, L);
   int in_slot = 2, out_slot = 0;
   // extents are kept per lane while the warp stays in one matrix and
   // published (one warp reduction, two atomics) when it moves on or finishes
@@ -317,7 +312,7 @@ __global__ void __launch_bounds__(256, 2) ns_norm_tiles_kernel(PrepParams p, int
     }
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      if (next < stop) issue_half(nloc, h, lane, ring + in_slot * kSlot);
+      if (next < total_tiles) issue_half(nloc, h, lane, ring + in_slot * kSlot);
       cp_async_commit();
       in_slot = in_slot + 1 == kRing ? 0 : in_slot + 1;
       cp_async_wait<kRing - 1>();  // this lane's copies of half h of `tile` have landed
@@ -331,11 +326,11 @@ __global__ void __launch_bounds__(256, 2) ns_norm_tiles_kernel(PrepParams p, int
     s = warp_sum(s);  // xor butterfly: every lane ends with the same value
     if (lane == 0) p.tile_partials[loc.wtile] = s;
     __syncwarp();
-    if (next >= stop) break;
+    if (next >= total_tiles) break;
     tile = next;
     loc = nloc;
-    next += 1;
-    if (next < stop) nloc = locate(p, next, L);
+    next += nwarps;
+    if (next < total_tiles) nloc = locate(p, next, L);
   }
   cp_async_wait<0>();
   publish_extents(p, ext_mat, ext_r, ext_c, lane);

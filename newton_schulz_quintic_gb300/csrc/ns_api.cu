@@ -173,7 +173,8 @@ struct Layout {
   std::vector<Tile> tiles01, tiles2;
   std::vector<int> prefix;   // prep tile prefix, big.size()+1
   size_t off_mats = 0, off_res = 0, off_t01 = 0, off_t2 = 0, off_prefix = 0, blob_end = 0;
-  size_t off_partials = 0, off_tilepart = 0, off_rscale = 0, off_ext = 0, off_done = 0, off_buffers = 0, total = 0;
+  size_t off_partials = 0, off_tilepart = 0, off_tileext = 0, off_rscale = 0, off_ext = 0, off_done = 0,
+         off_buffers = 0, total = 0;
 };
 
 int validate(void *const *X, const int64_t *shapes, int count, int steps, int dtype, bool check_ptrs) {
@@ -316,6 +317,8 @@ void build_layout(const int64_t *shapes, int count, int dtype, Layout &L) {
   off = align_up(off + L.big.size() * kNormBlocks * sizeof(float), 256);
   L.off_tilepart = off;
   off = align_up(off + static_cast<size_t>(L.prefix.back()) * sizeof(float), 256);
+  L.off_tileext = off;
+  off = align_up(off + static_cast<size_t>(L.prefix.back()) * 2 * sizeof(int), 256);
   L.off_rscale = off;
   off = align_up(off + L.big.size() * sizeof(float), 256);
   L.off_ext = off;
@@ -579,6 +582,7 @@ int execute(const Layout &L, uint8_t *ws, const uint8_t *blob, int steps, const 
   pp.dtype = L.dtype;
   pp.to_user = steps == 0;
   pp.tile_partials = reinterpret_cast<float *>(ws + L.off_tilepart);
+  pp.tile_ext = reinterpret_cast<int *>(ws + L.off_tileext);
   pp.rscale = reinterpret_cast<float *>(ws + L.off_rscale);
   pp.out_scale = opt.out_scale;
   // bf16 with steps: one pass sums Y (and copies it unscaled into the first

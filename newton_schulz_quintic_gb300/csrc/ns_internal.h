@@ -142,6 +142,7 @@ struct PrepParams {
   int dtype;             // StoreType of the caller's data == workspace store type
   int to_user;           // 1: write the normalised matrix back to the caller (steps == 0)
   float *tile_partials;  // bf16 path: one sum of squares per 64x64 tile of W
+  int *tile_ext;         // bf16 path: per 64x64 tile of Y, 1 + its last non-zero row and column (0: none)
   float *rscale;         // bf16 path: per matrix 1 / (||Y||_F + eps)
   float out_scale;       // to_user: the normalised matrix is multiplied by it
 };

@@ -2,7 +2,8 @@
 // matrix Y before the first step.
 //
 // For each matrix it produces the sum of squares of every 64 x 64 tile of W
-// (W = Y, or Y^T when M > N) and the last non-zero row and column of Y, and,
+// (W = Y, or Y^T when M > N) and the last non-zero row and column of every
+// tile of Y (the finish kernel reduces both per matrix, without atomics), and,
 // when the first step cannot read Y itself through TMA, an exact copy of Y in
 // the first iterate buffer. The scale 1/(||Y||_F + eps) is formed from the
 // tile sums by ns_norm_finish_kernel and applied inside the first step's GEMM
@@ -266,15 +267,6 @@ __device__ __forceinline__ void reduce_half(const TileLoc &t, int h, int lane, c
   slots[t.tr ? bc * 8 + br : br * 8 + bc] = subblock_sumsq(v, t.tr);
 }
 
-// Publish a warp's extents of one matrix (the whole warp calls this).
-__device__ __forceinline__ void publish_extents(const PrepParams &p, int mat, int ext_r, int ext_c, int lane) {
-  ext_r = warp_max(ext_r);
-  ext_c = warp_max(ext_c);
-  if (lane == 0 && mat >= 0) {
-    if (ext_r >= 0) atomicMax(&p.ext[2 * mat + 0], ext_r + 1);
-    if (ext_c >= 0) atomicMax(&p.ext[2 * mat + 1], ext_c + 1);
-  }
-}
 
 __global__ void __launch_bounds__(256, 2) ns_norm_tiles_kernel(PrepParams p, int total_tiles) {
   extern __shared__ __align__(16) uint8_t norm_smem[];
@@ -301,15 +293,8 @@ __global__ void __launch_bounds__(256, 2) ns_norm_tiles_kernel(PrepParams p, int
   TileLoc nloc = loc;
   if (next < total_tiles) nloc = locate(p, next, L);
   int in_slot = 2, out_slot = 0;
-  // extents are kept per lane while the warp stays in one matrix and
-  // published (one warp reduction, two atomics) when it moves on or finishes
-  int ext_mat = -1, ext_r = -1, ext_c = -1;
   for (;;) {
-    if (loc.mat != ext_mat) {
-      publish_extents(p, ext_mat, ext_r, ext_c, lane);
-      ext_mat = loc.mat;
-      ext_r = ext_c = -1;
-    }
+    int ext_r = -1, ext_c = -1;  // this tile's last non-zero row and column (caller's orientation)
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       if (next < total_tiles) issue_half(nloc, h, lane, ring + in_slot * kSlot);
@@ -324,7 +309,15 @@ __global__ void __launch_bounds__(256, 2) ns_norm_tiles_kernel(PrepParams p, int
     __syncwarp();
     float s = slots[2 * lane] + slots[2 * lane + 1];
     s = warp_sum(s);  // xor butterfly: every lane ends with the same value
-    if (lane == 0) p.tile_partials[loc.wtile] = s;
+    ext_r = warp_max(ext_r);
+    ext_c = warp_max(ext_c);
+    if (lane == 0) {
+      p.tile_partials[loc.wtile] = s;
+      // the tile's extents, one past the last non-zero row / column (0: none),
+      // at the tile's place in the caller's tile order; ns_norm_finish_kernel
+      // takes the maximum per matrix (no atomics)
+      reinterpret_cast<int2 *>(p.tile_ext)[tile] = make_int2(ext_r + 1, ext_c + 1);
+    }
     __syncwarp();
     if (next >= total_tiles) break;
     tile = next;
@@ -333,7 +326,6 @@ __global__ void __launch_bounds__(256, 2) ns_norm_tiles_kernel(PrepParams p, int
     if (next < total_tiles) nloc = locate(p, next, L);
   }
   cp_async_wait<0>();
-  publish_extents(p, ext_mat, ext_r, ext_c, lane);
 }
 
 }  // namespace

@@ -222,20 +222,41 @@ int launch_prep(const PrepParams &p, int total_tiles, cudaStream_t s) {
 }
 
 // One block per matrix: the tile partial sums of the matrix in a fixed order
-// (strided per thread, then a fixed tree) give r = 1 / (||Y||_F + eps).
+// (strided per thread, then a fixed tree) give r = 1 / (||Y||_F + eps), and
+// the largest of the tiles' extents gives the matrix's non-zero extent.
 __global__ void __launch_bounds__(256) ns_norm_finish_kernel(PrepParams p) {
   const int mat = blockIdx.x;
   const int t0 = p.tile_prefix[mat], t1 = p.tile_prefix[mat + 1];
   float v = 0.f;
-  for (int i = t0 + static_cast<int>(threadIdx.x); i < t1; i += 256) v += p.tile_partials[i];
+  int er = 0, ec = 0;
+  for (int i = t0 + static_cast<int>(threadIdx.x); i < t1; i += 256) {
+    v += p.tile_partials[i];
+    const int2 e = reinterpret_cast<const int2 *>(p.tile_ext)[i];
+    er = max(er, e.x);
+    ec = max(ec, e.y);
+  }
   __shared__ float s_sum[8];
+  __shared__ int s_r[8], s_c[8];
   v = warp_sum(v);
-  if ((threadIdx.x & 31) == 0) s_sum[threadIdx.x >> 5] = v;
+  er = warp_max(er);
+  ec = warp_max(ec);
+  if ((threadIdx.x & 31) == 0) {
+    s_sum[threadIdx.x >> 5] = v;
+    s_r[threadIdx.x >> 5] = er;
+    s_c[threadIdx.x >> 5] = ec;
+  }
   __syncthreads();
   if (threadIdx.x == 0) {
     float t = 0.f;
-    for (int w = 0; w < 8; ++w) t += s_sum[w];
+    int rr = 0, cc = 0;
+    for (int w = 0; w < 8; ++w) {
+      t += s_sum[w];
+      rr = max(rr, s_r[w]);
+      cc = max(cc, s_c[w]);
+    }
     p.rscale[mat] = 1.0f / (sqrtf(t) + p.eps);
+    p.ext[2 * mat + 0] = rr;
+    p.ext[2 * mat + 1] = cc;
   }
 }
 

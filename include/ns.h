@@ -62,6 +62,7 @@ extern "C" {
 #define NS_ETIMEOUT (-5) /* a bounded device-side wait gave up (reported by ns_get_status) */
 #define NS_ENODEV (-6)   /* no CUDA driver or device, or the current device is not sm_100-family */
 #define NS_ETOOBIG (-7)  /* batch needs more scratch than ns_orthogonalize_batched_noalloc holds */
+#define NS_EBOUNDS (-8)  /* a debug build's bounds check caught a store (reported by ns_get_status) */
 
 /*
  * ns_orthogonalize_batched -- Newton-Schulz of `count` matrices, in place.
@@ -221,10 +222,25 @@ int ns_plan_shards(const int64_t *shapes, const int64_t *numels, int count, int 
 /*
  * ns_get_status -- synchronise `stream`, then return and clear the device
  * status word of the current device: NS_OK, or NS_ETIMEOUT if a kernel's
- * bounded wait gave up (its outputs are then unspecified), or NS_ECUDA if
- * the synchronisation itself failed.
+ * bounded wait gave up (its outputs are then unspecified), NS_EBOUNDS if a
+ * debug build's bounds check caught a store outside its buffer (the store was
+ * not made; outputs unspecified), or NS_ECUDA if the synchronisation itself
+ * failed or a CTA pair's tensor-memory allocations disagreed.
  */
 int ns_get_status(void *stream);
+
+/*
+ * Debug builds. Compiled with NS_DEBUG_BOUNDS (e.g. NS_BUILD_TAG=debug
+ * NS_EXTRA_NVCC_FLAGS=-DNS_DEBUG_BOUNDS with the package's build script),
+ * every store of the library's kernels is checked against the buffer it
+ * belongs to; a store outside it is not made and the device status word
+ * records NS_EBOUNDS. Release builds compile the checks away.
+ * ns_selftest_bounds_check exercises the mechanism without touching memory:
+ * one thread asks whether a store one past the end of a 4-byte buffer is in
+ * bounds. Synchronises `stream`. Returns NS_OK in a debug build (the status
+ * word then reads NS_EBOUNDS), NS_EINVAL in a release build.
+ */
+int ns_selftest_bounds_check(void *stream);
 
 /* ns_strerror -- static description of a status code. */
 const char *ns_strerror(int code);

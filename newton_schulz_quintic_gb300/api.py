@@ -16,7 +16,7 @@ NS_F32 = 0
 NS_BF16 = 1
 
 _ERRORS = {0: "NS_OK", -1: "NS_EINVAL", -2: "NS_EALIGN", -3: "NS_ENOMEM", -4: "NS_ECUDA",
-           -5: "NS_ETIMEOUT", -6: "NS_ENODEV", -7: "NS_ETOOBIG"}
+           -5: "NS_ETIMEOUT", -6: "NS_ENODEV", -7: "NS_ETOOBIG", -8: "NS_EBOUNDS"}
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _lock = threading.Lock()
@@ -85,6 +85,8 @@ def load_library() -> ctypes.CDLL:
         lib.ns_muon_update_batched.restype = i32
         lib.ns_muon_update_batched.argtypes = [vp, vp, vp, vp, i32, i32, vp, ctypes.c_float, i32,
                                                ctypes.c_float, i32, vp]
+        lib.ns_selftest_bounds_check.restype = i32
+        lib.ns_selftest_bounds_check.argtypes = [vp]
         lib.ns_set_nvtx.restype = i32
         lib.ns_set_nvtx.argtypes = [i32]
         lib.ns_num_workspace_allocations.restype = i64
@@ -369,6 +371,14 @@ def selftest_dependency_timeout(limit_us: int = 20000, stream=None) -> int:
     s = stream if stream is not None else torch.cuda.current_stream()
     return int(load_library().ns_selftest_dependency_timeout(int(limit_us),
                                                              ctypes.c_void_p(s.cuda_stream)))
+
+
+def selftest_bounds_check(stream=None) -> int:
+    """Exercise a debug build's bounds checks (see include/ns.h); NS_OK in a
+    debug build, NS_EINVAL in a release build."""
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(load_library().ns_selftest_bounds_check(ctypes.c_void_p(s.cuda_stream)))
 
 
 def set_nvtx(enable: bool) -> None:

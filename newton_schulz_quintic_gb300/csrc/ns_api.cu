@@ -564,6 +564,7 @@ int execute(const Layout &L, uint8_t *ws, const uint8_t *blob, int steps, const 
       for (int u = 0; u < 3; ++u) rp.coef[k][u] = co[3 * k + u];
     rp.eps = eps;
     rp.out_scale = opt.out_scale;
+    rp.status = di->status;
     if (timed(5, s, [&] { return launch_resident(rp, g.smem, s); })) return NS_ECUDA;
   }
   if (L.big.empty()) return NS_OK;
@@ -585,6 +586,7 @@ int execute(const Layout &L, uint8_t *ws, const uint8_t *blob, int steps, const 
   pp.tile_ext = reinterpret_cast<int *>(ws + L.off_tileext);
   pp.rscale = reinterpret_cast<float *>(ws + L.off_rscale);
   pp.out_scale = opt.out_scale;
+  pp.status = di->status;
   // bf16 with steps: one pass sums Y (and copies it unscaled into the first
   // iterate buffer where step 0 cannot read Y itself); the first step's
   // epilogues apply 1/(||Y|| + eps). Otherwise: norm, then a scaled copy.
@@ -832,15 +834,18 @@ int ns_muon_update_batched(void *const *G, void *const *Mom, void *const *Out, c
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int sms = 0;
+  int *status = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_mu);
     DevInfo *di = nullptr;
     rc = device_info(&di);
     if (rc) return rc;
     sms = di->sms;
+    status = di->status;
   }
   for (int k0 = 0; k0 < count; k0 += kMomChunk) {
     MomentumParams mp{};
+    mp.status = status;
     mp.mu = mu;
     mp.nesterov = nesterov;
     for (int i = k0; i < std::min(count, k0 + kMomChunk); ++i) {
@@ -1004,7 +1009,9 @@ int ns_get_status(void *stream) {
   if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(int)) != cudaSuccess) return NS_ECUDA;
   const int zero = 0;
   if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int)) != cudaSuccess) return NS_ECUDA;
-  return v == 0 ? NS_OK : NS_ETIMEOUT;
+  // device status codes: 1 a bounded wait gave up, 2 a CTA pair's TMEM
+  // allocations disagreed, 3 a debug build's bounds check caught a store
+  return v == 0 ? NS_OK : v == 3 ? NS_EBOUNDS : v == 2 ? NS_ECUDA : NS_ETIMEOUT;
 }
 
 const char *ns_strerror(int code) {
@@ -1017,6 +1024,7 @@ const char *ns_strerror(int code) {
     case NS_ETIMEOUT: return "a bounded device-side wait gave up";
     case NS_ENODEV: return "no CUDA device or driver, or the current device is not sm_100-family";
     case NS_ETOOBIG: return "batch needs more scratch than the no-allocation entry point's 256 MiB array";
+    case NS_EBOUNDS: return "a debug build's bounds check caught a store outside its buffer (not made)";
     default: return "unknown status";
   }
 }
@@ -1104,6 +1112,23 @@ int ns_selftest_dependency_timeout(int limit_us, void *stream) {
   int v = 0;
   if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(int)) != cudaSuccess) return NS_ECUDA;
   return v != 0 ? NS_OK : NS_ECUDA;
+}
+
+int ns_selftest_bounds_check(void *stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DevInfo *di = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    const int rc = device_info(&di);
+    if (rc) return rc;
+  }
+#ifndef NS_DEBUG_BOUNDS
+  (void)s;
+  return NS_EINVAL;  // a release build: no bounds checks to exercise
+#else
+  if (launch_bounds_probe(di->status, di->probe, s)) return NS_ECUDA;
+  return cudaStreamSynchronize(s) == cudaSuccess ? NS_OK : NS_ECUDA;
+#endif
 }
 
 static void drop_timed() {

@@ -28,9 +28,28 @@ template <> struct Elem<kBF16> {
 // status codes written into the device status word (first writer wins)
 constexpr int kStatusTimeout = 1;
 constexpr int kStatusTmemMismatch = 2;  // a CTA pair got different TMEM addresses
+constexpr int kStatusBounds = 3;        // a debug build's bounds check caught an access (skipped)
 
 __device__ __forceinline__ void set_status(int *status, int code) {
   if (status) atomicCAS(status, 0, code);
+}
+
+// Debug builds (compiled with NS_DEBUG_BOUNDS) check every store of the
+// library's kernels against the buffer it belongs to: an access outside
+// [base, base + size) is not made, and the status word records
+// kStatusBounds. Release builds compile the checks away.
+#ifdef NS_DEBUG_BOUNDS
+constexpr bool kDebugBounds = true;
+#else
+constexpr bool kDebugBounds = false;
+#endif
+
+__device__ __forceinline__ bool in_bounds(const void *p, size_t bytes, const void *base, size_t size, int *status) {
+  if (!kDebugBounds) return true;
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(base);
+  if (a >= b && a - b <= size && bytes <= size - (a - b)) return true;
+  set_status(status, kStatusBounds);
+  return false;
 }
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {

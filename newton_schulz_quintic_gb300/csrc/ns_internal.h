@@ -145,6 +145,7 @@ struct PrepParams {
   int *tile_ext;         // bf16 path: per 64x64 tile of Y, 1 + its last non-zero row and column (0: none)
   float *rscale;         // bf16 path: per matrix 1 / (||Y||_F + eps)
   float out_scale;       // to_user: the normalised matrix is multiplied by it
+  int *status;           // device status word (debug bounds checks)
 };
 
 struct ResParams {
@@ -157,6 +158,7 @@ struct ResParams {
   float coef[kMaxTableSteps][3];    // (a, b, c)
   float eps;
   float out_scale;                  // the result is multiplied by it before the write
+  int *status;                      // device status word (debug bounds checks)
 };
 
 // Momentum step of ns_muon_update_batched: up to kMomChunk matrices per launch.
@@ -169,6 +171,7 @@ struct MomentumParams {
   int count;
   float mu;
   int nesterov;
+  int *status;  // device status word (debug bounds checks)
 };
 
 constexpr int kNormBlocks = 128;  // partial-sum blocks per matrix
@@ -199,6 +202,7 @@ int launch_tc(const TcParams &p, int max_ctas, cudaStream_t s);
 int tc_smem_bytes();
 int launch_wait_probe(int *status, uint64_t limit_ns, int *gave_up, cudaStream_t s);
 int launch_momentum(const MomentumParams &p, int dtype, int sms, cudaStream_t s);
+int launch_bounds_probe(int *status, const void *base, cudaStream_t s);
 int resident_smem_bytes(int m, int ns, int dtype);  // one CTA of a matrix split into ns-column slices
 int resident_cluster(int m, int n);                 // CTAs per matrix of the resident kernel
 int resident_slice(int n, int cluster);             // their slice width

@@ -53,20 +53,34 @@ __global__ void __launch_bounds__(256) ns_momentum_kernel(const __grid_constant_
       T *xe = reinterpret_cast<T *>(&xw);
 #pragma unroll
       for (int e = 0; e < V; ++e) momentum_elem<DT>(ge[e], me[e], xe[e], p.mu, p.nesterov);
-      *reinterpret_cast<uint4 *>(m + i * V) = mw;
-      *reinterpret_cast<uint4 *>(o + i * V) = xw;
+      if (in_bounds(m + i * V, 16, m, n * sizeof(T), p.status)) *reinterpret_cast<uint4 *>(m + i * V) = mw;
+      if (in_bounds(o + i * V, 16, o, n * sizeof(T), p.status)) *reinterpret_cast<uint4 *>(o + i * V) = xw;
     }
     done = nv * V;
   }
   for (int64_t i = done + first; i < n; i += stride) {
     T mv = m[i], xv;
     momentum_elem<DT>(g[i], mv, xv, p.mu, p.nesterov);
-    m[i] = mv;
-    o[i] = xv;
+    if (in_bounds(m + i, sizeof(T), m, n * sizeof(T), p.status)) m[i] = mv;
+    if (in_bounds(o + i, sizeof(T), o, n * sizeof(T), p.status)) o[i] = xv;
   }
 }
 
+// Self-test of the debug bounds checks: one thread asks whether a 16-byte
+// store one past the end of a 4-byte buffer is in bounds. Nothing is stored
+// either way; a debug build records kStatusBounds.
+__global__ void ns_bounds_probe_kernel(int *status, const void *base) {
+  const uint8_t *past = static_cast<const uint8_t *>(base) + 4;
+  (void)in_bounds(past, 16, base, 4, status);
+}
+
 }  // namespace
+
+int launch_bounds_probe(int *status, const void *base, cudaStream_t s) {
+  ns_bounds_probe_kernel<<<1, 1, 0, s>>>(status, base);
+  count_launch();
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
 
 int launch_momentum(const MomentumParams &p, int dtype, int sms, cudaStream_t s) {
   if (p.count <= 0) return 0;

@@ -226,7 +226,7 @@ __device__ __forceinline__ float subblock_sumsq(const uint4 (&v)[8], int tr) {
 // Reduce half h of a tile held in v: the sub-block sum into the warp's slot
 // table (by W index), the lane's extents, and the copy when there is one.
 __device__ __forceinline__ void reduce_half(const TileLoc &t, int h, int lane, const uint4 (&v)[8], float *slots,
-                                            int &ext_r, int &ext_c) {
+                                            int &ext_r, int &ext_c, int *status) {
   const int br = (lane >> 3) + 4 * h, bc = lane & 7;
   const int R0 = t.r0 + br * 8, C = t.c0 + bc * 8;
   // extents: the last of the 8 rows, and the last of the 8 columns, that
@@ -261,8 +261,11 @@ __device__ __forceinline__ void reduce_half(const TileLoc &t, int h, int lane, c
   if (t.copy && C < t.N) {
     const int ps = (t.N + 7) & ~7;
 #pragma unroll
-    for (int r = 0; r < 8; ++r)
-      if (R0 + r < t.M) *reinterpret_cast<uint4 *>(t.copy + static_cast<size_t>(R0 + r) * ps + C) = v[r];
+    for (int r = 0; r < 8; ++r) {
+      __nv_bfloat16 *dst = t.copy + static_cast<size_t>(R0 + r) * ps + C;
+      if (R0 + r < t.M && in_bounds(dst, 16, t.copy, static_cast<size_t>(t.M) * ps * 2, status))
+        *reinterpret_cast<uint4 *>(dst) = v[r];
+    }
   }
   slots[t.tr ? bc * 8 + br : br * 8 + bc] = subblock_sumsq(v, t.tr);
 }
@@ -304,7 +307,7 @@ __global__ void __launch_bounds__(256, 2) ns_norm_tiles_kernel(PrepParams p, int
       uint4 v[8];
       read_half(ring + out_slot * kSlot, v);
       out_slot = out_slot + 1 == kRing ? 0 : out_slot + 1;
-      reduce_half(loc, h, lane, v, slots, ext_r, ext_c);
+      reduce_half(loc, h, lane, v, slots, ext_r, ext_c, p.status);
     }
     __syncwarp();
     float s = slots[2 * lane] + slots[2 * lane + 1];

@@ -423,18 +423,20 @@ __global__ void __launch_bounds__(kResThreads, 1) ns_resident_kernel(const __gri
 
   // 4. write back the non-zero block (rows < meff, columns < nse, widened to
   //    16-byte words: the extra elements are the input's own zeros)
+  const size_t ybytes = static_cast<size_t>(M) * N * sizeof(T);
   if (!tr) {
     if (yvec) {
       const int per = (nse + V - 1) / V;
       for (int e = tid; e < meff * per; e += kResThreads) {
         const int i = e / per, j = (e - i * per) * V;
-        *reinterpret_cast<uint4 *>(y + static_cast<size_t>(i) * N + c0 + j) =
-            *reinterpret_cast<const uint4 *>(w + i * ld + j);
+        T *dst = y + static_cast<size_t>(i) * N + c0 + j;
+        if (in_bounds(dst, 16, y, ybytes, p.status)) *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(w + i * ld + j);
       }
     } else {
       for (int e = tid; e < meff * nse; e += kResThreads) {
         const int i = e / nse, j = e - i * nse;
-        y[static_cast<size_t>(i) * N + c0 + j] = w[i * ld + j];
+        T *dst = y + static_cast<size_t>(i) * N + c0 + j;
+        if (in_bounds(dst, sizeof(T), y, ybytes, p.status)) *dst = w[i * ld + j];
       }
     }
   } else {
@@ -446,12 +448,14 @@ __global__ void __launch_bounds__(kResThreads, 1) ns_resident_kernel(const __gri
         T *t = reinterpret_cast<T *>(&v);
 #pragma unroll
         for (int k = 0; k < V; ++k) t[k] = w[(i + k) * ld + j];
-        *reinterpret_cast<uint4 *>(y + static_cast<size_t>(c0 + j) * N + i) = v;
+        T *dst = y + static_cast<size_t>(c0 + j) * N + i;
+        if (in_bounds(dst, 16, y, ybytes, p.status)) *reinterpret_cast<uint4 *>(dst) = v;
       }
     } else {
       for (int e = tid; e < nse * meff; e += kResThreads) {
         const int j = e / meff, i = e - j * meff;
-        y[static_cast<size_t>(c0 + j) * N + i] = w[i * ld + j];
+        T *dst = y + static_cast<size_t>(c0 + j) * N + i;
+        if (in_bounds(dst, sizeof(T), y, ybytes, p.status)) *dst = w[i * ld + j];
       }
     }
   }

@@ -176,6 +176,7 @@ __global__ void __launch_bounds__(256) ns_prep_kernel(PrepParams p) {
   // writes: destination rows are 16-byte aligned (workspace pitches are
   // multiples of 8 elements; the caller's rows when `vec`)
   auto write_tile = [&](T *dst, int pitch, bool flip, int rows, int cols, bool dst_vec) {
+    const size_t dst_bytes = static_cast<size_t>(rows) * pitch * sizeof(T);  // the destination buffer
     // the tile as seen by the destination: rows x cols = (flip ? 64 cols of Y : 64 rows of Y)
     const int R0 = flip ? c0 : r0, C0 = flip ? r0 : c0;
 #pragma unroll
@@ -189,10 +190,11 @@ __global__ void __launch_bounds__(256) ns_prep_kernel(PrepParams p) {
         T *we = reinterpret_cast<T *>(&w);
 #pragma unroll
         for (int u = 0; u < V; ++u) we[u] = Elem<DT>::from_f(flip ? tile[cv * V + u][rr] : tile[rr][cv * V + u]);
-        *reinterpret_cast<uint4 *>(out) = w;
+        if (in_bounds(out, 16, dst, dst_bytes, p.status)) *reinterpret_cast<uint4 *>(out) = w;
       } else {
         for (int u = 0; u < V && C + u < cols; ++u)
-          out[u] = Elem<DT>::from_f(flip ? tile[cv * V + u][rr] : tile[rr][cv * V + u]);
+          if (in_bounds(out + u, sizeof(T), dst, dst_bytes, p.status))
+            out[u] = Elem<DT>::from_f(flip ? tile[cv * V + u][rr] : tile[rr][cv * V + u]);
       }
     }
   };
@@ -331,9 +333,11 @@ __global__ void __launch_bounds__(256) ns_simt_gemm_kernel(PhaseParams p) {
         if (r < m && c < m && r <= c) {
           float out = val;
           float *dst = static_cast<float *>(PHASE == 0 ? d.a : d.b);
+          const size_t bytes = static_cast<size_t>(m) * pm * 4;
           if (PHASE == 1) out = p.cb * static_cast<const float *>(d.a)[static_cast<size_t>(r) * pm + c] + p.cc * val;
-          dst[static_cast<size_t>(r) * pm + c] = out;
-          dst[static_cast<size_t>(c) * pm + r] = out;
+          float *d0 = dst + static_cast<size_t>(r) * pm + c, *d1 = dst + static_cast<size_t>(c) * pm + r;
+          if (in_bounds(d0, 4, dst, bytes, p.status)) *d0 = out;
+          if (in_bounds(d1, 4, dst, bytes, p.status)) *d1 = out;
         }
       } else {
         if (r < n && c < m) {
@@ -341,12 +345,14 @@ __global__ void __launch_bounds__(256) ns_simt_gemm_kernel(PhaseParams p) {
           const float out0 = p.ca * xt[static_cast<size_t>(r) * pm + c] + val;
           const float out = p.final_step ? out0 * p.out_scale : out0;
           if (!p.final_step) {
-            static_cast<float *>(d.xt[cur ^ 1])[static_cast<size_t>(r) * pm + c] = out;
-            static_cast<float *>(d.x)[static_cast<size_t>(c) * pn + r] = out;
+            float *xt1 = static_cast<float *>(d.xt[cur ^ 1]), *x = static_cast<float *>(d.x);
+            float *d0 = xt1 + static_cast<size_t>(r) * pm + c, *d1 = x + static_cast<size_t>(c) * pn + r;
+            if (in_bounds(d0, 4, xt1, static_cast<size_t>(n) * pm * 4, p.status)) *d0 = out;
+            if (in_bounds(d1, 4, x, static_cast<size_t>(m) * pn * 4, p.status)) *d1 = out;
           } else {
             float *u = static_cast<float *>(d.user);
-            if (d.transposed) u[static_cast<size_t>(r) * d.N + c] = out;
-            else u[static_cast<size_t>(c) * d.N + r] = out;
+            float *d0 = d.transposed ? u + static_cast<size_t>(r) * d.N + c : u + static_cast<size_t>(c) * d.N + r;
+            if (in_bounds(d0, 4, u, static_cast<size_t>(d.M) * d.N * 4, p.status)) *d0 = out;
           }
         }
       }

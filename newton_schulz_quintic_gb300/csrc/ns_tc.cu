@@ -508,6 +508,7 @@ __device__ __forceinline__ int units_before(const MatDesc &d, int step, int phas
 
 // Per-item constants of the epilogue.
 struct StepCtx {
+  int *status;      // device status word (debug bounds checks)
   int step;
   int final_step;   // apply writes the caller's matrix
   float ca, cb, cc;
@@ -518,6 +519,7 @@ struct StepCtx {
 __device__ __forceinline__ StepCtx step_ctx(const TcParams &p, int step, int mat) {
   const float *co = p.coef[p.ncoef == 1 ? 0 : step];
   StepCtx c;
+  c.status = p.status;
   c.step = step;
   c.final_step = step == p.steps - 1;
   c.ca = co[0];
@@ -545,18 +547,26 @@ __device__ __forceinline__ void unpack_row32(const uint4 (&w4)[4], float (&v)[32
 
 // Writes 8 bf16 (one 16-byte word, `o`) at dst = row R, columns C0..C0+7,
 // keeping only elements with column < col_lim and, when upper, column >= R.
+// The destination buffer of a store: where it starts and how many bytes it
+// has (debug builds check every store against it).
+struct StoreBuf {
+  const void *base;
+  size_t bytes;
+  int *status;
+};
+
 __device__ __forceinline__ void store_piece8(__nv_bfloat16 *dst, const uint4 &o, int R, int C0, int col_lim,
-                                             bool upper) {
+                                             bool upper, const StoreBuf &sb) {
   const bool all = (C0 + 8 <= col_lim) && (!upper || C0 >= R) && ((reinterpret_cast<uintptr_t>(dst) & 15) == 0);
   if (all) {
-    *reinterpret_cast<uint4 *>(dst) = o;
+    if (in_bounds(dst, 16, sb.base, sb.bytes, sb.status)) *reinterpret_cast<uint4 *>(dst) = o;
     return;
   }
   const uint32_t w[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
     const int C = C0 + e;
-    if (C < col_lim && (!upper || C >= R))
+    if (C < col_lim && (!upper || C >= R) && in_bounds(dst + e, 2, sb.base, sb.bytes, sb.status))
       dst[e] = __ushort_as_bfloat16(static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1))));
   }
 }
@@ -568,7 +578,9 @@ __device__ __forceinline__ void store_piece8(__nv_bfloat16 *dst, const uint4 &o,
 // row < row_lim, column < col_lim and, if upper, column >= row.
 __device__ __forceinline__ void warp_store_rows(uint32_t *stage, const float (&v)[32], __nv_bfloat16 *base,
                                                 size_t pitch, int row0, int row_lim, int col0, int col_lim,
-                                                bool upper) {
+                                                bool upper, int *status) {
+  // the buffer: row_lim rows of `pitch` elements
+  const StoreBuf sb{base, static_cast<size_t>(row_lim) * pitch * 2, status};
   const int lane = threadIdx.x & 31;
   uint4 *srow = reinterpret_cast<uint4 *>(stage + lane * kRowStageWords);
 #pragma unroll
@@ -583,7 +595,8 @@ __device__ __forceinline__ void warp_store_rows(uint32_t *stage, const float (&v
     const int R = row0 + rl;
     if (R < row_lim) {
       const uint4 o = reinterpret_cast<const uint4 *>(stage + rl * kRowStageWords)[piece];
-      store_piece8(base + static_cast<size_t>(R) * pitch + col0 + 8 * piece, o, R, col0 + 8 * piece, col_lim, upper);
+      store_piece8(base + static_cast<size_t>(R) * pitch + col0 + 8 * piece, o, R, col0 + 8 * piece, col_lim, upper,
+                   sb);
     }
   }
   __syncwarp();
@@ -656,7 +669,7 @@ __device__ __forceinline__ void epilogue_chunk(const StepCtx &p, const TileInfo 
     // the whole upper tile (both halves of a diagonal tile); readers take the
     // lower triangle from the mirrored upper tiles
     __nv_bfloat16 *O = static_cast<__nv_bfloat16 *>(PHASE == 0 ? d.a : d.b);
-    warp_store_rows(stage, f, O, pm, i0, m, jb, m, false);
+    warp_store_rows(stage, f, O, pm, i0, m, jb, m, false, p.status);
   } else {
     // tile rows R over the caller's M, columns C over N
     const int M = d.M, N = d.N;
@@ -680,9 +693,10 @@ __device__ __forceinline__ void epilogue_chunk(const StepCtx &p, const TileInfo 
     for (int t = 0; t < 32; ++t) f[t] = p.as * (p.ca * xo[t] + f[t]);  // r (a Y + B Y) on the first step
     if (!p.final_step)
       warp_store_rows(stage, f, static_cast<__nv_bfloat16 *>(d.s[(p.step + 1) & 1]), static_cast<size_t>(d.ps), R0,
-                      M, C, N, false);
+                      M, C, N, false, p.status);
     else
-      warp_store_rows(stage, f, static_cast<__nv_bfloat16 *>(d.user), static_cast<size_t>(N), R0, M, C, N, false);
+      warp_store_rows(stage, f, static_cast<__nv_bfloat16 *>(d.user), static_cast<size_t>(N), R0, M, C, N, false,
+                      p.status);
   }
 }
 

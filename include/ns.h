@@ -255,6 +255,17 @@ int ns_release_workspace(void);
  * since load (for launch accounting in benchmarks). */
 int64_t ns_num_kernel_launches(void);
 
+/*
+ * ns_set_workspace_limit -- cap, in bytes, on any one workspace the library's
+ * internal cache allocates (per device, stream and use); 0 removes the cap
+ * (the default). A call whose batch needs a larger workspace than the cap and
+ * than the cache already holds returns NS_ENOMEM before anything is allocated
+ * or launched, exactly as when the device allocation itself fails. Calls with
+ * a caller workspace (_ex) and ns_orthogonalize_batched_noalloc are not
+ * affected. Process-wide; returns NS_OK.
+ */
+int ns_set_workspace_limit(size_t bytes);
+
 /* ns_set_nvtx -- NVTX ranges for profilers' timelines: with enable != 0 every
  * call is bracketed by a range "ns call" and every kernel launch by a range
  * naming its class ("ns gram", "ns apply", ...). Off by default, unless the

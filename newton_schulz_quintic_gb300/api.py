@@ -87,6 +87,8 @@ def load_library() -> ctypes.CDLL:
                                                ctypes.c_float, i32, vp]
         lib.ns_selftest_bounds_check.restype = i32
         lib.ns_selftest_bounds_check.argtypes = [vp]
+        lib.ns_set_workspace_limit.restype = i32
+        lib.ns_set_workspace_limit.argtypes = [ctypes.c_size_t]
         lib.ns_set_nvtx.restype = i32
         lib.ns_set_nvtx.argtypes = [i32]
         lib.ns_num_workspace_allocations.restype = i64
@@ -379,6 +381,11 @@ def selftest_bounds_check(stream=None) -> int:
     import torch
     s = stream if stream is not None else torch.cuda.current_stream()
     return int(load_library().ns_selftest_bounds_check(ctypes.c_void_p(s.cuda_stream)))
+
+
+def set_workspace_limit(nbytes: int) -> None:
+    """Cap on any one workspace the library's cache allocates (0: none)."""
+    load_library().ns_set_workspace_limit(int(nbytes))
 
 
 def set_nvtx(enable: bool) -> None:

@@ -35,6 +35,9 @@ namespace ns {
 static std::atomic<int64_t> g_launches{0};
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 static std::atomic<int64_t> g_allocations{0};
+// Largest workspace the library's cache may hold per (device, stream, slot);
+// 0 = no limit (ns_set_workspace_limit).
+static std::atomic<size_t> g_ws_limit{0};
 
 int SmemOptIn::ensure(const void *kernel, int bytes) {
   int dev = 0;
@@ -462,6 +465,8 @@ std::map<WsKey, CachedWs> g_ws;
 
 int ensure_ws(CachedWs &c, size_t bytes, cudaStream_t s) {
   if (c.ptr && c.bytes >= bytes) return NS_OK;
+  const size_t limit = g_ws_limit.load();
+  if (limit && bytes > limit) return NS_ENOMEM;  // refused before any allocation
   drop_blobs(c, s);  // their descriptors point into the old scratch
   if (c.ptr) {
     if (cudaFreeAsync(c.ptr, s) != cudaSuccess) return NS_ECUDA;
@@ -1049,6 +1054,11 @@ int ns_release_workspace(void) {
 int64_t ns_num_kernel_launches(void) { return g_launches.load(); }
 
 int64_t ns_num_workspace_allocations(void) { return g_allocations.load(); }
+
+int ns_set_workspace_limit(size_t bytes) {
+  g_ws_limit.store(bytes);
+  return NS_OK;
+}
 
 int ns_set_nvtx(int enable) {
   g_nvtx.store(enable ? 1 : 0);

@@ -64,3 +64,25 @@ def test_dependency_counter_wait_times_out_and_context_survives():
     finally:
         api.set_gemm_schedule("phase")
 
+
+
+def test_workspace_allocation_failure_is_reported_before_launch():
+    # the host refuses the workspace (as if the allocation failed): NS_ENOMEM,
+    # nothing launched, the matrices untouched, and the library still works
+    g = torch.Generator().manual_seed(5)
+    x = (torch.randn((1024, 2048), generator=g) * 0.02).to(torch.bfloat16)
+    d = x.cuda()
+    api.release_workspace()                      # the cache holds nothing to reuse
+    launches = api.num_kernel_launches()
+    api.set_workspace_limit(1 << 20)             # far below the batch's workspace
+    try:
+        with pytest.raises(api.NSError) as e:
+            api.orthogonalize_batched([d])
+        assert e.value.code == -3                # NS_ENOMEM
+    finally:
+        api.set_workspace_limit(0)
+    torch.cuda.synchronize()
+    assert api.num_kernel_launches() == launches
+    assert torch.equal(d.cpu(), x)
+    assert api.get_status() == 0
+    _parity_call_still_works()

@@ -236,7 +236,8 @@ void build_layout(const int64_t *shapes, int count, int dtype, Layout &L) {
     bool res = resident_fits(m, n, dtype);
     if (res) {  // and one CTA's slice of it fits as laid out
       const int c = resident_cluster(static_cast<int>(m), static_cast<int>(n));
-      res = resident_smem_bytes(static_cast<int>(m), resident_slice(static_cast<int>(n), c), dtype) <= kResidentSmemMax;
+      res = resident_smem_bytes(static_cast<int>(m), resident_slice(static_cast<int>(n), c), dtype, c) <=
+            kResidentSmemMax;
     }
     if (res)
       L.res.push_back(i);
@@ -260,7 +261,7 @@ void build_layout(const int64_t *shapes, int count, int dtype, Layout &L) {
       L.res_groups.push_back(ResGroup{c, static_cast<int>(k), 0, 0});
     ResGroup &g = L.res_groups.back();
     ++g.count;
-    g.smem = std::max(g.smem, resident_smem_bytes(m, ns, dtype));
+    g.smem = std::max(g.smem, resident_smem_bytes(m, ns, dtype, c));
   }
   // largest Newton-Schulz cost first; ties keep the caller's order
   std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
@@ -1125,7 +1126,6 @@ int ns_selftest_dependency_timeout(int limit_us, void *stream) {
 }
 
 int ns_selftest_bounds_check(void *stream) {
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   DevInfo *di = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_mu);
@@ -1133,9 +1133,10 @@ int ns_selftest_bounds_check(void *stream) {
     if (rc) return rc;
   }
 #ifndef NS_DEBUG_BOUNDS
-  (void)s;
+  (void)stream;
   return NS_EINVAL;  // a release build: no bounds checks to exercise
 #else
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (launch_bounds_probe(di->status, di->probe, s)) return NS_ECUDA;
   return cudaStreamSynchronize(s) == cudaSuccess ? NS_OK : NS_ECUDA;
 #endif

@@ -203,7 +203,7 @@ int tc_smem_bytes();
 int launch_wait_probe(int *status, uint64_t limit_ns, int *gave_up, cudaStream_t s);
 int launch_momentum(const MomentumParams &p, int dtype, int sms, cudaStream_t s);
 int launch_bounds_probe(int *status, const void *base, cudaStream_t s);
-int resident_smem_bytes(int m, int ns, int dtype);  // one CTA of a matrix split into ns-column slices
+int resident_smem_bytes(int m, int ns, int dtype, int cluster);  // one CTA of a matrix split over `cluster` CTAs
 int resident_cluster(int m, int n);                 // CTAs per matrix of the resident kernel
 int resident_slice(int n, int cluster);             // their slice width
 

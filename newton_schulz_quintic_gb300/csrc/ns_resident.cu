@@ -11,15 +11,15 @@
 //           in rank order and takes the largest row extent;
 //   gram    every CTA forms the partial W_c W_c^T over its own columns (upper
 //           4 x 4 blocks; the contraction split into slices summed in slice
-//           order) and publishes it in its shared memory; after one cluster
-//           barrier every CTA adds the C partials in rank order through
-//           distributed shared memory (A, both triangles);
+//           order) and stores it into its slot of every CTA's receive buffer
+//           (remote stores through distributed shared memory); after one
+//           cluster barrier every CTA adds the C slots in rank order (A, both
+//           triangles);
 //   square  B = b A + c A A, by every CTA for itself (m <= 64);
 //   apply   W_c' = a W_c + B W_c on the CTA's own columns, in column panels
 //           written back in place.
-// The partials are double-buffered across steps, so one cluster barrier per
-// step orders every exchange. Remote shared memory is read with the loads of
-// several values in flight at once. The first step folds the normalisation in
+// The receive buffers are double-buffered across steps, so one cluster
+// barrier per step orders every exchange, and nothing waits on a remote load. The first step folds the normalisation in
 // (A = r^2 sum of partials, W_1 = r (a W + B W), r = 1 / (||Y||_F + eps)), so
 // the normalised input is never rounded; every later iterate is stored in the
 // working type (bf16 rounding to nearest even between steps, as on the
@@ -46,8 +46,9 @@ __host__ __device__ inline size_t res_align16(size_t v) { return (v + 15) & ~siz
 // and the two partial-gram buffers (mp x ap, fp32), the split-gram scratch.
 struct ResLayout {
   int mp, ld, ap;
-  size_t off_a, off_b, off_p0, off_p1, off_part, total;
-  __host__ __device__ ResLayout(int m, int ns, int elt) {
+  int nent;  // entries of the upper 4 x 4 blocks of an mp x mp matrix
+  size_t off_a, off_b, off_r, off_part, total;
+  __host__ __device__ ResLayout(int m, int ns, int elt, int C) {
     const int vec = 16 / elt;  // elements per 16 bytes
     mp = (m + 3) & ~3;
     ld = ns;
@@ -56,9 +57,10 @@ struct ResLayout {
     if ((ap / 4) % 2 == 0) ap += 4;
     off_a = res_align16(static_cast<size_t>(mp) * ld * elt);
     off_b = res_align16(off_a + static_cast<size_t>(mp) * ap * 4);
-    off_p0 = res_align16(off_b + static_cast<size_t>(mp) * ap * 4);
-    off_p1 = res_align16(off_p0 + static_cast<size_t>(mp) * ap * 4);
-    off_part = res_align16(off_p1 + static_cast<size_t>(mp) * ap * 4);
+    nent = (mp / 4) * (mp / 4 + 1) / 2 * 16;
+    // receive slots of the partial Grams: two step parities x C source ranks
+    off_r = res_align16(off_b + static_cast<size_t>(mp) * ap * 4);
+    off_part = res_align16(off_r + static_cast<size_t>(2) * C * nent * 4);
     total = off_part + static_cast<size_t>(kResPartials) * 4;
   }
 };
@@ -107,6 +109,12 @@ __device__ __forceinline__ float ld_cluster_f32(const float *local, int rank) {
 __device__ __forceinline__ int ld_cluster_i32(const int *local, int rank) {
   return static_cast<int>(ld_shared_cluster_u32(mapa_shared(smem_u32(local), static_cast<uint32_t>(rank))));
 }
+__device__ __forceinline__ void st_cluster_f32(float *local, int rank, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(mapa_shared(smem_u32(local), static_cast<uint32_t>(rank))),
+               "f"(v)
+               : "memory");
+}
+
 // Sum over the cluster's ranks, in rank order, of the float at `local`'s
 // offset in each CTA: the C remote loads are issued together, then added.
 template <int C>
@@ -127,8 +135,8 @@ __device__ __forceinline__ void res_sync(int C) {
 
 }  // namespace
 
-int resident_smem_bytes(int m, int ns, int dtype) {
-  const ResLayout L(m, ns, dtype == kBF16 ? 2 : 4);
+int resident_smem_bytes(int m, int ns, int dtype, int cluster) {
+  const ResLayout L(m, ns, dtype == kBF16 ? 2 : 4, cluster);
   return L.total > (size_t(1) << 30) ? (1 << 30) : static_cast<int>(L.total);
 }
 
@@ -164,12 +172,13 @@ __global__ void __launch_bounds__(kResThreads, 1) ns_resident_kernel(const __gri
   const int M = d.M, N = d.N, m = d.m, n = d.n, tr = d.transposed, ns = d.ns;
   const int c0 = rank * ns;                        // first W column of this CTA
   const int ncols = max(0, min(ns, n - c0));       // W columns held here
-  const ResLayout L(m, ns, sizeof(T));
+  const ResLayout L(m, ns, sizeof(T), C);
   const int ld = L.ld, ap = L.ap, mp = L.mp;
   T *w = reinterpret_cast<T *>(smem);
   float *A = reinterpret_cast<float *>(smem + L.off_a);
   float *B = reinterpret_cast<float *>(smem + L.off_b);
-  float *P0 = reinterpret_cast<float *>(smem + L.off_p0), *P1 = reinterpret_cast<float *>(smem + L.off_p1);
+  float *R = reinterpret_cast<float *>(smem + L.off_r);  // R[(parity * C + source rank) * nent + entry]
+  const int nent = L.nent;
   float *part = reinterpret_cast<float *>(smem + L.off_part);
   T *y = static_cast<T *>(d.user);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -276,7 +285,7 @@ __global__ void __launch_bounds__(kResThreads, 1) ns_resident_kernel(const __gri
     const float ca = co[0], cb = co[1], cc = co[2];
     const float gs = step == 0 ? r * r : 1.f, as0 = step == 0 ? r : 1.f;
     const float as = step == p.steps - 1 ? as0 * p.out_scale : as0;  // the last step applies the output scale
-    float *Pc = (step & 1) ? P1 : P0;
+    float *Rs = R + (step & 1) * C * nent;  // this step's receive slots
     // ---- gram: partial 4 x 4 blocks of W_c W_c^T over k-slices of this CTA's columns
     if (tid < nblk * S) {
       const int b = tid / S, sl = tid - b * S;
@@ -304,48 +313,35 @@ __global__ void __launch_bounds__(kResThreads, 1) ns_resident_kernel(const __gri
         for (int v = 0; v < 4; ++v) part[(sl * nblk + b) * 16 + u * 4 + v] = c4[u][v];
     }
     __syncthreads();
-    for (int e = tid; e < nblk * 16; e += kResThreads) {  // slices in order -> this CTA's partial
+    // slices in order -> this CTA's partial, stored into this rank's slot of
+    // every CTA of the cluster (remote stores: nothing waits on them)
+    for (int e = tid; e < nblk * 16; e += kResThreads) {
       const int b = e >> 4, u = (e >> 2) & 3, v = e & 3;
-      int bi, bj;
-      upper_block(b, mb, bi, bj);
       float sum = 0.f;
       for (int sl = 0; sl < S; ++sl) sum += part[(sl * nblk + b) * 16 + u * 4 + v];
-      Pc[(4 * bi + u) * ap + 4 * bj + v] = sum;
-    }
-    res_sync(C);  // every CTA's partial is published
-    // ---- A = gs * (sum of the partials in rank order), both triangles; each
-    //      thread takes four entries at a time with all their remote loads in
-    //      flight together
-    for (int e0 = tid; e0 < nblk * 16; e0 += 4 * kResThreads) {
-      float v[4][C];
-      int ri[4], rj[4];
+      float *slot = Rs + rank * nent + e;
+      if (C > 1) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int e = e0 + q * kResThreads;
-        ri[q] = -1;
-        rj[q] = 0;
-        if (e < nblk * 16) {
-          const int b = e >> 4, u = (e >> 2) & 3, w4 = e & 3;
-          int bi, bj;
-          upper_block(b, mb, bi, bj);
-          if (bi < bj || u <= w4) {
-            ri[q] = 4 * bi + u;
-            rj[q] = 4 * bj + w4;
-          }
-        }
-        const int src = ri[q] < 0 ? 0 : ri[q] * ap + rj[q];
-#pragma unroll
-        for (int c = 0; c < C; ++c) v[q][c] = C > 1 ? ld_cluster_f32(Pc + src, c) : Pc[src];
+        for (int c = 0; c < C; ++c) st_cluster_f32(slot, c, sum);
+      } else {
+        *slot = sum;
       }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if (ri[q] < 0) continue;
+    }
+    res_sync(C);  // every CTA's partial has landed in every CTA
+    // ---- A = gs * (sum of the partials in rank order), both triangles, from
+    //      this CTA's own receive slots
+    for (int e = tid; e < nblk * 16; e += kResThreads) {
+      const int b = e >> 4, u = (e >> 2) & 3, w4 = e & 3;
+      int bi, bj;
+      upper_block(b, mb, bi, bj);
+      if (bi < bj || u <= w4) {
         float sum = 0.f;
 #pragma unroll
-        for (int c = 0; c < C; ++c) sum += v[q][c];
+        for (int c = 0; c < C; ++c) sum += Rs[c * nent + e];
         sum *= gs;
-        A[ri[q] * ap + rj[q]] = sum;
-        A[rj[q] * ap + ri[q]] = sum;
+        const int i = 4 * bi + u, j = 4 * bj + w4;
+        A[i * ap + j] = sum;
+        A[j * ap + i] = sum;
       }
     }
     __syncthreads();

@@ -27,7 +27,11 @@
 //   warps 2..9  epilogue (both CTAs): tcgen05.ld of its 128 accumulator rows
 //               (two warps per TMEM lane quarter), the fused element-wise step
 //               in fp32, round-to-nearest-even to bf16 and the stores; the
-//               second accumulator lets the next tile's main loop overlap it;
+//               operand the step re-reads (A, or the iterate) is copied ahead
+//               (cp.async) and the results leave through two swizzled 32 x 32
+//               staging tiles per warp, so that every global access of the
+//               warp moves 8 rows x 64 contiguous bytes; the second
+//               accumulator lets the next tile's main loop overlap it;
 //   warp 10     publishes each stored item on its matrix's completion counter.
 // Phases (see ns_internal.h for the layout). Iterates stay in the caller's
 // orientation; step 0 reads the caller's Y directly when TMA can address it.
@@ -56,10 +60,12 @@ constexpr int kEpiWarps = 8;                        // two per TMEM lane quarter
 constexpr int kSignalWarp = 2 + kEpiWarps;          // publishes item completion GPU-wide
 constexpr int kThreads = 32 * (kSignalWarp + 1);    // producer, MMA, epilogue warps, signal warp
 constexpr int kChunksPerWarp = (kTcBN / 32) / (kEpiWarps / 4);
-// per-warp staging tile of the epilogue's coalesced stores: 32 rows of 32 bf16
-// (16 words + 4 pad)
-constexpr int kRowStageWords = 20;
-constexpr int kEpiStageBytes = 32 * kRowStageWords * 4;
+// per-warp staging tiles of the epilogue's coalesced loads and stores: 32 rows
+// of 32 bf16 (16 words), the four 16-byte pieces of a row permuted by an XOR
+// swizzle (see stage_word)
+constexpr int kRowStageWords = 16;
+constexpr int kStageTileWords = 32 * kRowStageWords;
+constexpr int kEpiStageBytes = 2 * kStageTileWords * 4;  // two tiles per warp
 constexpr int kStages = 6;
 constexpr int kABytes = kTcBM * kTcBK * 2;          // 16 KB: this CTA's 128 rows of the first operand
 constexpr int kBBytes = (kTcBN / 2) * kTcBK * 2;    // 16 KB: this CTA's half of the second operand
@@ -536,15 +542,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t *>(&v);
 }
 
-__device__ __forceinline__ void unpack_row32(const uint4 (&w4)[4], float (&v)[32]) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const __nv_bfloat16 *e = reinterpret_cast<const __nv_bfloat16 *>(&w4[q]);
-#pragma unroll
-    for (int u = 0; u < 8; ++u) v[8 * q + u] = __bfloat162float(e[u]);
-  }
-}
-
 // Writes 8 bf16 (one 16-byte word, `o`) at dst = row R, columns C0..C0+7,
 // keeping only elements with column < col_lim and, when upper, column >= R.
 // The destination buffer of a store: where it starts and how many bytes it
@@ -571,6 +568,17 @@ __device__ __forceinline__ void store_piece8(__nv_bfloat16 *dst, const uint4 &o,
   }
 }
 
+// Word offset of 16-byte piece `piece` (0..3) of row `row` (0..31) in a warp's
+// staging tile. The block moves between two layouts: one row per lane (lane l
+// holds row l), and coalesced (in access k, lane l holds piece l % 4 of row
+// 8k + l / 4, so that 8 rows x 64 contiguous bytes of global memory move per
+// instruction). A 16-byte shared-memory access is served eight lanes at a
+// time; XOR-ing the piece index with bits 1..2 of the row puts the eight
+// lanes of either layout on 32 different banks.
+__device__ __forceinline__ int stage_word(int row, int piece) {
+  return row * kRowStageWords + 4 * (piece ^ ((row >> 1) & 3));
+}
+
 // Warp-cooperative store of a 32 x 32 block held one row per lane: lane l
 // holds v[t] = element (row row0 + l, column col0 + t). The rows go through
 // the warp's staging tile so that each store instruction writes 8 rows x 64
@@ -582,11 +590,11 @@ __device__ __forceinline__ void warp_store_rows(uint32_t *stage, const float (&v
   // the buffer: row_lim rows of `pitch` elements
   const StoreBuf sb{base, static_cast<size_t>(row_lim) * pitch * 2, status};
   const int lane = threadIdx.x & 31;
-  uint4 *srow = reinterpret_cast<uint4 *>(stage + lane * kRowStageWords);
 #pragma unroll
   for (int q = 0; q < 4; ++q)
-    srow[q] = make_uint4(pack_bf16x2(v[8 * q + 0], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                         pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+    *reinterpret_cast<uint4 *>(stage + stage_word(lane, q)) =
+        make_uint4(pack_bf16x2(v[8 * q + 0], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                   pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
   __syncwarp();
   const int piece = lane & 3;
 #pragma unroll
@@ -594,7 +602,7 @@ __device__ __forceinline__ void warp_store_rows(uint32_t *stage, const float (&v
     const int rl = 8 * k + (lane >> 2);
     const int R = row0 + rl;
     if (R < row_lim) {
-      const uint4 o = reinterpret_cast<const uint4 *>(stage + rl * kRowStageWords)[piece];
+      const uint4 o = *reinterpret_cast<const uint4 *>(stage + stage_word(rl, piece));
       store_piece8(base + static_cast<size_t>(R) * pitch + col0 + 8 * piece, o, R, col0 + 8 * piece, col_lim, upper,
                    sb);
     }
@@ -602,36 +610,103 @@ __device__ __forceinline__ void warp_store_rows(uint32_t *stage, const float (&v
   __syncwarp();
 }
 
-// The global operand an epilogue chunk reads besides the accumulator (A for
-// square, the current iterate for apply), fetched ahead of time: 32 bf16 of this thread's
-// row when the whole chunk is in range (the common case); edge chunks are
-// read element by element inside epilogue_chunk instead. Both tensors are
-// read-only during the launch.
+// The global operand an epilogue reads besides the accumulator (A for square,
+// the current iterate for apply) over the warp's 32 rows of an item: where
+// its row r0 .. r0+31, column ti.col0 starts and its row pitch, or nullptr
+// when those rows are not all inside the matrix; chunks (32-column blocks)
+// below col_lim lie wholly inside it. Elements of the other blocks are read
+// one by one by epilogue_chunk.
+struct OperandRows {
+  const __nv_bfloat16 *base;
+  int pitch;
+  int col_lim;
+  __device__ __forceinline__ const __nv_bfloat16 *block(int chunk) const {
+    return (base && chunk * 32 + 32 <= col_lim) ? base + chunk * 32 : nullptr;
+  }
+};
+
 template <int PHASE>
-__device__ __forceinline__ void prefetch_chunk(const StepCtx &p, const TileInfo &ti, int r, int chunk,
-                                               uint4 (&out)[4]) {
-  if (PHASE == 0) return;
+__device__ __forceinline__ OperandRows operand_rows(const StepCtx &p, const TileInfo &ti, int r) {
   const MatDesc &d = *ti.d;
-  const uint4 *src = nullptr;
+  const int row = ti.row0 + (r & ~31);
+  OperandRows o;
   if (PHASE == 1) {
-    const int i = ti.row0 + r, jb = ti.col0 + chunk * 32;
-    if (i < d.m && jb + 32 <= d.m)
-      src = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(d.a) + static_cast<size_t>(i) * d.pm + jb);
+    o.pitch = d.pm;
+    o.col_lim = d.m - ti.col0;
+    o.base = row + 32 <= d.m
+                 ? static_cast<const __nv_bfloat16 *>(d.a) + static_cast<size_t>(row) * d.pm + ti.col0
+                 : nullptr;
   } else {
-    const int R = ti.row0 + r, C = ti.col0 + chunk * 32;
-    int sp;
-    const __nv_bfloat16 *S = iterate_src(d, p.step, sp);
-    if (R < d.M && C + 32 <= d.N) src = reinterpret_cast<const uint4 *>(S + static_cast<size_t>(R) * sp + C);
+    const __nv_bfloat16 *S = iterate_src(d, p.step, o.pitch);
+    o.col_lim = d.N - ti.col0;
+    o.base = row + 32 <= d.M ? S + static_cast<size_t>(row) * o.pitch + ti.col0 : nullptr;
+  }
+  return o;
+}
+
+// Fetches a chunk's operand block ahead of time into a staging tile of the
+// warp, coalesced and without registers: in access k lane l copies piece
+// l % 4 (8 bf16) of block row 8k + l / 4 (cp.async, through L2 only), so each
+// access of the warp reads 8 rows x 64 contiguous bytes. Nothing is copied
+// when the block is not whole. One commit group per call and lane.
+__device__ __forceinline__ void fetch_chunk(const OperandRows &op, int chunk, uint32_t *tile) {
+  const __nv_bfloat16 *blk = op.block(chunk);
+  const int lane = threadIdx.x & 31;
+  if (blk) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int row = 8 * k + (lane >> 2), piece = lane & 3;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(tile + stage_word(row, piece))),
+                   "l"(blk + static_cast<size_t>(row) * op.pitch + 8 * piece)
+                   : "memory");
+    }
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Waits until at most N of this lane's fetch_chunk groups are in flight.
+template <int N>
+__device__ __forceinline__ void fetch_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// A block fetched by fetch_chunk reaches one row per lane through the
+// staging tile: staged_row gives lane l the 32 elements (packed, 8 per word)
+// of block row l.
+__device__ __forceinline__ void staged_row(const uint32_t *stage, uint4 (&w4)[4]) {
+  const int lane = threadIdx.x & 31;
+  __syncwarp();
+#pragma unroll
+  for (int q = 0; q < 4; ++q) w4[q] = *reinterpret_cast<const uint4 *>(stage + stage_word(lane, q));
+  __syncwarp();
+}
+
+// The first n (0..32) bf16 of src, zero beyond, packed as staged_row packs a row.
+__device__ __forceinline__ void gather_row(const __nv_bfloat16 *src, int n, uint4 (&w4)[4]) {
+  uint32_t w[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    const uint32_t lo = 2 * e < n ? __bfloat16_as_ushort(src[2 * e]) : 0u;
+    const uint32_t hi = 2 * e + 1 < n ? __bfloat16_as_ushort(src[2 * e + 1]) : 0u;
+    w[e] = lo | (hi << 16);
   }
 #pragma unroll
-  for (int q = 0; q < 4; ++q) out[q] = src ? __ldg(src + q) : make_uint4(0, 0, 0, 0);
+  for (int q = 0; q < 4; ++q) w4[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+}
+
+// Element t (0..31) of a packed row.
+__device__ __forceinline__ float row_elem(const uint4 (&w4)[4], int t) {
+  const uint4 &q = w4[t >> 3];
+  const uint32_t w = ((t >> 1) & 3) == 0 ? q.x : ((t >> 1) & 3) == 1 ? q.y : ((t >> 1) & 3) == 2 ? q.z : q.w;
+  return __uint_as_float((t & 1) ? (w & 0xffff0000u) : (w << 16));
 }
 
 // Epilogue of one 32-column chunk held by one thread: tile row r, columns
-// chunk*32 .. chunk*32+31 of the tile; `pre` is prefetch_chunk's result.
+// chunk*32 .. chunk*32+31 of the tile. When the chunk's operand block is
+// whole (`staged`) it is already in the staging tile `stage` (fetch_chunk).
 template <int PHASE>
 __device__ __forceinline__ void epilogue_chunk(const StepCtx &p, const TileInfo &ti, int r, int chunk,
-                                               const uint32_t (&raw)[32], const uint4 (&pre)[4], uint32_t *stage) {
+                                               const uint32_t (&raw)[32], bool staged, uint32_t *stage) {
   const MatDesc &d = *ti.d;
   const int r0 = r & ~31;  // the warp's first tile row
   float f[32];
@@ -650,21 +725,15 @@ __device__ __forceinline__ void epilogue_chunk(const StepCtx &p, const TileInfo 
       for (int t = 0; t < 32; ++t) f[t] *= p.gs;  // A = r^2 Y Y^T on the first step
     }
     const bool mine = i < m;
-    const bool full = jb + 32 <= m;
     if (PHASE == 1) {
       const __nv_bfloat16 *A = static_cast<const __nv_bfloat16 *>(d.a) + static_cast<size_t>(i) * pm + jb;
-      float aold[32];
-      if (full) {
-        unpack_row32(pre, aold);
-      } else {
+      uint4 aold[4];
+      if (staged)  // warp-uniform
+        staged_row(stage, aold);
+      else
+        gather_row(A, mine ? min(32, m - jb) : 0, aold);
 #pragma unroll
-        for (int t = 0; t < 32; ++t) {
-          const int j = jb + t;
-          aold[t] = (mine && j < m) ? __bfloat162float(A[t]) : 0.f;
-        }
-      }
-#pragma unroll
-      for (int t = 0; t < 32; ++t) f[t] = p.cb * aold[t] + p.cc * f[t];
+      for (int t = 0; t < 32; ++t) f[t] = p.cb * row_elem(aold, t) + p.cc * f[t];
     }
     // the whole upper tile (both halves of a diagonal tile); readers take the
     // lower triangle from the mirrored upper tiles
@@ -678,19 +747,16 @@ __device__ __forceinline__ void epilogue_chunk(const StepCtx &p, const TileInfo 
     const int C = ti.col0 + chunk * 32;
     if (R0 >= M || C >= N) return;       // warp-uniform
     const bool mine = R < M;
-    const bool full = C + 32 <= N;
     int sp;
     const __nv_bfloat16 *S = iterate_src(d, p.step, sp);
     S += static_cast<size_t>(R) * sp + C;
-    float xo[32];
-    if (full) {
-      unpack_row32(pre, xo);
-    } else {
+    uint4 xo[4];
+    if (staged)  // warp-uniform
+      staged_row(stage, xo);
+    else
+      gather_row(S, mine ? min(32, N - C) : 0, xo);
 #pragma unroll
-      for (int t = 0; t < 32; ++t) xo[t] = (mine && C + t < N) ? __bfloat162float(S[t]) : 0.f;
-    }
-#pragma unroll
-    for (int t = 0; t < 32; ++t) f[t] = p.as * (p.ca * xo[t] + f[t]);  // r (a Y + B Y) on the first step
+    for (int t = 0; t < 32; ++t) f[t] = p.as * (p.ca * row_elem(xo, t) + f[t]);  // r (a Y + B Y) on the first step
     if (!p.final_step)
       warp_store_rows(stage, f, static_cast<__nv_bfloat16 *>(d.s[(p.step + 1) & 1]), static_cast<size_t>(d.ps), R0,
                       M, C, N, false, p.status);
@@ -720,10 +786,18 @@ template <int PHASE>
 __device__ __forceinline__ bool epilogue_item(const StepCtx &sc, const TileInfo &ti, int r, int c0, uint32_t tbase,
                                               uint32_t *stage, uint64_t *tfull, uint32_t parity, const Waiter &w) {
   // the operand does not depend on the accumulator: fetch it while the MMAs run
-  uint4 pre[2][4];
-  prefetch_chunk<PHASE>(sc, ti, r, c0, pre[0]);
-  prefetch_chunk<PHASE>(sc, ti, r, c0 + 1, pre[1]);
-  if (!mbar_wait<true>(tfull, parity, w)) return false;
+  // staging tiles: chunk c0 + k uses tile k % 2 for its operand block and its stores
+  uint32_t *tiles[2] = {stage, stage + kStageTileWords};
+  OperandRows op{};
+  if (PHASE != 0) {
+    op = operand_rows<PHASE>(sc, ti, r);
+    fetch_chunk(op, c0, tiles[0]);
+    fetch_chunk(op, c0 + 1, tiles[1]);
+  }
+  if (!mbar_wait<true>(tfull, parity, w)) {
+    fetch_wait<0>();  // no copy into the staging tiles outlives the item
+    return false;
+  }
   tc_fence_after();
   // TMEM loads double-buffered: chunk c+1 is read while chunk c is stored
   uint32_t va[32], vb[32];
@@ -739,11 +813,18 @@ __device__ __forceinline__ bool epilogue_item(const StepCtx &sc, const TileInfo 
       __syncwarp();
       tmem_ld32(tbase + static_cast<uint32_t>((c + 1) * 32), next_v);
     }
-    uint4 px[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) px[u] = pre[k & 1][u];
-    if (k + 2 < kChunksPerWarp) prefetch_chunk<PHASE>(sc, ti, r, c + 2, pre[k & 1]);
-    epilogue_chunk<PHASE>(sc, ti, r, c, cur_v, px, stage);
+    bool staged = false;
+    if (PHASE != 0) {
+      staged = op.block(c) != nullptr;
+      // this chunk's copies have landed (chunk c + 1's may still be in flight)
+      if (k + 1 < kChunksPerWarp)
+        fetch_wait<1>();
+      else
+        fetch_wait<0>();
+    }
+    epilogue_chunk<PHASE>(sc, ti, r, c, cur_v, staged, tiles[k & 1]);
+    // the tile is free again (epilogue_chunk ends converged): chunk c + 2's operand into it
+    if (PHASE != 0 && k + 2 < kChunksPerWarp) fetch_chunk(op, c + 2, tiles[k & 1]);
     if (k + 1 < kChunksPerWarp) {
       __syncwarp();
       tmem_ld_wait(next_v);
@@ -1011,6 +1092,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
         bool ready = true;
         if (lane == 0) ready = wait_count(p.done + ti.mat, units_before(*ti.d, it.step(), it.phase()), w);
         if (!__shfl_sync(0xffffffffu, ready ? 1 : 0, 0)) break;
+        __syncwarp();  // orders the other lanes' reads after lane 0's acquire
       }
       ti.row0 += my_rows;
       const StepCtx sc = step_ctx(p, it.step(), ti.mat);
@@ -1276,6 +1358,9 @@ int launch_tc_kernel(const TcParams &p, int max_ctas, cudaStream_t s) {
 }
 
 }  // namespace
+
+static_assert(1024 + kStages * kStageBytes + kBarrierBytes + kEpiWarps * kEpiStageBytes <= 227 * 1024,
+              "shared memory of the tensor-core kernel");
 
 int tc_smem_bytes() { return 1024 + kStages * kStageBytes + kBarrierBytes + kEpiWarps * kEpiStageBytes; }
 

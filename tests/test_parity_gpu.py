@@ -460,6 +460,35 @@ def test_capture_in_cuda_graph_after_warmup(dtype, shapes):
             assert torch.equal(r, d.cpu())
 
 
+def test_remainder_pair_in_one_cuda_graph():
+    # a batch called as a full group and its remainder (64 + 12, no zero
+    # matrices), both calls captured in one graph: every replay gives the bits
+    # of the two plain calls, and the oracle's result within tolerance
+    xs = [seeded((256, 768), torch.bfloat16, seed=300 + i) for i in range(76)]
+    calls = [slice(0, 64), slice(64, 76)]
+    ref = run_gpu(xs, calls=calls)
+    dev = [x.cuda() for x in xs]
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for sl in calls:                        # warm-up on the capture stream
+            api.orthogonalize_batched(dev[sl])
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for sl in calls:
+            api.orthogonalize_batched(dev[sl])
+    for _ in range(2):
+        for d, x in zip(dev, xs):
+            d.copy_(x.cuda())
+        g.replay()
+        torch.cuda.synchronize()
+        assert api.get_status() == 0
+        for r, d in zip(ref, dev):
+            assert torch.equal(r, d.cpu())
+    for i in (0, 63, 64, 75):
+        check_one(xs[i], ref[i])
+
+
 def test_prepared_batch_matches_plain_call():
     # arguments marshalled once, called twice on fresh inputs: the same bits
     # as the plain call every time

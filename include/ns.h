@@ -306,14 +306,37 @@ int ns_get_kernel_times(double *ms, int64_t *launches, int n);
  *                    step and phase; an item waits, on a per-matrix completion
  *                    counter, until the earlier phases of its matrix are done,
  *                    so phases of different matrices overlap. On GB300 it
- *                    measured 10-20% slower than NS_SCHED_PHASE on the
+ *                    measured 0-3% slower than NS_SCHED_PHASE on the
  *                    8 x 8192x6144, 76 x 2048x6144 and mixed 120-matrix
  *                    batches, so it is not the default.
- * Results are the same in both. Returns NS_OK or NS_EINVAL.
+ * Results are the same in both. The fp32 tensor-core path (ns_set_f32_gemm)
+ * always uses NS_SCHED_PHASE. Returns NS_OK or NS_EINVAL.
  */
 #define NS_SCHED_PHASE 0
 #define NS_SCHED_SINGLE 1
 int ns_set_gemm_schedule(int mode);
+
+/*
+ * ns_set_f32_gemm -- how later calls compute the GEMMs of large fp32 matrices
+ * (those not on the shared-memory resident path), process-wide:
+ *   NS_F32_TENSOR  tcgen05 tensor cores (default): every fp32 tensor (the
+ *                  iterate, A and B) is held as three bf16 slices
+ *                  x = h + m + l, h = bf16(x), m = bf16(x - h),
+ *                  l = bf16(x - h - m) (24 significant bits), and each
+ *                  product is the fp32-accumulated sum of the six slice
+ *                  products of weight 2^-16 or more: (h,h), (h,m), (m,h),
+ *                  (h,l), (l,h), (m,m). The three dropped products are below
+ *                  2^-24 of the leading one, so results stay within fp32's
+ *                  1e-4 parity bar of the fp64 oracle.
+ *   NS_F32_SIMT    CUDA-core fp32 FMA GEMMs.
+ * Both follow the same definition (the quintic iteration in fp32 between
+ * phases); their rounding differs, so their results differ in the last
+ * bits. The workspace size (ns_workspace_bytes) depends on the mode in effect
+ * when it is computed. Returns NS_OK or NS_EINVAL.
+ */
+#define NS_F32_TENSOR 0
+#define NS_F32_SIMT 1
+int ns_set_f32_gemm(int mode);
 
 /*
  * ns_selftest_wait_timeout -- failure-detection self-test. Launches one CTA

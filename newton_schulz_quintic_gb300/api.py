@@ -97,6 +97,8 @@ def load_library() -> ctypes.CDLL:
         lib.ns_plan_shards.argtypes = [vp, vp, i32, i32, ctypes.c_double, i32, vp, vp]
         lib.ns_set_gemm_schedule.restype = i32
         lib.ns_set_gemm_schedule.argtypes = [i32]
+        lib.ns_set_f32_gemm.restype = i32
+        lib.ns_set_f32_gemm.argtypes = [i32]
         lib.ns_set_kernel_timing.restype = i32
         lib.ns_set_kernel_timing.argtypes = [i32]
         lib.ns_get_kernel_times.restype = i32
@@ -423,6 +425,17 @@ def plan_shards(shapes, nshards: int, numel_eps: float = 0.3, order: str = "cost
 
 
 GEMM_SCHEDULES = {"phase": 0, "single": 1}
+
+
+F32_GEMMS = {"tensor": 0, "simt": 1}
+
+
+def set_f32_gemm(mode: str) -> None:
+    """GEMMs of large fp32 matrices: 'tensor' (default; tcgen05 on three bf16
+    slices per tensor, six slice products per GEMM) or 'simt' (CUDA-core fp32)."""
+    rc = load_library().ns_set_f32_gemm(F32_GEMMS[mode])
+    if rc != 0:
+        raise NSError(rc, "ns_set_f32_gemm")
 
 
 def set_gemm_schedule(mode: str) -> None:

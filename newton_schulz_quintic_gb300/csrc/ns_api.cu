@@ -143,6 +143,29 @@ int encode_bf16(CUtensorMap *map, void *base, int64_t rows, int64_t cols, int64_
   return r == CUDA_SUCCESS ? NS_OK : NS_ECUDA;
 }
 
+// The three bf16 slices of a rows x cols tensor (fp32 path), `slice` elements
+// apart, as one 3-D map whose third coordinate is the slice; boxes
+// {64 columns, box_rows rows, 1 slice} with 128-byte swizzle.
+int encode_bf16_sliced(CUtensorMap *map, void *base, int64_t rows, int64_t cols, int64_t pitch, int64_t slice,
+                       int box_rows) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(std::max<int64_t>(cols, 1)),
+                        static_cast<cuuint64_t>(std::max<int64_t>(rows, 1)), 3};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(pitch * 2), static_cast<cuuint64_t>(slice * 2)};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? NS_OK : NS_ECUDA;
+}
+
+int encode_iterate_sliced(CUtensorMap *kmajor, CUtensorMap *mnmajor, void *base, int64_t rows, int64_t cols,
+                          int64_t pitch) {
+  const int64_t slice = rows * pitch;
+  int rc = encode_bf16_sliced(kmajor, base, rows, cols, pitch, slice, kTcBM);
+  return rc ? rc : encode_bf16_sliced(mnmajor, base, rows, cols, pitch, slice, 64);
+}
+
 // The two maps of one tensor read both ways: K-major box {64, 128}, MN-major box {64, 64}.
 int encode_iterate(CUtensorMap *kmajor, CUtensorMap *mnmajor, void *base, int64_t rows, int64_t cols,
                    int64_t pitch) {
@@ -169,6 +192,8 @@ struct ResGroup {
 struct Layout {
   int dtype = 0;
   int elt = 2;
+  bool split = false;        // fp32 on the tensor cores (three bf16 slices per tensor)
+  bool tc() const { return dtype == NS_BF16 || split; }
   std::vector<BigMat> big;   // cost order
   std::vector<int> res;      // caller indices on the resident path, grouped by cluster size
   std::vector<int> res_ns;   // their slice widths
@@ -223,10 +248,16 @@ bool resident_fits(int64_t m, int64_t n, int dtype) {
   return mp * np * elt + 2 * mp * (mp + 1) * 4 + 16 * 1024 <= kResidentSmemMax;
 }
 
+// Large fp32 matrices: the tensor-core path (three bf16 slices per tensor,
+// six slice products per GEMM) by default, or the CUDA-core GEMMs
+// (ns_set_f32_gemm).
+std::atomic<int> g_f32_gemm{NS_F32_TENSOR};
+
 void build_layout(const int64_t *shapes, int count, int dtype, Layout &L) {
   L = Layout();
   L.dtype = dtype;
   L.elt = dtype == NS_BF16 ? 2 : 4;
+  L.split = dtype == NS_F32 && g_f32_gemm.load() == NS_F32_TENSOR;
   std::vector<int> order;
   std::vector<int> res_cluster;  // indexed by caller index
   for (int i = 0; i < count; ++i) {
@@ -267,8 +298,8 @@ void build_layout(const int64_t *shapes, int count, int dtype, Layout &L) {
   std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
     return ns_cost(shapes[2 * a], shapes[2 * a + 1]) > ns_cost(shapes[2 * b], shapes[2 * b + 1]);
   });
-  const int BM = dtype == NS_BF16 ? kTcPairM : kSimtBM;  // bf16: rows of one CTA pair
-  const int BN = dtype == NS_BF16 ? kTcBN : kSimtBN;
+  const int BM = L.tc() ? kTcPairM : kSimtBM;  // tensor cores: rows of one CTA pair
+  const int BN = L.tc() ? kTcBN : kSimtBN;
   L.prefix.push_back(0);
   for (int idx : order) {
     BigMat b{};
@@ -292,9 +323,9 @@ void build_layout(const int64_t *shapes, int count, int dtype, Layout &L) {
       for (int64_t c0 = 0; c0 < b.m; c0 += BN)
         for (int64_t r0 = g0; r0 < std::min(b.m, g0 + gstep); r0 += BM)
           if (c0 + BN > r0) L.tiles01.push_back(Tile{mi, static_cast<int>(r0), static_cast<int>(c0), 0});
-    // apply: bf16, tiles of the next iterate in the caller's orientation
-    // (M x N); fp32, tiles of W'^T (n x m)
-    const int64_t arows = dtype == NS_BF16 ? b.M : b.n, acols = dtype == NS_BF16 ? b.N : b.m;
+    // apply: tensor cores, tiles of the next iterate in the caller's
+    // orientation (M x N); CUDA cores, tiles of W'^T (n x m)
+    const int64_t arows = L.tc() ? b.M : b.n, acols = L.tc() ? b.N : b.m;
     for (int64_t g0 = 0; g0 < arows; g0 += gstep)
       for (int64_t c0 = 0; c0 < acols; c0 += BN)
         for (int64_t r0 = g0; r0 < std::min(arows, g0 + gstep); r0 += BM)
@@ -331,6 +362,17 @@ void build_layout(const int64_t *shapes, int count, int dtype, Layout &L) {
   off = align_up(off + (L.big.size() + 1) * sizeof(int), kAlign);
   L.off_buffers = off;
   for (BigMat &b : L.big) {
+    if (L.split) {  // iterates, A and B as three bf16 slices each
+      b.off_s0 = off;
+      off = align_up(off + 3 * static_cast<size_t>(b.M * b.ps) * 2, kAlign);
+      b.off_s1 = off;
+      off = align_up(off + 3 * static_cast<size_t>(b.M * b.ps) * 2, kAlign);
+      b.off_a = off;
+      off = align_up(off + 3 * static_cast<size_t>(b.m * b.pm) * 2, kAlign);
+      b.off_b = off;
+      off = align_up(off + 3 * static_cast<size_t>(b.m * b.pm) * 2, kAlign);
+      continue;
+    }
     if (dtype == NS_BF16) {  // two iterate buffers in the caller's orientation
       b.off_s0 = off;
       off = align_up(off + static_cast<size_t>(b.M * b.ps) * L.elt, kAlign);
@@ -362,7 +404,7 @@ bool reads_y_directly(const void *y, int64_t N, int steps) {
 int build_blob(const Layout &L, void *const *X, const int64_t *shapes, int steps, uint8_t *ws,
                std::vector<uint8_t> &blob) {
   blob.assign(L.blob_end, 0);
-  if (L.dtype == NS_BF16 && !L.big.empty()) {
+  if (L.tc() && !L.big.empty()) {
     int rc = get_encode();
     if (rc) return rc;
   }
@@ -371,7 +413,7 @@ int build_blob(const Layout &L, void *const *X, const int64_t *shapes, int steps
     const BigMat &b = L.big[k];
     MatDesc d;
     std::memset(&d, 0, sizeof(d));
-    if (L.dtype == NS_BF16) {
+    if (L.tc()) {
       d.s[0] = ws + b.off_s0;
       d.s[1] = ws + b.off_s1;
     } else {
@@ -393,7 +435,13 @@ int build_blob(const Layout &L, void *const *X, const int64_t *shapes, int steps
     d.index = b.index;
     d.t01 = b.t01;
     d.t2 = b.t2;
-    if (L.dtype == NS_BF16) {
+    if (L.split) {  // step 0 reads s[0], which the preparation fills
+      int rc = encode_iterate_sliced(&d.tm_a, &d.tm_a_mn, d.a, b.m, b.m, b.pm);
+      rc = rc ? rc : encode_iterate_sliced(&d.tm_b, &d.tm_b_mn, d.b, b.m, b.m, b.pm);
+      rc = rc ? rc : encode_iterate_sliced(&d.tm_s[0], &d.tm_s_mn[0], d.s[0], b.M, b.N, b.ps);
+      rc = rc ? rc : encode_iterate_sliced(&d.tm_s[1], &d.tm_s_mn[1], d.s[1], b.M, b.N, b.ps);
+      if (rc) return rc;
+    } else if (L.dtype == NS_BF16) {
       d.direct = reads_y_directly(d.user, b.N, steps);
       int rc = encode_iterate(&d.tm_a, &d.tm_a_mn, d.a, b.m, b.m, b.pm);
       rc = rc ? rc : encode_iterate(&d.tm_b, &d.tm_b_mn, d.b, b.m, b.m, b.pm);
@@ -600,6 +648,9 @@ int execute(const Layout &L, uint8_t *ws, const uint8_t *blob, int steps, const 
   if (fused) {
     if (timed(0, s, [&] { return launch_norm_tiles(pp, L.prefix.back(), 2 * di->sms, s); })) return NS_ECUDA;
     if (timed(1, s, [&] { return launch_norm_finish(pp, s); })) return NS_ECUDA;
+  } else if (L.split && steps > 0) {  // fp32 on the tensor cores: the slices of Y / (||Y|| + eps) into s[0]
+    if (timed(0, s, [&] { return launch_norm(pp, s); })) return NS_ECUDA;
+    if (timed(7, s, [&] { return launch_split_prep(pp, L.prefix.back(), s); })) return NS_ECUDA;
   } else {
     if (timed(0, s, [&] { return launch_norm(pp, s); })) return NS_ECUDA;
     if (timed(7, s, [&] { return launch_prep(pp, L.prefix.back(), s); })) return NS_ECUDA;
@@ -607,7 +658,7 @@ int execute(const Layout &L, uint8_t *ws, const uint8_t *blob, int steps, const 
   const Tile *t01 = reinterpret_cast<const Tile *>(blob + L.off_t01);
   const Tile *t2 = reinterpret_cast<const Tile *>(blob + L.off_t2);
   if (steps == 0) return NS_OK;
-  if (L.dtype == NS_BF16) {
+  if (L.tc()) {
     TcParams tp{};
     tp.tiles01 = t01;
     tp.tiles2 = t2;
@@ -619,7 +670,8 @@ int execute(const Layout &L, uint8_t *ws, const uint8_t *blob, int steps, const 
     tp.status = di->status;
     tp.done = done;
     tp.ticket = done + nbig;
-    tp.rscale = pp.rscale;
+    tp.rscale = L.split ? nullptr : pp.rscale;  // the fp32 slices are already normalised
+    tp.split = L.split ? 1 : 0;
     tp.wait_limit_ns = opt.wait_limit_ns;
     tp.out_scale = opt.out_scale;
     tp.hold_signals = opt.hold_signals ? 1 : 0;
@@ -628,7 +680,8 @@ int execute(const Layout &L, uint8_t *ws, const uint8_t *blob, int steps, const 
       for (int u = 0; u < 3; ++u) tp.coef[k][u] = co[3 * k + u];
     const int per_step = 2 * tp.n01 + tp.n2;
     int rc = 1;
-    if ((opt.hold_signals || !phase_launches()) && static_cast<int64_t>(steps) * per_step < (int64_t(1) << 30)) {
+    if (!L.split && (opt.hold_signals || !phase_launches()) &&
+        static_cast<int64_t>(steps) * per_step < (int64_t(1) << 30)) {
       // one launch: every step and phase, items ordered by per-matrix counters
       tp.g_begin = 0;
       tp.g_end = steps * per_step;
@@ -1063,6 +1116,12 @@ int ns_set_workspace_limit(size_t bytes) {
 
 int ns_set_nvtx(int enable) {
   g_nvtx.store(enable ? 1 : 0);
+  return NS_OK;
+}
+
+int ns_set_f32_gemm(int mode) {
+  if (mode != NS_F32_TENSOR && mode != NS_F32_SIMT) return NS_EINVAL;
+  g_f32_gemm.store(mode);
   return NS_OK;
 }
 

@@ -195,6 +195,17 @@ __device__ __forceinline__ void tma_load_2d_pair(void *smem_dst, const void *map
       : "memory");
 }
 
+// As tma_load_2d_pair for a 3-D tensor map: z selects the slice (the fp32
+// path keeps each tensor as three bf16 slices, see ns_tc.cu).
+__device__ __forceinline__ void tma_load_3d_pair(void *smem_dst, const void *map, int x, int y, int z,
+                                                 uint32_t bar_cluster, uint64_t cache_hint) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar_cluster), "l"(cache_hint)
+      : "memory");
+}
+
 // Bring a TMA descriptor (in global memory) into the descriptor cache ahead
 // of the copies that use it.
 __device__ __forceinline__ void prefetch_tensormap(const void *map) {

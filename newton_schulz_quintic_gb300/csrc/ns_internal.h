@@ -20,7 +20,12 @@
 //   apply   not transposed: D = B W   (W read MN-major), D[i,j] over m x n
 //           transposed:     D = W^T B (W^T = the iterate, K-major), D over n x m
 //           either way D is the next iterate in the caller's orientation.
-// fp32 CUDA-core path: both orientations are kept, all reads K-major:
+// fp32 tensor-core path: as the bf16 path, but every tensor (s[2], a, b) is
+// three bf16 slices x = h + m + l (h = bf16(x), m = bf16(x - h),
+// l = bf16(x - h - m)), stored as three consecutive buffers of the shape
+// above; step 0 reads s[0], which the preparation fills with the slices of
+// Y / (||Y||_F + eps), and the last step writes fp32 into the caller's Y.
+// fp32 CUDA-core path (optional): both orientations are kept, all reads K-major:
 //   x      W      m x n   row pitch pn = round_up(n, 8)
 //   xt[2]  W^T    n x m   row pitch pm; ping-pong across steps
 //   a, b   as above
@@ -123,6 +128,7 @@ struct TcParams {
   int *done;            // per matrix completion counter (zeroed by the host per call)
   int *ticket;          // next item to hand out, relative to g_begin (zeroed by the host per call)
   int tickets;          // 1: items by ticket; 0: static stride
+  int split;            // 1: fp32 path, every tensor three bf16 slices (per-phase launches only)
   const float *rscale;  // per matrix 1 / (||Y||_F + eps): step 0 scales gram by its square and apply by it
   uint64_t wait_limit_ns;  // limit of every bounded wait in the kernel
   float out_scale;      // the last step's result is multiplied by it before the write
@@ -194,6 +200,7 @@ constexpr int kSimtBN = 64;
 // host-side launchers (defined in the .cu files)
 int launch_norm(const PrepParams &p, cudaStream_t s);
 int launch_prep(const PrepParams &p, int total_tiles, cudaStream_t s);
+int launch_split_prep(const PrepParams &p, int total_tiles, cudaStream_t s);
 int launch_norm_tiles(const PrepParams &p, int total_tiles, int max_blocks, cudaStream_t s);
 int launch_norm_finish(const PrepParams &p, cudaStream_t s);
 int launch_resident(const ResParams &p, int smem_bytes, cudaStream_t s);

@@ -3,8 +3,9 @@
 //   * the per-matrix scale from the bf16 norm pass's tile sums,
 //   * preparation: normalise by ||Y||_F + eps, round to the working type and
 //     write both orientations W and W^T,
-//   * the fp32 tiled GEMM phases (gram / square / apply) for large fp32
-//     matrices.
+//   * the fp32 path's preparation for the tensor cores (three bf16 slices),
+//   * the fp32 tiled CUDA-core GEMM phases (gram / square / apply), used for
+//     large fp32 matrices under ns_set_f32_gemm(NS_F32_SIMT).
 // The bf16 norm pass lives in ns_norm.cu, the bf16 tensor-core phases in
 // ns_tc.cu, the shared-memory resident kernel for small matrices in
 // ns_resident.cu.
@@ -219,6 +220,94 @@ int launch_prep(const PrepParams &p, int total_tiles, cudaStream_t s) {
     ns_prep_kernel<kBF16><<<total_tiles, 256, 0, s>>>(p);
   else
     ns_prep_kernel<kF32><<<total_tiles, 256, 0, s>>>(p);
+  count_launch();
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+// fp32 tensor-core path: one block per 64x64 tile of the caller's Y (tiles
+// located as in ns_prep_kernel). Writes w = y / (||Y||_F + eps), computed in
+// fp32, as its three bf16 slices h = bf16(w), m = bf16(w - h),
+// l = bf16(w - h - m) into the three slices of the first iterate buffer s[0]
+// (the caller's orientation, row pitch ps, slices M * ps elements apart).
+// Each thread moves runs of 8 elements: two 16-byte loads of Y when its rows
+// are 16-byte aligned, one 16-byte store per slice.
+__global__ void __launch_bounds__(256) ns_split_prep_kernel(PrepParams p) {
+  const int bid = blockIdx.x;
+  int lo = 0, hi = p.nmats;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (p.tile_prefix[mid] <= bid) lo = mid; else hi = mid;
+  }
+  const int mat = lo;
+  const MatDesc &d = p.mats[mat];
+  const int M = d.M, N = d.N, ps = d.ps;
+  const int local = bid - p.tile_prefix[mat];
+  const int tcols = (N + kPrepTile - 1) / kPrepTile;
+  const int r0 = (local / tcols) * kPrepTile, c0 = (local % tcols) * kPrepTile;
+  const float *y = static_cast<const float *>(d.user);
+  const bool vec = (N % 4 == 0) && ((reinterpret_cast<uintptr_t>(y) & 15) == 0);
+  __nv_bfloat16 *s0 = static_cast<__nv_bfloat16 *>(d.s[0]);
+  const size_t slice = static_cast<size_t>(M) * ps;
+
+  __shared__ float s_denom;
+  const int tid = threadIdx.x;
+  if (tid < 32) {
+    float v = 0.f;
+    for (int i = tid; i < kNormBlocks; i += 32) v += p.partials[mat * kNormBlocks + i];
+    v = warp_sum(v);
+    if (tid == 0) s_denom = 1.0f / (sqrtf(v) + p.eps);  // 1 / (||Y||_F + eps)
+  }
+  __syncthreads();
+  const float inv = s_denom;
+  constexpr int kRuns = kPrepTile * kPrepTile / 8 / 256;  // runs of 8 per thread
+#pragma unroll
+  for (int k = 0; k < kRuns; ++k) {
+    const int q = tid + k * 256, rr = q / (kPrepTile / 8), cg = q % (kPrepTile / 8);
+    const int r = r0 + rr, c = c0 + cg * 8;
+    if (r >= M || c >= N) continue;
+    const float *src = y + static_cast<size_t>(r) * N + c;
+    const int n = min(8, N - c);
+    float w[8];
+    if (vec && n == 8) {
+      const float4 a = __ldg(reinterpret_cast<const float4 *>(src));
+      const float4 b = __ldg(reinterpret_cast<const float4 *>(src) + 1);
+      w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+      w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+    } else {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) w[u] = u < n ? src[u] : 0.f;
+    }
+    uint32_t bits[3][8];  // the slices' bf16 bit patterns
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      float v = w[u] * inv;
+#pragma unroll
+      for (int z = 0; z < 3; ++z) {
+        const __nv_bfloat16 h = __float2bfloat16_rn(v);
+        bits[z][u] = __bfloat16_as_ushort(h);
+        v -= __bfloat162float(h);  // exact
+      }
+    }
+#pragma unroll
+    for (int z = 0; z < 3; ++z) {
+      __nv_bfloat16 *base = s0 + z * slice;
+      __nv_bfloat16 *dst = base + static_cast<size_t>(r) * ps + c;  // 16-byte aligned: ps and c are multiples of 8
+      if (n == 8) {
+        const uint4 o = make_uint4(bits[z][0] | (bits[z][1] << 16), bits[z][2] | (bits[z][3] << 16),
+                                   bits[z][4] | (bits[z][5] << 16), bits[z][6] | (bits[z][7] << 16));
+        if (in_bounds(dst, 16, base, slice * 2, p.status)) *reinterpret_cast<uint4 *>(dst) = o;
+      } else {
+        for (int u = 0; u < n; ++u)
+          if (in_bounds(dst + u, 2, base, slice * 2, p.status))
+            dst[u] = __ushort_as_bfloat16(static_cast<unsigned short>(bits[z][u]));
+      }
+    }
+  }
+}
+
+int launch_split_prep(const PrepParams &p, int total_tiles, cudaStream_t s) {
+  if (total_tiles <= 0) return 0;
+  ns_split_prep_kernel<<<total_tiles, 256, 0, s>>>(p);
   count_launch();
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }

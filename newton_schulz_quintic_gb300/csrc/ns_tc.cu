@@ -471,16 +471,39 @@ __device__ __forceinline__ void prefetch_item_maps_exact(const MatDesc &d, int s
 // K-major: one box of 128 rows. MN-major: box rows are K indices and the tile
 // index runs along them, 64 per box row, so two 64 x 64 boxes 8 KB apart.
 // MN is a template parameter so the producer issues only the copies it needs.
-template <int MN>
-__device__ __forceinline__ void load_operand(uint8_t *dst, const void *map, int mn0, int k0, uint32_t bar_cluster,
-                                             uint64_t pol) {
-  if (MN) {
+// kSplit: the tensor is three bf16 slices behind a 3-D map, z the slice.
+template <int MN, int kSplit>
+__device__ __forceinline__ void load_operand(uint8_t *dst, const void *map, int mn0, int k0, int z,
+                                             uint32_t bar_cluster, uint64_t pol) {
+  if (kSplit) {
+    if (MN) {
+      tma_load_3d_pair(dst, map, mn0, k0, z, bar_cluster, pol);
+      tma_load_3d_pair(dst + kBoxBytes, map, mn0 + 64, k0, z, bar_cluster, pol);
+    } else {
+      tma_load_3d_pair(dst, map, k0, mn0, z, bar_cluster, pol);
+    }
+  } else if (MN) {
     tma_load_2d_pair(dst, map, mn0, k0, bar_cluster, pol);
     tma_load_2d_pair(dst + kBoxBytes, map, mn0 + 64, k0, bar_cluster, pol);
   } else {
     tma_load_2d_pair(dst, map, k0, mn0, bar_cluster, pol);
   }
 }
+
+// fp32 path: every tensor W, A, B is held as three bf16 slices x = h + m + l
+// (h = bf16(x), m = bf16(x - h), l = bf16(x - h - m): 24 significant bits),
+// and a product X Y is the sum of the six slice products whose weights are
+// at least 2^-16 of the leading one -- (h,h), (h,m), (m,h), (h,l), (l,h),
+// (m,m) -- accumulated in one fp32 accumulator; the dropped three are below
+// 2^-24 relative. Part p of an item multiplies slice part_a(p) of the first
+// operand by slice part_b(p) of the second over the whole k range.
+constexpr int kSplitParts = 6;
+__host__ __device__ constexpr int part_a(int part) { return (0x120100 >> (4 * part)) & 15; }  // 0 0 1 0 2 1
+__host__ __device__ constexpr int part_b(int part) { return (0x102010 >> (4 * part)) & 15; }  // 0 1 0 2 0 1
+static_assert(part_a(0) == 0 && part_b(0) == 0 && part_a(1) == 0 && part_b(1) == 1 && part_a(2) == 1 &&
+                  part_b(2) == 0 && part_a(3) == 0 && part_b(3) == 2 && part_a(4) == 2 && part_b(4) == 0 &&
+                  part_a(5) == 1 && part_b(5) == 1,
+              "slice pairs (h,h) (h,m) (m,h) (h,l) (l,h) (m,m)");
 
 // Operand descriptor of the share at `addr` for K sub-step kk (16 K each).
 template <int MN>
@@ -833,6 +856,169 @@ __device__ __forceinline__ bool epilogue_item(const StepCtx &sc, const TileInfo 
   return true;
 }
 
+// ---------------------------------------------------------------- fp32 path
+// Each of the iterates, A and B is three bf16 slices (see part_a); the
+// slices of one tensor are consecutive buffers, `slice` elements apart.
+__device__ __forceinline__ size_t slice_m(const MatDesc &d) { return static_cast<size_t>(d.m) * d.pm; }
+__device__ __forceinline__ size_t slice_s(const MatDesc &d) { return static_cast<size_t>(d.M) * d.ps; }
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t w, int hi) {
+  return __uint_as_float(hi ? (w & 0xffff0000u) : (w << 16));
+}
+
+// Row `row` (< row_lim), columns col .. col+31 (zero at and past col_lim) of
+// a sliced tensor, as the sum of its three slices (h + m first, then l).
+__device__ __forceinline__ void sliced_row(const void *base_v, size_t slice, int pitch, int row, int row_lim,
+                                           int col, int col_lim, float (&v)[32]) {
+  const __nv_bfloat16 *base = static_cast<const __nv_bfloat16 *>(base_v);
+  if (row >= row_lim) {
+#pragma unroll
+    for (int t = 0; t < 32; ++t) v[t] = 0.f;
+    return;
+  }
+  const __nv_bfloat16 *p = base + static_cast<size_t>(row) * pitch + col;
+  if (col + 32 <= col_lim) {  // 16-byte words: pitches are multiples of 8 elements, col of 32
+    uint4 w[3][4];
+#pragma unroll
+    for (int z = 0; z < 3; ++z)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) w[z][q] = __ldg(reinterpret_cast<const uint4 *>(p + z * slice) + q);
+#pragma unroll
+    for (int t = 0; t < 32; ++t) {
+      float e[3];
+#pragma unroll
+      for (int z = 0; z < 3; ++z) {
+        const uint4 &q = w[z][t >> 3];
+        const int i = (t >> 1) & 3;
+        e[z] = bf16_bits_to_float(i == 0 ? q.x : i == 1 ? q.y : i == 2 ? q.z : q.w, t & 1);
+      }
+      v[t] = (e[0] + e[1]) + e[2];
+    }
+  } else {
+#pragma unroll
+    for (int t = 0; t < 32; ++t)
+      v[t] = col + t < col_lim ? (__bfloat162float(p[t]) + __bfloat162float(p[slice + t])) +
+                                     __bfloat162float(p[2 * slice + t])
+                               : 0.f;
+  }
+}
+
+// Stores the 32 x 32 block v (one row per lane, rows row0.., columns col0..)
+// as the three bf16 slices of a sliced tensor; v is consumed.
+__device__ __forceinline__ void store_sliced(uint32_t *stage, float (&v)[32], void *base_v, size_t slice,
+                                             size_t pitch, int row0, int row_lim, int col0, int col_lim,
+                                             int *status) {
+  __nv_bfloat16 *base = static_cast<__nv_bfloat16 *>(base_v);
+  float g[32];
+#pragma unroll
+  for (int z = 0; z < 2; ++z) {
+#pragma unroll
+    for (int t = 0; t < 32; ++t) g[t] = __bfloat162float(__float2bfloat16_rn(v[t]));
+    warp_store_rows(stage, g, base + z * slice, pitch, row0, row_lim, col0, col_lim, false, status);
+#pragma unroll
+    for (int t = 0; t < 32; ++t) v[t] -= g[t];  // exact: v and g agree in their leading bits
+  }
+  warp_store_rows(stage, v, base + 2 * slice, pitch, row0, row_lim, col0, col_lim, false, status);
+}
+
+// Word offset of 16-byte piece `piece` (0..7) of row `row` (0..31) in a
+// 32 x 32 fp32 staging block (both staging tiles of a warp): the row-per-lane
+// layout and the coalesced one (access k, lane l: piece l % 8 of row
+// 4k + l / 8) are both bank-conflict free.
+__device__ __forceinline__ int stage_word_f32(int row, int piece) { return row * 32 + 4 * (piece ^ (row & 7)); }
+
+// As warp_store_rows for an fp32 destination (the caller's Y on the last
+// step of the fp32 path): each store instruction writes 4 rows x 128 bytes.
+__device__ __forceinline__ void warp_store_rows_f32(uint32_t *stage, const float (&v)[32], float *base, size_t pitch,
+                                                    int row0, int row_lim, int col0, int col_lim, int *status) {
+  const size_t bytes = static_cast<size_t>(row_lim) * pitch * 4;
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    *reinterpret_cast<uint4 *>(stage + stage_word_f32(lane, q)) =
+        make_uint4(__float_as_uint(v[4 * q]), __float_as_uint(v[4 * q + 1]), __float_as_uint(v[4 * q + 2]),
+                   __float_as_uint(v[4 * q + 3]));
+  __syncwarp();
+  const int piece = lane & 7;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int rl = 4 * k + (lane >> 3);
+    const int R = row0 + rl, C0 = col0 + 4 * piece;
+    if (R < row_lim && C0 < col_lim) {
+      const uint4 o = *reinterpret_cast<const uint4 *>(stage + stage_word_f32(rl, piece));
+      float *dst = base + static_cast<size_t>(R) * pitch + C0;
+      if (C0 + 4 <= col_lim && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+        if (in_bounds(dst, 16, base, bytes, status)) *reinterpret_cast<uint4 *>(dst) = o;
+      } else {
+        const uint32_t e[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (C0 + u < col_lim && in_bounds(dst + u, 4, base, bytes, status)) dst[u] = __uint_as_float(e[u]);
+      }
+    }
+  }
+  __syncwarp();
+}
+
+// Epilogue of one 32-column chunk on the fp32 path: as epilogue_chunk, with
+// the re-read operand summed from its slices and the results stored as
+// slices (fp32 into the caller's Y on the last step).
+template <int PHASE>
+__device__ __forceinline__ void epilogue_chunk_split(const StepCtx &p, const TileInfo &ti, int r, int chunk,
+                                                     const uint32_t (&raw)[32], uint32_t *stage) {
+  const MatDesc &d = *ti.d;
+  const int r0 = r & ~31;
+  float f[32];
+#pragma unroll
+  for (int t = 0; t < 32; ++t) f[t] = __uint_as_float(raw[t]);
+  if (PHASE == 0 || PHASE == 1) {
+    const int m = d.m, pm = d.pm;
+    const int i = ti.row0 + r, i0 = ti.row0 + r0, jb = ti.col0 + chunk * 32;
+    if (i0 >= m || jb >= m) return;  // warp-uniform
+    if (PHASE == 0) {
+#pragma unroll
+      for (int t = 0; t < 32; ++t) f[t] *= p.gs;
+    } else {
+      float aold[32];
+      sliced_row(d.a, slice_m(d), pm, i, m, jb, m, aold);
+#pragma unroll
+      for (int t = 0; t < 32; ++t) f[t] = p.cb * aold[t] + p.cc * f[t];
+    }
+    store_sliced(stage, f, PHASE == 0 ? d.a : d.b, slice_m(d), pm, i0, m, jb, m, p.status);
+  } else {
+    const int M = d.M, N = d.N;
+    const int R = ti.row0 + r, R0 = ti.row0 + r0, C = ti.col0 + chunk * 32;
+    if (R0 >= M || C >= N) return;  // warp-uniform
+    float xo[32];
+    sliced_row(d.s[p.step & 1], slice_s(d), d.ps, R, M, C, N, xo);
+#pragma unroll
+    for (int t = 0; t < 32; ++t) f[t] = p.as * (p.ca * xo[t] + f[t]);
+    if (!p.final_step)
+      store_sliced(stage, f, d.s[(p.step + 1) & 1], slice_s(d), static_cast<size_t>(d.ps), R0, M, C, N, p.status);
+    else
+      warp_store_rows_f32(stage, f, static_cast<float *>(d.user), static_cast<size_t>(N), R0, M, C, N, p.status);
+  }
+}
+
+// Epilogue of one item on the fp32 path (its k-loop is six times as long,
+// so the chunks are drained one TMEM load at a time).
+template <int PHASE>
+__device__ __forceinline__ bool epilogue_item_split(const StepCtx &sc, const TileInfo &ti, int r, int c0,
+                                                    uint32_t tbase, uint32_t *stage, uint64_t *tfull, uint32_t parity,
+                                                    const Waiter &w) {
+  if (!mbar_wait<true>(tfull, parity, w)) return false;
+  tc_fence_after();
+  uint32_t v[32];
+#pragma unroll 1
+  for (int k = 0; k < kChunksPerWarp; ++k) {
+    __syncwarp();
+    tmem_ld32(tbase + static_cast<uint32_t>((c0 + k) * 32), v);
+    tmem_ld_wait(v);
+    epilogue_chunk_split<PHASE>(sc, ti, r, c0 + k, v, stage);
+  }
+  return true;
+}
+
 // A wait of a whole warp that only lane 0 polls (the other lanes sleep in
 // the shuffle that broadcasts the outcome), leaving the warp converged.
 template <bool kCluster>
@@ -846,19 +1032,19 @@ __device__ __forceinline__ bool warp_mbar_wait(uint64_t *bar, uint32_t parity, c
 // k-block, wait for the stage to be free, and load this CTA's share of both
 // operands (a0, b0: first tile row of each share) onto the leader's full
 // barrier.
-template <int AMN, int BMN>
+template <int AMN, int BMN, int kSplit = 0>
 __device__ __forceinline__ bool produce_segment(int kb0, int kb1, const void *map_a, const void *map_b, int a0, int b0,
                                                 uint8_t *sA, uint8_t *sB, Barriers *bar, bool leader, int &stage,
                                                 uint32_t &phase_bit, int *issued_phase, uint64_t pol,
-                                                const Waiter &w) {
+                                                const Waiter &w, int za = 0, int zb = 0) {
   for (int kb = kb0; kb < kb1; ++kb) {
     if (!warp_mbar_wait<true>(&bar->empty[stage], phase_bit ^ 1u, w)) return false;
     if (elect_one()) {
       if (leader) mbar_arrive_expect_tx(&bar->full[stage], kPairStageBytes);
       const uint32_t full_leader = mapa_shared(smem_u32(&bar->full[stage]), 0);
       const int kx = kb * kTcBK;
-      load_operand<AMN>(sA + stage * kABytes, map_a, a0, kx, full_leader, pol);
-      load_operand<BMN>(sB + stage * kBBytes, map_b, b0, kx, full_leader, pol);
+      load_operand<AMN, kSplit>(sA + stage * kABytes, map_a, a0, kx, za, full_leader, pol);
+      load_operand<BMN, kSplit>(sB + stage * kBBytes, map_b, b0, kx, zb, full_leader, pol);
     }
     __syncwarp();
     issued_phase[stage] = static_cast<int>(phase_bit);
@@ -872,11 +1058,12 @@ __device__ __forceinline__ bool produce_segment(int kb0, int kb1, const void *ma
 
 // The leader's MMAs of one segment of an item: for each k-block, wait for
 // both CTAs' operand shares, issue the four K = 16 pair MMAs into `d_tmem`
-// (accumulating from the item's first k-block on) and release the stage to
-// both producers. AMN / BMN: MN-major first / second operand.
+// (accumulating from the item's first k-block of its first part on) and
+// release the stage to both producers. AMN / BMN: MN-major first / second operand.
 template <int AMN, int BMN>
 __device__ __forceinline__ bool mma_segment(uint32_t d_tmem, int kb0, int kb1, uint8_t *sA, uint8_t *sB,
-                                            Barriers *bar, int &stage, uint32_t &phase_bit, const Waiter &w) {
+                                            Barriers *bar, int &stage, uint32_t &phase_bit, const Waiter &w,
+                                            int part = 0) {
   constexpr uint32_t idesc = umma_idesc_bf16(kTcCluster * kTcBM, kTcBN, AMN, BMN);
   constexpr uint16_t kPairMask = (1u << kTcCluster) - 1;
   for (int kb = kb0; kb < kb1; ++kb) {
@@ -888,7 +1075,7 @@ __device__ __forceinline__ bool mma_segment(uint32_t d_tmem, int kb0, int kb1, u
 #pragma unroll
       for (int k = 0; k < kTcBK / 16; ++k)
         umma_bf16_pair(d_tmem, operand_desc<AMN>(a_addr, k), operand_desc<BMN>(b_addr, k), idesc,
-                       (kb | k) != 0 ? 1u : 0u);
+                       (part | kb | k) != 0 ? 1u : 0u);
       umma_commit_pair_multicast(&bar->empty[stage], kPairMask);
     }
     __syncwarp();
@@ -904,8 +1091,11 @@ __device__ __forceinline__ bool mma_segment(uint32_t d_tmem, int kb0, int kb1, u
 // shared-memory queue (tickets or stride; the single-launch schedule);
 // otherwise every role walks the pair's static stride itself (per-phase
 // launches), which keeps that kernel's code and registers to what it needs.
-template <bool kQueued>
+// kSplit: the fp32 path (per-phase launches only), every tensor three bf16
+// slices and every item six slice products (see part_a).
+template <bool kQueued, int kSplit = 0>
 __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_constant__ TcParams p) {
+  static_assert(!(kQueued && kSplit), "the fp32 path runs per-phase launches");
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *sA = smem;
@@ -1178,14 +1368,18 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
         const ItemPlan pl = plan_item(*ti.d, step, phase, ti.tr, direct, ti.row0, ti.col0, ti.nk);
         const int a0 = ti.row0 + my_rows, b0 = ti.col0 + static_cast<int>(rank) * (kTcBN / 2);
         // one k-loop per operand order, so the copies issued are exactly the ones needed
-        ok = produce_segment<1, 1>(0, pl.e0, pl.map[0][0], pl.map[0][1], a0, b0, sA, sB, bar, leader, stage, phase_bit,
-                                   issued_phase, pol, w);
-        if (ok)
-          ok = produce_segment<0, 1>(pl.e0, pl.e1, pl.map[1][0], pl.map[1][1], a0, b0, sA, sB, bar, leader, stage,
-                                     phase_bit, issued_phase, pol, w);
-        if (ok)
-          ok = produce_segment<0, 0>(pl.e1, ti.nk, pl.map[2][0], pl.map[2][1], a0, b0, sA, sB, bar, leader, stage,
-                                     phase_bit, issued_phase, pol, w);
+        // (per slice product on the fp32 path)
+        for (int part = 0; ok && part < (kSplit ? kSplitParts : 1); ++part) {
+          const int za = kSplit ? part_a(part) : 0, zb = kSplit ? part_b(part) : 0;
+          ok = produce_segment<1, 1, kSplit>(0, pl.e0, pl.map[0][0], pl.map[0][1], a0, b0, sA, sB, bar, leader, stage,
+                                             phase_bit, issued_phase, pol, w, za, zb);
+          if (ok)
+            ok = produce_segment<0, 1, kSplit>(pl.e0, pl.e1, pl.map[1][0], pl.map[1][1], a0, b0, sA, sB, bar, leader,
+                                               stage, phase_bit, issued_phase, pol, w, za, zb);
+          if (ok)
+            ok = produce_segment<0, 0, kSplit>(pl.e1, ti.nk, pl.map[2][0], pl.map[2][1], a0, b0, sA, sB, bar, leader,
+                                               stage, phase_bit, issued_phase, pol, w, za, zb);
+        }
       }
       if (*abort && leader && lane == 0) {
         for (int s = 0; s < kStages; ++s)
@@ -1213,9 +1407,12 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
         tc_fence_after();
         const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * kTcBN);
         // one k-loop per operand order, so descriptors stay compile-time
-        ok = mma_segment<1, 1>(d_tmem, 0, pl.e0, sA, sB, bar, stage, phase_bit, w);
-        if (ok) ok = mma_segment<0, 1>(d_tmem, pl.e0, pl.e1, sA, sB, bar, stage, phase_bit, w);
-        if (ok) ok = mma_segment<0, 0>(d_tmem, pl.e1, ti.nk, sA, sB, bar, stage, phase_bit, w);
+        // (per slice product on the fp32 path)
+        for (int part = 0; ok && part < (kSplit ? kSplitParts : 1); ++part) {
+          ok = mma_segment<1, 1>(d_tmem, 0, pl.e0, sA, sB, bar, stage, phase_bit, w, part);
+          if (ok) ok = mma_segment<0, 1>(d_tmem, pl.e0, pl.e1, sA, sB, bar, stage, phase_bit, w, part);
+          if (ok) ok = mma_segment<0, 0>(d_tmem, pl.e1, ti.nk, sA, sB, bar, stage, phase_bit, w, part);
+        }
         if (!ok) break;
         if (elect_one()) umma_commit_pair_multicast(&bar->tfull[acc], kPairMask);
         __syncwarp();
@@ -1256,12 +1453,21 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
       const StepCtx sc = step_ctx(p, step, ti.mat);
       const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kTcBN);
       bool ok;
-      if (phase == 0)
-        ok = epilogue_item<0>(sc, ti, r, c0, tbase, stage, &bar->tfull[acc], acc_phase, w);
-      else if (phase == 1)
-        ok = epilogue_item<1>(sc, ti, r, c0, tbase, stage, &bar->tfull[acc], acc_phase, w);
-      else
-        ok = epilogue_item<2>(sc, ti, r, c0, tbase, stage, &bar->tfull[acc], acc_phase, w);
+      if constexpr (kSplit) {
+        if (phase == 0)
+          ok = epilogue_item_split<0>(sc, ti, r, c0, tbase, stage, &bar->tfull[acc], acc_phase, w);
+        else if (phase == 1)
+          ok = epilogue_item_split<1>(sc, ti, r, c0, tbase, stage, &bar->tfull[acc], acc_phase, w);
+        else
+          ok = epilogue_item_split<2>(sc, ti, r, c0, tbase, stage, &bar->tfull[acc], acc_phase, w);
+      } else {
+        if (phase == 0)
+          ok = epilogue_item<0>(sc, ti, r, c0, tbase, stage, &bar->tfull[acc], acc_phase, w);
+        else if (phase == 1)
+          ok = epilogue_item<1>(sc, ti, r, c0, tbase, stage, &bar->tfull[acc], acc_phase, w);
+        else
+          ok = epilogue_item<2>(sc, ti, r, c0, tbase, stage, &bar->tfull[acc], acc_phase, w);
+      }
       if (!ok) break;
       tc_fence_before();
       __syncwarp();
@@ -1313,9 +1519,10 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_gemm_kernel(const __grid_co
 
 int launch_tc_kernel(const TcParams &p, int max_ctas, cudaStream_t s) {
   const int smem = tc_smem_bytes();
-  auto kernel = p.tickets ? ns_tc_gemm_kernel<true> : ns_tc_gemm_kernel<false>;
-  static SmemOptIn opt_in[2];
-  if (opt_in[p.tickets ? 1 : 0].ensure(reinterpret_cast<const void *>(kernel), smem)) return -1;
+  const int variant = p.tickets ? 1 : (p.split ? 2 : 0);
+  auto kernel = variant == 1 ? ns_tc_gemm_kernel<true> : (variant == 2 ? ns_tc_gemm_kernel<false, 1> : ns_tc_gemm_kernel<false>);
+  static SmemOptIn opt_in[3];
+  if (opt_in[variant].ensure(reinterpret_cast<const void *>(kernel), smem)) return -1;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -157,7 +157,7 @@ def test_steps_zero_is_normalisation(dtype, shape):
     check_one(x, y, steps=0)
 
 
-# ------------------------------------------------------------ fp32 CUDA-core path
+# ------------------------------------------------------------ fp32 large matrices
 
 F32_SHAPES = [(100, 300), (300, 100), (200, 200), (65, 1000), (129, 257)]
 
@@ -167,6 +167,36 @@ def test_f32_large_shapes(shape):
     x = seeded(shape, torch.float32, seed=shape[0] + 3 * shape[1], std=1.0)
     (y,) = run_gpu([x])
     check_one(x, y)
+
+
+@pytest.mark.parametrize("mode", ["tensor", "simt"])
+@pytest.mark.parametrize("shape", F32_SHAPES + [(640, 1200), (1200, 640), (70, 4000)])
+def test_f32_gemm_modes(mode, shape):
+    # both fp32 GEMM paths -- tensor cores on three bf16 slices per tensor, and
+    # CUDA-core fp32 -- meet the fp32 bar against the oracle, each bitwise
+    # repeatable
+    api.set_f32_gemm(mode)
+    try:
+        x = seeded(shape, torch.float32, seed=7 * shape[0] + shape[1], std=1.0)
+        (y,) = run_gpu([x])
+        (y2,) = run_gpu([x])
+        assert torch.equal(y, y2)
+        check_one(x, y)
+    finally:
+        api.set_f32_gemm("tensor")
+
+
+def test_f32_tensor_batch_cost_order_and_extents():
+    # a batch of several fp32 shapes on the tensor cores (cost-ordered tiles
+    # across matrices, ragged edges) with zero trailing rows and columns:
+    # every matrix meets the bar and its zero lines stay exactly zero
+    shapes = [(300, 520), (520, 300), (129, 1031), (70, 4000), (256, 256)]
+    xs = [seeded(s, torch.float32, seed=400 + i, std=1.0) for i, s in enumerate(shapes)]
+    xs[0][290:] = 0
+    xs[1][:, 280:] = 0
+    ys = run_gpu(xs)
+    for x, y in zip(xs, ys):
+        check_one(x, y)
 
 
 def test_f32_zero_rows_and_custom_eps():

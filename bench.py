@@ -262,6 +262,12 @@ def time_steps(steps, restore, one_step, stream):
     return [s.elapsed_time(e) for s, e in ev]
 
 
+def small_f32(wl) -> bool:
+    """Whether every matrix of an fp32 workload takes the shared-memory
+    resident path (m <= 64), not the tensor cores."""
+    return all(min(M, N) <= 64 for M, N in wl.shapes)
+
+
 def measure_workload(wl, dev, steps, warmup, graph=False):
     """Matrices/s of one workload on this GPU alone (the per-config record):
     direct library calls, and optionally the same calls replayed from a CUDA
@@ -322,6 +328,15 @@ def measure_workload(wl, dev, steps, warmup, graph=False):
            "tflops_nominal": round(nominal / (mean / 1e3) / 1e12, 2)}
     rec["executed_frac"] = {"burst": round(rec["tflops_executed"] / peaks["bf16_tflops"], 4),
                             "sustained": round(rec["tflops_executed"] / peaks["bf16_tflops_sustained"], 4)}
+    if wl.dtype == "f32" and not small_f32(wl):
+        # large fp32 matrices run on the bf16 tensor cores as six slice products
+        # per GEMM: their bf16 tensor work is six times the fp32 flops
+        bf16_work = 6 * rec["tflops_executed"]
+        rec["executed_frac"] = {"note": "fp32 flops; the bf16 tensor work is 6x (three bf16 slices per tensor, "
+                                        "six slice products per GEMM)",
+                                "bf16_tensor_tflops": round(bf16_work, 2),
+                                "bf16_tensor_burst": round(bf16_work / peaks["bf16_tflops"], 4),
+                                "bf16_tensor_sustained": round(bf16_work / peaks["bf16_tflops_sustained"], 4)}
     rec["ms_per_step_prepared"] = round(statistics.mean(ptimes), 4)
     rec["ms_per_step_prepared_median"] = round(statistics.median(ptimes), 4)
     rec["host_us_per_call"] = round(host_us, 1)

@@ -137,6 +137,8 @@ WORKLOADS = {
     # MoE expert stack: 76 x 2048x6144 as remainder batches of 64 and 12
     "bf16-moe-76x2048x6144": Workload("bf16-moe-76x2048x6144", ((2048, 6144),) * 76, "bf16",
                                       0.02, 1005, calls=(64, 12)),
+    # the expert shape in fp32 (large fp32 matrices: the fp32 tensor-core path)
+    "f32-8x2048x6144": Workload("f32-8x2048x6144", ((2048, 6144),) * 8, "f32", 0.02, 1006),
 }
 
 HEADLINE = "bf16-8x8192x6144"

@@ -296,6 +296,17 @@ def test_full_bf16_moe_64_plus_12_sampled():
         check_one(xs[i], ys[i], ref=_closed(xs[i]))
 
 
+def test_full_f32_8x2048x6144_sampled():
+    # the expert shape in fp32 on the tensor-core fp32 path (three bf16 slices
+    # per tensor): the fp32 bar against the closed form
+    wl = inputs.WORKLOADS["f32-8x2048x6144"]
+    xs = wl.matrices()
+    ys = run_gpu(xs)
+    for i in (0, 7):
+        err = check_one(xs[i], ys[i], ref=_closed(xs[i]))
+        print(f"fp32 2048x6144 matrix {i}: rel err {err:.4e}")
+
+
 def test_full_bf16_mixed_120_sampled():
     wl = inputs.WORKLOADS["bf16-mixed-120"]
     xs = wl.matrices()

@@ -181,7 +181,8 @@ def test_f32_gemm_modes(mode, shape):
         (y,) = run_gpu([x])
         (y2,) = run_gpu([x])
         assert torch.equal(y, y2)
-        check_one(x, y)
+        err = check_one(x, y)
+        print(f"fp32 {mode} {shape}: rel err {err:.3e}")
     finally:
         api.set_f32_gemm("tensor")
 

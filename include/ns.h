@@ -322,12 +322,18 @@ int ns_set_gemm_schedule(int mode);
  *   NS_F32_TENSOR  tcgen05 tensor cores (default): every fp32 tensor (the
  *                  iterate, A and B) is held as three bf16 slices
  *                  x = h + m + l, h = bf16(x), m = bf16(x - h),
- *                  l = bf16(x - h - m) (24 significant bits), and each
+ *                  l = bf16(x - h - m) (x to 2^-27 relative), and each
  *                  product is the fp32-accumulated sum of the six slice
- *                  products of weight 2^-16 or more: (h,h), (h,m), (m,h),
- *                  (h,l), (l,h), (m,m). The three dropped products are below
- *                  2^-24 of the leading one, so results stay within fp32's
- *                  1e-4 parity bar of the fp64 oracle.
+ *                  products of weight 2^-18 or more, smallest first:
+ *                  (h,l), (l,h), (m,m), (h,m), (m,h), (h,h). The dropped
+ *                  products weigh 2^-27 or less. The tensor cores' fp32
+ *                  accumulation loses up to about a unit in the last place
+ *                  per instruction, so the error grows with the contraction
+ *                  length: measured 2.2e-5 relative after 5 steps for
+ *                  2048 x 6144 (fp32 CUDA cores: 5.0e-6). A call whose
+ *                  largest fp32 matrix has max(M, N) > 16384 therefore runs
+ *                  on the CUDA cores, keeping every result within fp32's
+ *                  1e-4 bar.
  *   NS_F32_SIMT    CUDA-core fp32 FMA GEMMs.
  * Both follow the same definition (the quintic iteration in fp32 between
  * phases); their rounding differs, so their results differ in the last

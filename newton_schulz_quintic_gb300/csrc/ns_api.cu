@@ -250,8 +250,11 @@ bool resident_fits(int64_t m, int64_t n, int dtype) {
 
 // Large fp32 matrices: the tensor-core path (three bf16 slices per tensor,
 // six slice products per GEMM) by default, or the CUDA-core GEMMs
-// (ns_set_f32_gemm).
+// (ns_set_f32_gemm). The tensor cores' accumulation error grows with the
+// contraction length (max(M, N) in gram); past kF32TensorMaxK a call runs on
+// the CUDA cores, whose fp32 FMAs round to nearest.
 std::atomic<int> g_f32_gemm{NS_F32_TENSOR};
+constexpr int64_t kF32TensorMaxK = 16384;
 
 void build_layout(const int64_t *shapes, int count, int dtype, Layout &L) {
   L = Layout();
@@ -294,6 +297,9 @@ void build_layout(const int64_t *shapes, int count, int dtype, Layout &L) {
     ++g.count;
     g.smem = std::max(g.smem, resident_smem_bytes(m, ns, dtype, c));
   }
+  if (L.split)
+    for (int i : order)
+      if (std::max(shapes[2 * i], shapes[2 * i + 1]) > kF32TensorMaxK) L.split = false;
   // largest Newton-Schulz cost first; ties keep the caller's order
   std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
     return ns_cost(shapes[2 * a], shapes[2 * a + 1]) > ns_cost(shapes[2 * b], shapes[2 * b + 1]);

@@ -493,17 +493,21 @@ __device__ __forceinline__ void load_operand(uint8_t *dst, const void *map, int 
 // fp32 path: every tensor W, A, B is held as three bf16 slices x = h + m + l
 // (h = bf16(x), m = bf16(x - h), l = bf16(x - h - m): 24 significant bits),
 // and a product X Y is the sum of the six slice products whose weights are
-// at least 2^-16 of the leading one -- (h,h), (h,m), (m,h), (h,l), (l,h),
-// (m,m) -- accumulated in one fp32 accumulator; the dropped three are below
-// 2^-24 relative. Part p of an item multiplies slice part_a(p) of the first
-// operand by slice part_b(p) of the second over the whole k range.
+// at least 2^-18 of the leading one -- (h,h), (h,m), (m,h), (h,l), (l,h),
+// (m,m) -- accumulated in one fp32 accumulator; the dropped three weigh
+// 2^-27 or less. Part p of an item multiplies slice part_a(p) of the first
+// operand by slice part_b(p) of the second over the whole k range. The parts
+// run smallest first: the tensor core's accumulation loses up to about one
+// unit in the last place of the running sum per instruction, so the small
+// parts, added while the sum is still ~2^-9 of its final size, contribute
+// almost nothing to the error, and only the (h,h) pass adds at full size.
 constexpr int kSplitParts = 6;
-__host__ __device__ constexpr int part_a(int part) { return (0x120100 >> (4 * part)) & 15; }  // 0 0 1 0 2 1
-__host__ __device__ constexpr int part_b(int part) { return (0x102010 >> (4 * part)) & 15; }  // 0 1 0 2 0 1
-static_assert(part_a(0) == 0 && part_b(0) == 0 && part_a(1) == 0 && part_b(1) == 1 && part_a(2) == 1 &&
-                  part_b(2) == 0 && part_a(3) == 0 && part_b(3) == 2 && part_a(4) == 2 && part_b(4) == 0 &&
-                  part_a(5) == 1 && part_b(5) == 1,
-              "slice pairs (h,h) (h,m) (m,h) (h,l) (l,h) (m,m)");
+__host__ __device__ constexpr int part_a(int part) { return (0x010120 >> (4 * part)) & 15; }  // 0 2 1 0 1 0
+__host__ __device__ constexpr int part_b(int part) { return (0x001102 >> (4 * part)) & 15; }  // 2 0 1 1 0 0
+static_assert(part_a(0) == 0 && part_b(0) == 2 && part_a(1) == 2 && part_b(1) == 0 && part_a(2) == 1 &&
+                  part_b(2) == 1 && part_a(3) == 0 && part_b(3) == 1 && part_a(4) == 1 && part_b(4) == 0 &&
+                  part_a(5) == 0 && part_b(5) == 0,
+              "slice pairs (h,l) (l,h) (m,m) (h,m) (m,h) (h,h)");
 
 // Operand descriptor of the share at `addr` for K sub-step kk (16 K each).
 template <int MN>

@@ -71,9 +71,26 @@ def test_workspace_bytes(lib):
     # bf16: two iterates in the caller's orientation, A and B (6144 x 6144)
     need = 2 * (2 * 8192 * 6144 + 2 * 6144 * 6144)
     assert need <= big < need + (1 << 20)
-    # fp32: W, two W^T buffers, A and B
+    # fp32 on the tensor cores (default): iterates, A and B as three bf16 slices each
     big32 = api.workspace_bytes([(8192, 6144)], api.NS_F32)
-    assert big32 >= 4 * (3 * 6144 * 8192 + 2 * 6144 * 6144)
+    need32 = 3 * need
+    assert need32 <= big32 < need32 + (1 << 20)
+    # fp32 on the CUDA cores: W, two W^T buffers, A and B
+    api.set_f32_gemm("simt")
+    try:
+        simt32 = api.workspace_bytes([(8192, 6144)], api.NS_F32)
+        long_simt = api.workspace_bytes([(70, 20000)], api.NS_F32)
+        edge_simt = api.workspace_bytes([(70, 16384)], api.NS_F32)
+    finally:
+        api.set_f32_gemm("tensor")
+    need_simt = 4 * (3 * 6144 * 8192 + 2 * 6144 * 6144)
+    assert need_simt <= simt32 < need_simt + (1 << 20)
+    # a call with an fp32 matrix longer than 16384 runs on the CUDA cores in either mode
+    assert api.workspace_bytes([(70, 20000)], api.NS_F32) == long_simt
+    assert api.workspace_bytes([(70, 16384)], api.NS_F32) != edge_simt
+    with pytest.raises(KeyError):
+        api.set_f32_gemm("fp64")
+    assert lib.ns_set_f32_gemm(7) == -1  # NS_EINVAL
     assert small < 1 << 20
     assert api.workspace_bytes([(-1, 5)], api.NS_BF16) == 0
     assert api.workspace_bytes([(5, 5)], 7) == 0

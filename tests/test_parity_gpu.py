@@ -187,6 +187,17 @@ def test_f32_gemm_modes(mode, shape):
         api.set_f32_gemm("tensor")
 
 
+def test_f32_long_contraction():
+    # 16384 columns: the longest contraction the fp32 tensor-core path takes
+    # (its accumulation error grows with it); 20000: the call runs on the
+    # CUDA cores. Both within the fp32 bar.
+    for shape in [(96, 16384), (70, 20000)]:
+        x = seeded(shape, torch.float32, seed=shape[1], std=1.0)
+        (y,) = run_gpu([x])
+        err = check_one(x, y)
+        print(f"fp32 {shape}: rel err {err:.3e}")
+
+
 def test_f32_tensor_batch_cost_order_and_extents():
     # a batch of several fp32 shapes on the tensor cores (cost-ordered tiles
     # across matrices, ragged edges) with zero trailing rows and columns:

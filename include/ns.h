@@ -49,7 +49,7 @@ extern "C" {
 #endif
 
 /* element types of X */
-#define NS_F32 0  /* float32 in, float32 out, float32 arithmetic throughout */
+#define NS_F32 0  /* float32 in, float32 out, fp32-accurate arithmetic throughout (see ns_set_f32_gemm) */
 #define NS_BF16 1 /* bfloat16 in/out; bf16 tensor-core operands, fp32 accumulation */
 
 /* status codes */
@@ -290,7 +290,8 @@ int64_t ns_num_workspace_allocations(void);
  * them in place; fp32 the sums and extents), 1 norm finish (bf16: the
  * per-matrix scale from the tile sums), 2 gram, 3 square, 4 apply,
  * 5 resident, 6 gemm (the tensor-core kernel running every step and phase of
- * a call in one launch), 7 prep (fp32: the normalising copy), 8 momentum
+ * a call in one launch), 7 prep (fp32: the normalising copy, or its bf16
+ * slices on the tensor cores), 8 momentum
  * (ns_muon_update_batched's element-wise step), the total milliseconds into
  * ms[k] and the launch count into launches[k] for k < n (n <= 9). Returns
  * NS_OK or NS_EINVAL / NS_ECUDA.

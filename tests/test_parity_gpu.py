@@ -453,6 +453,28 @@ def test_many_matrices_one_call():
     assert all(torch.equal(a, b) for a, b in zip(ys, ref))
 
 
+def test_f32_explicit_workspace_and_host_entry_point_agree():
+    # the fp32 tensor-core path through a caller workspace and through host
+    # buffers gives the plain call's bits
+    xs = [seeded((300, 520), torch.float32, 19, std=1.0), seeded((520, 300), torch.float32, 20, std=1.0),
+          seeded((64, 128), torch.float32, 21, std=1.0)]
+    ref = run_gpu(xs)
+    dev = [x.cuda() for x in xs]
+    need = api.workspace_bytes([tuple(x.shape) for x in xs], torch.float32)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    api.orthogonalize_batched(dev, workspace=ws)
+    torch.cuda.synchronize()
+    assert api.get_status() == 0
+    for r, d in zip(ref, dev):
+        assert torch.equal(r, d.cpu())
+    host = [x.clone().pin_memory() for x in xs]
+    api.orthogonalize_batched_host(host)
+    for r, h in zip(ref, host):
+        assert torch.equal(r, h)
+    for x, r in zip(xs, ref):
+        check_one(x, r)
+
+
 def test_host_entry_point_pageable_buffers():
     xs = [seeded((640, 1200), torch.bfloat16, 72), seeded((1200, 640), torch.bfloat16, 73),
           seeded((24, 100), torch.bfloat16, 74)]

@@ -198,6 +198,23 @@ def test_f32_long_contraction():
         print(f"fp32 {shape}: rel err {err:.3e}")
 
 
+def test_f32_tensor_unaligned_matrix():
+    # a matrix whose base is 4 bytes past a 16-byte boundary and whose rows are
+    # not a multiple of 16 bytes: read and written element by element where it
+    # must be, nothing outside it touched
+    M, N = 130, 257
+    x = seeded((M, N), torch.float32, seed=77, std=1.0)
+    buf = torch.full((M * N + 2,), 7.0, dtype=torch.float32, device="cuda")
+    d = buf[1:1 + M * N].view(M, N)
+    assert d.data_ptr() % 16 == 4
+    d.copy_(x.cuda())
+    api.orthogonalize_batched([d])
+    torch.cuda.synchronize()
+    assert api.get_status() == 0
+    assert float(buf[0]) == 7.0 and float(buf[-1]) == 7.0
+    check_one(x, d.cpu())
+
+
 def test_f32_tensor_batch_cost_order_and_extents():
     # a batch of several fp32 shapes on the tensor cores (cost-ordered tiles
     # across matrices, ragged edges) with zero trailing rows and columns:

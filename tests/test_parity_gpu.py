@@ -109,6 +109,27 @@ def test_bf16_tensor_core_shapes(shape):
     check_one(x, y)
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("shape", [(8, 50000), (50000, 8), (257, 8192), (4096, 66)])
+def test_extreme_aspect_ratios(dtype, shape):
+    # a handful of rows against tens of thousands of columns (one partial tile
+    # row, a k-loop of hundreds of k-blocks; fp32 with more than 16384 columns
+    # runs on the CUDA cores), a matrix one row past a tile edge, and a tall one
+    x = seeded(shape, dtype, seed=shape[0] + shape[1], std=0.02 if dtype == torch.bfloat16 else 1.0)
+    (y,) = run_gpu([x])
+    check_one(x, y)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("steps", [1, 2])
+def test_one_and_two_steps_large_path(dtype, steps):
+    # the first step is also the last (the caller's matrix written from the
+    # first iterate) or the one before it, on the tensor-core paths
+    x = seeded((300, 700), dtype, seed=90 + steps, std=0.02 if dtype == torch.bfloat16 else 1.0)
+    (y,) = run_gpu([x], steps=steps)
+    check_one(x, y, steps=steps)
+
+
 def test_bf16_mixed_batch_one_call():
     xs = [seeded(s, torch.bfloat16, seed=i) for i, s in enumerate(TC_SHAPES + [(24, 100), (1, 300)])]
     ys = run_gpu(xs)
